@@ -1,0 +1,70 @@
+"""Algorithmic byte and FLOP counts of one absorbed MLA decode step.
+
+These are the figures the roofline is taken against, counted from the problem
+statement, not from any kernel:
+
+* each cached token is ``d_c + d_h^R = 512 + 64 = 576`` scalars, 1152 bytes in
+  bf16, and is read once per sequence per step (DeepSeek-MLA-Principle, "KV
+  cache per token" and the decode HBM-traffic comparison in "那为什么 MLA 仍可能更快");
+* per (query token, visible cache token) the absorbed path does
+  ``2*n_h*d_c + n_h*d_h^R`` multiply-adds: logits over the 576-wide row and the
+  weighted sum over the 512-wide latent (same page, "推理计算：FLOPs 可能增加",
+  the MLA history-interaction count), i.e. 139,264 MACs = 278,528 FLOP;
+* query token ``j`` of a sequence with ``L`` prior tokens sees ``L + j + 1``
+  cache tokens (causal among the new tokens).
+"""
+
+from __future__ import annotations
+
+from .workloads import D_LATENT, D_NOPE, D_ROPE, N_HEADS
+
+BF16_BYTES = 2
+
+
+def cache_scalars_per_token() -> int:
+    return D_LATENT + D_ROPE
+
+
+def mha_cache_scalars_per_token() -> int:
+    """Per-token K and V of plain multi-head attention with 128 heads of 128."""
+    return 2 * N_HEADS * D_NOPE
+
+
+def cache_bytes_per_token(dtype_bytes: int = BF16_BYTES) -> int:
+    return cache_scalars_per_token() * dtype_bytes
+
+
+def mla_history_macs(L: int) -> int:
+    """Multiply-adds of one query token against L cache tokens (absorbed form)."""
+    return 2 * L * N_HEADS * D_LATENT + L * N_HEADS * D_ROPE
+
+
+def mha_history_macs(L: int) -> int:
+    """Multiply-adds of one query token against L cached K/V rows (plain MHA)."""
+    return 2 * L * N_HEADS * D_NOPE
+
+
+def flops_per_token_pair() -> int:
+    return 2 * mla_history_macs(1)
+
+
+def step_cache_bytes(kv_lens) -> int:
+    """Cache bytes one decode step reads: every cached token once per sequence."""
+    return sum(int(n) for n in kv_lens) * cache_bytes_per_token()
+
+
+def step_attention_flops(kv_lens, n_q: int) -> int:
+    """Attention FLOPs of one step; query j of a sequence sees kv_len - n_q + j + 1 tokens."""
+    tot = 0
+    for n in kv_lens:
+        L = int(n) - n_q
+        for j in range(n_q):
+            tot += (L + j + 1) * flops_per_token_pair()
+    return tot
+
+
+def roofline_seconds(kv_lens, n_q: int, hbm_gbs: float, tflops: float) -> tuple[float, str]:
+    """Slower of cache bytes at HBM bandwidth and FLOPs at dense bf16 tensor peak."""
+    t_mem = step_cache_bytes(kv_lens) / (hbm_gbs * 1e9)
+    t_flop = step_attention_flops(kv_lens, n_q) / (tflops * 1e12)
+    return (t_mem, "hbm") if t_mem >= t_flop else (t_flop, "tensor")

@@ -1,0 +1,298 @@
+"""CPU oracle for absorbed MLA decode.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  It shares no code with the CUDA path and
+imports nothing from it; both sides only consume the same seeded inputs.
+
+Sources (three web pages on MLA weight absorption):
+
+* [MA]  "MLA 矩阵吸收 & 吸收分离 原理详解" (chang-wenbin.github.io, MLA_Matrix_Absorption)
+* [DP]  "DeepSeek-MLA-Principle" (senjlearning.space)
+* [N1]  "DeepSeek MLA 架构详解：多头潜向量注意力如何将 KV Cache 降低 93%" (explore.n1n.ai)
+
+What it computes: the plain, *non-absorbed* definition of one MLA decode step
+([DP] §2 "注意力计算", equations (2)/(5), (4), (9), the scaled score, the softmax
+and (10)): per head, decompress ``k_t = [W_UK[h] c_t ; k^R_t]`` and
+``v_t = W_UV[h] c_t`` for every visible cached token, score with the 192-wide
+query ``[q^C ; RoPE(q^R)]`` scaled by ``1/sqrt(d_h + d_h^R)``, softmax over the
+visible tokens, and sum the values.  It also returns the latent output
+``O' = sum_t alpha_t c_t`` and the log-sum-exp of the scores, which the absorbed
+path produces along the way.  Everything is float64 on values read back from
+the bf16 cache image that :func:`append_kv` builds.
+
+The absorbed fp64 form ([DP] "3) MLA 中怎么吸收", key and value absorption;
+[MA] §2.1, §4.1) is here only to cross-check the identity.
+
+Readings where the pages leave a step open (each listed in the design notes):
+
+* the tokens appended this step are attended to: query ``j`` of a sequence with
+  ``L`` prior tokens sits at position ``L + j`` and sees tokens ``0 .. L + j``;
+* RoPE is the half-split ("rotate half") form of [N1] ``apply_rope``:
+  ``inv_freq_i = theta^(-i/half)``, ``theta = 10000``, ``half = d_R / 2``,
+  ``out[i] = x[i] cos - x[i+half] sin``, ``out[i+half] = x[i+half] cos + x[i] sin``;
+* the cache holds the rotated key ``k^R`` in bf16 ([N1] rotates before the append);
+  its exact bf16 bits follow a fixed fp32 recipe (:func:`rope_key_bf16_bits`).
+"""
+
+from __future__ import annotations
+
+import math
+from functools import lru_cache
+
+import numpy as np
+
+THETA = 10000.0
+PAGE = 64
+
+
+# --------------------------------------------------------------------------- bf16
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """Exact widening of bf16 bit patterns to float32."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    return bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def f32_to_bf16_bits(x) -> np.ndarray:
+    """Round float32 to bf16, round-to-nearest-even (NaN stays a quiet NaN)."""
+    x = np.asarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    r = ((u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        r[nan] = ((u[nan] >> np.uint64(16)) | np.uint64(0x40)).astype(np.uint16)
+    return r
+
+
+# --------------------------------------------------------------------------- RoPE
+def rope_inv_freq(d_rope: int) -> np.ndarray:
+    """inv_freq_i = theta^(-i/half), i = 0 .. half-1 ([N1] apply_rope)."""
+    half = d_rope // 2
+    return np.array([THETA ** (-(i / half)) for i in range(half)], dtype=np.float64)
+
+
+def rope_f64(x, pos) -> np.ndarray:
+    """Exact (float64) half-split RoPE of ``x[..., d_R]`` at integer positions ``pos``.
+
+    [DP] eq. (3) and (8) apply RoPE to the decoupled key/query branch; the
+    rotation itself is [N1] ``apply_rope``: ``x*cos + rotate_half(x)*sin`` with
+    ``rotate_half(x) = [-x2, x1]``.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    half = x.shape[-1] // 2
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * rope_inv_freq(2 * half)
+    c, s = np.cos(ang), np.sin(ang)
+    x1, x2 = x[..., :half], x[..., half:]
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+
+
+@lru_cache(maxsize=8)
+def rope_table_f32(n_pos: int, d_rope: int = 64) -> tuple[np.ndarray, np.ndarray]:
+    """cos/sin of ``pos * inv_freq_i`` computed in float64 by libm, rounded to float32.
+
+    This is the fixed table the bit-exact append recipe rotates with: angle in
+    double (``pos`` times ``10000^(-i/32)`` from ``pow``), ``cos``/``sin`` in double,
+    one rounding to float32.
+    """
+    half = d_rope // 2
+    inv = [THETA ** (-(i / half)) for i in range(half)]
+    cos = np.empty((n_pos, half), dtype=np.float32)
+    sin = np.empty((n_pos, half), dtype=np.float32)
+    for p in range(n_pos):
+        cos[p] = [math.cos(p * f) for f in inv]
+        sin[p] = [math.sin(p * f) for f in inv]
+    return cos, sin
+
+
+def rope_key_bf16_bits(k_pe_bits, pos) -> np.ndarray:
+    """Rotated key as the cache stores it: the fixed fp32 recipe, then bf16.
+
+    ``k_pe_bits`` is ``[n, d_R]`` bf16 bits (pre-RoPE), ``pos`` is ``[n]``.  With
+    ``c, s`` from :func:`rope_table_f32`, each output is one float32 product per
+    term and one float32 add/subtract, every step rounded (no fused multiply-add),
+    then rounded to bf16 (nearest even):
+    ``r1 = (x1*c) - (x2*s)``, ``r2 = (x2*c) + (x1*s)``.
+    """
+    x = bf16_bits_to_f32(k_pe_bits)
+    pos = np.asarray(pos, dtype=np.int64)
+    half = x.shape[-1] // 2
+    need = int(pos.max()) + 1 if pos.size else 1
+    cos_t, sin_t = rope_table_f32(-(-need // 4096) * 4096, 2 * half)
+    c, s = cos_t[pos], sin_t[pos]
+    x1, x2 = x[..., :half], x[..., half:]
+    r1 = np.subtract(np.multiply(x1, c, dtype=np.float32), np.multiply(x2, s, dtype=np.float32), dtype=np.float32)
+    r2 = np.add(np.multiply(x2, c, dtype=np.float32), np.multiply(x1, s, dtype=np.float32), dtype=np.float32)
+    return f32_to_bf16_bits(np.concatenate([r1, r2], axis=-1))
+
+
+# --------------------------------------------------------------------------- paged cache
+def append_kv(cache_bits, c_kv_new_bits, k_pe_new_bits, seq_lens_before, page_table) -> np.ndarray:
+    """Append n_new tokens per sequence to a paged cache image (returns a new image).
+
+    Token ``j`` of sequence ``b`` sits at position ``pos = seq_lens_before[b] + j``
+    and lands in page ``page_table[b][pos // 64]``, slot ``pos % 64``
+    ([MA] §6: 64-token pages; [DP] FlashMLA point 4: paged cache with a block
+    table).  The row is ``[c_kv ; RoPE(k_pe, pos)]``: the latent is copied, the
+    RoPE key is rotated before it is cached ([N1] forward_decode step 1;
+    [DP] eq. (3)).  Shapes: cache ``[P, 64, 576]``, c_kv ``[B, n, 512]``,
+    k_pe ``[B, n, 64]``, all uint16 bf16 bits.
+    """
+    out = np.array(cache_bits, dtype=np.uint16, copy=True)
+    c_new = np.asarray(c_kv_new_bits, dtype=np.uint16)
+    k_new = np.asarray(k_pe_new_bits, dtype=np.uint16)
+    B, n_new, d_c = c_new.shape
+    if B == 0 or n_new == 0:
+        return out
+    lens = np.asarray(seq_lens_before, dtype=np.int64)
+    pt = np.asarray(page_table, dtype=np.int64)
+    pos = lens[:, None] + np.arange(n_new)[None, :]            # [B, n]
+    pages = np.take_along_axis(pt, pos // PAGE, axis=1)         # [B, n]
+    slots = pos % PAGE
+    out[pages, slots, :d_c] = c_new
+    out[pages, slots, d_c:] = rope_key_bf16_bits(k_new.reshape(B * n_new, -1), pos.reshape(-1)).reshape(B, n_new, -1)
+    return out
+
+
+def gather_sequence(cache_bits, page_table_row, kv_len: int, d_c: int = 512):
+    """Tokens 0..kv_len-1 of one sequence read back from the cache as float64: (c [kv, d_c], k^R [kv, d_R])."""
+    t = np.arange(kv_len)
+    pages = np.asarray(page_table_row, dtype=np.int64)[t // PAGE]
+    rows = np.asarray(cache_bits, dtype=np.uint16)[pages, t % PAGE]
+    return bf16_bits_to_f64(rows[:, :d_c]), bf16_bits_to_f64(rows[:, d_c:])
+
+
+# --------------------------------------------------------------------------- attention
+def _softmax_lse(s: np.ndarray):
+    """Max-subtracted softmax and natural log-sum-exp of a score vector ([DP] Softmax_j)."""
+    m = s.max()
+    e = np.exp(s - m)
+    z = e.sum()
+    return e / z, m + math.log(z)
+
+
+def attention_weights_mha(q_nope_h, q_rope_h, w_uk_h, c, kr, pos: int) -> np.ndarray:
+    """alpha_{t} for one head and one query at position ``pos`` (non-absorbed form).
+
+    ``score_t = q^T k_t / sqrt(d_h + d_h^R)`` with ``q = [q^C ; RoPE(q^R, pos)]``
+    ([DP] eq. (9)) and ``k_t = [W_UK[h] c_t ; k^R_t]`` ([DP] eq. (2), (4)), over
+    the visible tokens ``t <= pos`` ([DP] eq. (10) sums ``j = 1..t``).
+    """
+    d_h, d_r = q_nope_h.shape[-1], q_rope_h.shape[-1]
+    vis = pos + 1
+    k = np.concatenate([c[:vis] @ np.asarray(w_uk_h, np.float64).T, kr[:vis]], axis=1)
+    q = np.concatenate([np.asarray(q_nope_h, np.float64), rope_f64(q_rope_h, pos)])
+    alpha, _ = _softmax_lse((k @ q) / math.sqrt(d_h + d_r))
+    return alpha
+
+
+def decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len: int, heads=None):
+    """One sequence's decode outputs by the plain definition (non-absorbed, fp64).
+
+    Inputs (float64 or anything numpy converts): ``q_nope [n_q, H, d_h]``,
+    ``q_rope [n_q, H, d_R]`` (pre-RoPE), ``w_uk``/``w_uv [H, d_h, d_c]``,
+    ``c [kv, d_c]`` and rotated ``kr [kv, d_R]`` of the sequence's cached tokens.
+    Query ``j`` is at position ``prior_len + j``.  Returns ``o [n_q, nh, d_v]``
+    ([DP] eq. (10): ``o = sum_t alpha_t W_UV[h] c_t``), ``o_lat [n_q, nh, d_c]``
+    (``sum_t alpha_t c_t``) and ``lse [n_q, nh]`` (natural log-sum-exp of the
+    scaled scores) for the heads in ``heads`` (default: all).
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    w_uk = np.asarray(w_uk, np.float64)
+    w_uv = np.asarray(w_uv, np.float64)
+    n_q, n_h, d_h = q_nope.shape
+    d_r = q_rope.shape[-1]
+    d_c = c.shape[1]
+    heads = list(range(n_h)) if heads is None else list(heads)
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    o = np.zeros((n_q, len(heads), w_uv.shape[1]))
+    o_lat = np.zeros((n_q, len(heads), d_c))
+    lse = np.zeros((n_q, len(heads)))
+    for hi, h in enumerate(heads):
+        k = np.concatenate([c @ w_uk[h].T, kr], axis=1)   # [kv, d_h + d_R]
+        v = c @ w_uv[h].T                                 # [kv, d_v]
+        for j in range(n_q):
+            pos = prior_len + j
+            q = np.concatenate([q_nope[j, h], rope_f64(q_rope[j, h], pos)])
+            alpha, lse[j, hi] = _softmax_lse((k[:pos + 1] @ q) * scale)
+            o[j, hi] = alpha @ v[:pos + 1]
+            o_lat[j, hi] = alpha @ c[:pos + 1]
+    return o, o_lat, lse
+
+
+def decode_absorbed(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len: int, heads=None,
+                    token_range: tuple[int, int] | None = None):
+    """The absorbed form in fp64, used only to cross-check the absorption identity.
+
+    ``q~ = W_UK[h]^T q^C`` ([DP] key absorption; [MA] §2.1 ``Q' = Q W_UK^T``),
+    ``score_t = (q~ . c_t + RoPE(q^R) . k^R_t) / sqrt(d_h + d_h^R)`` ([MA] §4.1 score
+    split), ``m = sum_t alpha_t c_t`` and ``o = W_UV[h] m`` ([DP] value absorption).
+    With ``token_range=(t0, t1)`` only tokens in ``[t0, t1)`` take part and the
+    result is that split's partial: ``o_lat`` normalised within the split and its
+    ``lse`` (``-inf`` and zeros when the split holds no visible token).
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_rope = np.asarray(q_rope, np.float64)
+    w_uk = np.asarray(w_uk, np.float64)
+    w_uv = np.asarray(w_uv, np.float64)
+    n_q, n_h, d_h = q_nope.shape
+    d_r = q_rope.shape[-1]
+    d_c = c.shape[1]
+    heads = list(range(n_h)) if heads is None else list(heads)
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    t0, t1 = token_range if token_range is not None else (0, c.shape[0])
+    o = np.zeros((n_q, len(heads), w_uv.shape[1]))
+    o_lat = np.zeros((n_q, len(heads), d_c))
+    lse = np.full((n_q, len(heads)), -np.inf)
+    for hi, h in enumerate(heads):
+        for j in range(n_q):
+            pos = prior_len + j
+            hi_t = min(t1, pos + 1)
+            if hi_t <= t0:
+                continue
+            q_t = w_uk[h].T @ q_nope[j, h]
+            q_r = rope_f64(q_rope[j, h], pos)
+            s = (c[t0:hi_t] @ q_t + kr[t0:hi_t] @ q_r) * scale
+            alpha, lse[j, hi] = _softmax_lse(s)
+            o_lat[j, hi] = alpha @ c[t0:hi_t]
+            o[j, hi] = w_uv[h] @ o_lat[j, hi]
+    return o, o_lat, lse
+
+
+def combine_splits(o_parts, lse_parts):
+    """Merge per-split partials by log-sum-exp ([DP] FlashMLA point 3: blocked,
+    online-normalised softmax over the history).
+
+    ``o_parts [S, ..., d]`` are split-normalised outputs, ``lse_parts [S, ...]``
+    their log-sum-exps (``-inf`` for empty splits).  Returns ``(o, lse)`` with
+    ``lse = log sum_s exp(lse_s)`` and ``o = sum_s exp(lse_s - lse) o_s``.
+    """
+    o_parts = np.asarray(o_parts, np.float64)
+    lse_parts = np.asarray(lse_parts, np.float64)
+    m = lse_parts.max(axis=0)
+    w = np.exp(lse_parts - m)
+    z = w.sum(axis=0)
+    lse = m + np.log(z)
+    o = (w[..., None] * o_parts).sum(axis=0) / z[..., None]
+    return o, lse
+
+
+def out_absorb(o_lat, w_uv):
+    """``O[h] = W_UV[h] O'[h]`` for ``o_lat [..., H, d_c]`` ([N1] final einsum 'bhm,hdm->bhd')."""
+    return np.einsum("...hm,hdm->...hd", np.asarray(o_lat, np.float64), np.asarray(w_uv, np.float64))
+
+
+def absorb_query(q_nope, q_rope, w_uk, pos):
+    """``[W_UK[h]^T q^C ; RoPE(q^R, pos)]`` per head: the 576-wide absorbed query in fp64.
+
+    ``q_nope [..., H, d_h]``, ``q_rope [..., H, d_R]``, ``pos`` broadcast over the
+    leading axes ([N1] step 3 einsum 'bhd,hdm->bhm'; [DP] eq. (8) for the RoPE part).
+    """
+    q_nope = np.asarray(q_nope, np.float64)
+    q_t = np.einsum("...hd,hdm->...hm", q_nope, np.asarray(w_uk, np.float64))
+    pos = np.asarray(pos)[..., None]
+    q_r = rope_f64(q_rope, np.broadcast_to(pos, q_rope.shape[:-1]))
+    return np.concatenate([q_t, q_r], axis=-1)
