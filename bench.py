@@ -1,0 +1,385 @@
+#!/usr/bin/env python
+"""Benchmark of one absorbed MLA decode step on GB300.
+
+A step is one pass of the whole path over one batch: append the n_q new tokens,
+absorb the query, split attention, log-sum-exp combine, output up-projection.
+The default workload is the batched decode (B=32, prior context 4096, one new
+token per sequence, 64-token pages with a shuffled page table).
+
+Printed (rank 0, one JSON line): ``value`` = latent-cache bytes the step reads
+(every cached token once per sequence, 1152 B per token) summed over ranks,
+divided by the mean step time (device time from CUDA events on the launching
+stream, L2 flushed before every step, inputs resident in HBM).  ``e2e`` repeats
+the measurement through the same calls with the step's inputs copied from
+pinned host memory and the output copied back inside the timed region.
+``roofline`` rates the split-attention kernel against the measured HBM copy
+bandwidth (or dense bf16 peak when FLOPs bind).  ``cpu_baseline`` times the
+fp64 CPU oracle on a bounded sample of the same workload.
+
+``--impl reference`` times that CPU oracle alone (rank 0 only) as the
+reference arm.  Multi-GPU runs (torchrun) are independent replicas: each rank
+decodes its own batch of the same workload, no collective on the data path.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from mla_absorbed_decode_absorb_gb300 import accounting as A  # noqa: E402
+from mla_absorbed_decode_absorb_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MLA absorbed decode µs/step, latent-cache GB/s and TFLOP/s vs GB300 roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+DOMINANT_KERNEL = "split attention (mla_decode_attn_partial)"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=W.DEFAULT_BENCH_WORKLOAD, choices=sorted(W.WORKLOADS))
+    p.add_argument("--split-pages", type=int, default=None, help="override the workload's KV split size")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-oracle sample budget")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------------------- helpers
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def blas_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k, "").isdigit():
+            return int(os.environ[k])
+    return host_cores()
+
+
+def workload_config(wl: W.Workload, inp: W.Inputs | None, world: int, extra=None):
+    cfg = {"workload": wl.name, "description": wl.description, "B": wl.batch, "n_q": wl.n_q,
+           "n_h": W.N_HEADS, "d_c": W.D_LATENT, "d_rope": W.D_ROPE, "page_size": W.PAGE,
+           "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+           "l2": "flushed (256 MiB write) before every timed step; per-step CUDA-event times summed"}
+    if wl.ragged:
+        cfg["L_range"] = list(wl.ragged)
+    else:
+        cfg["L"] = wl.context
+    if inp is not None:
+        cfg["kv_tokens"] = int(inp.kv_lens.sum())
+    cfg.update(extra or {})
+    return cfg
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.t0 = self.t1 = None
+        self.path = os.path.join("/tmp", f"mla_bench_clocks_{os.getpid()}.csv")
+        sel = []
+        try:
+            bus = torch.cuda.get_device_properties(device_index).pci_bus_id
+            sel = ["-i", str(bus)]
+        except Exception:
+            pass
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(inp: W.Inputs, budget_s: float, max_seqs: int | None = None):
+    """Run the fp64 oracle over whole sequences until the budget is spent; returns (bytes, seconds, seqs)."""
+    import numpy as np
+
+    from oracle import mla_oracle as O
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    w_uk, w_uv = O.bf16_bits_to_f64(bits(inp.w_uk)), O.bf16_bits_to_f64(bits(inp.w_uv))
+    done, nbytes, t = 0, 0, 0.0
+    for b in range(inp.batch if max_seqs is None else min(max_seqs, inp.batch)):
+        c_bits, k_bits = (bits(x) for x in inp.sequence(b))
+        q_nope, q_rope = O.bf16_bits_to_f64(bits(inp.q_nope[b])), O.bf16_bits_to_f64(bits(inp.q_rope[b]))
+        t0 = time.perf_counter()
+        kv = c_bits.shape[0]
+        c = O.bf16_bits_to_f64(c_bits)
+        kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(kv)))
+        O.decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, int(inp.prior_lens[b]))
+        t += time.perf_counter() - t0
+        done += 1
+        nbytes += kv * A.cache_bytes_per_token()
+        if t >= budget_s:
+            break
+    return nbytes, t, done
+
+
+def run_reference(args, wl):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    inp = W.generate(wl, seed=0)
+    for _ in range(args.warmup):
+        oracle_sample(inp, 0.0, max_seqs=1)
+    per_step = []
+    nbytes = 0
+    for _ in range(args.steps):
+        nb, t, _ = oracle_sample(inp, 0.0, max_seqs=1)
+        per_step.append(t)
+        nbytes = nb
+    mean_t = sum(per_step) / len(per_step)
+    value = nbytes / mean_t / 1e9
+    sample = f"one sequence ({int(inp.kv_lens[0])} cached tokens, all 128 heads) of the workload per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl, inp, world, {"sample": sample}),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# --------------------------------------------------------------------------- our path
+def kernel_source_hash():
+    src = os.path.join(ROOT, "mla_absorbed_decode_absorb_gb300", "csrc", "decode_attn.cu")
+    with open(src, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the split-attention kernel from the committed ncu summary, if it is current."""
+    path = os.path.join(ROOT, "profiles", "decode_attn_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_sha256_16") != kernel_source_hash():
+            return None
+        rec = d.get("workloads", {}).get(workload)
+        return None if rec is None else float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def run_ours(args, wl):
+    import torch.distributed as dist
+
+    from mla_absorbed_decode_absorb_gb300 import ops
+    from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    inp = W.generate(wl, seed=rank)
+    s = DecodeSession(inp, device=dev, split_pages=args.split_pages)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    step_bytes = A.step_cache_bytes(inp.kv_lens.tolist())
+    step_flops = A.step_attention_flops(inp.kv_lens.tolist(), wl.n_q)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        s.step()
+    torch.cuda.synchronize()
+    if ops.mla_get_device_status() != ops.MLA_OK:
+        raise RuntimeError("device status set during warm-up")
+
+    stages = ["append", "absorb", "attend_partial", "combine", "project_out"]
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(K)]
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for k in range(K):
+        flush.zero_()
+        e = ev[k]
+        e[0].record(stream)
+        for i, name in enumerate(stages):
+            getattr(s, name)()
+            e[i + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop() if clocks else None
+
+    per_stage = [[ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)] for i in range(len(stages))]
+    step_ms = [sum(per_stage[i][k] for i in range(len(stages))) for k in range(K)]
+    mean_ms = sum(step_ms) / K
+    attn_ms = sum(per_stage[2]) / K
+    t = torch.tensor([mean_ms, attn_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    mean_ms, attn_ms = float(t[0]), float(t[1])
+    if ops.mla_get_device_status() != ops.MLA_OK:
+        raise RuntimeError("device status set during the timed region")
+
+    # end to end: inputs from pinned host memory, output back to host, inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host_in = [x.cpu().pin_memory() for x in (s.c_new, s.k_new, s.q_nope, s.q_rope, s.prior_lens, s.kv_lens)]
+        dev_in = [s.c_new, s.k_new, s.q_nope, s.q_rope, s.prior_lens, s.kv_lens]
+        host_out = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+        K2 = min(K, 200)
+        e2e_ms = []
+        for k in range(K2 + 3):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for h, d in zip(host_in, dev_in):
+                d.copy_(h, non_blocking=True)
+            s.step()
+            host_out.copy_(s.out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if k >= 3:
+                e2e_ms.append(a.elapsed_time(b))
+        m = torch.tensor([sum(e2e_ms) / len(e2e_ms)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(m, op=dist.ReduceOp.MAX)
+        e2e = {"value": step_bytes * world / (float(m[0]) * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": float(m[0]), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    t_mem, bound = A.roofline_seconds(inp.kv_lens.tolist(), wl.n_q, peaks["hbm_gbs"], peaks["bf16_tflops"])
+    attn_s = attn_ms * 1e-3
+    if bound == "hbm":
+        achieved, peak, unit = step_bytes / attn_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = step_flops / attn_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": profiled_traffic(wl.name), "peak_source": peak_src,
+                "kernel": DOMINANT_KERNEL, "algorithmic_bytes": step_bytes, "algorithmic_flops": step_flops}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        nb, secs, nseq = oracle_sample(inp, args.cpu_seconds)
+        cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{nseq} of {inp.batch} sequences, all 128 heads, fp64 non-absorbed form ({secs:.1f} s)"}
+
+    line = {
+        "metric": METRIC, "value": step_bytes * world / (mean_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": mean_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": workload_config(wl, inp, world, {"split_pages": s.split_pages, "num_splits": s.num_splits}),
+        "us_per_step": mean_ms * 1e3,
+        "attn_us": attn_ms * 1e3,
+        "attn_tflops": step_flops / attn_s / 1e12,
+        "attn_gbs": step_bytes / attn_s / 1e9,
+        "stage_us": {n: 1e3 * sum(v) / K for n, v in zip(stages, per_stage)},
+        "roofline_time_us": t_mem * 1e6,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": s.launches_per_step() * K,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,207 @@
+/*
+ * mla_decode.h -- C ABI of the absorbed Multi-Head Latent Attention decode path
+ * for GB300 (sm_103a).
+ *
+ * The decode step reads only the compressed per-token cache: a 512-wide latent
+ * c_kv plus a 64-wide RoPE key shared by all heads, 576 bf16 scalars per token,
+ * stored in pages of 64 tokens.  Per-head keys and values are never formed:
+ * W_UK is folded into the query and W_UV is applied once to the latent output
+ * ("MLA 矩阵吸收 & 吸收分离 原理详解", sections 2.1 and 4.1;
+ * "DeepSeek-MLA-Principle", "3) MLA 中怎么吸收", key and value absorption).
+ *
+ * Fixed dimensions (DeepSeek-V3, "DeepSeek-MLA-Principle" section 3 table):
+ *   n_h = 128 heads, d_h = 128 (content part of q/k per head), d_h^R = 64
+ *   (RoPE part), d_c = 512 (latent), d_v = 128; score scale 1/sqrt(192);
+ *   RoPE theta = 10000, half-split rotation; page size 64 tokens.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, row-major and densely packed as
+ *     the shape comments say, owned by the caller.  The library allocates no
+ *     memory.  bf16 tensors are passed as their 16-bit patterns (mla_bf16).
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns MLA_ERR_INVALID_ARG (or MLA_ERR_UNSUPPORTED /
+ *     MLA_ERR_WORKSPACE) and launches nothing.
+ *   - Work is enqueued asynchronously on `stream` (0 = the legacy default
+ *     stream).  A launch failure returns MLA_ERR_CUDA.
+ *   - Faults found by the kernels themselves (a page id or position out of
+ *     range, a bounded wait that ran out) never trap: the kernel skips the
+ *     access, records the first such code in a per-device status word and
+ *     returns.  mla_get_device_status() reads and clears that word.
+ *   - A 16-byte-aligned base address is required for every tensor.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mla_bf16; /* bit pattern of a bfloat16 value */
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null pointer, bad size or alignment */
+  MLA_ERR_UNSUPPORTED = 2, /* shape outside what the kernels handle */
+  MLA_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  MLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  MLA_ERR_TIMEOUT = 5,     /* (device status) a bounded wait ran out */
+  MLA_ERR_BOUNDS = 6       /* (device status) page id / position out of range */
+} mla_status;
+
+enum {
+  MLA_N_HEADS = 128,
+  MLA_D_NOPE = 128,
+  MLA_D_LATENT = 512,
+  MLA_D_ROPE = 64,
+  MLA_D_ROW = 576, /* MLA_D_LATENT + MLA_D_ROPE scalars per cached token */
+  MLA_PAGE = 64,
+  MLA_MAX_NQ = 8   /* new query tokens per sequence per step */
+};
+
+/* Version of this ABI (bumped on any signature change). */
+int mla_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mla_status_string(mla_status status);
+
+/*
+ * RoPE table.  RoPE is the half-split rotation of "DeepSeek MLA 架构详解"
+ * (apply_rope in its decode listing): inv_freq_i = 10000^(-i/32), i < 32,
+ * angle = pos * inv_freq_i, out[i] = x[i] cos - x[i+32] sin,
+ * out[i+32] = x[i+32] cos + x[i] sin.
+ *
+ * mla_rope_table_bytes: bytes of a table covering positions [0, max_positions).
+ * mla_rope_table_init: fills a caller-owned device buffer `table`
+ *   [max_positions][64] float32 (cos of the 32 frequencies, then sin) with the
+ *   angles' cos/sin computed in double on the host and rounded once to float.
+ *   Blocking: returns after the copy to `table` has completed on `stream`.
+ *   The table is an input of mla_append_kv and mla_absorb_q; any position they
+ *   rotate must be < max_positions.
+ */
+size_t mla_rope_table_bytes(int max_positions);
+mla_status mla_rope_table_init(float* table, int max_positions, cudaStream_t stream);
+
+/*
+ * mla_append_kv -- write n_new tokens per sequence into the paged cache.
+ * ("DeepSeek MLA 架构详解", decode listing step 1: rotate the key, then append;
+ *  "DeepSeek-MLA-Principle" eq. (3) and FlashMLA point 4, paged cache with a
+ *  block table; "MLA 矩阵吸收 …" section 6, page_size = 64.)
+ *
+ *   c_kv_new        [B, n_new, 512] bf16   latent of the new tokens
+ *   k_pe_new        [B, n_new, 64]  bf16   RoPE key of the new tokens, NOT yet rotated
+ *   seq_lens_before [B] int32              position of each sequence's first new token
+ *   page_table      [B, pt_stride] int32   page ids of each sequence's pages, in order
+ *   rope_table      from mla_rope_table_init, covering positions < rope_max_pos
+ *   cache           [num_pages, 64, 576] bf16, updated in place
+ *
+ * Token j of sequence b has position pos = seq_lens_before[b] + j and is written
+ * to cache[page_table[b][pos/64]][pos%64] as [c_kv ; RoPE(k_pe, pos)].  The
+ * rotation is done in float32 with separately rounded products and sums (no
+ * fused multiply-add) and rounded to bf16 to nearest even, so the cache image
+ * is reproducible bit for bit.  A token whose position, page slot or page id is
+ * out of range is skipped and sets MLA_ERR_BOUNDS in the device status.
+ * B >= 0, n_new >= 0 (0 launches nothing).
+ */
+mla_status mla_append_kv(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
+                         const int32_t* seq_lens_before, const int32_t* page_table,
+                         int pt_stride, const float* rope_table, int rope_max_pos,
+                         mla_bf16* cache, int64_t num_pages, int B, int n_new,
+                         cudaStream_t stream);
+
+/*
+ * mla_absorb_q -- the absorbed query, 576 wide per head.
+ * ("MLA 矩阵吸收 …" section 2.1, Q' = Q W_UK^T; "DeepSeek-MLA-Principle"
+ *  key absorption q~ = (W_UK[h])^T q^C; "DeepSeek MLA 架构详解" step 3,
+ *  einsum 'bhd,hdm->bhm'; RoPE of the query branch, eq. (8).)
+ *
+ *   q_nope          [B, n_q, 128, 128] bf16  content query q^C per head
+ *   q_rope          [B, n_q, 128, 64]  bf16  RoPE query q^R per head, NOT yet rotated
+ *   seq_lens_before [B] int32                query j of sequence b is at position
+ *                                            seq_lens_before[b] + j
+ *   w_uk            [128, 128, 512] bf16     W_UK[h][d][m]
+ *   q_abs           [B, n_q, 128, 576] bf16  out: [sum_d q^C[d] W_UK[h][d][:] ; RoPE(q^R)]
+ *
+ * Accumulation is float32; results are rounded to bf16.  1 <= n_q <= MLA_MAX_NQ.
+ */
+mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope,
+                        const int32_t* seq_lens_before, const mla_bf16* w_uk,
+                        const float* rope_table, int rope_max_pos, mla_bf16* q_abs,
+                        int B, int n_q, cudaStream_t stream);
+
+/*
+ * Split-KV attention over the paged latent cache.
+ * ("DeepSeek-MLA-Principle" section 2: score = q.k / sqrt(d_h + d_h^R), softmax,
+ *  eq. (10); the absorbed score Q'_nope c^T + Q_rope k_rope^T of "MLA 矩阵吸收 …"
+ *  section 4.1; value absorption O' = softmax . c; FlashMLA point 3: blocked,
+ *  online-normalised softmax over the history, split-KV.)
+ *
+ *   q_abs      [B, n_q, 128, 576] bf16 (from mla_absorb_q)
+ *   cache      [num_pages, 64, 576] bf16; must already hold the n_q new tokens
+ *   page_table [B, pt_stride] int32
+ *   kv_lens    [B] int32: cached tokens of each sequence INCLUDING the n_q new
+ *              ones; query j of sequence b sees tokens 0 .. kv_lens[b] - n_q + j
+ *              (causal among the new tokens); kv_lens[b] >= n_q.
+ *   max_kv_len host-side upper bound of kv_lens (sizes the grid without a sync);
+ *              a sequence longer than it sets MLA_ERR_BOUNDS.
+ *   split_pages pages per KV split (0 = choose automatically).
+ *   workspace  device scratch of at least mla_decode_workspace_size() bytes
+ *              (may be NULL when that size is 0).
+ *   o_latent   [B, n_q, 128, 512] float32 out: O'[h] = sum_t alpha_t c_t
+ *   lse        [B, n_q, 128] float32 out (nullable): natural log-sum-exp of the
+ *              scaled scores.
+ *
+ * mla_decode_attn runs the split kernel and, when there is more than one
+ * split, the float32 log-sum-exp combine.  The two halves are also exposed
+ * separately (same arguments): mla_decode_attn_partial writes per-split partials
+ * into the workspace (or the final outputs when there is a single split) and
+ * mla_decode_combine merges them (a no-op for a single split).
+ */
+mla_status mla_decode_workspace_size(int B, int n_q, int max_kv_len, int split_pages,
+                                     size_t* bytes);
+mla_status mla_decode_num_splits(int B, int n_q, int max_kv_len, int split_pages,
+                                 int* num_splits);
+mla_status mla_decode_attn(const mla_bf16* q_abs, const mla_bf16* cache, int64_t num_pages,
+                           const int32_t* page_table, int pt_stride, const int32_t* kv_lens,
+                           int B, int n_q, int max_kv_len, int split_pages,
+                           void* workspace, size_t workspace_bytes,
+                           float* o_latent, float* lse, cudaStream_t stream);
+mla_status mla_decode_attn_partial(const mla_bf16* q_abs, const mla_bf16* cache, int64_t num_pages,
+                                   const int32_t* page_table, int pt_stride, const int32_t* kv_lens,
+                                   int B, int n_q, int max_kv_len, int split_pages,
+                                   void* workspace, size_t workspace_bytes,
+                                   float* o_latent, float* lse, cudaStream_t stream);
+mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
+                              const void* workspace, size_t workspace_bytes,
+                              float* o_latent, float* lse, cudaStream_t stream);
+
+/*
+ * mla_out_absorb -- O[h] = W_UV[h] O'[h], the value up-projection applied once.
+ * ("MLA 矩阵吸收 …" section 2.1, V side: O = (Attn c) W_UV, once per step;
+ *  "DeepSeek MLA 架构详解" step 5, einsum 'bhm,hdm->bhd'.)
+ *
+ *   o_latent [B, n_q, 128, 512] float32 (from mla_decode_attn)
+ *   w_uv     [128, 128, 512] bf16   W_UV[h][d][m]
+ *   out      [B, n_q, 128, 128] bf16 out
+ *
+ * o_latent is rounded to bf16 before the product; accumulation is float32.
+ */
+mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16* out,
+                          int B, int n_q, cudaStream_t stream);
+
+/*
+ * Device status: synchronizes `stream`, returns the first fault code any kernel
+ * of this library recorded on the current device since the last call
+ * (MLA_OK if none) and clears it.  MLA_ERR_CUDA if the synchronisation fails.
+ */
+mla_status mla_get_device_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

@@ -1,0 +1,243 @@
+// The C ABI of include/mla_decode.h: argument validation, split planning,
+// the per-device status word, the RoPE table, and the launches.
+#include <math.h>
+#include <stdlib.h>
+
+#include <mutex>
+#include <vector>
+
+#include "internal.cuh"
+
+// Per-device fault word written by the kernels (first code wins).
+__device__ int g_mla_device_status;
+
+namespace {
+
+using namespace mla;
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mutex;
+int* g_status_ptr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+// Device address of the status word on the current device (nullptr on failure).
+int* status_ptr() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mla_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+int num_sms() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_num_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_num_sms[dev] = n;
+  }
+  return g_num_sms[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Split-KV partition.  Automatic choice: enough (sequence, query, split) units
+// to give every SM about two, without splits shorter than one page.
+bool make_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan) {
+  if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ || max_kv_len < n_q || split_pages < 0) return false;
+  plan->max_pages = (max_kv_len + kPage - 1) / kPage;
+  if (split_pages == 0) {
+    const int units = B * n_q > 0 ? B * n_q : 1;
+    int per_seq = (2 * num_sms() + units - 1) / units;
+    if (per_seq < 1) per_seq = 1;
+    if (per_seq > plan->max_pages) per_seq = plan->max_pages;
+    split_pages = (plan->max_pages + per_seq - 1) / per_seq;
+  }
+  plan->split_pages = split_pages;
+  plan->num_splits = (plan->max_pages + split_pages - 1) / split_pages;
+  const size_t rows = static_cast<size_t>(B) * n_q * plan->num_splits * kHeads;
+  plan->o_part_bytes = round_up(rows * kLatent * sizeof(float), 256);
+  plan->lse_part_bytes = round_up(rows * sizeof(float), 256);
+  plan->workspace_bytes = plan->num_splits > 1 ? plan->o_part_bytes + plan->lse_part_bytes : 0;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_abi_version(void) { return 1; }
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: null pointer, bad size or alignment";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: shape outside what the kernels handle";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA runtime call or launch failed";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded wait in a kernel ran out";
+    case MLA_ERR_BOUNDS: return "MLA_ERR_BOUNDS: a page id or position was out of range";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+size_t mla_rope_table_bytes(int max_positions) {
+  return max_positions > 0 ? static_cast<size_t>(max_positions) * kRope * sizeof(float) : 0;
+}
+
+mla_status mla_rope_table_init(float* table, int max_positions, cudaStream_t stream) {
+  if (table == nullptr || max_positions <= 0 || !aligned16(table)) return MLA_ERR_INVALID_ARG;
+  std::vector<float> host(static_cast<size_t>(max_positions) * kRope);
+  double inv_freq[kHalfRope];
+  for (int i = 0; i < kHalfRope; ++i) inv_freq[i] = pow(10000.0, -static_cast<double>(i) / kHalfRope);
+  for (int p = 0; p < max_positions; ++p) {
+    float* row = host.data() + static_cast<size_t>(p) * kRope;
+    for (int i = 0; i < kHalfRope; ++i) {
+      const double a = static_cast<double>(p) * inv_freq[i];
+      row[i] = static_cast<float>(cos(a));
+      row[kHalfRope + i] = static_cast<float>(sin(a));
+    }
+  }
+  cudaError_t e = cudaMemcpyAsync(table, host.data(), host.size() * sizeof(float),
+                                  cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return from_cuda(e);
+}
+
+mla_status mla_append_kv(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
+                         const int32_t* seq_lens_before, const int32_t* page_table,
+                         int pt_stride, const float* rope_table, int rope_max_pos,
+                         mla_bf16* cache, int64_t num_pages, int B, int n_new,
+                         cudaStream_t stream) {
+  if (B < 0 || n_new < 0) return MLA_ERR_INVALID_ARG;
+  if (B == 0 || n_new == 0) return MLA_OK;
+  if (!c_kv_new || !k_pe_new || !seq_lens_before || !page_table || !rope_table || !cache)
+    return MLA_ERR_INVALID_ARG;
+  if (pt_stride < 1 || rope_max_pos < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c_kv_new) || !aligned16(cache)) return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_append_kv(c_kv_new, k_pe_new, seq_lens_before, page_table, pt_stride,
+                                    rope_table, rope_max_pos, cache, num_pages, B, n_new, st, stream));
+}
+
+mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope,
+                        const int32_t* seq_lens_before, const mla_bf16* w_uk,
+                        const float* rope_table, int rope_max_pos, mla_bf16* q_abs,
+                        int B, int n_q, cudaStream_t stream) {
+  if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_nope || !q_rope || !seq_lens_before || !w_uk || !rope_table || !q_abs || rope_max_pos < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) || !aligned16(q_abs))
+    return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_absorb_q(q_nope, q_rope, seq_lens_before, w_uk, rope_table, rope_max_pos,
+                                   q_abs, B, n_q, st, stream));
+}
+
+mla_status mla_decode_workspace_size(int B, int n_q, int max_kv_len, int split_pages, size_t* bytes) {
+  SplitPlan plan;
+  if (bytes == nullptr || !make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
+  *bytes = plan.workspace_bytes;
+  return MLA_OK;
+}
+
+mla_status mla_decode_num_splits(int B, int n_q, int max_kv_len, int split_pages, int* num_splits) {
+  SplitPlan plan;
+  if (num_splits == nullptr || !make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
+  *num_splits = plan.num_splits;
+  return MLA_OK;
+}
+
+mla_status mla_decode_attn_partial(const mla_bf16* q_abs, const mla_bf16* cache, int64_t num_pages,
+                                   const int32_t* page_table, int pt_stride, const int32_t* kv_lens,
+                                   int B, int n_q, int max_kv_len, int split_pages,
+                                   void* workspace, size_t workspace_bytes,
+                                   float* o_latent, float* lse, cudaStream_t stream) {
+  SplitPlan plan;
+  if (!make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_abs || !cache || !page_table || !kv_lens || !o_latent || num_pages < 1 || pt_stride < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache) || !aligned16(o_latent)) return MLA_ERR_INVALID_ARG;
+  if (plan.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
+                                   !aligned16(workspace)))
+    return MLA_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  float* o_out = o_latent;
+  float* lse_out = lse;
+  if (plan.num_splits > 1) {
+    o_out = static_cast<float*>(workspace);
+    lse_out = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.o_part_bytes);
+  }
+  return from_cuda(launch_decode_partial(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q,
+                                         max_kv_len, plan, o_out, lse_out, st, stream));
+}
+
+mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
+                              const void* workspace, size_t workspace_bytes,
+                              float* o_latent, float* lse, cudaStream_t stream) {
+  SplitPlan plan;
+  if (!make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
+  if (B == 0 || plan.num_splits == 1) return MLA_OK;
+  if (!o_latent || !aligned16(o_latent)) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return MLA_ERR_WORKSPACE;
+  const float* o_part = static_cast<const float*>(workspace);
+  const float* lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + plan.o_part_bytes);
+  return from_cuda(launch_combine(o_part, lse_part, B, n_q, plan.num_splits, o_latent, lse, stream));
+}
+
+mla_status mla_decode_attn(const mla_bf16* q_abs, const mla_bf16* cache, int64_t num_pages,
+                           const int32_t* page_table, int pt_stride, const int32_t* kv_lens,
+                           int B, int n_q, int max_kv_len, int split_pages,
+                           void* workspace, size_t workspace_bytes,
+                           float* o_latent, float* lse, cudaStream_t stream) {
+  mla_status s = mla_decode_attn_partial(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q,
+                                         max_kv_len, split_pages, workspace, workspace_bytes, o_latent,
+                                         lse, stream);
+  if (s != MLA_OK) return s;
+  return mla_decode_combine(B, n_q, max_kv_len, split_pages, workspace, workspace_bytes, o_latent, lse,
+                            stream);
+}
+
+mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16* out, int B, int n_q,
+                          cudaStream_t stream) {
+  if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!o_latent || !w_uv || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_latent) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  return from_cuda(launch_out_absorb(o_latent, w_uv, out, B, n_q, stream));
+}
+
+mla_status mla_get_device_status(cudaStream_t stream) {
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  int value = 0;
+  if (cudaMemcpy(&value, st, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MLA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MLA_ERR_CUDA;
+  return static_cast<mla_status>(value);
+}
+
+}  // extern "C"

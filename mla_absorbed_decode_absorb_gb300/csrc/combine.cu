@@ -1,0 +1,57 @@
+// Split-KV merge by log-sum-exp, in float32.
+//
+// "DeepSeek-MLA-Principle", FlashMLA point 3: the history is processed in
+// blocks with the softmax normalisation updated online; splitting the blocks
+// over CTAs needs this final merge.  With split outputs O'_s normalised within
+// their split and natural log-sum-exps lse_s:
+//   lse = log sum_s exp(lse_s),  O' = sum_s exp(lse_s - lse) O'_s.
+// Empty splits carry lse_s = -inf and weigh nothing.
+#include "internal.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 128;  // 4 latent columns per thread
+
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+               int num_splits, float* __restrict__ o_latent, float* __restrict__ lse) {
+  const int64_t row = blockIdx.x;  // (b*n_q + j)*128 + h
+  const int64_t bj = row / kHeads;
+  const int h = static_cast<int>(row % kHeads);
+  float m = -INFINITY;
+  for (int s = 0; s < num_splits; ++s) m = fmaxf(m, lse_part[(bj * num_splits + s) * kHeads + h]);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float z = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < num_splits; ++s) {
+      const float l = lse_part[(bj * num_splits + s) * kHeads + h];
+      if (l == -INFINITY) continue;
+      const float w = expf(l - m);
+      z += w;
+      const float4 v = reinterpret_cast<const float4*>(
+          o_part + ((bj * num_splits + s) * kHeads + h) * kLatent)[threadIdx.x];
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    const float inv = 1.f / z;
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+  }
+  reinterpret_cast<float4*>(o_latent + row * kLatent)[threadIdx.x] = acc;
+  if (lse != nullptr && threadIdx.x == 0) lse[row] = m == -INFINITY ? m : m + logf(z);
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
+                           int num_splits, float* o_latent, float* lse, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(B) * n_q * kHeads;
+  if (rows == 0) return cudaSuccess;
+  combine_kernel<<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(o_part, lse_part, num_splits,
+                                                                      o_latent, lse);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

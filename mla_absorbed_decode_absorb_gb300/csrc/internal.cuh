@@ -1,0 +1,70 @@
+// Internal declarations shared by the CUDA translation units of libmla_decode.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mla_decode.h"
+
+namespace mla {
+
+constexpr int kHeads = MLA_N_HEADS;    // n_h
+constexpr int kNope = MLA_D_NOPE;      // d_h
+constexpr int kLatent = MLA_D_LATENT;  // d_c
+constexpr int kRope = MLA_D_ROPE;      // d_h^R
+constexpr int kRow = MLA_D_ROW;        // d_c + d_h^R
+constexpr int kPage = MLA_PAGE;
+constexpr int kHalfRope = kRope / 2;
+// 1/sqrt(d_h + d_h^R) and that times log2(e): scores are exponentiated with exp2.
+constexpr float kScale = 0.07216878364870323f;         // 1/sqrt(192)
+constexpr float kScaleLog2 = 0.10411754627697264f;     // log2(e)/sqrt(192)
+constexpr float kLn2 = 0.6931471805599453f;
+
+// First fault code wins; later ones are dropped.
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Split-KV layout shared by the attention kernel, the combine and the workspace.
+struct SplitPlan {
+  int max_pages;    // ceil(max_kv_len / 64)
+  int split_pages;  // pages per split
+  int num_splits;   // ceil(max_pages / split_pages)
+  size_t o_part_bytes;
+  size_t lse_part_bytes;
+  size_t workspace_bytes;  // 0 when num_splits == 1
+};
+
+// ---- launchers (each defined in its own .cu; return cudaGetLastError()) ----
+cudaError_t launch_append_kv(const uint16_t* c_kv_new, const uint16_t* k_pe_new,
+                             const int32_t* seq_lens_before, const int32_t* page_table,
+                             int pt_stride, const float* rope_table, int rope_max_pos,
+                             uint16_t* cache, int64_t num_pages, int B, int n_new,
+                             int* status, cudaStream_t stream);
+
+cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
+                            const int32_t* seq_lens_before, const uint16_t* w_uk,
+                            const float* rope_table, int rope_max_pos, uint16_t* q_abs,
+                            int B, int n_q, int* status, cudaStream_t stream);
+
+cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
+                                  int64_t num_pages, const int32_t* page_table, int pt_stride,
+                                  const int32_t* kv_lens, int B, int n_q, int max_kv_len,
+                                  const SplitPlan& plan, float* o_out, float* lse_out,
+                                  int* status, cudaStream_t stream);
+
+cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
+                           int num_splits, float* o_latent, float* lse, cudaStream_t stream);
+
+cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint16_t* out,
+                              int B, int n_q, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,222 @@
+"""Thin Python binding over ``libmla_decode.so`` (the C ABI of include/mla_decode.h).
+
+Argument marshalling only: every function checks dtypes, devices and
+contiguity, passes raw device pointers and the current CUDA stream to the
+C entry point of the same name, and raises :class:`MLAError` on a non-OK
+status.  Outputs not supplied by the caller are allocated with torch (the
+library itself never allocates).  There is no fallback: if the library has
+not been built, importing this module raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .workloads import D_LATENT, D_NOPE, D_ROPE, D_ROW, N_HEADS
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmla_decode.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m mla_absorbed_decode_absorb_gb300.build` "
+        "(or __graft_entry__.build()); there is no non-CUDA fallback")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_p = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+
+_SIGS = {
+    "mla_abi_version": ([], _i),
+    "mla_status_string": ([_i], ctypes.c_char_p),
+    "mla_rope_table_bytes": ([_i], _sz),
+    "mla_rope_table_init": ([_p, _i, _p], _i),
+    "mla_append_kv": ([_p, _p, _p, _p, _i, _p, _i, _p, _i64, _i, _i, _p], _i),
+    "mla_absorb_q": ([_p, _p, _p, _p, _p, _i, _p, _i, _i, _p], _i),
+    "mla_decode_workspace_size": ([_i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
+    "mla_decode_num_splits": ([_i, _i, _i, _i, ctypes.POINTER(_i)], _i),
+    "mla_decode_attn": ([_p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
+    "mla_decode_attn_partial": ([_p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
+    "mla_decode_combine": ([_i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
+    "mla_out_absorb": ([_p, _p, _p, _i, _i, _p], _i),
+    "mla_get_device_status": ([_p], _i),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, \
+    MLA_ERR_BOUNDS = range(7)
+
+
+class MLAError(RuntimeError):
+    def __init__(self, where: str, status: int):
+        super().__init__(f"{where}: {mla_status_string(status)}")
+        self.status = status
+
+
+def mla_status_string(status: int) -> str:
+    return lib.mla_status_string(int(status)).decode()
+
+
+def _check(where: str, status: int) -> None:
+    if status != MLA_OK:
+        raise MLAError(where, status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype, shape=None) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr()
+
+
+def mla_abi_version() -> int:
+    return lib.mla_abi_version()
+
+
+def rope_table(max_positions: int, device=None, stream=None) -> torch.Tensor:
+    """[max_positions, 64] float32: cos then sin of the 32 RoPE frequencies (mla_rope_table_init)."""
+    t = torch.empty(max_positions, D_ROPE, dtype=torch.float32, device=device or "cuda")
+    _check("mla_rope_table_init", lib.mla_rope_table_init(t.data_ptr(), int(max_positions), _stream(stream)))
+    return t
+
+
+def mla_append_kv(c_kv_new, k_pe_new, seq_lens_before, page_table, rope, cache, stream=None):
+    B, n_new = c_kv_new.shape[:2]
+    args = (
+        _dev(c_kv_new, "c_kv_new", torch.bfloat16, (B, n_new, D_LATENT)),
+        _dev(k_pe_new, "k_pe_new", torch.bfloat16, (B, n_new, D_ROPE)),
+        _dev(seq_lens_before, "seq_lens_before", torch.int32, (B,)),
+        _dev(page_table, "page_table", torch.int32),
+        int(page_table.shape[1]),
+        _dev(rope, "rope_table", torch.float32),
+        int(rope.shape[0]),
+        _dev(cache, "cache", torch.bfloat16),
+        int(cache.shape[0]),
+        int(B), int(n_new), _stream(stream))
+    if page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages]")
+    if tuple(cache.shape[1:]) != (64, D_ROW):
+        raise ValueError("cache must be [num_pages, 64, 576]")
+    _check("mla_append_kv", lib.mla_append_kv(*args))
+    return cache
+
+
+def mla_absorb_q(q_nope, q_rope, seq_lens_before, w_uk, rope, q_abs=None, stream=None):
+    B, n_q = q_nope.shape[:2]
+    if q_abs is None:
+        q_abs = torch.empty(B, n_q, N_HEADS, D_ROW, dtype=torch.bfloat16, device=q_nope.device)
+    _check("mla_absorb_q", lib.mla_absorb_q(
+        _dev(q_nope, "q_nope", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        _dev(q_rope, "q_rope", torch.bfloat16, (B, n_q, N_HEADS, D_ROPE)),
+        _dev(seq_lens_before, "seq_lens_before", torch.int32, (B,)),
+        _dev(w_uk, "w_uk", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
+        _dev(rope, "rope_table", torch.float32), int(rope.shape[0]),
+        _dev(q_abs, "q_abs", torch.bfloat16, (B, n_q, N_HEADS, D_ROW)),
+        int(B), int(n_q), _stream(stream)))
+    return q_abs
+
+
+def mla_decode_workspace_size(B: int, n_q: int, max_kv_len: int, split_pages: int = 0) -> int:
+    out = _sz(0)
+    _check("mla_decode_workspace_size",
+           lib.mla_decode_workspace_size(int(B), int(n_q), int(max_kv_len), int(split_pages), ctypes.byref(out)))
+    return int(out.value)
+
+
+def mla_decode_num_splits(B: int, n_q: int, max_kv_len: int, split_pages: int = 0) -> int:
+    out = _i(0)
+    _check("mla_decode_num_splits",
+           lib.mla_decode_num_splits(int(B), int(n_q), int(max_kv_len), int(split_pages), ctypes.byref(out)))
+    return int(out.value)
+
+
+def alloc_workspace(B, n_q, max_kv_len, split_pages=0, device=None):
+    n = mla_decode_workspace_size(B, n_q, max_kv_len, split_pages)
+    return torch.empty(max(n, 16), dtype=torch.uint8, device=device or "cuda")
+
+
+def _decode_args(q_abs, cache, page_table, kv_lens, n_q, max_kv_len, split_pages, workspace, o_latent,
+                 lse, stream):
+    B = kv_lens.shape[0]
+    return (
+        _dev(q_abs, "q_abs", torch.bfloat16, (B, n_q, N_HEADS, D_ROW)),
+        _dev(cache, "cache", torch.bfloat16), int(cache.shape[0]),
+        _dev(page_table, "page_table", torch.int32), int(page_table.shape[1]),
+        _dev(kv_lens, "kv_lens", torch.int32, (B,)),
+        int(B), int(n_q), int(max_kv_len), int(split_pages),
+        0 if workspace is None else _dev(workspace, "workspace", torch.uint8),
+        0 if workspace is None else workspace.numel(),
+        _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
+        0 if lse is None else _dev(lse, "lse", torch.float32, (B, n_q, N_HEADS)),
+        _stream(stream))
+
+
+def mla_decode_attn(q_abs, cache, page_table, kv_lens, n_q, max_kv_len, split_pages=0, workspace=None,
+                    o_latent=None, lse=None, stream=None, want_lse=True):
+    """Split attention plus combine; returns (o_latent [B,n_q,128,512] f32, lse [B,n_q,128] f32 or None)."""
+    B = kv_lens.shape[0]
+    if o_latent is None:
+        o_latent = torch.empty(B, n_q, N_HEADS, D_LATENT, dtype=torch.float32, device=q_abs.device)
+    if lse is None and want_lse:
+        lse = torch.empty(B, n_q, N_HEADS, dtype=torch.float32, device=q_abs.device)
+    if workspace is None:
+        workspace = alloc_workspace(B, n_q, max_kv_len, split_pages, q_abs.device)
+    _check("mla_decode_attn", lib.mla_decode_attn(*_decode_args(
+        q_abs, cache, page_table, kv_lens, n_q, max_kv_len, split_pages, workspace, o_latent, lse, stream)))
+    return o_latent, lse
+
+
+def mla_decode_attn_partial(q_abs, cache, page_table, kv_lens, n_q, max_kv_len, split_pages, workspace,
+                            o_latent, lse=None, stream=None):
+    _check("mla_decode_attn_partial", lib.mla_decode_attn_partial(*_decode_args(
+        q_abs, cache, page_table, kv_lens, n_q, max_kv_len, split_pages, workspace, o_latent, lse, stream)))
+
+
+def mla_decode_combine(B, n_q, max_kv_len, split_pages, workspace, o_latent, lse=None, stream=None):
+    _check("mla_decode_combine", lib.mla_decode_combine(
+        int(B), int(n_q), int(max_kv_len), int(split_pages),
+        0 if workspace is None else _dev(workspace, "workspace", torch.uint8),
+        0 if workspace is None else workspace.numel(),
+        _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
+        0 if lse is None else _dev(lse, "lse", torch.float32, (B, n_q, N_HEADS)),
+        _stream(stream)))
+
+
+def mla_out_absorb(o_latent, w_uv, out=None, stream=None):
+    B, n_q = o_latent.shape[:2]
+    if out is None:
+        out = torch.empty(B, n_q, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=o_latent.device)
+    _check("mla_out_absorb", lib.mla_out_absorb(
+        _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
+        _dev(w_uv, "w_uv", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
+        _dev(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        int(B), int(n_q), _stream(stream)))
+    return out
+
+
+def mla_get_device_status(stream=None) -> int:
+    return int(lib.mla_get_device_status(_stream(stream)))

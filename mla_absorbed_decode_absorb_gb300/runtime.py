@@ -1,0 +1,87 @@
+"""Device-resident decode state for one workload, and one decode step over it.
+
+A :class:`DecodeSession` owns (as torch tensors) the weights, the paged cache
+with each sequence's history already appended, the page table, the RoPE table,
+the step's inputs and every output/workspace buffer, so that a step is just the
+four ABI calls with no allocation:
+
+1. ``mla_append_kv``   -- write this step's n_q tokens into the cache;
+2. ``mla_absorb_q``    -- ``q_abs = [q^C W_UK ; RoPE(q^R)]``;
+3. ``mla_decode_attn`` -- split attention (+ log-sum-exp combine);
+4. ``mla_out_absorb``  -- ``O = O' W_UV^T``.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import ops
+from .workloads import D_LATENT, D_NOPE, D_ROW, N_HEADS, Inputs, empty_cache
+
+
+class DecodeSession:
+    def __init__(self, inp: Inputs, device="cuda", split_pages: int | None = None, stream=None):
+        self.inp = inp
+        self.device = torch.device(device)
+        wl = inp.workload
+        self.B, self.n_q = wl.batch, wl.n_q
+        self.split_pages = wl.split_pages if split_pages is None else int(split_pages)
+        dev = self.device
+        self.max_kv_len = int(inp.kv_lens.max()) if self.B else self.n_q
+        self.rope = ops.rope_table(self.max_kv_len + 1, dev, stream)
+        self.w_uk = inp.w_uk.to(dev)
+        self.w_uv = inp.w_uv.to(dev)
+        self.page_table = inp.page_table.to(dev)
+        self.prior_lens = inp.prior_lens.to(dev)
+        self.kv_lens = inp.kv_lens.to(dev)
+        self.cache = empty_cache(inp.num_pages, dev)
+        zero = torch.zeros(1, dtype=torch.int32, device=dev)
+        for b in range(self.B):
+            hc, hk = inp.history(b)
+            if hc.shape[0] == 0:
+                continue
+            ops.mla_append_kv(hc.to(dev)[None], hk.to(dev)[None], zero, self.page_table[b:b + 1], self.rope,
+                              self.cache, stream=stream)
+        c_new, k_new = inp.new_tokens()
+        self.c_new = c_new.to(dev).contiguous()
+        self.k_new = k_new.to(dev).contiguous()
+        self.q_nope = inp.q_nope.to(dev)
+        self.q_rope = inp.q_rope.to(dev)
+        self.q_abs = torch.empty(self.B, self.n_q, N_HEADS, D_ROW, dtype=torch.bfloat16, device=dev)
+        self.o_latent = torch.empty(self.B, self.n_q, N_HEADS, D_LATENT, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(self.B, self.n_q, N_HEADS, dtype=torch.float32, device=dev)
+        self.out = torch.empty(self.B, self.n_q, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=dev)
+        self.workspace = ops.alloc_workspace(self.B, self.n_q, self.max_kv_len, self.split_pages, dev)
+        self.num_splits = ops.mla_decode_num_splits(self.B, self.n_q, self.max_kv_len, self.split_pages)
+
+    # individual stages (the bench times them one by one)
+    def append(self, stream=None):
+        ops.mla_append_kv(self.c_new, self.k_new, self.prior_lens, self.page_table, self.rope, self.cache,
+                          stream=stream)
+
+    def absorb(self, stream=None):
+        ops.mla_absorb_q(self.q_nope, self.q_rope, self.prior_lens, self.w_uk, self.rope, self.q_abs,
+                         stream=stream)
+
+    def attend_partial(self, stream=None):
+        ops.mla_decode_attn_partial(self.q_abs, self.cache, self.page_table, self.kv_lens, self.n_q,
+                                    self.max_kv_len, self.split_pages, self.workspace, self.o_latent,
+                                    self.lse, stream=stream)
+
+    def combine(self, stream=None):
+        ops.mla_decode_combine(self.B, self.n_q, self.max_kv_len, self.split_pages, self.workspace,
+                               self.o_latent, self.lse, stream=stream)
+
+    def project_out(self, stream=None):
+        ops.mla_out_absorb(self.o_latent, self.w_uv, self.out, stream=stream)
+
+    def step(self, stream=None):
+        self.append(stream)
+        self.absorb(stream)
+        self.attend_partial(stream)
+        self.combine(stream)
+        self.project_out(stream)
+        return self.out
+
+    def launches_per_step(self) -> int:
+        return 4 + (1 if self.num_splits > 1 else 0)

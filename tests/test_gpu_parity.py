@@ -1,0 +1,191 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, element by element.
+
+Tolerances: the append's cache image must match bit for bit; the final output O
+must match the fp64 oracle within max-abs 1e-2 and relative L2 5e-3 (bf16
+operands, fp32 accumulation).  O' and the log-sum-exp are checked too.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mla_oracle as O
+from mla_absorbed_decode_absorb_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_MAX_ABS, O_REL_L2 = 1e-2, 5e-3       # final output O
+LAT_REL_L2 = 5e-3                      # latent output O'
+LSE_MAX_ABS = 2e-2                     # natural-log units
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def rel_l2(a, b):
+    a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+
+
+def oracle_cache_image(inp: W.Inputs) -> np.ndarray:
+    """The oracle's own append of every sequence's history, then of this step's tokens."""
+    img = np.full((inp.num_pages, 64, 576), W.CACHE_SENTINEL_BITS, dtype=np.uint16)
+    pt = inp.page_table.numpy()
+    for b in range(inp.batch):
+        hc, hk = inp.history(b)
+        if hc.shape[0]:
+            img = O.append_kv(img, bits(hc)[None], bits(hk)[None], [0], pt[b:b + 1])
+    c_new, k_new = inp.new_tokens()
+    return O.append_kv(img, bits(c_new), bits(k_new), inp.prior_lens.numpy(), pt)
+
+
+def oracle_sequence(inp: W.Inputs, b: int, heads=None):
+    """Oracle outputs for sequence b from the cache rows the oracle's append writes."""
+    c_bits, k_bits = (bits(x) for x in inp.sequence(b))
+    kv = c_bits.shape[0]
+    c = O.bf16_bits_to_f64(c_bits)
+    kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(kv)))
+    q_nope = O.bf16_bits_to_f64(bits(inp.q_nope[b]))
+    q_rope = O.bf16_bits_to_f64(bits(inp.q_rope[b]))
+    w_uk = O.bf16_bits_to_f64(bits(inp.w_uk))
+    w_uv = O.bf16_bits_to_f64(bits(inp.w_uv))
+    return O.decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, int(inp.prior_lens[b]), heads)
+
+
+def run_session(inp, split_pages=None):
+    from mla_absorbed_decode_absorb_gb300 import ops
+    from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
+    s = DecodeSession(inp, split_pages=split_pages)
+    s.step()
+    torch.cuda.synchronize()
+    assert ops.mla_get_device_status() == ops.MLA_OK
+    return s
+
+
+def check_outputs(s, inp, seqs, heads=None):
+    o_gpu = s.out.float().cpu().numpy()
+    lat_gpu = s.o_latent.cpu().numpy()
+    lse_gpu = s.lse.cpu().numpy()
+    hsel = slice(None) if heads is None else list(heads)
+    o_all, o_ref_all, lat_all, lat_ref_all = [], [], [], []
+    for b in seqs:
+        o_ref, lat_ref, lse_ref = oracle_sequence(inp, b, heads)
+        o, lat, lse = o_gpu[b][:, hsel], lat_gpu[b][:, hsel], lse_gpu[b][:, hsel]
+        assert np.isfinite(o).all() and np.isfinite(lat).all()
+        assert np.abs(lse - lse_ref).max() <= LSE_MAX_ABS, (b, np.abs(lse - lse_ref).max())
+        o_all.append(o), o_ref_all.append(o_ref), lat_all.append(lat), lat_ref_all.append(lat_ref)
+    o, o_ref = np.concatenate(o_all), np.concatenate(o_ref_all)
+    lat, lat_ref = np.concatenate(lat_all), np.concatenate(lat_ref_all)
+    assert np.abs(o - o_ref).max() <= O_MAX_ABS, np.abs(o - o_ref).max()
+    assert rel_l2(o, o_ref) <= O_REL_L2, rel_l2(o, o_ref)
+    assert rel_l2(lat, lat_ref) <= LAT_REL_L2, rel_l2(lat, lat_ref)
+    return rel_l2(o, o_ref), rel_l2(lat, lat_ref)
+
+
+# ------------------------------------------------------------------------ small cases
+SMALL = {
+    # kv_len = L + n_q spans: a single token, one short of a page, exactly a page, one over,
+    # several pages with a ragged tail
+    "edges_q1": W.custom("edges_q1", [0, 62, 63, 64, 127, 300], n_q=1),
+    "mtp_q4": W.custom("mtp_q4", [0, 1, 61, 124, 200], n_q=4),
+    "mtp_q2": W.custom("mtp_q2", [0, 63, 64, 255], n_q=2),
+    "long_tail": W.custom("long_tail", [1500, 1029], n_q=1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_append_bit_exact(name):
+    inp = W.generate(SMALL[name], seed=1)
+    s = run_session(inp)
+    assert np.array_equal(bits(s.cache), oracle_cache_image(inp))
+
+
+def test_absorb_q_parity():
+    inp = W.generate(W.custom("absorb", [5, 70, 4000], n_q=3), seed=2)
+    s = run_session(inp)
+    pos = inp.prior_lens.numpy()[:, None] + np.arange(3)[None, :]
+    ref = O.absorb_query(O.bf16_bits_to_f64(bits(inp.q_nope)), O.bf16_bits_to_f64(bits(inp.q_rope)),
+                         O.bf16_bits_to_f64(bits(inp.w_uk)), pos)
+    got = s.q_abs.float().cpu().numpy()
+    tol = 2.0 ** -8 * np.abs(ref) + 1e-6 * np.abs(ref).max()
+    assert (np.abs(got - ref) <= tol).all(), np.abs(got - ref).max()
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("split_pages", [0, 1, 3])
+def test_decode_parity_small(name, split_pages):
+    inp = W.generate(SMALL[name], seed=3)
+    s = run_session(inp, split_pages=split_pages)
+    check_outputs(s, inp, range(inp.batch))
+
+
+def test_split_count_invariance():
+    inp = W.generate(W.custom("splits", [700, 1000, 64], n_q=2), seed=4)
+    ref = run_session(inp, split_pages=1000)
+    assert ref.num_splits == 1
+    for sp in [1, 2, 5]:
+        s = run_session(inp, split_pages=sp)
+        assert s.num_splits > 1
+        assert rel_l2(s.o_latent.cpu().numpy(), ref.o_latent.cpu().numpy()) < 1e-5
+        assert np.abs(s.lse.cpu().numpy() - ref.lse.cpu().numpy()).max() < 1e-4
+
+
+def test_out_of_range_page_is_reported():
+    from mla_absorbed_decode_absorb_gb300 import ops
+    from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
+    inp = W.generate(W.custom("bad", [100, 100], n_q=1), seed=5)
+    s = DecodeSession(inp)
+    torch.cuda.synchronize()
+    assert ops.mla_get_device_status() == ops.MLA_OK
+    bad = s.page_table.clone()
+    bad[1, 1] = inp.num_pages + 7   # past the pool
+    s.page_table = bad
+    s.step()
+    assert ops.mla_get_device_status() == ops.MLA_ERR_BOUNDS
+    assert ops.mla_get_device_status() == ops.MLA_OK  # read-and-clear
+    s.page_table = inp.page_table.to(s.device)
+    s.step()
+    assert ops.mla_get_device_status() == ops.MLA_OK
+
+
+def test_invalid_arguments_raise():
+    from mla_absorbed_decode_absorb_gb300 import ops
+    x = torch.zeros(1, 1, 512, dtype=torch.float32, device="cuda")
+    with pytest.raises(TypeError):
+        ops.mla_append_kv(x, x, None, None, None, None)
+    q = torch.zeros(1, 9, 128, 128, dtype=torch.bfloat16, device="cuda")
+    r = torch.zeros(1, 9, 128, 64, dtype=torch.bfloat16, device="cuda")
+    lens = torch.zeros(1, dtype=torch.int32, device="cuda")
+    w = torch.zeros(128, 128, 512, dtype=torch.bfloat16, device="cuda")
+    rope = ops.rope_table(16)
+    with pytest.raises(ops.MLAError):
+        ops.mla_absorb_q(q, r, lens, w, rope)   # n_q = 9 > MLA_MAX_NQ
+
+
+# ------------------------------------------------------------------------ full-size workloads
+FULL = ["tiny_b1_l256", "batched_b32_l4096", "ragged_b128_l1024_8192", "long_b8_l32768", "mtp_b64_l8192_q4"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_workload_sampled(name):
+    """The five benchmark workloads at full size, in the bench's launch configuration.
+
+    The oracle checks sampled sequences (first, middle, last) on sampled heads,
+    and the cache rows of those sequences bit for bit.
+    """
+    wl = W.WORKLOADS[name]
+    inp = W.generate(wl, seed=0)
+    s = run_session(inp)
+    seqs = sorted({0, inp.batch // 2, inp.batch - 1})
+    heads = [0, 41, 127] if inp.batch > 1 else None
+    check_outputs(s, inp, seqs, heads)
+    cache = s.cache
+    pt = inp.page_table.numpy()
+    for b in seqs:
+        kv = int(inp.kv_lens[b])
+        rows = bits(cache[torch.as_tensor(pt[b][np.arange(kv) // 64]).long().to(cache.device),
+                          torch.as_tensor(np.arange(kv) % 64).to(cache.device)])
+        c_bits, k_bits = (bits(x) for x in inp.sequence(b))
+        assert np.array_equal(rows[:, :512], c_bits)
+        assert np.array_equal(rows[:, 512:], O.rope_key_bf16_bits(k_bits, np.arange(kv)))
