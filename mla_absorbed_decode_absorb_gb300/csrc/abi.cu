@@ -226,7 +226,9 @@ mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16*
   if (B == 0) return MLA_OK;
   if (!o_latent || !w_uv || !out) return MLA_ERR_INVALID_ARG;
   if (!aligned16(o_latent) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
-  return from_cuda(launch_out_absorb(o_latent, w_uv, out, B, n_q, stream));
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_out_absorb(o_latent, w_uv, out, B, n_q, st, stream));
 }
 
 mla_status mla_get_device_status(cudaStream_t stream) {

@@ -5,72 +5,129 @@
 // "DeepSeek-MLA-Principle" key absorption q~ = (W_UK[h])^T q^C and eq. (8);
 // "DeepSeek MLA 架构详解" step 3 (einsum 'bhd,hdm->bhm').
 //
-// CUDA-core version: one block per (head, chunk of 32 query tokens); the
-// block's query rows sit in shared memory as float32, each thread owns two of
-// the 512 latent columns for all 32 tokens and streams its W_UK[h] column.
-#include "internal.cuh"
+// tcgen05 version, operands swapped so the large side is M: per head h the CTA
+// computes D[m, t] = sum_d W_UK[h][d][m] * q_nope[t][h][d] for 128 latent
+// columns m (M = 128) and up to 256 query tokens t (N).  A = W_UK[h] is
+// MN-major (m contiguous), B = q_nope rows are K-major (d contiguous); both are
+// staged into shared memory in the 128-byte-swizzled canonical layouts, one MMA
+// chain of 8 x (K = 16) accumulates into TMEM, and four warps read their 32
+// TMEM lanes back (lane = m, column = token) and store bf16.
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kTokTile = 32;
-constexpr int kThreads = 256;
+using namespace sm100;
+
+constexpr int kMTile = 128;   // latent columns per CTA
+constexpr int kNMax = 256;    // query tokens per CTA
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kAChunk = 128 * 128;          // bytes of one 64-column MN chunk: 128 d rows x 128 B
+constexpr int kSmemA = 2 * kAChunk;         // 32 KB
+constexpr int kSmemB = 2 * kNMax * 128;     // two 64-wide K chunks of up to 256 rows: 64 KB
+constexpr int kSmemBytes = kSmemA + kSmemB + 1024 /*align*/ + 64;
 
 __global__ void __launch_bounds__(kThreads)
-absorb_q_simt_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restrict__ q_rope,
-                     const int32_t* __restrict__ lens, const uint16_t* __restrict__ w_uk,
-                     const float* __restrict__ rope, int rope_max_pos,
-                     uint16_t* __restrict__ q_abs, int T, int n_q, int* status) {
-  __shared__ float qs[kTokTile][kNope];
-  const int h = blockIdx.x;
-  const int t0 = blockIdx.y * kTokTile;
-  const int nt = min(kTokTile, T - t0);
-  for (int i = threadIdx.x; i < kTokTile * kNope; i += kThreads) {
-    const int t = i / kNope, d = i % kNope;
-    qs[t][d] = t < nt ? bf16_bits_to_f32(q_nope[(static_cast<int64_t>(t0 + t) * kHeads + h) * kNope + d]) : 0.f;
+absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restrict__ q_rope,
+                   const int32_t* __restrict__ lens, const uint16_t* __restrict__ w_uk,
+                   const float* __restrict__ rope, int rope_max_pos, uint16_t* __restrict__ q_abs,
+                   int T, int n_q, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kSmemA;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + kSmemB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int m0 = blockIdx.x * kMTile;
+  const int h = blockIdx.y;
+  const int t0 = blockIdx.z * kNMax;
+  const int nt = min(kNMax, T - t0);
+  const int npad = (nt + 15) & ~15;
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
   }
+  if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    fence_mbar_init();
+  }
+
+  // A: W_UK[h][d][m0 .. m0+128) -> two MN-major chunks of 64 columns, rows d.
+  const uint4* wsrc = reinterpret_cast<const uint4*>(w_uk + (static_cast<int64_t>(h) * kNope) * kLatent + m0);
+  for (int v = tid; v < kNope * 16; v += kThreads) {
+    const int d = v >> 4, u = v & 15, c = u >> 3;
+    const uint4 x = wsrc[d * (kLatent / 8) + u];
+    *reinterpret_cast<uint4*>(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)) = x;
+  }
+  // B: q_nope[t0 + t][h][0 .. 128) -> two K-major chunks of 64, rows t (zero past nt).
+  for (int v = tid; v < npad * 16; v += kThreads) {
+    const int t = v >> 4, u = v & 15, c = u >> 3;
+    uint4 x = make_uint4(0, 0, 0, 0);
+    if (t < nt) x = reinterpret_cast<const uint4*>(q_nope + (static_cast<int64_t>(t0 + t) * kHeads + h) * kNope)[u];
+    *reinterpret_cast<uint4*>(sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16)) = x;
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  const int m0 = threadIdx.x, m1 = threadIdx.x + kThreads;
-  float acc0[kTokTile], acc1[kTokTile];
+  if (tid == 0) {
+    const uint32_t idesc = idesc_bf16(128, npad, /*a_mn=*/1, /*b_mn=*/0);
+    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
-  for (int t = 0; t < kTokTile; ++t) acc0[t] = acc1[t] = 0.f;
-  const uint16_t* w = w_uk + static_cast<int64_t>(h) * kNope * kLatent;
-  for (int d = 0; d < kNope; ++d) {
-    const float w0 = bf16_bits_to_f32(w[d * kLatent + m0]);
-    const float w1 = bf16_bits_to_f32(w[d * kLatent + m1]);
-#pragma unroll
-    for (int t = 0; t < kTokTile; ++t) {
-      acc0[t] = fmaf(qs[t][d], w0, acc0[t]);
-      acc1[t] = fmaf(qs[t][d], w1, acc1[t]);
+    for (int k = 0; k < kNope / 16; ++k) {
+      const uint64_t ad = smem_desc(a0 + k * 16 * 128, kAChunk, 1024, kSw128);
+      const uint64_t bd = smem_desc(b0 + (k >> 2) * npad * 128 + (k & 3) * 32, 16, 1024, kSw128);
+      mma_ss(tmem, ad, bd, idesc, k > 0);
     }
+    mma_commit(smem_u32(bar));
   }
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), 0, status));
+  tc_fence_after();
+
+  if (ok) {
+    const int m = m0 + warp * 32 + lane;
+    const uint32_t row_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int c0 = 0; c0 < npad; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(row_addr + c0, r);
+      tmem_wait_ld();
 #pragma unroll
-  for (int t = 0; t < kTokTile; ++t) {
-    if (t < nt) {
-      uint16_t* row = q_abs + (static_cast<int64_t>(t0 + t) * kHeads + h) * kRow;
-      row[m0] = f32_to_bf16_bits(acc0[t]);
-      row[m1] = f32_to_bf16_bits(acc1[t]);
+      for (int i = 0; i < 16; ++i) {
+        const int t = c0 + i;
+        if (t < nt) q_abs[(static_cast<int64_t>(t0 + t) * kHeads + h) * kRow + m] = f32_to_bf16_bits(__uint_as_float(r[i]));
+      }
     }
   }
 
-  // RoPE of the query's position branch, one (token, frequency) pair per thread.
-  for (int i = threadIdx.x; i < nt * kHalfRope; i += kThreads) {
-    const int t = t0 + i / kHalfRope, f = i % kHalfRope;
-    const int b = t / n_q, j = t % n_q;
-    const int64_t pos = static_cast<int64_t>(lens[b]) + j;
-    uint16_t* row = q_abs + (static_cast<int64_t>(t) * kHeads + h) * kRow + kLatent;
-    if (pos < 0 || pos >= rope_max_pos) {
-      record_status(status, MLA_ERR_BOUNDS);
-      row[f] = row[f + kHalfRope] = 0;
-      continue;
+  // RoPE of the query's position branch (done by the first M tile of each head).
+  if (blockIdx.x == 0) {
+    for (int i = tid; i < nt * kHalfRope; i += kThreads) {
+      const int t = t0 + i / kHalfRope, f = i % kHalfRope;
+      const int b = t / n_q, j = t % n_q;
+      const int64_t pos = static_cast<int64_t>(lens[b]) + j;
+      uint16_t* row = q_abs + (static_cast<int64_t>(t) * kHeads + h) * kRow + kLatent;
+      if (pos < 0 || pos >= rope_max_pos) {
+        record_status(status, MLA_ERR_BOUNDS);
+        row[f] = row[f + kHalfRope] = 0;
+        continue;
+      }
+      const uint16_t* x = q_rope + (static_cast<int64_t>(t) * kHeads + h) * kRope;
+      const float x1 = bf16_bits_to_f32(x[f]), x2 = bf16_bits_to_f32(x[f + kHalfRope]);
+      const float c = rope[pos * kRope + f], s = rope[pos * kRope + kHalfRope + f];
+      row[f] = f32_to_bf16_bits(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
+      row[f + kHalfRope] = f32_to_bf16_bits(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
     }
-    const uint16_t* x = q_rope + (static_cast<int64_t>(t) * kHeads + h) * kRope;
-    const float x1 = bf16_bits_to_f32(x[f]), x2 = bf16_bits_to_f32(x[f + kHalfRope]);
-    const float c = rope[pos * kRope + f], s = rope[pos * kRope + kHalfRope + f];
-    row[f] = f32_to_bf16_bits(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
-    row[f + kHalfRope] = f32_to_bf16_bits(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
   }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -81,9 +138,15 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
                             int B, int n_q, int* status, cudaStream_t stream) {
   const int T = B * n_q;
   if (T == 0) return cudaSuccess;
-  dim3 grid(kHeads, (T + kTokTile - 1) / kTokTile);
-  absorb_q_simt_kernel<<<grid, kThreads, 0, stream>>>(q_nope, q_rope, seq_lens_before, w_uk,
-                                                      rope_table, rope_max_pos, q_abs, T, n_q, status);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(absorb_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(kLatent / kMTile, kHeads, (T + kNMax - 1) / kNMax);
+  absorb_q_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_nope, q_rope, seq_lens_before, w_uk, rope_table,
+                                                             rope_max_pos, q_abs, T, n_q, status);
   return cudaGetLastError();
 }
 

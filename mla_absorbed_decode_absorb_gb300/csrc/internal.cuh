@@ -65,6 +65,6 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, in
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream);
 
 cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint16_t* out,
-                              int B, int n_q, cudaStream_t stream);
+                              int B, int n_q, int* status, cudaStream_t stream);
 
 }  // namespace mla

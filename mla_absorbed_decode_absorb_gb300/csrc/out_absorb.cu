@@ -4,57 +4,128 @@
 // of the history length); "DeepSeek-MLA-Principle" value absorption
 // o = W_UV[h] m; "DeepSeek MLA 架构详解" step 5 (einsum 'bhm,hdm->bhd').
 //
-// CUDA-core version: one block per (head, chunk of 16 query tokens).  O' is
-// rounded to bf16 on the way into shared memory (the documented operand
-// precision); each warp walks W_UV[h] rows with lanes along the latent axis and
-// reduces across the warp.
-#include "internal.cuh"
+// tcgen05 version, operands swapped so the large side is M: per head h the CTA
+// computes D[d, t] = sum_m W_UV[h][d][m] * O'[t][h][m] with the 128 output
+// dimensions d as M and up to 256 query tokens as N.  Both operands are
+// K-major (m contiguous).  The 512-long K axis is staged in four 128-wide
+// steps; O' is rounded from float32 to bf16 as it is staged.
+#include "sm100.cuh"
 
 namespace mla {
 namespace {
 
-constexpr int kTokTile = 16;
-constexpr int kThreads = 256;
+using namespace sm100;
+
+constexpr int kNMax = 256;
+constexpr int kThreads = 128;
+constexpr uint32_t kTmemCols = 256;
+constexpr int kKStep = 128;                       // latent columns per stage
+constexpr int kAChunk = 128 * 128;                // 128 d rows x 64 m (128 B)
+constexpr int kSmemA = 2 * kAChunk;               // 32 KB
+constexpr int kSmemB = 2 * kNMax * 128;           // 64 KB
+constexpr int kSmemBytes = kSmemA + kSmemB + 1024 + 64;
 
 __global__ void __launch_bounds__(kThreads)
-out_absorb_simt_kernel(const float* __restrict__ o_lat, const uint16_t* __restrict__ w_uv,
-                       uint16_t* __restrict__ out, int T) {
-  __shared__ float os[kTokTile][kLatent];
+out_absorb_tc_kernel(const float* __restrict__ o_lat, const uint16_t* __restrict__ w_uv,
+                     uint16_t* __restrict__ out, int T, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kSmemA;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + kSmemB);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.x;
-  const int t0 = blockIdx.y * kTokTile;
-  const int nt = min(kTokTile, T - t0);
-  for (int i = threadIdx.x; i < kTokTile * kLatent; i += kThreads) {
-    const int t = i / kLatent, m = i % kLatent;
-    float v = 0.f;
-    if (t < nt) v = bf16_bits_to_f32(f32_to_bf16_bits(o_lat[(static_cast<int64_t>(t0 + t) * kHeads + h) * kLatent + m]));
-    os[t][m] = v;
+  const int t0 = blockIdx.y * kNMax;
+  const int nt = min(kNMax, T - t0);
+  const int npad = (nt + 15) & ~15;
+
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
   }
+  if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t idesc = idesc_bf16(128, npad, /*a_mn=*/0, /*b_mn=*/0);
   const uint16_t* wh = w_uv + static_cast<int64_t>(h) * kNope * kLatent;
-  for (int d = warp; d < kNope; d += kThreads / 32) {
-    float w[16];
+  bool ok = true;
+
+  for (int step = 0; step < kLatent / kKStep && ok; ++step) {
+    const int mk = step * kKStep;
+    // A: W_UV[h][d][mk .. mk+128): rows d, two K-major chunks of 64.
+    for (int v = tid; v < kNope * 16; v += kThreads) {
+      const int d = v >> 4, u = v & 15, c = u >> 3;
+      const uint4 x = reinterpret_cast<const uint4*>(wh + d * kLatent + mk)[u];
+      *reinterpret_cast<uint4*>(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)) = x;
+    }
+    // B: O'[t0+t][h][mk .. mk+128) rounded to bf16: rows t, two K-major chunks of 64.
+    for (int v = tid; v < npad * 16; v += kThreads) {
+      const int t = v >> 4, u = v & 15, c = u >> 3;
+      uint4 x = make_uint4(0, 0, 0, 0);
+      if (t < nt) {
+        const float4* src = reinterpret_cast<const float4*>(o_lat + (static_cast<int64_t>(t0 + t) * kHeads + h) * kLatent + mk + u * 8);
+        const float4 a = src[0], b = src[1];
+        x = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+      }
+      *reinterpret_cast<uint4*>(sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16)) = x;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
-    for (int k = 0; k < 16; ++k) w[k] = bf16_bits_to_f32(wh[d * kLatent + k * 32 + lane]);
-    for (int t = 0; t < nt; ++t) {
-      float p = 0.f;
+      for (int k = 0; k < kKStep / 16; ++k) {
+        const uint64_t ad = smem_desc(a0 + (k >> 2) * kAChunk + (k & 3) * 32, 16, 1024, kSw128);
+        const uint64_t bd = smem_desc(b0 + (k >> 2) * npad * 128 + (k & 3) * 32, 16, 1024, kSw128);
+        mma_ss(tmem, ad, bd, idesc, (step > 0 || k > 0) ? 1u : 0u);
+      }
+      mma_commit(smem_u32(bar));
+    }
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), step & 1, status));  // stage reusable once the MMAs finished
+    tc_fence_after();
+  }
+
+  if (ok) {
+    const int d = warp * 32 + lane;
+    const uint32_t row_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int c0 = 0; c0 < npad; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(row_addr + c0, r);
+      tmem_wait_ld();
 #pragma unroll
-      for (int k = 0; k < 16; ++k) p = fmaf(w[k], os[t][k * 32 + lane], p);
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-      if (lane == 0) out[(static_cast<int64_t>(t0 + t) * kHeads + h) * kNope + d] = f32_to_bf16_bits(p);
+      for (int i = 0; i < 16; ++i) {
+        const int t = c0 + i;
+        if (t < nt) out[(static_cast<int64_t>(t0 + t) * kHeads + h) * kNope + d] = f32_to_bf16_bits(__uint_as_float(r[i]));
+      }
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
-cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint16_t* out,
-                              int B, int n_q, cudaStream_t stream) {
+cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint16_t* out, int B, int n_q,
+                              int* status, cudaStream_t stream) {
   const int T = B * n_q;
   if (T == 0) return cudaSuccess;
-  dim3 grid(kHeads, (T + kTokTile - 1) / kTokTile);
-  out_absorb_simt_kernel<<<grid, kThreads, 0, stream>>>(o_latent, w_uv, out, T);
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(out_absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  dim3 grid(kHeads, (T + kNMax - 1) / kNMax);
+  out_absorb_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(o_latent, w_uv, out, T, status);
   return cudaGetLastError();
 }
 
