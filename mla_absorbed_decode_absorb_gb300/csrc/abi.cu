@@ -19,7 +19,6 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_mutex;
 int* g_status_ptr[kMaxDevices];
-int g_num_sms[kMaxDevices];
 
 int current_device() {
   int dev = -1;
@@ -40,35 +39,34 @@ int* status_ptr() {
   return g_status_ptr[dev];
 }
 
-int num_sms() {
-  const int dev = current_device();
-  if (dev < 0 || dev >= kMaxDevices) return 148;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_num_sms[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-    g_num_sms[dev] = n;
-  }
-  return g_num_sms[dev];
-}
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Split-KV partition.  Automatic choice: enough (sequence, query, split) units
-// to give every SM about two, without splits shorter than one page.
+// Split-KV partition.  Automatic choice: the split count s per (sequence,
+// query) that minimises waves(s) * (pages per split + 3), where a wave is as
+// many units as attention clusters fit on the GPU at once and 3 pages stand for
+// a unit's fixed cost (query load, pipeline fill, epilogue, partial write).
 bool make_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan) {
   if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ || max_kv_len < n_q || split_pages < 0) return false;
   plan->max_pages = (max_kv_len + kPage - 1) / kPage;
   if (split_pages == 0) {
-    const int units = B * n_q > 0 ? B * n_q : 1;
-    int per_seq = (2 * num_sms() + units - 1) / units;
-    if (per_seq < 1) per_seq = 1;
-    if (per_seq > plan->max_pages) per_seq = plan->max_pages;
-    split_pages = (plan->max_pages + per_seq - 1) / per_seq;
+    const int64_t units = static_cast<int64_t>(B > 0 ? B : 1) * n_q;
+    const int64_t slots = decode_cluster_slots();
+    int64_t best_cost = -1;
+    split_pages = plan->max_pages;
+    for (int s = 1; s <= plan->max_pages && s <= 256; ++s) {
+      const int sp = (plan->max_pages + s - 1) / s;
+      const int s_eff = (plan->max_pages + sp - 1) / sp;
+      const int64_t waves = (units * s_eff + slots - 1) / slots;
+      const int64_t cost = waves * (sp + 3);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        split_pages = sp;
+      }
+    }
   }
   plan->split_pages = split_pages;
   plan->num_splits = (plan->max_pages + split_pages - 1) / split_pages;

@@ -55,6 +55,9 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
                             const float* rope_table, int rope_max_pos, uint16_t* q_abs,
                             int B, int n_q, int* status, cudaStream_t stream);
 
+// Clusters of the attention kernel that fit on the current device at once.
+int decode_cluster_slots();
+
 cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   int64_t num_pages, const int32_t* page_table, int pt_stride,
                                   const int32_t* kv_lens, int B, int n_q, int max_kv_len,

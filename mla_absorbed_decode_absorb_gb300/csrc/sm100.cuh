@@ -10,9 +10,16 @@
 namespace mla {
 namespace sm100 {
 
-// Spin limit of every mbarrier wait.  A wait that runs out records
-// MLA_ERR_TIMEOUT and returns false; callers then stop issuing work.
-constexpr uint32_t kWaitLimit = 1u << 26;
+// Every mbarrier wait is bounded in time: after kWaitNs of polling it records
+// MLA_ERR_TIMEOUT in the device status word and returns false, and the caller
+// stops issuing work.  Nothing in this library spins unboundedly.
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -58,18 +65,30 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "memory");
   return ok != 0;
 }
-// Bounded wait for phase `parity` of `bar` to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  record_status(status, MLA_ERR_TIMEOUT);
-  return false;
+// Bounded wait for phase `parity` of `bar` to complete.  `abort` (optional,
+// shared by the CTA) makes every other waiter give up too once one has timed out.
+template <bool kClusterScope>
+__device__ __forceinline__ bool mbar_wait_impl(uint32_t bar, uint32_t parity, int* status, volatile int* abort) {
+  if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (abort != nullptr && *abort) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) {
+        record_status(status, MLA_ERR_TIMEOUT);
+        if (abort != nullptr) *abort = 1;
+        return false;
+      }
+    }
+  }
 }
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-  record_status(status, MLA_ERR_TIMEOUT);
-  return false;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, volatile int* abort = nullptr) {
+  return mbar_wait_impl<false>(bar, parity, status, abort);
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, int* status,
+                                                  volatile int* abort = nullptr) {
+  return mbar_wait_impl<true>(bar, parity, status, abort);
 }
 
 // Generic-proxy shared-memory writes become visible to the async proxy (TMA, tcgen05.mma).
@@ -216,6 +235,9 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
