@@ -21,10 +21,13 @@
 //   * runs the same online softmax as its peer on that S, so both use identical
 //     P, running max and sum, and accumulates its half of O' = P c.
 // Warp roles: warp 0 issues TMA loads (the query tile once, then a 3-stage ring
-// of half-pages), warp 1 allocates TMEM and issues tcgen05.mma (QK^T into one of
-// two TMEM score buffers while the softmax works on the other; P V with P read
-// from TMEM), warps 2-5 are the softmax/epilogue warpgroup with one thread per
-// head row.  The softmax keeps a lazily updated reference max: O' in TMEM is
+// of half-pages; page ids are prefetched 32 at a time), warp 1 allocates TMEM
+// and issues tcgen05.mma (QK^T into one of two TMEM score buffers; P V with P
+// read from TMEM), warps 6-9 are the exchange warpgroup (per page: read the
+// partial scores, swap them with the peer, write the full scores back into
+// TMEM), warps 2-5 are the softmax/epilogue warpgroup.  Both warpgroups have one
+// thread per head row, and the exchange for page i+1 overlaps the softmax of
+// page i.  The softmax keeps a lazily updated reference max: O' in TMEM is
 // rescaled only when a page raises a row's max by more than 2^8.
 #include "sm100.cuh"
 #include "tmap.cuh"
@@ -35,9 +38,10 @@ namespace {
 using namespace sm100;
 
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
+constexpr int kExchangeWarp0 = 6;
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;    // O' half: [0, 256)
@@ -65,7 +69,8 @@ struct Bars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
   uint64_t q_full;
-  uint64_t s_full[2];
+  uint64_t s_full[2];   // partial scores of this CTA are in TMEM
+  uint64_t s_ready[2];  // full scores are in TMEM
   uint64_t p_full[2];
   uint64_t pv_done;
   uint64_t x_full;
@@ -127,12 +132,13 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     mbar_init(bar_addr(bars.q_full), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_addr(bars.s_full[s]), 1);
+      mbar_init(bar_addr(bars.s_ready[s]), kSoftmaxThreads);
       mbar_init(bar_addr(bars.p_full[s]), kSoftmaxThreads);
     }
     mbar_init(bar_addr(bars.pv_done), 1);
     mbar_init(bar_addr(bars.x_full), 1);
     mbar_init(bar_addr(bars.x_free), 1);
-    mbar_init(bar_addr(bars.x_read), kSoftmaxThreads);
+    mbar_init(bar_addr(bars.x_read), kSoftmaxThreads);  // the 128 exchange threads
     mbar_init(bar_addr(bars.drain), 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -151,31 +157,49 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_pages > 0) {
-      tma_prefetch_desc(&tm_q128);
-      tma_prefetch_desc(&tm_q64);
-      tma_prefetch_desc(&tm_c128);
-      tma_prefetch_desc(&tm_c64);
-      const int q_row = bj * kHeads;
-      const uint32_t qb = smem_u32(smem + kOffQ);
-      mbar_arrive_expect_tx(bar_addr(bars.q_full), kQBytes);
-      for (int c = 0; c < 4; ++c)
-        tma_load_2d(qb + c * kQChunk, &tm_q128, 64 * (4 * rank + c), q_row, bar_addr(bars.q_full));
-      tma_load_2d(qb + 4 * kQChunk, &tm_q64, kLatent + 32 * rank, q_row, bar_addr(bars.q_full));
+    if (n_pages > 0) {
       const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride + page_begin;
-      for (int i = 0; i < n_pages; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort)) break;
-        int page = pt[i];
-        if (page < 0 || page >= p.num_pages) {
-          record_status(p.status, MLA_ERR_BOUNDS);
-          page = 0;  // stay in bounds; the result of this unit is not meaningful
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_q128);
+        tma_prefetch_desc(&tm_q64);
+        tma_prefetch_desc(&tm_c128);
+        tma_prefetch_desc(&tm_c64);
+        const int q_row = bj * kHeads;
+        const uint32_t qb = smem_u32(smem + kOffQ);
+        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQBytes);
+        for (int c = 0; c < 4; ++c)
+          tma_load_2d(qb + c * kQChunk, &tm_q128, 64 * (4 * rank + c), q_row, bar_addr(bars.q_full));
+        tma_load_2d(qb + 4 * kQChunk, &tm_q64, kLatent + 32 * rank, q_row, bar_addr(bars.q_full));
+      }
+      // page ids, 32 per coalesced load, one chunk ahead
+      int ids = lane < n_pages ? pt[lane] : 0;
+      bool ok = true;
+      for (int base = 0; base < n_pages && ok; base += 32) {
+        const int next_i = base + 32 + lane;
+        const int ids_next = next_i < n_pages ? pt[next_i] : 0;
+        const int cnt = min(32, n_pages - base);
+        for (int k = 0; k < cnt && ok; ++k) {
+          const int i = base + k;
+          int page = __shfl_sync(0xffffffffu, ids, k);
+          if (lane == 0) {
+            const int s = i % kStages;
+            ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
+            if (ok) {
+              if (page < 0 || page >= p.num_pages) {
+                record_status(p.status, MLA_ERR_BOUNDS);
+                page = 0;  // stay in bounds; the result of this unit is not meaningful
+              }
+              const uint32_t sb = smem_u32(smem + kOffStage + s * kStageBytes);
+              const uint32_t fb = bar_addr(bars.full[s]);
+              mbar_arrive_expect_tx(fb, kStageBytes);
+              for (int c = 0; c < 4; ++c)
+                tma_load_2d(sb + c * kPChunk, &tm_c128, 64 * (4 * rank + c), page * kPage, fb);
+              tma_load_2d(sb + 4 * kPChunk, &tm_c64, kLatent + 32 * rank, page * kPage, fb);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
         }
-        const uint32_t sb = smem_u32(smem + kOffStage + s * kStageBytes);
-        const uint32_t fb = bar_addr(bars.full[s]);
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        for (int c = 0; c < 4; ++c) tma_load_2d(sb + c * kPChunk, &tm_c128, 64 * (4 * rank + c), page * kPage, fb);
-        tma_load_2d(sb + 4 * kPChunk, &tm_c64, kLatent + 32 * rank, page * kPage, fb);
+        ids = ids_next;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -246,6 +270,70 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
       __syncwarp();
       mbar_wait(bar_addr(bars.drain), 0, p.status, nullptr);
     }
+  } else if (warp >= kExchangeWarp0) {
+    // ------------------------------------------------------------ score exchange
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // head
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    float* xrow = reinterpret_cast<float*>(smem + kOffX) + row * kXStride;
+    const uint32_t x_remote = mapa(smem_u32(xrow), peer);
+    const uint32_t xfull_remote = mapa(bar_addr(bars.x_full), peer);
+    const uint32_t xfree_remote = mapa(bar_addr(bars.x_free), peer);
+    bool ok = true;
+    for (int i = 0; i < n_pages && ok; ++i) {
+      const int buf = i & 1;
+      const uint32_t s_addr = tmem + lane_off + kTmemS + buf * 64;
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[buf]), (i >> 1) & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv0[32], sv1[32];
+      tmem_ld32(s_addr, sv0);
+      tmem_ld32(s_addr + 32, sv1);
+      tmem_wait_ld();
+      // send this CTA's partial scores to the peer
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free), (i & 1) ^ 1, p.status, abort));
+      if (!ok) break;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        st_async_v4(x_remote + 16 * q, sv0[4 * q], sv0[4 * q + 1], sv0[4 * q + 2], sv0[4 * q + 3], xfull_remote);
+        st_async_v4(x_remote + 128 + 16 * q, sv1[4 * q], sv1[4 * q + 1], sv1[4 * q + 2], sv1[4 * q + 3],
+                    xfull_remote);
+      }
+      // receive the peer's partial scores and add them
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full), i & 1, p.status, abort));
+      if (!ok) break;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = reinterpret_cast<const float4*>(xrow)[q];
+        const float4 y = reinterpret_cast<const float4*>(xrow)[q + 8];
+        sv0[4 * q + 0] = __float_as_uint(__uint_as_float(sv0[4 * q + 0]) + x.x);
+        sv0[4 * q + 1] = __float_as_uint(__uint_as_float(sv0[4 * q + 1]) + x.y);
+        sv0[4 * q + 2] = __float_as_uint(__uint_as_float(sv0[4 * q + 2]) + x.z);
+        sv0[4 * q + 3] = __float_as_uint(__uint_as_float(sv0[4 * q + 3]) + x.w);
+        sv1[4 * q + 0] = __float_as_uint(__uint_as_float(sv1[4 * q + 0]) + y.x);
+        sv1[4 * q + 1] = __float_as_uint(__uint_as_float(sv1[4 * q + 1]) + y.y);
+        sv1[4 * q + 2] = __float_as_uint(__uint_as_float(sv1[4 * q + 2]) + y.z);
+        sv1[4 * q + 3] = __float_as_uint(__uint_as_float(sv1[4 * q + 3]) + y.w);
+      }
+      // once every row has read the exchange buffer, one thread re-arms it and
+      // tells the peer it may send the next page's partial scores
+      mbar_arrive(bar_addr(bars.x_read));
+      if (row == 0) {
+        ok = mbar_wait(bar_addr(bars.x_read), i & 1, p.status, abort);
+        if (ok) {
+          mbar_arrive_expect_tx(bar_addr(bars.x_full), kXTxBytes);
+          mbar_arrive_remote(xfree_remote);
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // full scores back into the same TMEM buffer for the softmax warpgroup
+      tmem_st32(s_addr, sv0);
+      tmem_st32(s_addr + 32, sv1);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(bars.s_ready[buf]));
+    }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int quad = warp & 3;
@@ -257,75 +345,47 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     bool ok = n_pages > 0;
 
     if (ok) {
-      float* xrow = reinterpret_cast<float*>(smem + kOffX) + row * kXStride;
-      const uint32_t x_remote = mapa(smem_u32(xrow), peer);
-      const uint32_t xfull_remote = mapa(bar_addr(bars.x_full), peer);
-      const uint32_t xfree_remote = mapa(bar_addr(bars.x_free), peer);
       for (int i = 0; i < n_pages && ok; ++i) {
         const int buf = i & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[buf]), (i >> 1) & 1, p.status, abort));
+        const uint32_t s_addr = tmem + lane_off + kTmemS + buf * 64;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_ready[buf]), (i >> 1) & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after();
-        uint32_t sv0[32], sv1[32];
-        tmem_ld32(tmem + lane_off + kTmemS + buf * 64, sv0);
-        tmem_ld32(tmem + lane_off + kTmemS + buf * 64 + 32, sv1);
+        uint32_t sv[64];
+        tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_wait_ld();
-        // send this CTA's partial scores to the peer
-        ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free), (i & 1) ^ 1, p.status, abort));
-        if (!ok) break;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          st_async_v4(x_remote + 16 * q, sv0[4 * q], sv0[4 * q + 1], sv0[4 * q + 2], sv0[4 * q + 3], xfull_remote);
-          st_async_v4(x_remote + 128 + 16 * q, sv1[4 * q], sv1[4 * q + 1], sv1[4 * q + 2], sv1[4 * q + 3],
-                      xfull_remote);
-        }
-        // receive the peer's partial scores and form the full score row
-        ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full), i & 1, p.status, abort));
-        if (!ok) break;
-        float s[64];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const float4 x = reinterpret_cast<const float4*>(xrow)[q];
-          const uint32_t* mine = q < 8 ? &sv0[4 * q] : &sv1[4 * (q - 8)];
-          s[4 * q + 0] = __uint_as_float(mine[0]) + x.x;
-          s[4 * q + 1] = __uint_as_float(mine[1]) + x.y;
-          s[4 * q + 2] = __uint_as_float(mine[2]) + x.z;
-          s[4 * q + 3] = __uint_as_float(mine[3]) + x.w;
-        }
-        // once every row has read the exchange buffer, one thread re-arms it and
-        // tells the peer it may send the next page's partial scores
-        mbar_arrive(bar_addr(bars.x_read));
-        if (row == 0) {
-          ok = mbar_wait(bar_addr(bars.x_read), i & 1, p.status, abort);
-          if (ok) {
-            mbar_arrive_expect_tx(bar_addr(bars.x_full), kXTxBytes);
-            mbar_arrive_remote(xfree_remote);
-          }
-        }
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        // mask, scale to the log2 domain, row max
+        // raw-score row max over the visible tokens (the scale is positive)
         const int n_valid = min(kPage, t_end - (page_begin + i) * kPage);
         float mx = -INFINITY;
+        if (n_valid == kPage) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          s[c] = c < n_valid ? s[c] * kScaleLog2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
+          for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+        } else {
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < n_valid) mx = fmaxf(mx, __uint_as_float(sv[c]));
         }
+        mx *= kScaleLog2;
         float factor = 1.f;
         bool rescale = false;
         if (i == 0) {
           m_ref = mx;
         } else if (mx > m_ref + kRescaleLog2) {
-          factor = exp2f(m_ref - mx);
+          factor = ex2_approx(m_ref - mx);
           m_ref = mx;
           rescale = true;
         }
+        const float neg_m = -m_ref;
         uint32_t pk[32];
         float sum = 0.f;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          pk[c] = pack_bf16x2(exp2f(s[2 * c] - m_ref), exp2f(s[2 * c + 1] - m_ref));
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * c]), kScaleLog2, neg_m));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * c + 1]), kScaleLog2, neg_m));
+          if (2 * c >= n_valid) p0 = 0.f;
+          if (2 * c + 1 >= n_valid) p1 = 0.f;
+          pk[c] = pack_bf16x2(p0, p1);
           sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
         }
         l = l * factor + sum;
@@ -345,7 +405,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
             tmem_st32(tmem + lane_off + kTmemO + c0, r);
           }
         }
-        tmem_st32(tmem + lane_off + kTmemS + buf * 64, pk);
+        tmem_st32(s_addr, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_addr(bars.p_full[buf]));

@@ -3,6 +3,7 @@
 // (distributed shared memory) operations the attention kernel uses.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "internal.cuh"
@@ -107,6 +108,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
       : "memory");
+}
+
+// Pull a box into L2 ahead of its load (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+               ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y)
+               : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -255,6 +263,21 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
 // 128-byte swizzle of a byte offset inside a 1024-byte-aligned atom (16-byte
 // unit index XOR row index within the 8-row group), as TMA and tcgen05 apply it.
 __device__ __forceinline__ uint32_t sw128(uint32_t off) { return off ^ (((off >> 7) & 7u) << 4); }
+
+// 2^x by the hardware approximation (MUFU.EX2; ~2 ulp, flushes subnormals).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
