@@ -50,7 +50,9 @@ typedef enum {
   MLA_ERR_WORKSPACE = 3,   /* workspace missing or too small */
   MLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
   MLA_ERR_TIMEOUT = 5,     /* (device status) a bounded wait ran out */
-  MLA_ERR_BOUNDS = 6       /* (device status) page id / position out of range */
+  MLA_ERR_BOUNDS = 6,      /* (device status) page id / position out of range */
+  MLA_ERR_RANGE = 7        /* (device status) a partial attention score exceeded the
+                              kernel's exchange range (|q . row| over half a row > 1.6e7) */
 } mla_status;
 
 enum {

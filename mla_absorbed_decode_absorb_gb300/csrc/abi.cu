@@ -92,6 +92,7 @@ const char* mla_status_string(mla_status s) {
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA runtime call or launch failed";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded wait in a kernel ran out";
     case MLA_ERR_BOUNDS: return "MLA_ERR_BOUNDS: a page id or position was out of range";
+    case MLA_ERR_RANGE: return "MLA_ERR_RANGE: a partial attention score exceeded the exchange range";
   }
   return "MLA_ERR_UNKNOWN";
 }

@@ -15,20 +15,25 @@
 //   * owns latent columns [256r, 256r + 256) of O' (256 fp32 TMEM columns);
 //   * loads only its 288 columns of each 64-token page: latent [256r, 256r+256)
 //     and RoPE [32r, 32r + 32), i.e. 36 KB per page instead of 72 KB;
-//   * computes the partial score over those 288 columns and swaps partial S
-//     (128 x 64 fp32) with its peer through distributed shared memory, so both
-//     CTAs hold the same full S = S_0 + S_1 (bitwise equal: fp addition commutes);
+//   * computes the partial score over those 288 columns and swaps it with its
+//     peer through distributed shared memory; both CTAs round both partials to
+//     fp16 (scaled by 2^-8 for range) and add them in the same order, so they
+//     hold bitwise-equal scores S = S_0 + S_1;
 //   * runs the same online softmax as its peer on that S, so both use identical
 //     P, running max and sum, and accumulates its half of O' = P c.
-// Warp roles: warp 0 issues TMA loads (the query tile once, then a 3-stage ring
-// of half-pages; page ids are prefetched 32 at a time), warp 1 allocates TMEM
-// and issues tcgen05.mma (QK^T into one of two TMEM score buffers; P V with P
-// read from TMEM), warps 6-9 are the exchange warpgroup (per page: read the
-// partial scores, swap them with the peer, write the full scores back into
-// TMEM), warps 2-5 are the softmax/epilogue warpgroup.  Both warpgroups have one
-// thread per head row, and the exchange for page i+1 overlaps the softmax of
-// page i.  The softmax keeps a lazily updated reference max: O' in TMEM is
-// rescaled only when a page raises a row's max by more than 2^8.
+// The CTA's 256 latent columns of the query sit in TMEM (the QK^T MMAs read A
+// from TMEM), which leaves shared memory for a 5-stage ring of half-pages; the
+// producer also prefetches pages into L2 ahead of the ring.
+//
+// Warp roles: warp 0 issues TMA loads and L2 prefetches (page ids are read 32 at
+// a time), warp 1 allocates TMEM and issues tcgen05.mma (QK^T into one of two
+// TMEM score buffers; P V with P read from TMEM), warps 6-9 are the exchange
+// warpgroup (query into TMEM at start; per page: read the partial scores, swap
+// them with the peer, write the full scores back into TMEM), warps 2-5 are the
+// softmax/epilogue warpgroup.  Both warpgroups have one thread per head row, and
+// the exchange for page i+1 overlaps the softmax of page i.  The softmax keeps a
+// lazily updated reference max: O' in TMEM is rescaled only when a page raises a
+// row's max by more than 2^8.
 #include "sm100.cuh"
 #include "tmap.cuh"
 
@@ -37,45 +42,49 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 3;
+constexpr int kStages = 5;
+constexpr int kPrefetchAhead = 6;   // L2 prefetch distance beyond the page being loaded
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kExchangeWarp0 = 6;
-constexpr int kSoftmaxThreads = 128;
+constexpr int kRowThreads = 128;    // threads of each row warpgroup
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 0;    // O' half: [0, 256)
-constexpr uint32_t kTmemS = 256;  // two score buffers: [256, 320), [320, 384); P aliases their first 32 columns
+constexpr uint32_t kTmemO = 0;      // O' half: [0, 256)
+constexpr uint32_t kTmemS = 256;    // two score buffers: [256, 320), [320, 384); P aliases their first 32 columns
+constexpr uint32_t kTmemQ = 384;    // the CTA's 256 latent query columns as bf16 pairs: [384, 512)
 
-constexpr int kQChunk = 128 * 128;    // 64 latent columns x 128 heads, 128-byte rows
-constexpr int kQRope = 128 * 64;      // 32 RoPE columns x 128 heads, 64-byte rows
-constexpr int kQBytes = 4 * kQChunk + kQRope;
-constexpr int kPChunk = 64 * 128;     // 64 latent columns x 64 tokens
-constexpr int kPRope = 64 * 64;       // 32 RoPE columns x 64 tokens
+constexpr int kQRope = 128 * 64;      // 32 RoPE columns x 128 heads, 64-byte rows (SW64)
+constexpr int kPChunk = 64 * 128;     // 64 latent columns x 64 tokens (SW128)
+constexpr int kPRope = 64 * 64;       // 32 RoPE columns x 64 tokens (SW64)
 constexpr int kStageBytes = 4 * kPChunk + kPRope;
-constexpr int kXStride = 68;          // floats per exchanged score row (64 + 4 pad: conflict-free v4 access)
-constexpr int kXBytes = kSoftmaxThreads * kXStride * 4;
-constexpr uint32_t kXTxBytes = kSoftmaxThreads * 64 * 4;
+constexpr int kXRowBytes = 144;       // 64 fp16 scores + 16 B pad: conflict-free 16-byte accesses
+constexpr int kXBufBytes = kRowThreads * kXRowBytes;
+constexpr uint32_t kXTxBytes = kRowThreads * 128;
+constexpr float kXScale = 1.f / 256.f;  // exchanged partial scores are fp16(S_r * 2^-8)
+constexpr float kXUnscale = 256.f;
 
 constexpr int kOffQ = 0;
-constexpr int kOffStage = kOffQ + kQBytes;
+constexpr int kOffStage = kOffQ + kQRope;
 constexpr int kOffX = kOffStage + kStages * kStageBytes;
-constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kOffBar = kOffX + 2 * kXBufBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + 1 KB alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr float kRescaleLog2 = 8.f;
 
 struct Bars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t q_full;
+  uint64_t q_full;      // RoPE query columns in shared memory
+  uint64_t q_tmem;      // latent query columns in TMEM
   uint64_t s_full[2];   // partial scores of this CTA are in TMEM
   uint64_t s_ready[2];  // full scores are in TMEM
   uint64_t p_full[2];
   uint64_t pv_done;
-  uint64_t x_full;
-  uint64_t x_free;
-  uint64_t x_read;
+  uint64_t x_full[2];   // peer's partial scores landed in exchange buffer k
+  uint64_t x_free[2];   // peer has read our partial scores from its buffer k
+  uint64_t x_read[2];   // all rows have read exchange buffer k
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -85,6 +94,7 @@ static_assert(sizeof(Bars) <= 256, "barrier block");
 struct Params {
   const int32_t* page_table;
   const int32_t* kv_lens;
+  const uint16_t* q_abs;
   float* o_out;
   float* lse_out;
   int* status;
@@ -99,9 +109,8 @@ struct Params {
 __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
-                      const __grid_constant__ CUtensorMap tm_c128, const __grid_constant__ CUtensorMap tm_c64,
-                      const Params p) {
+decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_constant__ CUtensorMap tm_c128,
+                      const __grid_constant__ CUtensorMap tm_c64, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBar);
@@ -130,20 +139,22 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
       mbar_init(bar_addr(bars.empty[s]), 1);
     }
     mbar_init(bar_addr(bars.q_full), 1);
+    mbar_init(bar_addr(bars.q_tmem), kRowThreads);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_addr(bars.s_full[s]), 1);
-      mbar_init(bar_addr(bars.s_ready[s]), kSoftmaxThreads);
-      mbar_init(bar_addr(bars.p_full[s]), kSoftmaxThreads);
+      mbar_init(bar_addr(bars.s_ready[s]), kRowThreads);
+      mbar_init(bar_addr(bars.p_full[s]), kRowThreads);
+      mbar_init(bar_addr(bars.x_full[s]), 1);
+      mbar_init(bar_addr(bars.x_free[s]), 1);
+      mbar_init(bar_addr(bars.x_read[s]), kRowThreads);
     }
     mbar_init(bar_addr(bars.pv_done), 1);
-    mbar_init(bar_addr(bars.x_full), 1);
-    mbar_init(bar_addr(bars.x_free), 1);
-    mbar_init(bar_addr(bars.x_read), kSoftmaxThreads);  // the 128 exchange threads
     mbar_init(bar_addr(bars.drain), 1);
     bars.abort = 0;
     fence_mbar_init();
-    // arm the first exchange phase: 32 KB of the peer's partial scores
-    mbar_arrive_expect_tx(bar_addr(bars.x_full), kXTxBytes);
+    // arm the first use of both exchange buffers: 16 KB of the peer's partial scores each
+    mbar_arrive_expect_tx(bar_addr(bars.x_full[0]), kXTxBytes);
+    mbar_arrive_expect_tx(bar_addr(bars.x_full[1]), kXTxBytes);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars.tmem_base), kTmemCols);
@@ -159,33 +170,38 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     // ------------------------------------------------------------ TMA producer
     if (n_pages > 0) {
       const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride + page_begin;
+      auto valid_page = [&](int page) { return page >= 0 && page < p.num_pages; };
+      auto prefetch_page = [&](int page) {
+        if (!valid_page(page)) return;
+        for (int c = 0; c < 4; ++c) tma_prefetch_l2_2d(&tm_c128, 64 * (4 * rank + c), page * kPage);
+        tma_prefetch_l2_2d(&tm_c64, kLatent + 32 * rank, page * kPage);
+      };
+      int ids = lane < n_pages ? pt[lane] : 0;
+      int ids_next = 32 + lane < n_pages ? pt[32 + lane] : 0;
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q128);
         tma_prefetch_desc(&tm_q64);
         tma_prefetch_desc(&tm_c128);
         tma_prefetch_desc(&tm_c64);
-        const int q_row = bj * kHeads;
-        const uint32_t qb = smem_u32(smem + kOffQ);
-        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQBytes);
-        for (int c = 0; c < 4; ++c)
-          tma_load_2d(qb + c * kQChunk, &tm_q128, 64 * (4 * rank + c), q_row, bar_addr(bars.q_full));
-        tma_load_2d(qb + 4 * kQChunk, &tm_q64, kLatent + 32 * rank, q_row, bar_addr(bars.q_full));
+        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQRope);
+        tma_load_2d(smem_u32(smem + kOffQ), &tm_q64, kLatent + 32 * rank, bj * kHeads, bar_addr(bars.q_full));
       }
-      // page ids, 32 per coalesced load, one chunk ahead
-      int ids = lane < n_pages ? pt[lane] : 0;
+      // warm L2 with the pages just past the first ring fill
+      if (lane >= kStages && lane < kStages + kPrefetchAhead && lane < n_pages) prefetch_page(ids);
       bool ok = true;
       for (int base = 0; base < n_pages && ok; base += 32) {
-        const int next_i = base + 32 + lane;
-        const int ids_next = next_i < n_pages ? pt[next_i] : 0;
         const int cnt = min(32, n_pages - base);
         for (int k = 0; k < cnt && ok; ++k) {
           const int i = base + k;
+          const int pf = k + kStages + kPrefetchAhead;  // < 64
           int page = __shfl_sync(0xffffffffu, ids, k);
+          const int pf_lo = __shfl_sync(0xffffffffu, ids, pf & 31);
+          const int pf_hi = __shfl_sync(0xffffffffu, ids_next, pf & 31);
+          const int pf_page = pf < 32 ? pf_lo : pf_hi;
           if (lane == 0) {
             const int s = i % kStages;
             ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
             if (ok) {
-              if (page < 0 || page >= p.num_pages) {
+              if (!valid_page(page)) {
                 record_status(p.status, MLA_ERR_BOUNDS);
                 page = 0;  // stay in bounds; the result of this unit is not meaningful
               }
@@ -195,11 +211,13 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
               for (int c = 0; c < 4; ++c)
                 tma_load_2d(sb + c * kPChunk, &tm_c128, 64 * (4 * rank + c), page * kPage, fb);
               tma_load_2d(sb + 4 * kPChunk, &tm_c64, kLatent + 32 * rank, page * kPage, fb);
+              if (base + pf < n_pages) prefetch_page(pf_page);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
         }
         ids = ids_next;
+        ids_next = base + 64 + lane < n_pages ? pt[base + 64 + lane] : 0;
       }
     }
   } else if (warp == kMmaWarp) {
@@ -207,21 +225,27 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     if (n_pages > 0) {
       const uint32_t idesc_qk = idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
       const uint32_t idesc_pv = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/1);
-      const uint32_t qb = smem_u32(smem + kOffQ);
+      // Descriptors of stage 0; a stage, chunk or K step is a byte offset added to
+      // the start-address field (16-byte units in the low bits).
+      const uint32_t st0 = smem_u32(smem + kOffStage);
+      const uint64_t d_k128 = smem_desc(st0, 16, 1024, kSw128);             // keys, latent chunk 0
+      const uint64_t d_k64 = smem_desc(st0 + 4 * kPChunk, 16, 512, kSw64);  // keys, RoPE half
+      const uint64_t d_v = smem_desc(st0, kPChunk, 1024, kSw128);           // values (MN-major)
+      const uint64_t d_qr = smem_desc(smem_u32(smem + kOffQ), 16, 512, kSw64);
       const int last_rows = t_end - (page_begin + n_pages - 1) * kPage;  // valid rows of the last page
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.q_full), 0, p.status, abort));
+      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.q_full), 0, p.status, abort) &&
+                                            mbar_wait(bar_addr(bars.q_tmem), 0, p.status, abort));
 
       auto issue_pv = [&](int i) -> bool {
         const bool w = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.p_full[i & 1]), (i >> 1) & 1, p.status, abort));
         if (!w) return false;
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t sb = smem_u32(smem + kOffStage + (i % kStages) * kStageBytes);
+          const uint64_t vb = d_v + static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
           const uint32_t a = tmem + kTmemS + (i & 1) * 64;
+          mma_ts(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ts(tmem + kTmemO, a + 8 * k, smem_desc(sb + 2048 * k, kPChunk, 1024, kSw128), idesc_pv,
-                   (i > 0 || k > 0) ? 1u : 0u);
+          for (int k = 1; k < 4; ++k) mma_ts(tmem + kTmemO, a + 8 * k, vb + 128 * k, idesc_pv, 1u);
           mma_commit(bar_addr(bars.empty[i % kStages]));
           mma_commit(bar_addr(bars.pv_done));
         }
@@ -247,18 +271,16 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
         }
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t sb = smem_u32(stage);
+          const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
           const uint32_t d = tmem + kTmemS + (i & 1) * 64;
+          // latent part: A = query columns in TMEM (8 columns per K step of 16)
+          mma_ts(d, tmem + kTmemQ, d_k128 + so, idesc_qk, 0u);
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(d, smem_desc(qb + c * kQChunk + 32 * k, 16, 1024, kSw128),
-                     smem_desc(sb + c * kPChunk + 32 * k, 16, 1024, kSw128), idesc_qk, (c | k) ? 1u : 0u);
-#pragma unroll
-          for (int k = 0; k < 2; ++k)
-            mma_ss(d, smem_desc(qb + 4 * kQChunk + 32 * k, 16, 512, kSw64),
-                   smem_desc(sb + 4 * kPChunk + 32 * k, 16, 512, kSw64), idesc_qk, 1u);
+          for (int k = 1; k < 16; ++k)
+            mma_ts(d, tmem + kTmemQ + 8 * k, d_k128 + so + (k >> 2) * (kPChunk >> 4) + (k & 3) * 2, idesc_qk, 1u);
+          // RoPE part: A = query RoPE columns in shared memory
+          mma_ss(d, d_qr, d_k64 + so, idesc_qk, 1u);
+          mma_ss(d, d_qr + 2, d_k64 + so + 2, idesc_qk, 1u);
           mma_commit(bar_addr(bars.s_full[i & 1]));
         }
         __syncwarp();
@@ -275,65 +297,106 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // head
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    float* xrow = reinterpret_cast<float*>(smem + kOffX) + row * kXStride;
-    const uint32_t x_remote = mapa(smem_u32(xrow), peer);
-    const uint32_t xfull_remote = mapa(bar_addr(bars.x_full), peer);
-    const uint32_t xfree_remote = mapa(bar_addr(bars.x_free), peer);
-    bool ok = true;
+    bool ok = n_pages > 0;
+    if (ok) {
+      // this CTA's 256 latent query columns of the row into TMEM as bf16 pairs
+      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<int64_t>(bj) * kHeads + row) * kRow +
+                                                         256 * rank);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t w[32];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = qsrc[c0 / 4 + q];
+          w[4 * q] = v.x;
+          w[4 * q + 1] = v.y;
+          w[4 * q + 2] = v.z;
+          w[4 * q + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + kTmemQ + c0, w);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(bars.q_tmem));
+    }
+    uint8_t* xrow0 = smem + kOffX + row * kXRowBytes;
+    const uint32_t x_remote0 = mapa(smem_u32(xrow0), peer);
+    float range_max = 0.f;
     for (int i = 0; i < n_pages && ok; ++i) {
-      const int buf = i & 1;
+      const int buf = i & 1;        // TMEM score buffer and exchange buffer
+      const uint32_t use = (i >> 1) & 1;
       const uint32_t s_addr = tmem + lane_off + kTmemS + buf * 64;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[buf]), (i >> 1) & 1, p.status, abort));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[buf]), use, p.status, abort));
       if (!ok) break;
       tc_fence_after();
-      uint32_t sv0[32], sv1[32];
-      tmem_ld32(s_addr, sv0);
-      tmem_ld32(s_addr + 32, sv1);
-      tmem_wait_ld();
-      // send this CTA's partial scores to the peer
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free), (i & 1) ^ 1, p.status, abort));
-      if (!ok) break;
+      uint32_t mine[32];
+      {
+        uint32_t a[32], c[32];
+        tmem_ld32(s_addr, a);
+        tmem_ld32(s_addr + 32, c);
+        tmem_wait_ld();
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        st_async_v4(x_remote + 16 * q, sv0[4 * q], sv0[4 * q + 1], sv0[4 * q + 2], sv0[4 * q + 3], xfull_remote);
-        st_async_v4(x_remote + 128 + 16 * q, sv1[4 * q], sv1[4 * q + 1], sv1[4 * q + 2], sv1[4 * q + 3],
-                    xfull_remote);
-      }
-      // receive the peer's partial scores and add them
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full), i & 1, p.status, abort));
-      if (!ok) break;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = reinterpret_cast<const float4*>(xrow)[q];
-        const float4 y = reinterpret_cast<const float4*>(xrow)[q + 8];
-        sv0[4 * q + 0] = __float_as_uint(__uint_as_float(sv0[4 * q + 0]) + x.x);
-        sv0[4 * q + 1] = __float_as_uint(__uint_as_float(sv0[4 * q + 1]) + x.y);
-        sv0[4 * q + 2] = __float_as_uint(__uint_as_float(sv0[4 * q + 2]) + x.z);
-        sv0[4 * q + 3] = __float_as_uint(__uint_as_float(sv0[4 * q + 3]) + x.w);
-        sv1[4 * q + 0] = __float_as_uint(__uint_as_float(sv1[4 * q + 0]) + y.x);
-        sv1[4 * q + 1] = __float_as_uint(__uint_as_float(sv1[4 * q + 1]) + y.y);
-        sv1[4 * q + 2] = __float_as_uint(__uint_as_float(sv1[4 * q + 2]) + y.z);
-        sv1[4 * q + 3] = __float_as_uint(__uint_as_float(sv1[4 * q + 3]) + y.w);
-      }
-      // once every row has read the exchange buffer, one thread re-arms it and
-      // tells the peer it may send the next page's partial scores
-      mbar_arrive(bar_addr(bars.x_read));
-      if (row == 0) {
-        ok = mbar_wait(bar_addr(bars.x_read), i & 1, p.status, abort);
-        if (ok) {
-          mbar_arrive_expect_tx(bar_addr(bars.x_full), kXTxBytes);
-          mbar_arrive_remote(xfree_remote);
+        for (int q = 0; q < 16; ++q) {
+          const float x0 = __uint_as_float(a[2 * q]), x1 = __uint_as_float(a[2 * q + 1]);
+          const float y0 = __uint_as_float(c[2 * q]), y1 = __uint_as_float(c[2 * q + 1]);
+          range_max = fmaxf(range_max, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(y0), fabsf(y1))));
+          mine[q] = pack_f16x2(x0 * kXScale, x1 * kXScale);
+          mine[16 + q] = pack_f16x2(y0 * kXScale, y1 * kXScale);
         }
       }
-      ok = __all_sync(0xffffffffu, ok);
+      // send: wait until the peer has read what we sent into this buffer two pages ago
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free[buf]), use ^ 1u, p.status, abort));
       if (!ok) break;
-      // full scores back into the same TMEM buffer for the softmax warpgroup
-      tmem_st32(s_addr, sv0);
-      tmem_st32(s_addr + 32, sv1);
+      const uint32_t x_remote = x_remote0 + buf * kXBufBytes;
+      const uint32_t xfull_remote = mapa(bar_addr(bars.x_full[buf]), peer);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_async_v4(x_remote + 16 * q, mine[4 * q], mine[4 * q + 1], mine[4 * q + 2], mine[4 * q + 3], xfull_remote);
+      // receive the peer's partial scores; both CTAs add fp16(S_0) + fp16(S_1) in fp32
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full[buf]), use, p.status, abort));
+      if (!ok) break;
+      uint32_t full0[32], full1[32];
+      {
+        const uint4* xr = reinterpret_cast<const uint4*>(xrow0 + buf * kXBufBytes);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = xr[q];
+          const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int w = 4 * q + e;  // packed word index: columns 2w, 2w+1
+            const float2 a = unpack_f16x2(mine[w]);
+            const float2 c = unpack_f16x2(pw[e]);
+            const uint32_t lo = __float_as_uint((a.x + c.x) * kXUnscale);
+            const uint32_t hi = __float_as_uint((a.y + c.y) * kXUnscale);
+            if (w < 16) {
+              full0[2 * w] = lo;
+              full0[2 * w + 1] = hi;
+            } else {
+              full1[2 * (w - 16)] = lo;
+              full1[2 * (w - 16) + 1] = hi;
+            }
+          }
+        }
+      }
+      tmem_st32(s_addr, full0);
+      tmem_st32(s_addr + 32, full1);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(bars.s_ready[buf]));
+      // buffer read: re-arm it for its next use and let the peer refill it
+      mbar_arrive(bar_addr(bars.x_read[buf]));
+      if (row == 0) {
+        ok = mbar_wait(bar_addr(bars.x_read[buf]), use, p.status, abort);
+        if (ok) {
+          mbar_arrive_expect_tx(bar_addr(bars.x_full[buf]), kXTxBytes);
+          mbar_arrive_remote(mapa(bar_addr(bars.x_free[buf]), peer));
+        }
+      }
+      ok = __all_sync(0xffffffffu, ok);
     }
+    // exchanged partials are fp16(S_r / 256): beyond this magnitude they overflow
+    if (range_max > 1.6e7f) record_status(p.status, MLA_ERR_RANGE);
   } else {
     // ------------------------------------------------------------ softmax + epilogue
     const int quad = warp & 3;
@@ -439,6 +502,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
   cluster_sync();  // no CTA leaves while its peer may still address its shared memory
 }
 
+
 int g_cluster_slots[64];
 bool g_configured[64];
 
@@ -493,17 +557,17 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   if (units == 0) return cudaSuccess;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || !configure(dev)) return cudaErrorInvalidDevice;
-  CUtensorMap tq128, tq64, tc128, tc64;
+  CUtensorMap tq64, tc128, tc64;
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * kHeads;
   const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
-  if (!make_tmap_bf16_2d(&tq128, q_abs, q_rows, kRow, kRow, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_bf16_2d(&tc128, cache, c_rows, kRow, kRow, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   Params prm;
   prm.page_table = page_table;
   prm.kv_lens = kv_lens;
+  prm.q_abs = q_abs;
   prm.o_out = o_out;
   prm.lse_out = lse_out;
   prm.status = status;
@@ -513,8 +577,7 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   prm.max_kv_len = max_kv_len;
   prm.split_pages = plan.split_pages;
   prm.num_splits = plan.num_splits;
-  decode_attn_tc_kernel<<<static_cast<unsigned>(2 * units), kThreads, kSmemBytes, stream>>>(tq128, tq64, tc128, tc64,
-                                                                                           prm);
+  decode_attn_tc_kernel<<<static_cast<unsigned>(2 * units), kThreads, kSmemBytes, stream>>>(tq64, tc128, tc64, prm);
   return cudaGetLastError();
 }
 

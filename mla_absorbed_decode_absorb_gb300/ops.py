@@ -53,7 +53,7 @@ for _name, (_args, _res) in _SIGS.items():
     _f.restype = _res
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, \
-    MLA_ERR_BOUNDS = range(7)
+    MLA_ERR_BOUNDS, MLA_ERR_RANGE = range(8)
 
 
 class MLAError(RuntimeError):
