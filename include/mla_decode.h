@@ -182,6 +182,34 @@ mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
                               float* o_latent, float* lse, cudaStream_t stream);
 
 /*
+ * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate
+ * device memory.  (The MLA pages have no counterpart to this call; it exists for
+ * deployment.)  Some callers may not call cudaMalloc when they run a decode
+ * step: a serving runtime whose device memory is reserved up front by its own
+ * pool, a plugin that may only touch the buffers it is handed, or a hot path
+ * where allocation is forbidden.  This variant takes no workspace: the split
+ * partials live in a 16 MiB array inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *
+ * Arguments, outputs and semantics are those of mla_decode_attn without
+ * `workspace`/`workspace_bytes`.  Limit: the split plan must fit the array,
+ * i.e. B * n_q * num_splits <= 63 units of split partials (each 128 x 513
+ * floats); a single-split plan needs none.  A larger plan returns
+ * MLA_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress with that device current); make that first call before
+ * any stream capture.  All calls share the one array, so calls whose work
+ * overlaps on the GPU (different streams, no ordering between them) race and
+ * corrupt each other's partials; the array keeps the last call's contents,
+ * which are fully rewritten by each call before they are read.  No memory is
+ * allocated or freed by this call.
+ */
+mla_status mla_decode_attn_noalloc(const mla_bf16* q_abs, const mla_bf16* cache, int64_t num_pages,
+                                   const int32_t* page_table, int pt_stride, const int32_t* kv_lens,
+                                   int B, int n_q, int max_kv_len, int split_pages,
+                                   float* o_latent, float* lse, cudaStream_t stream);
+
+/*
  * mla_out_absorb -- O[h] = W_UV[h] O'[h], the value up-projection applied once.
  * ("MLA 矩阵吸收 …" section 2.1, V side: O = (Attn c) W_UV, once per step;
  *  "DeepSeek MLA 架构详解" step 5, einsum 'bhm,hdm->bhd'.)

@@ -79,6 +79,14 @@ bool make_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan)
 
 }  // namespace
 
+namespace mla {
+// Shared with other translation units of the library.
+bool split_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan) {
+  return make_plan(B, n_q, max_kv_len, split_pages, plan);
+}
+int* device_status_word() { return status_ptr(); }
+}  // namespace mla
+
 extern "C" {
 
 int mla_abi_version(void) { return 1; }

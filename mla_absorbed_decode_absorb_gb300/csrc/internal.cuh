@@ -58,6 +58,11 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
 // Clusters of the attention kernel that fit on the current device at once.
 int decode_cluster_slots();
 
+// The split-KV plan every decode entry point uses (false for invalid sizes), and
+// the device address of the current device's status word (nullptr on failure).
+bool split_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan);
+int* device_status_word();
+
 cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   int64_t num_pages, const int32_t* page_table, int pt_stride,
                                   const int32_t* kv_lens, int B, int n_q, int max_kv_len,
