@@ -21,16 +21,19 @@
 //     hold bitwise-equal scores S = S_0 + S_1;
 //   * runs the same online softmax as its peer on that S, so both use identical
 //     P, running max and sum, and accumulates its half of O' = P c.
-// The CTA's 256 latent columns of the query sit in TMEM (the QK^T MMAs read A
-// from TMEM), which leaves shared memory for a 5-stage ring of half-pages; the
-// producer also prefetches pages into L2 ahead of the ring.
+// Half of the CTA's 256 latent query columns sit in TMEM (QK^T MMAs with A read
+// from TMEM), the other half and the RoPE columns in shared memory, which leaves
+// room for a 4-stage ring of half-pages.  P has TMEM buffers of its own, so a
+// score buffer is free as soon as the softmax has read it: QK^T of page i+1 is
+// issued while the softmax of page i is still running.
 //
-// Warp roles: warp 0 issues TMA loads and L2 prefetches (page ids are read 32 at
-// a time), warp 1 allocates TMEM and issues tcgen05.mma (QK^T into one of two
+// Warp roles: warp 0 issues TMA loads (page ids are read 32 at a time), warp 1 allocates TMEM and issues tcgen05.mma (QK^T into one of two
 // TMEM score buffers; P V with P read from TMEM), warps 6-9 are the exchange
 // warpgroup (query into TMEM at start; per page: read the partial scores, swap
 // them with the peer, write the full scores back into TMEM), warps 2-5 are the
-// softmax/epilogue warpgroup.  Both warpgroups have one thread per head row, and
+// softmax/epilogue warpgroup, and warp 10 re-arms each exchange buffer once it
+// has been read and tells the peer (a cluster-scope release that would
+// otherwise stall the exchange warpgroup).  Both warpgroups have one thread per head row, and
 // the exchange for page i+1 overlaps the softmax of page i.  The softmax keeps a
 // lazily updated reference max: O' in TMEM is rescaled only when a page raises a
 // row's max by more than 2^8.
@@ -42,19 +45,22 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 5;
-constexpr int kPrefetchAhead = 6;   // L2 prefetch distance beyond the page being loaded
-constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr int kThreads = 352;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kExchangeWarp0 = 6;
+constexpr int kSignalWarp = 10;
 constexpr int kRowThreads = 128;    // threads of each row warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O' half: [0, 256)
-constexpr uint32_t kTmemS = 256;    // two score buffers: [256, 320), [320, 384); P aliases their first 32 columns
-constexpr uint32_t kTmemQ = 384;    // the CTA's 256 latent query columns as bf16 pairs: [384, 512)
+constexpr uint32_t kTmemS = 256;    // two score buffers: [256, 320), [320, 384)
+constexpr uint32_t kTmemP = 384;    // two P buffers (64 bf16 per row = 32 columns): [384, 416), [416, 448)
+constexpr uint32_t kTmemQ = 448;    // the CTA's first 128 latent query columns as bf16 pairs: [448, 512)
 
+constexpr int kQChunk = 128 * 128;    // 64 latent query columns x 128 heads, 128-byte rows (SW128)
 constexpr int kQRope = 128 * 64;      // 32 RoPE columns x 128 heads, 64-byte rows (SW64)
+constexpr int kQBytes = 2 * kQChunk + kQRope;  // query columns kept in shared memory
 constexpr int kPChunk = 64 * 128;     // 64 latent columns x 64 tokens (SW128)
 constexpr int kPRope = 64 * 64;       // 32 RoPE columns x 64 tokens (SW64)
 constexpr int kStageBytes = 4 * kPChunk + kPRope;
@@ -65,7 +71,7 @@ constexpr float kXScale = 1.f / 256.f;  // exchanged partial scores are fp16(S_r
 constexpr float kXUnscale = 256.f;
 
 constexpr int kOffQ = 0;
-constexpr int kOffStage = kOffQ + kQRope;
+constexpr int kOffStage = kOffQ + kQBytes;
 constexpr int kOffX = kOffStage + kStages * kStageBytes;
 constexpr int kOffBar = kOffX + 2 * kXBufBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + 1 KB alignment slack
@@ -76,10 +82,11 @@ constexpr float kRescaleLog2 = 8.f;
 struct Bars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t q_full;      // RoPE query columns in shared memory
+  uint64_t q_full;      // query columns in shared memory
   uint64_t q_tmem;      // latent query columns in TMEM
   uint64_t s_full[2];   // partial scores of this CTA are in TMEM
   uint64_t s_ready[2];  // full scores are in TMEM
+  uint64_t s_free[2];   // the softmax has read the full scores of this buffer
   uint64_t p_full[2];
   uint64_t pv_done;
   uint64_t x_full[2];   // peer's partial scores landed in exchange buffer k
@@ -109,8 +116,9 @@ struct Params {
 __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_constant__ CUtensorMap tm_c128,
-                      const __grid_constant__ CUtensorMap tm_c64, const Params p) {
+decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
+                      const __grid_constant__ CUtensorMap tm_c128, const __grid_constant__ CUtensorMap tm_c64,
+                      const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBar);
@@ -143,6 +151,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_addr(bars.s_full[s]), 1);
       mbar_init(bar_addr(bars.s_ready[s]), kRowThreads);
+      mbar_init(bar_addr(bars.s_free[s]), kRowThreads);
       mbar_init(bar_addr(bars.p_full[s]), kRowThreads);
       mbar_init(bar_addr(bars.x_full[s]), 1);
       mbar_init(bar_addr(bars.x_free[s]), 1);
@@ -170,38 +179,32 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     // ------------------------------------------------------------ TMA producer
     if (n_pages > 0) {
       const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride + page_begin;
-      auto valid_page = [&](int page) { return page >= 0 && page < p.num_pages; };
-      auto prefetch_page = [&](int page) {
-        if (!valid_page(page)) return;
-        for (int c = 0; c < 4; ++c) tma_prefetch_l2_2d(&tm_c128, 64 * (4 * rank + c), page * kPage);
-        tma_prefetch_l2_2d(&tm_c64, kLatent + 32 * rank, page * kPage);
-      };
       int ids = lane < n_pages ? pt[lane] : 0;
       int ids_next = 32 + lane < n_pages ? pt[32 + lane] : 0;
       if (lane == 0) {
+        tma_prefetch_desc(&tm_q128);
         tma_prefetch_desc(&tm_q64);
         tma_prefetch_desc(&tm_c128);
         tma_prefetch_desc(&tm_c64);
-        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQRope);
-        tma_load_2d(smem_u32(smem + kOffQ), &tm_q64, kLatent + 32 * rank, bj * kHeads, bar_addr(bars.q_full));
+        // query columns [256r + 128, 256r + 256) and the RoPE half r into shared memory
+        const uint32_t qb = smem_u32(smem + kOffQ);
+        const int q_row = bj * kHeads;
+        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQBytes);
+        for (int c = 0; c < 2; ++c)
+          tma_load_2d(qb + c * kQChunk, &tm_q128, 256 * rank + 128 + 64 * c, q_row, bar_addr(bars.q_full));
+        tma_load_2d(qb + 2 * kQChunk, &tm_q64, kLatent + 32 * rank, q_row, bar_addr(bars.q_full));
       }
-      // warm L2 with the pages just past the first ring fill
-      if (lane >= kStages && lane < kStages + kPrefetchAhead && lane < n_pages) prefetch_page(ids);
       bool ok = true;
       for (int base = 0; base < n_pages && ok; base += 32) {
         const int cnt = min(32, n_pages - base);
         for (int k = 0; k < cnt && ok; ++k) {
           const int i = base + k;
-          const int pf = k + kStages + kPrefetchAhead;  // < 64
           int page = __shfl_sync(0xffffffffu, ids, k);
-          const int pf_lo = __shfl_sync(0xffffffffu, ids, pf & 31);
-          const int pf_hi = __shfl_sync(0xffffffffu, ids_next, pf & 31);
-          const int pf_page = pf < 32 ? pf_lo : pf_hi;
           if (lane == 0) {
             const int s = i % kStages;
             ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
             if (ok) {
-              if (!valid_page(page)) {
+              if (page < 0 || page >= p.num_pages) {
                 record_status(p.status, MLA_ERR_BOUNDS);
                 page = 0;  // stay in bounds; the result of this unit is not meaningful
               }
@@ -211,7 +214,6 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
               for (int c = 0; c < 4; ++c)
                 tma_load_2d(sb + c * kPChunk, &tm_c128, 64 * (4 * rank + c), page * kPage, fb);
               tma_load_2d(sb + 4 * kPChunk, &tm_c64, kLatent + 32 * rank, page * kPage, fb);
-              if (base + pf < n_pages) prefetch_page(pf_page);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -225,38 +227,25 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     if (n_pages > 0) {
       const uint32_t idesc_qk = idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
       const uint32_t idesc_pv = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/1);
-      // Descriptors of stage 0; a stage, chunk or K step is a byte offset added to
-      // the start-address field (16-byte units in the low bits).
+      // Descriptors of stage 0 and of the query in shared memory; a stage, chunk
+      // or K step is a byte offset added to the start-address field (16-byte units).
       const uint32_t st0 = smem_u32(smem + kOffStage);
       const uint64_t d_k128 = smem_desc(st0, 16, 1024, kSw128);             // keys, latent chunk 0
       const uint64_t d_k64 = smem_desc(st0 + 4 * kPChunk, 16, 512, kSw64);  // keys, RoPE half
       const uint64_t d_v = smem_desc(st0, kPChunk, 1024, kSw128);           // values (MN-major)
-      const uint64_t d_qr = smem_desc(smem_u32(smem + kOffQ), 16, 512, kSw64);
+      const uint64_t d_ql = smem_desc(smem_u32(smem + kOffQ), 16, 1024, kSw128);               // query chunks 2, 3
+      const uint64_t d_qr = smem_desc(smem_u32(smem + kOffQ + 2 * kQChunk), 16, 512, kSw64);   // query RoPE half
       const int last_rows = t_end - (page_begin + n_pages - 1) * kPage;  // valid rows of the last page
       bool ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.q_full), 0, p.status, abort) &&
                                             mbar_wait(bar_addr(bars.q_tmem), 0, p.status, abort));
 
-      auto issue_pv = [&](int i) -> bool {
-        const bool w = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.p_full[i & 1]), (i >> 1) & 1, p.status, abort));
-        if (!w) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t vb = d_v + static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
-          const uint32_t a = tmem + kTmemS + (i & 1) * 64;
-          mma_ts(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 1; k < 4; ++k) mma_ts(tmem + kTmemO, a + 8 * k, vb + 128 * k, idesc_pv, 1u);
-          mma_commit(bar_addr(bars.empty[i % kStages]));
-          mma_commit(bar_addr(bars.pv_done));
-        }
-        __syncwarp();
-        return true;
-      };
-
-      for (int i = 0; i < n_pages && ok; ++i) {
-        const int s = i % kStages;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.full[s]), (i / kStages) & 1, p.status, abort));
-        if (!ok) break;
+      // S(i) = Q K(i)^T into score buffer i & 1, once page i has landed and the
+      // softmax has read the scores of page i - 2 from that buffer.
+      auto issue_qk = [&](int i) -> bool {
+        const int s = i % kStages, buf = i & 1;
+        bool w = mbar_wait(bar_addr(bars.full[s]), (i / kStages) & 1, p.status, abort);
+        w = w && mbar_wait(bar_addr(bars.s_free[buf]), ((i >> 1) & 1) ^ 1, p.status, abort);
+        if (!__all_sync(0xffffffffu, w)) return false;
         uint8_t* stage = smem + kOffStage + s * kStageBytes;
         if (i == n_pages - 1 && last_rows < kPage) {
           // Rows past the last visible token may hold anything (NaN in unwritten
@@ -272,25 +261,65 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         tc_fence_after();
         if (lane == 0) {
           const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
-          const uint32_t d = tmem + kTmemS + (i & 1) * 64;
-          // latent part: A = query columns in TMEM (8 columns per K step of 16)
+          const uint32_t d = tmem + kTmemS + buf * 64;
+          // latent chunks 0, 1: A = query columns in TMEM (8 columns per K step of 16)
           mma_ts(d, tmem + kTmemQ, d_k128 + so, idesc_qk, 0u);
 #pragma unroll
-          for (int k = 1; k < 16; ++k)
+          for (int k = 1; k < 8; ++k)
             mma_ts(d, tmem + kTmemQ + 8 * k, d_k128 + so + (k >> 2) * (kPChunk >> 4) + (k & 3) * 2, idesc_qk, 1u);
-          // RoPE part: A = query RoPE columns in shared memory
+          // latent chunks 2, 3: A = query columns in shared memory
+#pragma unroll
+          for (int k = 8; k < 16; ++k)
+            mma_ss(d, d_ql + ((k - 8) >> 2) * (kQChunk >> 4) + (k & 3) * 2,
+                   d_k128 + so + (k >> 2) * (kPChunk >> 4) + (k & 3) * 2, idesc_qk, 1u);
+          // RoPE part
           mma_ss(d, d_qr, d_k64 + so, idesc_qk, 1u);
           mma_ss(d, d_qr + 2, d_k64 + so + 2, idesc_qk, 1u);
-          mma_commit(bar_addr(bars.s_full[i & 1]));
+          mma_commit(bar_addr(bars.s_full[buf]));
         }
         __syncwarp();
-        if (i >= 1) ok = issue_pv(i - 1);
+        return true;
+      };
+      // O' += P(i) V(i), then page i's stage goes back to the producer.
+      auto issue_pv = [&](int i) -> bool {
+        const bool w = mbar_wait(bar_addr(bars.p_full[i & 1]), (i >> 1) & 1, p.status, abort);
+        if (!__all_sync(0xffffffffu, w)) return false;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint64_t vb = d_v + static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
+          const uint32_t a = tmem + kTmemP + (i & 1) * 32;
+          mma_ts(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 1; k < 4; ++k) mma_ts(tmem + kTmemO, a + 8 * k, vb + 128 * k, idesc_pv, 1u);
+          mma_commit(bar_addr(bars.empty[i % kStages]));
+          mma_commit(bar_addr(bars.pv_done));
+        }
+        __syncwarp();
+        return true;
+      };
+
+      // QK^T runs two pages ahead of P V: S(i + 2) only needs the softmax to have
+      // read S(i), while P V(i) needs the whole softmax of page i.
+      if (ok) ok = issue_qk(0);
+      if (ok && n_pages > 1) ok = issue_qk(1);
+      for (int i = 0; i < n_pages && ok; ++i) {
+        if (i + 2 < n_pages) ok = issue_qk(i + 2);
+        if (ok) ok = issue_pv(i);
       }
-      if (ok) issue_pv(n_pages - 1);
       // no tcgen05 operation may still be running when TMEM is released
       if (lane == 0) mma_commit(bar_addr(bars.drain));
       __syncwarp();
       mbar_wait(bar_addr(bars.drain), 0, p.status, nullptr);
+    }
+  } else if (warp == kSignalWarp) {
+    // ------------------------------------------------------------ exchange buffer recycling
+    if (lane == 0) {
+      for (int i = 0; i < n_pages; ++i) {
+        const int buf = i & 1;
+        if (!mbar_wait(bar_addr(bars.x_read[buf]), (i >> 1) & 1, p.status, abort)) break;
+        mbar_arrive_expect_tx(bar_addr(bars.x_full[buf]), kXTxBytes);   // armed for the buffer's next use
+        mbar_arrive_remote(mapa(bar_addr(bars.x_free[buf]), peer));      // the peer may refill it
+      }
     }
   } else if (warp >= kExchangeWarp0) {
     // ------------------------------------------------------------ score exchange
@@ -299,11 +328,11 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     bool ok = n_pages > 0;
     if (ok) {
-      // this CTA's 256 latent query columns of the row into TMEM as bf16 pairs
+      // this CTA's first 128 latent query columns of the row into TMEM as bf16 pairs
       const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<int64_t>(bj) * kHeads + row) * kRow +
                                                          256 * rank);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t w[32];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -384,16 +413,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(bars.s_ready[buf]));
-      // buffer read: re-arm it for its next use and let the peer refill it
+      // this row is done with the exchange buffer (warp 10 recycles it)
       mbar_arrive(bar_addr(bars.x_read[buf]));
-      if (row == 0) {
-        ok = mbar_wait(bar_addr(bars.x_read[buf]), use, p.status, abort);
-        if (ok) {
-          mbar_arrive_expect_tx(bar_addr(bars.x_full[buf]), kXTxBytes);
-          mbar_arrive_remote(mapa(bar_addr(bars.x_free[buf]), peer));
-        }
-      }
-      ok = __all_sync(0xffffffffu, ok);
     }
     // exchanged partials are fp16(S_r / 256): beyond this magnitude they overflow
     if (range_max > 1.6e7f) record_status(p.status, MLA_ERR_RANGE);
@@ -418,6 +439,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
         tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_addr(bars.s_free[buf]));  // the MMA issuer may overwrite this buffer
         // raw-score row max over the visible tokens (the scale is positive)
         const int n_valid = min(kPage, t_end - (page_begin + i) * kPage);
         float mx = -INFINITY;
@@ -468,7 +491,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
             tmem_st32(tmem + lane_off + kTmemO + c0, r);
           }
         }
-        tmem_st32(s_addr, pk);
+        tmem_st32(tmem + lane_off + kTmemP + buf * 32, pk);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(bar_addr(bars.p_full[buf]));
@@ -557,10 +580,11 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   if (units == 0) return cudaSuccess;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || !configure(dev)) return cudaErrorInvalidDevice;
-  CUtensorMap tq64, tc128, tc64;
+  CUtensorMap tq128, tq64, tc128, tc64;
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * kHeads;
   const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
-  if (!make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_tmap_bf16_2d(&tq128, q_abs, q_rows, kRow, kRow, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_bf16_2d(&tc128, cache, c_rows, kRow, kRow, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
@@ -577,7 +601,7 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   prm.max_kv_len = max_kv_len;
   prm.split_pages = plan.split_pages;
   prm.num_splits = plan.num_splits;
-  decode_attn_tc_kernel<<<static_cast<unsigned>(2 * units), kThreads, kSmemBytes, stream>>>(tq64, tc128, tc64, prm);
+  decode_attn_tc_kernel<<<static_cast<unsigned>(2 * units), kThreads, kSmemBytes, stream>>>(tq128, tq64, tc128, tc64, prm);
   return cudaGetLastError();
 }
 
