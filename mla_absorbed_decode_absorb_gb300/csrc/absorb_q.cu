@@ -22,11 +22,20 @@ using namespace sm100;
 constexpr int kMTile = 128;   // latent columns per CTA
 constexpr int kNMax = 256;    // query tokens per CTA
 constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 256;
 constexpr int kAChunk = 128 * 128;          // bytes of one 64-column MN chunk: 128 d rows x 128 B
 constexpr int kSmemA = 2 * kAChunk;         // 32 KB
 constexpr int kSmemB = 2 * kNMax * 128;     // two 64-wide K chunks of up to 256 rows: 64 KB
 constexpr int kSmemBytes = kSmemA + kSmemB + 1024 /*align*/ + 64;
+
+// Tokens of the widest tile (rounded up to the MMA's N granularity of 16), and
+// the TMEM columns for its fp32 accumulator (a power of two, at least 32).
+__host__ __device__ inline int tile_tokens(int T) { return (min(kNMax, T) + 15) & ~15; }
+__host__ __device__ inline uint32_t tmem_cols_for(int nb) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(nb)) c <<= 1;
+  return c;
+}
+__host__ __device__ inline int smem_bytes_for(int T) { return kSmemA + 2 * tile_tokens(T) * 128 + 1024 + 64; }
 
 __global__ void __launch_bounds__(kThreads)
 absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restrict__ q_rope,
@@ -37,7 +46,10 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSmemA;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + kSmemB);
+  // B and TMEM are sized for the widest token tile of this launch (<= 256)
+  const int nb = tile_tokens(T);
+  const uint32_t tmem_cols = tmem_cols_for(nb);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + 2 * nb * 128);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -48,7 +60,7 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
   const int npad = (nt + 15) & ~15;
 
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -56,20 +68,24 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
     fence_mbar_init();
   }
 
-  // A: W_UK[h][d][m0 .. m0+128) -> two MN-major chunks of 64 columns, rows d.
+  // A: W_UK[h][d][m0 .. m0+128) -> two MN-major chunks of 64 columns, rows d;
+  // B: q_nope[t0 + t][h][0 .. 128) -> two K-major chunks of 64, rows t (zero past nt).
+  // Asynchronous 16-byte copies, all in flight at once.
   const uint4* wsrc = reinterpret_cast<const uint4*>(w_uk + (static_cast<int64_t>(h) * kNope) * kLatent + m0);
+#pragma unroll 4
   for (int v = tid; v < kNope * 16; v += kThreads) {
     const int d = v >> 4, u = v & 15, c = u >> 3;
-    const uint4 x = wsrc[d * (kLatent / 8) + u];
-    *reinterpret_cast<uint4*>(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)) = x;
+    cp_async16(smem_u32(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)), wsrc + d * (kLatent / 8) + u);
   }
-  // B: q_nope[t0 + t][h][0 .. 128) -> two K-major chunks of 64, rows t (zero past nt).
   for (int v = tid; v < npad * 16; v += kThreads) {
     const int t = v >> 4, u = v & 15, c = u >> 3;
-    uint4 x = make_uint4(0, 0, 0, 0);
-    if (t < nt) x = reinterpret_cast<const uint4*>(q_nope + (static_cast<int64_t>(t0 + t) * kHeads + h) * kNope)[u];
-    *reinterpret_cast<uint4*>(sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16)) = x;
+    uint8_t* dst = sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16);
+    if (t < nt)
+      cp_async16(smem_u32(dst), reinterpret_cast<const uint4*>(q_nope + (static_cast<int64_t>(t0 + t) * kHeads + h) * kNope) + u);
+    else
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
   }
+  cp_async_wait_all();
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
@@ -127,7 +143,7 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
 }  // namespace
@@ -145,7 +161,7 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
     configured = true;
   }
   dim3 grid(kLatent / kMTile, kHeads, (T + kNMax - 1) / kNMax);
-  absorb_q_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(q_nope, q_rope, seq_lens_before, w_uk, rope_table,
+  absorb_q_tc_kernel<<<grid, kThreads, smem_bytes_for(T), stream>>>(q_nope, q_rope, seq_lens_before, w_uk, rope_table,
                                                              rope_max_pos, q_abs, T, n_q, status);
   return cudaGetLastError();
 }

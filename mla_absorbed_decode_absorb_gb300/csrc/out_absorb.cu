@@ -18,12 +18,21 @@ using namespace sm100;
 
 constexpr int kNMax = 256;
 constexpr int kThreads = 128;
-constexpr uint32_t kTmemCols = 256;
 constexpr int kKStep = 128;                       // latent columns per stage
 constexpr int kAChunk = 128 * 128;                // 128 d rows x 64 m (128 B)
 constexpr int kSmemA = 2 * kAChunk;               // 32 KB
 constexpr int kSmemB = 2 * kNMax * 128;           // 64 KB
 constexpr int kSmemBytes = kSmemA + kSmemB + 1024 + 64;
+
+// Tokens of the widest tile (rounded up to the MMA's N granularity of 16), and
+// the TMEM columns for its fp32 accumulator (a power of two, at least 32).
+__host__ __device__ inline int tile_tokens(int T) { return (min(kNMax, T) + 15) & ~15; }
+__host__ __device__ inline uint32_t tmem_cols_for(int nb) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(nb)) c <<= 1;
+  return c;
+}
+__host__ __device__ inline int smem_bytes_for(int T) { return kSmemA + 2 * tile_tokens(T) * 128 + 1024 + 64; }
 
 __global__ void __launch_bounds__(kThreads)
 out_absorb_tc_kernel(const float* __restrict__ o_lat, const uint16_t* __restrict__ w_uv,
@@ -32,7 +41,10 @@ out_absorb_tc_kernel(const float* __restrict__ o_lat, const uint16_t* __restrict
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSmemA;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + kSmemB);
+  // B and TMEM are sized for the widest token tile of this launch (<= 256)
+  const int nb = tile_tokens(T);
+  const uint32_t tmem_cols = tmem_cols_for(nb);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sB + 2 * nb * 128);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -42,7 +54,7 @@ out_absorb_tc_kernel(const float* __restrict__ o_lat, const uint16_t* __restrict
   const int npad = (nt + 15) & ~15;
 
   if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
     tmem_relinquish();
   }
   if (tid == 0) {
@@ -59,23 +71,38 @@ out_absorb_tc_kernel(const float* __restrict__ o_lat, const uint16_t* __restrict
 
   for (int step = 0; step < kLatent / kKStep && ok; ++step) {
     const int mk = step * kKStep;
-    // A: W_UV[h][d][mk .. mk+128): rows d, two K-major chunks of 64.
+    // A: W_UV[h][d][mk .. mk+128): rows d, two K-major chunks of 64 (asynchronous
+    // 16-byte copies, completed below before the MMAs read them).
+#pragma unroll 4
     for (int v = tid; v < kNope * 16; v += kThreads) {
       const int d = v >> 4, u = v & 15, c = u >> 3;
-      const uint4 x = reinterpret_cast<const uint4*>(wh + d * kLatent + mk)[u];
-      *reinterpret_cast<uint4*>(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)) = x;
+      cp_async16(smem_u32(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)),
+                 reinterpret_cast<const uint4*>(wh + d * kLatent + mk) + u);
     }
     // B: O'[t0+t][h][mk .. mk+128) rounded to bf16: rows t, two K-major chunks of 64.
-    for (int v = tid; v < npad * 16; v += kThreads) {
-      const int t = v >> 4, u = v & 15, c = u >> 3;
-      uint4 x = make_uint4(0, 0, 0, 0);
-      if (t < nt) {
-        const float4* src = reinterpret_cast<const float4*>(o_lat + (static_cast<int64_t>(t0 + t) * kHeads + h) * kLatent + mk + u * 8);
-        const float4 a = src[0], b = src[1];
-        x = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+    for (int v0 = 0; v0 < npad * 16; v0 += 4 * kThreads) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int v = v0 + tid + k * kThreads, t = v >> 4, u = v & 15;
+        a[k] = b[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (v < npad * 16 && t < nt) {
+          const float4* src = reinterpret_cast<const float4*>(
+              o_lat + (static_cast<int64_t>(t0 + t) * kHeads + h) * kLatent + mk + u * 8);
+          a[k] = src[0];
+          b[k] = src[1];
+        }
       }
-      *reinterpret_cast<uint4*>(sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16)) = x;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int v = v0 + tid + k * kThreads, t = v >> 4, u = v & 15, c = u >> 3;
+        if (v < npad * 16)
+          *reinterpret_cast<uint4*>(sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16)) =
+              make_uint4(pack_bf16x2(a[k].x, a[k].y), pack_bf16x2(a[k].z, a[k].w), pack_bf16x2(b[k].x, b[k].y),
+                         pack_bf16x2(b[k].z, b[k].w));
+      }
     }
+    cp_async_wait_all();
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -109,7 +136,7 @@ out_absorb_tc_kernel(const float* __restrict__ o_lat, const uint16_t* __restrict
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
 }  // namespace
@@ -125,7 +152,7 @@ cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint1
     configured = true;
   }
   dim3 grid(kHeads, (T + kNMax - 1) / kNMax);
-  out_absorb_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(o_latent, w_uv, out, T, status);
+  out_absorb_tc_kernel<<<grid, kThreads, smem_bytes_for(T), stream>>>(o_latent, w_uv, out, T, status);
   return cudaGetLastError();
 }
 
