@@ -224,6 +224,55 @@ mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16*
                           int B, int n_q, cudaStream_t stream);
 
 /*
+ * mla_combine_out_absorb -- mla_decode_combine and mla_out_absorb in one launch:
+ * out[h] = W_UV[h] O'[h] with O' the log-sum-exp merge of the split partials.
+ * (FlashMLA point 3 of "DeepSeek-MLA-Principle": the per-split results of the
+ *  blocked softmax are merged by their log-sum-exps; "MLA 矩阵吸收 …" section
+ *  2.1, V side: the up-projection W_UV is applied once, after the attention.)
+ *
+ *   B, n_q, max_kv_len, split_pages, workspace, workspace_bytes: as given to the
+ *              mla_decode_attn_partial call whose results are consumed
+ *   o_latent   [B, n_q, 128, 512] float32: read only when the plan has a single
+ *              split (mla_decode_attn_partial then wrote the final O' there)
+ *   w_uv       [128, 128, 512] bf16   W_UV[h][d][m]
+ *   out        [B, n_q, 128, 128] bf16 out
+ *   lse        [B, n_q, 128] float32 out (nullable), written only when there is
+ *              more than one split (otherwise the partial call already wrote it)
+ *
+ * The merged O' is formed in float32 with the same operations in the same order
+ * as mla_decode_combine, rounded to bf16 and multiplied as in mla_out_absorb, so
+ * `out` equals combine-then-out_absorb bit for bit; O' itself is not written to
+ * o_latent.  Errors: MLA_ERR_INVALID_ARG for bad sizes or unaligned pointers,
+ * MLA_ERR_WORKSPACE if the workspace is smaller than the plan needs.
+ */
+mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_pages,
+                                  const void* workspace, size_t workspace_bytes, const float* o_latent,
+                                  const mla_bf16* w_uv, mla_bf16* out, float* lse, cudaStream_t stream);
+
+/*
+ * mla_set_launch_overlap / mla_get_launch_overlap -- how consecutive launches
+ * of this library on one stream may overlap.  (The MLA pages have no
+ * counterpart; this is a launch-latency setting of the GPU runtime.)
+ *
+ *   0  plain stream order: a kernel starts after the previous one has finished.
+ *   1  (default) programmatic dependent launch: a kernel may be scheduled while
+ *      the previous kernel of its stream drains and set up its shared memory,
+ *      barriers and tensor memory; it reads or writes global memory only after
+ *      that kernel has completed and its writes are visible.  Same results and
+ *      the same ordering guarantees as 0.
+ *   2  as 1, and the weight matrices w_uk (mla_absorb_q) and w_uv
+ *      (mla_out_absorb, mla_combine_out_absorb) are read BEFORE the previous
+ *      kernel has completed.  Only valid while no work still running on the
+ *      stream writes those weights (fixed inference weights).
+ *
+ * The level is process-wide and read at each launch.  MLA_ERR_INVALID_ARG for a
+ * level outside 0..2.  A launch whose predecessor on the stream is not a kernel
+ * (a copy, an event wait) is ordered as in level 0.
+ */
+mla_status mla_set_launch_overlap(int level);
+int mla_get_launch_overlap(void);
+
+/*
  * Device status: synchronizes `stream`, returns the first fault code any kernel
  * of this library recorded on the current device since the last call
  * (MLA_OK if none) and clears it.  MLA_ERR_CUDA if the synchronisation fails.

@@ -3,6 +3,7 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -19,6 +20,7 @@ constexpr int kMaxDevices = 64;
 
 std::mutex g_mutex;
 int* g_status_ptr[kMaxDevices];
+std::atomic<int> g_launch_overlap{1};
 
 int current_device() {
   int dev = -1;
@@ -85,6 +87,7 @@ bool split_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan
   return make_plan(B, n_q, max_kv_len, split_pages, plan);
 }
 int* device_status_word() { return status_ptr(); }
+int launch_overlap() { return g_launch_overlap.load(std::memory_order_relaxed); }
 }  // namespace mla
 
 extern "C" {
@@ -237,6 +240,30 @@ mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16*
   if (st == nullptr) return MLA_ERR_CUDA;
   return from_cuda(launch_out_absorb(o_latent, w_uv, out, B, n_q, st, stream));
 }
+
+mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_pages,
+                                  const void* workspace, size_t workspace_bytes, const float* o_latent,
+                                  const mla_bf16* w_uv, mla_bf16* out, float* lse, cudaStream_t stream) {
+  SplitPlan plan;
+  if (!make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (plan.num_splits == 1) return mla_out_absorb(o_latent, w_uv, out, B, n_q, stream);
+  if (!w_uv || !out || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return MLA_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  const float* o_part = static_cast<const float*>(workspace);
+  const float* lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + plan.o_part_bytes);
+  return from_cuda(launch_combine_out_absorb(o_part, lse_part, plan.num_splits, w_uv, out, lse, B, n_q, st, stream));
+}
+
+mla_status mla_set_launch_overlap(int level) {
+  if (level < 0 || level > 2) return MLA_ERR_INVALID_ARG;
+  g_launch_overlap.store(level, std::memory_order_relaxed);
+  return MLA_OK;
+}
+
+int mla_get_launch_overlap(void) { return g_launch_overlap.load(std::memory_order_relaxed); }
 
 mla_status mla_get_device_status(cudaStream_t stream) {
   int* st = status_ptr();

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kThreads)
 absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restrict__ q_rope,
                    const int32_t* __restrict__ lens, const uint16_t* __restrict__ w_uk,
                    const float* __restrict__ rope, int rope_max_pos, uint16_t* __restrict__ q_abs,
-                   int T, int n_q, int* status) {
+                   int T, int n_q, int* status, bool weights_early) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -59,6 +59,19 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
   const int nt = min(kNMax, T - t0);
   const int npad = (nt + 15) & ~15;
 
+  // A: W_UK[h][d][m0 .. m0+128) -> two MN-major chunks of 64 columns, rows d;
+  // B: q_nope[t0 + t][h][0 .. 128) -> two K-major chunks of 64, rows t (zero past nt).
+  // Asynchronous 16-byte copies, all in flight at once; the weights may be
+  // requested before the previous kernel of the stream has finished.
+  auto load_w = [&]() {
+    const uint4* wsrc = reinterpret_cast<const uint4*>(w_uk + (static_cast<int64_t>(h) * kNope) * kLatent + m0);
+#pragma unroll 4
+    for (int v = tid; v < kNope * 16; v += kThreads) {
+      const int d = v >> 4, u = v & 15, c = u >> 3;
+      cp_async16(smem_u32(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)), wsrc + d * (kLatent / 8) + u);
+    }
+  };
+  if (weights_early) load_w();
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), tmem_cols);
     tmem_relinquish();
@@ -67,16 +80,9 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
     mbar_init(smem_u32(bar), 1);
     fence_mbar_init();
   }
-
-  // A: W_UK[h][d][m0 .. m0+128) -> two MN-major chunks of 64 columns, rows d;
-  // B: q_nope[t0 + t][h][0 .. 128) -> two K-major chunks of 64, rows t (zero past nt).
-  // Asynchronous 16-byte copies, all in flight at once.
-  const uint4* wsrc = reinterpret_cast<const uint4*>(w_uk + (static_cast<int64_t>(h) * kNope) * kLatent + m0);
-#pragma unroll 4
-  for (int v = tid; v < kNope * 16; v += kThreads) {
-    const int d = v >> 4, u = v & 15, c = u >> 3;
-    cp_async16(smem_u32(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)), wsrc + d * (kLatent / 8) + u);
-  }
+  grid_dep_wait();
+  grid_dep_launch();
+  if (!weights_early) load_w();
   for (int v = tid; v < npad * 16; v += kThreads) {
     const int t = v >> 4, u = v & 15, c = u >> 3;
     uint8_t* dst = sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16);
@@ -84,6 +90,24 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
       cp_async16(smem_u32(dst), reinterpret_cast<const uint4*>(q_nope + (static_cast<int64_t>(t0 + t) * kHeads + h) * kNope) + u);
     else
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+  }
+  // RoPE of the query's position branch while the copies are in flight; the
+  // head's M tiles share the (token, frequency) pairs.
+  for (int i = blockIdx.x * kThreads + tid; i < nt * kHalfRope; i += gridDim.x * kThreads) {
+    const int t = t0 + i / kHalfRope, f = i % kHalfRope;
+    const int b = t / n_q, j = t % n_q;
+    const int64_t pos = static_cast<int64_t>(lens[b]) + j;
+    uint16_t* row = q_abs + (static_cast<int64_t>(t) * kHeads + h) * kRow + kLatent;
+    if (pos < 0 || pos >= rope_max_pos) {
+      record_status(status, MLA_ERR_BOUNDS);
+      row[f] = row[f + kHalfRope] = 0;
+      continue;
+    }
+    const uint16_t* x = q_rope + (static_cast<int64_t>(t) * kHeads + h) * kRope;
+    const float x1 = bf16_bits_to_f32(x[f]), x2 = bf16_bits_to_f32(x[f + kHalfRope]);
+    const float c = rope[pos * kRope + f], s = rope[pos * kRope + kHalfRope + f];
+    row[f] = f32_to_bf16_bits(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
+    row[f + kHalfRope] = f32_to_bf16_bits(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
   }
   cp_async_wait_all();
   fence_proxy_async_smem();
@@ -121,26 +145,6 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
     }
   }
 
-  // RoPE of the query's position branch (done by the first M tile of each head).
-  if (blockIdx.x == 0) {
-    for (int i = tid; i < nt * kHalfRope; i += kThreads) {
-      const int t = t0 + i / kHalfRope, f = i % kHalfRope;
-      const int b = t / n_q, j = t % n_q;
-      const int64_t pos = static_cast<int64_t>(lens[b]) + j;
-      uint16_t* row = q_abs + (static_cast<int64_t>(t) * kHeads + h) * kRow + kLatent;
-      if (pos < 0 || pos >= rope_max_pos) {
-        record_status(status, MLA_ERR_BOUNDS);
-        row[f] = row[f + kHalfRope] = 0;
-        continue;
-      }
-      const uint16_t* x = q_rope + (static_cast<int64_t>(t) * kHeads + h) * kRope;
-      const float x1 = bf16_bits_to_f32(x[f]), x2 = bf16_bits_to_f32(x[f + kHalfRope]);
-      const float c = rope[pos * kRope + f], s = rope[pos * kRope + kHalfRope + f];
-      row[f] = f32_to_bf16_bits(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
-      row[f + kHalfRope] = f32_to_bf16_bits(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
-    }
-  }
-
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, tmem_cols);
@@ -161,9 +165,8 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
     configured = true;
   }
   dim3 grid(kLatent / kMTile, kHeads, (T + kNMax - 1) / kNMax);
-  absorb_q_tc_kernel<<<grid, kThreads, smem_bytes_for(T), stream>>>(q_nope, q_rope, seq_lens_before, w_uk, rope_table,
-                                                             rope_max_pos, q_abs, T, n_q, status);
-  return cudaGetLastError();
+  return launch_kernel(absorb_q_tc_kernel, grid, dim3(kThreads), smem_bytes_for(T), stream, q_nope, q_rope,
+                       seq_lens_before, w_uk, rope_table, rope_max_pos, q_abs, T, n_q, status, launch_overlap() >= 2);
 }
 
 }  // namespace mla

@@ -22,6 +22,8 @@ append_kv_kernel(const uint16_t* __restrict__ c_new, const uint16_t* __restrict_
                  int pt_stride, const float* __restrict__ rope, int rope_max_pos,
                  uint16_t* __restrict__ cache, int64_t num_pages, int B, int n_new,
                  int* status) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int64_t token = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
@@ -65,10 +67,9 @@ cudaError_t launch_append_kv(const uint16_t* c_kv_new, const uint16_t* k_pe_new,
   const int64_t tokens = static_cast<int64_t>(B) * n_new;
   if (tokens == 0) return cudaSuccess;
   const int64_t blocks = (tokens + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  append_kv_kernel<<<static_cast<unsigned>(blocks), kWarpsPerBlock * 32, 0, stream>>>(
-      c_kv_new, k_pe_new, seq_lens_before, page_table, pt_stride, rope_table, rope_max_pos,
-      cache, num_pages, B, n_new, status);
-  return cudaGetLastError();
+  return launch_kernel(append_kv_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kWarpsPerBlock * 32), 0, stream,
+                       c_kv_new, k_pe_new, seq_lens_before, page_table, pt_stride, rope_table, rope_max_pos,
+                       cache, num_pages, B, n_new, status);
 }
 
 }  // namespace mla

@@ -16,6 +16,8 @@ constexpr int kThreads = 128;  // 4 latent columns per thread
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                int num_splits, float* __restrict__ o_latent, float* __restrict__ lse) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int64_t row = blockIdx.x;  // (b*n_q + j)*128 + h
   const int64_t bj = row / kHeads;
   const int h = static_cast<int>(row % kHeads);
@@ -49,9 +51,8 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, in
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(B) * n_q * kHeads;
   if (rows == 0) return cudaSuccess;
-  combine_kernel<<<static_cast<unsigned>(rows), kThreads, 0, stream>>>(o_part, lse_part, num_splits,
-                                                                      o_latent, lse);
-  return cudaGetLastError();
+  return launch_kernel(combine_kernel, dim3(static_cast<unsigned>(rows)), dim3(kThreads), 0, stream, o_part, lse_part,
+                       num_splits, o_latent, lse);
 }
 
 }  // namespace mla

@@ -132,16 +132,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
   const int split = unit % p.num_splits;
   const int b = bj / p.n_q, j = bj % p.n_q;
 
-  // The unit's token range [t_begin, t_end): identical in both CTAs of the cluster.
-  const int kv = p.kv_lens[b];
-  const bool bad = kv > p.max_kv_len || kv < p.n_q || (kv + kPage - 1) / kPage > p.pt_stride;
-  const int t_begin = split * p.split_pages * kPage;
-  const int t_end = bad ? t_begin : min(t_begin + p.split_pages * kPage, kv - p.n_q + j + 1);
-  const int page_begin = t_begin / kPage;
-  const int n_pages = t_end > t_begin ? (t_end + kPage - 1) / kPage - page_begin : 0;
-
   if (tid == 0) {
-    if (bad && rank == 0) record_status(p.status, MLA_ERR_BOUNDS);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_addr(bars.full[s]), 1);
       mbar_init(bar_addr(bars.empty[s]), 1);
@@ -174,6 +165,18 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
   cluster_sync();  // the peer's barriers exist before any remote traffic
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  // global memory only from here on: the previous kernel of the stream has finished
+  grid_dep_wait();
+  grid_dep_launch();
+
+  // The unit's token range [t_begin, t_end): identical in both CTAs of the cluster.
+  const int kv = p.kv_lens[b];
+  const bool bad = kv > p.max_kv_len || kv < p.n_q || (kv + kPage - 1) / kPage > p.pt_stride;
+  const int t_begin = split * p.split_pages * kPage;
+  const int t_end = bad ? t_begin : min(t_begin + p.split_pages * kPage, kv - p.n_q + j + 1);
+  const int page_begin = t_begin / kPage;
+  const int n_pages = t_end > t_begin ? (t_end + kPage - 1) / kPage - page_begin : 0;
+  if (tid == 0 && bad && rank == 0) record_status(p.status, MLA_ERR_BOUNDS);
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -601,8 +604,8 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   prm.max_kv_len = max_kv_len;
   prm.split_pages = plan.split_pages;
   prm.num_splits = plan.num_splits;
-  decode_attn_tc_kernel<<<static_cast<unsigned>(2 * units), kThreads, kSmemBytes, stream>>>(tq128, tq64, tc128, tc64, prm);
-  return cudaGetLastError();
+  return launch_kernel(decode_attn_tc_kernel, dim3(static_cast<unsigned>(2 * units)), dim3(kThreads), kSmemBytes, stream,
+                       tq128, tq64, tc128, tc64, prm);
 }
 
 }  // namespace mla

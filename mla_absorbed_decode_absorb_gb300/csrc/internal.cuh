@@ -26,6 +26,16 @@ __device__ __forceinline__ void record_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// Programmatic dependent launch.  A kernel launched with the programmatic
+// stream-serialization attribute may start while the previous kernel of its
+// stream is still running; grid_dep_wait() returns once that kernel has finished
+// and its memory operations are visible (immediately when launched without the
+// attribute).  Every kernel of this library touches global memory written or
+// read by earlier stream work only after it.  grid_dep_launch() lets the next
+// kernel's CTAs be scheduled once every CTA of this grid has executed it.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(x));
 }
@@ -61,6 +71,27 @@ int decode_cluster_slots();
 // The split-KV plan every decode entry point uses (false for invalid sizes), and
 // the device address of the current device's status word (nullptr on failure).
 bool split_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan);
+
+// Launch overlap level (mla_set_launch_overlap): 0 plain stream order; 1 launch
+// with programmatic stream serialization (prologues overlap the previous
+// kernel); 2 as 1, and weight matrices are also read before grid_dep_wait().
+int launch_overlap();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = launch_overlap() > 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 int* device_status_word();
 
 cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
@@ -74,5 +105,9 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, in
 
 cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint16_t* out,
                               int B, int n_q, int* status, cudaStream_t stream);
+
+cudaError_t launch_combine_out_absorb(const float* o_part, const float* lse_part, int num_splits,
+                                      const uint16_t* w_uv, uint16_t* out, float* lse, int B, int n_q,
+                                      int* status, cudaStream_t stream);
 
 }  // namespace mla

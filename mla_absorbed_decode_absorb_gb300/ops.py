@@ -45,7 +45,10 @@ _SIGS = {
     "mla_decode_attn_partial": ([_p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
     "mla_decode_combine": ([_i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
     "mla_out_absorb": ([_p, _p, _p, _i, _i, _p], _i),
+    "mla_combine_out_absorb": ([_i, _i, _i, _i, _p, _sz, _p, _p, _p, _p, _p], _i),
     "mla_get_device_status": ([_p], _i),
+    "mla_set_launch_overlap": ([_i], _i),
+    "mla_get_launch_overlap": ([], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -216,6 +219,34 @@ def mla_out_absorb(o_latent, w_uv, out=None, stream=None):
         _dev(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
         int(B), int(n_q), _stream(stream)))
     return out
+
+
+def mla_combine_out_absorb(B, n_q, max_kv_len, split_pages, workspace, o_latent, w_uv, out=None, lse=None,
+                           stream=None):
+    """Split merge + value up-projection in one launch (the merged O' is not written)."""
+    if out is None:
+        out = torch.empty(B, n_q, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=w_uv.device)
+    _check("mla_combine_out_absorb", lib.mla_combine_out_absorb(
+        int(B), int(n_q), int(max_kv_len), int(split_pages),
+        0 if workspace is None else _dev(workspace, "workspace", torch.uint8),
+        0 if workspace is None else workspace.numel(),
+        0 if o_latent is None else _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
+        _dev(w_uv, "w_uv", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
+        _dev(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        0 if lse is None else _dev(lse, "lse", torch.float32, (B, n_q, N_HEADS)),
+        _stream(stream)))
+    return out
+
+
+def mla_set_launch_overlap(level: int):
+    """0: plain stream order; 1: programmatic dependent launch (prologues overlap
+    the previous kernel); 2: as 1 and the weights are read before the previous
+    kernel finishes (only while nothing in flight writes them)."""
+    _check("mla_set_launch_overlap", lib.mla_set_launch_overlap(int(level)))
+
+
+def mla_get_launch_overlap() -> int:
+    return int(lib.mla_get_launch_overlap())
 
 
 def mla_get_device_status(stream=None) -> int:

@@ -5,10 +5,19 @@ with each sequence's history already appended, the page table, the RoPE table,
 the step's inputs and every output/workspace buffer, so that a step is just the
 four ABI calls with no allocation:
 
-1. ``mla_append_kv``   -- write this step's n_q tokens into the cache;
-2. ``mla_absorb_q``    -- ``q_abs = [q^C W_UK ; RoPE(q^R)]``;
-3. ``mla_decode_attn`` -- split attention (+ log-sum-exp combine);
-4. ``mla_out_absorb``  -- ``O = O' W_UV^T``.
+1. ``mla_append_kv``           -- write this step's n_q tokens into the cache;
+2. ``mla_absorb_q``            -- ``q_abs = [q^C W_UK ; RoPE(q^R)]``;
+3. ``mla_decode_attn_partial`` -- split attention (per-split partials);
+4. ``mla_combine_out_absorb``  -- log-sum-exp merge of the splits and
+   ``O = O' W_UV^T`` in one launch.
+
+With ``fused_finish=False`` step 4 is the two separate calls
+``mla_decode_combine`` (which also writes the merged O' to ``o_latent``) and
+``mla_out_absorb``.  Steps 1 and 2 are independent; with ``overlap_append``
+step 1 runs on a side stream forked from the caller's stream and joined before
+step 3.  By default all launches stay on the caller's stream, where the
+library's programmatic dependent launch (``mla_set_launch_overlap``) lets each
+kernel's prologue overlap the previous one.
 """
 
 from __future__ import annotations
@@ -20,8 +29,11 @@ from .workloads import D_LATENT, D_NOPE, D_ROW, N_HEADS, Inputs, empty_cache
 
 
 class DecodeSession:
-    def __init__(self, inp: Inputs, device="cuda", split_pages: int | None = None, stream=None):
+    def __init__(self, inp: Inputs, device="cuda", split_pages: int | None = None, stream=None,
+                 fused_finish: bool = True, overlap_append: bool = False):
         self.inp = inp
+        self.fused_finish = bool(fused_finish)
+        self.overlap_append = bool(overlap_append)
         self.device = torch.device(device)
         wl = inp.workload
         self.B, self.n_q = wl.batch, wl.n_q
@@ -53,17 +65,36 @@ class DecodeSession:
         self.out = torch.empty(self.B, self.n_q, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=dev)
         self.workspace = ops.alloc_workspace(self.B, self.n_q, self.max_kv_len, self.split_pages, dev)
         self.num_splits = ops.mla_decode_num_splits(self.B, self.n_q, self.max_kv_len, self.split_pages)
+        if self.overlap_append:
+            self.side = torch.cuda.Stream(device=dev)
+            self._forked = torch.cuda.Event()
+            self._appended = torch.cuda.Event()
+
+    def _main(self, stream):
+        if stream is None:
+            return torch.cuda.current_stream(self.device)
+        if isinstance(stream, torch.cuda.Stream):
+            return stream
+        return torch.cuda.ExternalStream(int(stream), device=self.device)
 
     # individual stages (the bench times them one by one)
     def append(self, stream=None):
+        if self.overlap_append:
+            self._forked.record(self._main(stream))
+            self.side.wait_event(self._forked)
+            stream = self.side
         ops.mla_append_kv(self.c_new, self.k_new, self.prior_lens, self.page_table, self.rope, self.cache,
                           stream=stream)
+        if self.overlap_append:
+            self._appended.record(self.side)
 
     def absorb(self, stream=None):
         ops.mla_absorb_q(self.q_nope, self.q_rope, self.prior_lens, self.w_uk, self.rope, self.q_abs,
                          stream=stream)
 
     def attend_partial(self, stream=None):
+        if self.overlap_append:
+            self._main(stream).wait_event(self._appended)  # the cache holds the new tokens
         ops.mla_decode_attn_partial(self.q_abs, self.cache, self.page_table, self.kv_lens, self.n_q,
                                     self.max_kv_len, self.split_pages, self.workspace, self.o_latent,
                                     self.lse, stream=stream)
@@ -75,13 +106,20 @@ class DecodeSession:
     def project_out(self, stream=None):
         ops.mla_out_absorb(self.o_latent, self.w_uv, self.out, stream=stream)
 
+    def finish(self, stream=None):
+        ops.mla_combine_out_absorb(self.B, self.n_q, self.max_kv_len, self.split_pages, self.workspace,
+                                   self.o_latent, self.w_uv, self.out, self.lse, stream=stream)
+
+    def stage_names(self) -> list[str]:
+        tail = ["finish"] if self.fused_finish else ["combine", "project_out"]
+        return ["append", "absorb", "attend_partial"] + tail
+
     def step(self, stream=None):
-        self.append(stream)
-        self.absorb(stream)
-        self.attend_partial(stream)
-        self.combine(stream)
-        self.project_out(stream)
+        for name in self.stage_names():
+            getattr(self, name)(stream)
         return self.out
 
     def launches_per_step(self) -> int:
+        if self.fused_finish:
+            return 4
         return 4 + (1 if self.num_splits > 1 else 0)

@@ -53,10 +53,10 @@ def oracle_sequence(inp: W.Inputs, b: int, heads=None):
     return O.decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, int(inp.prior_lens[b]), heads)
 
 
-def run_session(inp, split_pages=None):
+def run_session(inp, split_pages=None, **kw):
     from mla_absorbed_decode_absorb_gb300 import ops
     from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
-    s = DecodeSession(inp, split_pages=split_pages)
+    s = DecodeSession(inp, split_pages=split_pages, **kw)
     s.step()
     torch.cuda.synchronize()
     assert ops.mla_get_device_status() == ops.MLA_OK
@@ -64,6 +64,9 @@ def run_session(inp, split_pages=None):
 
 
 def check_outputs(s, inp, seqs, heads=None):
+    if s.fused_finish and s.num_splits > 1:
+        s.combine()  # the fused finish does not write the merged O'; the partials are still there
+        torch.cuda.synchronize()
     o_gpu = s.out.float().cpu().numpy()
     lat_gpu = s.o_latent.cpu().numpy()
     lse_gpu = s.lse.cpu().numpy()
@@ -120,6 +123,50 @@ def test_decode_parity_small(name, split_pages):
     check_outputs(s, inp, range(inp.batch))
 
 
+@pytest.mark.parametrize("split_pages", [0, 1, 3, 1000])
+def test_fused_finish_matches_combine_then_out_absorb(split_pages):
+    """mla_combine_out_absorb performs the merge with the same float32 operations
+    as mla_decode_combine and the product as mla_out_absorb: equal bit for bit."""
+    inp = W.generate(W.custom("fused", [0, 63, 700, 2500, 64], n_q=2), seed=6)
+    a = run_session(inp, split_pages=split_pages, fused_finish=True)
+    b = run_session(inp, split_pages=split_pages, fused_finish=False)
+    assert np.array_equal(bits(a.out), bits(b.out))
+    assert np.array_equal(a.lse.cpu().numpy().view(np.uint32), b.lse.cpu().numpy().view(np.uint32))
+
+
+def test_append_on_side_stream_matches_in_order():
+    inp = W.generate(W.custom("overlap", [10, 64, 333], n_q=3), seed=7)
+    a = run_session(inp, overlap_append=True)
+    b = run_session(inp, overlap_append=False)
+    assert np.array_equal(bits(a.cache), bits(b.cache))
+    assert np.array_equal(bits(a.out), bits(b.out))
+
+
+def test_launch_overlap_levels_give_identical_results():
+    """Programmatic dependent launch only moves prologues (and, at level 2, the
+    weight reads) ahead of the previous kernel's completion: same bits."""
+    from mla_absorbed_decode_absorb_gb300 import ops
+    inp = W.generate(W.custom("pdl", [5, 700, 4000], n_q=2), seed=8)
+    before = ops.mla_get_launch_overlap()
+    try:
+        runs = []
+        for level in (0, 1, 2):
+            ops.mla_set_launch_overlap(level)
+            assert ops.mla_get_launch_overlap() == level
+            s = run_session(inp, split_pages=3)
+            s.step()  # a second step: every launch now follows one of ours
+            torch.cuda.synchronize()
+            assert ops.mla_get_device_status() == ops.MLA_OK
+            runs.append((bits(s.q_abs), bits(s.out), s.lse.cpu().numpy().view(np.uint32), bits(s.cache)))
+        for r in runs[1:]:
+            for x, y in zip(r, runs[0]):
+                assert np.array_equal(x, y)
+        with pytest.raises(ops.MLAError):
+            ops.mla_set_launch_overlap(3)
+    finally:
+        ops.mla_set_launch_overlap(before)
+
+
 def test_split_count_invariance():
     """Split count changes only rounding: P is a bf16 MMA operand and each split
     rounds it against its own running max, so two split layouts differ by about
@@ -129,7 +176,7 @@ def test_split_count_invariance():
     ref = run_session(inp, split_pages=1000)
     assert ref.num_splits == 1
     for sp in [1, 2, 5]:
-        s = run_session(inp, split_pages=sp)
+        s = run_session(inp, split_pages=sp, fused_finish=False)
         assert s.num_splits > 1
         assert rel_l2(s.o_latent.cpu().numpy(), ref.o_latent.cpu().numpy()) < 3e-3
         assert np.abs(s.lse.cpu().numpy() - ref.lse.cpu().numpy()).max() < 2e-3
