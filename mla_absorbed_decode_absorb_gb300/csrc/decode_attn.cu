@@ -22,21 +22,28 @@
 //   * runs the same online softmax as its peer on that S, so both use identical
 //     P, running max and sum, and accumulates its half of O' = P c.
 // Half of the CTA's 256 latent query columns sit in TMEM (QK^T MMAs with A read
-// from TMEM), the other half and the RoPE columns in shared memory, which leaves
-// room for a 4-stage ring of half-pages.  P has TMEM buffers of its own, so a
-// score buffer is free as soon as the softmax has read it: QK^T of page i+1 is
-// issued while the softmax of page i is still running.
+// from TMEM), the other half and the RoPE columns in shared memory.
 //
-// Warp roles: warp 0 issues TMA loads (page ids are read 32 at a time), warp 1 allocates TMEM and issues tcgen05.mma (QK^T into one of two
-// TMEM score buffers; P V with P read from TMEM), warps 6-9 are the exchange
-// warpgroup (query into TMEM at start; per page: read the partial scores, swap
-// them with the peer, write the full scores back into TMEM), warps 2-5 are the
-// softmax/epilogue warpgroup, and warp 10 re-arms each exchange buffer once it
-// has been read and tells the peer (a cluster-scope release that would
-// otherwise stall the exchange warpgroup).  Both warpgroups have one thread per head row, and
-// the exchange for page i+1 overlaps the softmax of page i.  The softmax keeps a
-// lazily updated reference max: O' in TMEM is rescaled only when a page raises a
-// row's max by more than 2^8.
+// Pages land in a ring of four 64-token slots stored chunk by chunk (all slots'
+// rows of one 64-column chunk are contiguous), so two consecutive slots form one
+// 128-token operand: QK^T is issued per tile of two pages with N = 128, which
+// keeps the tensor pipe at its full rate (N = 64 runs it at about half), while
+// P V stays per page (N = 256).
+//
+// Warp roles: warp 0 issues TMA loads (page ids are read 32 at a time); warp 1
+// allocates TMEM and one of its threads issues tcgen05.mma, polling its
+// barriers so that P V of a page whose P is ready goes out first (it releases a
+// slot) and QK^T of a landed tile otherwise; warps 2-9 are two row warpgroups,
+// one thread per head row, and warpgroup g handles the pages i = g (mod 2), i.e.
+// the score columns [64g, 64g + 64) of each tile: it reads its partial scores
+// from TMEM, swaps them with the peer CTA, adds them, runs the softmax step and
+// writes P(i) into its own TMEM P buffer.  The two warpgroups pass only the
+// running reference max to each other, so the exchange of page i + 1 overlaps
+// the softmax of page i.  Warp 10 re-arms each exchange buffer once it has been
+// read and tells the peer (a cluster-scope release that would otherwise stall a
+// row warpgroup).  The reference max is updated lazily: O' in TMEM is rescaled
+// only when a page raises a row's max by more than 2^8; each warpgroup keeps
+// its own partial row sum relative to the max it last used.
 #include "sm100.cuh"
 #include "tmap.cuh"
 
@@ -45,53 +52,65 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 4;
+constexpr int kSlots = 4;           // 64-token page slots: two tiles of two pages
 constexpr int kThreads = 352;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kExchangeWarp0 = 6;
+constexpr int kRowWarp0 = 2;        // warps 2-5: row warpgroup 0, warps 6-9: row warpgroup 1
 constexpr int kSignalWarp = 10;
 constexpr int kRowThreads = 128;    // threads of each row warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O' half: [0, 256)
-constexpr uint32_t kTmemS = 256;    // two score buffers: [256, 320), [320, 384)
-constexpr uint32_t kTmemP = 384;    // two P buffers (64 bf16 per row = 32 columns): [384, 416), [416, 448)
+constexpr uint32_t kTmemS = 256;    // tile scores, page g of the tile in [256 + 64g, 320 + 64g)
+constexpr uint32_t kTmemP = 384;    // P of warpgroup g (64 bf16 per row = 32 columns): [384 + 32g, 416 + 32g)
 constexpr uint32_t kTmemQ = 448;    // the CTA's first 128 latent query columns as bf16 pairs: [448, 512)
 
 constexpr int kQChunk = 128 * 128;    // 64 latent query columns x 128 heads, 128-byte rows (SW128)
 constexpr int kQRope = 128 * 64;      // 32 RoPE columns x 128 heads, 64-byte rows (SW64)
 constexpr int kQBytes = 2 * kQChunk + kQRope;  // query columns kept in shared memory
-constexpr int kPChunk = 64 * 128;     // 64 latent columns x 64 tokens (SW128)
-constexpr int kPRope = 64 * 64;       // 32 RoPE columns x 64 tokens (SW64)
-constexpr int kStageBytes = 4 * kPChunk + kPRope;
-constexpr int kXRowBytes = 144;       // 64 fp16 scores + 16 B pad: conflict-free 16-byte accesses
-constexpr int kXBufBytes = kRowThreads * kXRowBytes;
-constexpr uint32_t kXTxBytes = kRowThreads * 128;
-constexpr float kXScale = 1.f / 256.f;  // exchanged partial scores are fp16(S_r * 2^-8)
-constexpr float kXUnscale = 256.f;
+constexpr int kSlotChunk = 64 * 128;  // one page's 64 latent columns (SW128 rows of 128 B)
+constexpr int kSlotRope = 64 * 64;    // one page's 32 RoPE columns (SW64 rows of 64 B)
+constexpr int kChunkRing = kSlots * kSlotChunk;  // stride between the four latent chunks of the ring
+constexpr int kRingBytes = 4 * kChunkRing + kSlots * kSlotRope;
+constexpr uint32_t kPageTx = 4 * kSlotChunk + kSlotRope;  // bytes of one page's TMA loads
+// Exchange buffer: 64 fp16 partial scores per row, stored unit-major (16-byte unit
+// q of row r at q * 2048 + r * 16), so that each warp's stores and loads of one
+// unit cover 512 contiguous bytes: whole 128-byte lines, which matters because
+// the SS MMAs of QK^T want nearly all of the shared-memory bandwidth.
+constexpr int kXBufBytes = kRowThreads * 128;
+constexpr uint32_t kXTxBytes = kXBufBytes;
+// Exchanged partial scores are fp16(S_r * 2^-8); their fp32 sum times 2^8 kScale
+// is the scaled score, so the softmax folds 2^8 into its log2-domain scale.
+constexpr float kXScale = 1.f / 256.f;
+constexpr float kSumScaleLog2 = kScaleLog2 * 256.f;
 
 constexpr int kOffQ = 0;
-constexpr int kOffStage = kOffQ + kQBytes;
-constexpr int kOffX = kOffStage + kStages * kStageBytes;
+constexpr int kOffRing = kOffQ + kQBytes;
+constexpr int kOffRope = kOffRing + 4 * kChunkRing;
+constexpr int kOffX = kOffRing + kRingBytes;
 constexpr int kOffBar = kOffX + 2 * kXBufBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers + 1 KB alignment slack
+constexpr int kOffMax = kOffBar + 256;          // per-row reference max handed between warpgroups
+constexpr int kOffFin = kOffMax + 4 * kHeads;     // per-warpgroup (max, sum) per row at the end
+constexpr int kSmemBytes = kOffFin + 8 * 2 * kHeads + 1024;  // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffRing % 1024 == 0 && kOffRope % 1024 == 0, "swizzled tiles start on 1 KB");
 
 constexpr float kRescaleLog2 = 8.f;
 
 struct Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
-  uint64_t q_full;      // query columns in shared memory
-  uint64_t q_tmem;      // latent query columns in TMEM
-  uint64_t s_full[2];   // partial scores of this CTA are in TMEM
-  uint64_t s_ready[2];  // full scores are in TMEM
-  uint64_t s_free[2];   // the softmax has read the full scores of this buffer
-  uint64_t p_full[2];
-  uint64_t pv_done;
-  uint64_t x_full[2];   // peer's partial scores landed in exchange buffer k
-  uint64_t x_free[2];   // peer has read our partial scores from its buffer k
-  uint64_t x_read[2];   // all rows have read exchange buffer k
+  uint64_t full[kSlots];   // page landed in the slot
+  uint64_t empty[kSlots];  // P V of the slot's page has finished
+  uint64_t q_full;         // query columns in shared memory
+  uint64_t q_tmem;         // latent query columns in TMEM
+  uint64_t s_full;         // partial scores of the current tile are in TMEM
+  uint64_t s_free;         // both warpgroups have read them
+  uint64_t p_full[2];      // P of warpgroup g's current page is in its TMEM buffer
+  uint64_t pv_done[2];     // P V of the last page of warpgroup g has finished
+  uint64_t x_full[2];      // peer's partial scores landed in exchange buffer g
+  uint64_t x_free[2];      // peer has read our partial scores from its buffer g
+  uint64_t x_read[2];      // all rows of warpgroup g have read exchange buffer g
+  uint64_t hand[2];        // warpgroup g has published the reference max of its page
+  uint64_t fin;            // both warpgroups have published their final (max, sum)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -133,22 +152,23 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
   const int b = bj / p.n_q, j = bj % p.n_q;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kSlots; ++s) {
       mbar_init(bar_addr(bars.full[s]), 1);
       mbar_init(bar_addr(bars.empty[s]), 1);
     }
     mbar_init(bar_addr(bars.q_full), 1);
-    mbar_init(bar_addr(bars.q_tmem), kRowThreads);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_addr(bars.s_full[s]), 1);
-      mbar_init(bar_addr(bars.s_ready[s]), kRowThreads);
-      mbar_init(bar_addr(bars.s_free[s]), kRowThreads);
-      mbar_init(bar_addr(bars.p_full[s]), kRowThreads);
-      mbar_init(bar_addr(bars.x_full[s]), 1);
-      mbar_init(bar_addr(bars.x_free[s]), 1);
-      mbar_init(bar_addr(bars.x_read[s]), kRowThreads);
+    mbar_init(bar_addr(bars.q_tmem), 2 * kRowThreads);
+    mbar_init(bar_addr(bars.s_full), 1);
+    mbar_init(bar_addr(bars.s_free), 2 * kRowThreads);
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(bar_addr(bars.p_full[g]), kRowThreads);
+      mbar_init(bar_addr(bars.pv_done[g]), 1);
+      mbar_init(bar_addr(bars.x_full[g]), 1);
+      mbar_init(bar_addr(bars.x_free[g]), 1);
+      mbar_init(bar_addr(bars.x_read[g]), kRowThreads);
+      mbar_init(bar_addr(bars.hand[g]), kRowThreads);
     }
-    mbar_init(bar_addr(bars.pv_done), 1);
+    mbar_init(bar_addr(bars.fin), 2 * kRowThreads);
     mbar_init(bar_addr(bars.drain), 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -204,19 +224,19 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
           const int i = base + k;
           int page = __shfl_sync(0xffffffffu, ids, k);
           if (lane == 0) {
-            const int s = i % kStages;
-            ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
+            const int s = i % kSlots;
+            ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kSlots) & 1) ^ 1, p.status, abort);
             if (ok) {
               if (page < 0 || page >= p.num_pages) {
                 record_status(p.status, MLA_ERR_BOUNDS);
                 page = 0;  // stay in bounds; the result of this unit is not meaningful
               }
-              const uint32_t sb = smem_u32(smem + kOffStage + s * kStageBytes);
               const uint32_t fb = bar_addr(bars.full[s]);
-              mbar_arrive_expect_tx(fb, kStageBytes);
+              mbar_arrive_expect_tx(fb, kPageTx);
               for (int c = 0; c < 4; ++c)
-                tma_load_2d(sb + c * kPChunk, &tm_c128, 64 * (4 * rank + c), page * kPage, fb);
-              tma_load_2d(sb + 4 * kPChunk, &tm_c64, kLatent + 32 * rank, page * kPage, fb);
+                tma_load_2d(smem_u32(smem + kOffRing + c * kChunkRing + s * kSlotChunk), &tm_c128,
+                            64 * (4 * rank + c), page * kPage, fb);
+              tma_load_2d(smem_u32(smem + kOffRope + s * kSlotRope), &tm_c64, kLatent + 32 * rank, page * kPage, fb);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -227,138 +247,144 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
-    if (n_pages > 0) {
-      const uint32_t idesc_qk = idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
+    // One thread schedules and issues everything; the rest of the warp waits.
+    if (n_pages > 0 && lane == 0) {
+      const int n_tiles = (n_pages + 1) >> 1;
+      const uint32_t idesc_qk2 = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/0);  // two-page tile
+      const uint32_t idesc_qk1 = idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);   // last tile of an odd count
       const uint32_t idesc_pv = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/1);
-      // Descriptors of stage 0 and of the query in shared memory; a stage, chunk
-      // or K step is a byte offset added to the start-address field (16-byte units).
-      const uint32_t st0 = smem_u32(smem + kOffStage);
-      const uint64_t d_k128 = smem_desc(st0, 16, 1024, kSw128);             // keys, latent chunk 0
-      const uint64_t d_k64 = smem_desc(st0 + 4 * kPChunk, 16, 512, kSw64);  // keys, RoPE half
-      const uint64_t d_v = smem_desc(st0, kPChunk, 1024, kSw128);           // values (MN-major)
+      // Descriptors at the ring's origin; a slot, chunk or K step is a byte
+      // offset added to the start-address field (16-byte units).
+      const uint64_t d_k = smem_desc(smem_u32(smem + kOffRing), 16, 1024, kSw128);          // keys, latent
+      const uint64_t d_kr = smem_desc(smem_u32(smem + kOffRope), 16, 512, kSw64);           // keys, RoPE half
+      const uint64_t d_v = smem_desc(smem_u32(smem + kOffRing), kChunkRing, 1024, kSw128);  // values (MN-major)
       const uint64_t d_ql = smem_desc(smem_u32(smem + kOffQ), 16, 1024, kSw128);               // query chunks 2, 3
       const uint64_t d_qr = smem_desc(smem_u32(smem + kOffQ + 2 * kQChunk), 16, 512, kSw64);   // query RoPE half
-      const int last_rows = t_end - (page_begin + n_pages - 1) * kPage;  // valid rows of the last page
-      bool ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.q_full), 0, p.status, abort) &&
-                                            mbar_wait(bar_addr(bars.q_tmem), 0, p.status, abort));
+      bool ok = mbar_wait(bar_addr(bars.q_full), 0, p.status, abort) &&
+                mbar_wait(bar_addr(bars.q_tmem), 0, p.status, abort);
 
-      // S(i) = Q K(i)^T into score buffer i & 1, once page i has landed and the
-      // softmax has read the scores of page i - 2 from that buffer.
-      auto issue_qk = [&](int i) -> bool {
-        const int s = i % kStages, buf = i & 1;
-        bool w = mbar_wait(bar_addr(bars.full[s]), (i / kStages) & 1, p.status, abort);
-        w = w && mbar_wait(bar_addr(bars.s_free[buf]), ((i >> 1) & 1) ^ 1, p.status, abort);
-        if (!__all_sync(0xffffffffu, w)) return false;
-        uint8_t* stage = smem + kOffStage + s * kStageBytes;
-        if (i == n_pages - 1 && last_rows < kPage) {
-          // Rows past the last visible token may hold anything (NaN in unwritten
-          // slots); zero their latent columns so P = 0 there cannot make 0 * NaN.
-          const int nrow = kPage - last_rows;
-          for (int v = lane; v < 4 * nrow * 8; v += 32) {
-            const int c = v / (nrow * 8), r = last_rows + (v / 8) % nrow, u = v & 7;
-            *reinterpret_cast<uint4*>(stage + c * kPChunk + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+      // S(u) = Q K(u)^T for the tile of pages 2u, 2u + 1 (slots 2(u % 2), +1).
+      auto issue_qk = [&](int u) {
+        tc_fence_after();
+        const int s0 = 2 * (u & 1);
+        const uint32_t idesc = 2 * u + 1 < n_pages ? idesc_qk2 : idesc_qk1;
+        const uint64_t so = static_cast<uint64_t>((s0 * kSlotChunk) >> 4);
+        const uint64_t sr = static_cast<uint64_t>((s0 * kSlotRope) >> 4);
+        const uint32_t d = tmem + kTmemS;
+        // latent chunks 0, 1: A = query columns in TMEM (8 columns per K step of 16)
+        mma_ts(d, tmem + kTmemQ, d_k + so, idesc, 0u);
+#pragma unroll
+        for (int k = 1; k < 8; ++k)
+          mma_ts(d, tmem + kTmemQ + 8 * k, d_k + so + (k >> 2) * (kChunkRing >> 4) + (k & 3) * 2, idesc, 1u);
+        // latent chunks 2, 3: A = query columns in shared memory
+#pragma unroll
+        for (int k = 8; k < 16; ++k)
+          mma_ss(d, d_ql + ((k - 8) >> 2) * (kQChunk >> 4) + (k & 3) * 2,
+                 d_k + so + (k >> 2) * (kChunkRing >> 4) + (k & 3) * 2, idesc, 1u);
+        // RoPE part
+        mma_ss(d, d_qr, d_kr + sr, idesc, 1u);
+        mma_ss(d, d_qr + 2, d_kr + sr + 2, idesc, 1u);
+        mma_commit(bar_addr(bars.s_full));
+      };
+      // O' += P(i) V(i); then page i's slot goes back to the producer and
+      // warpgroup i & 1 may reuse its P buffer.
+      auto issue_pv = [&](int i) {
+        tc_fence_after();
+        const int s = i % kSlots;
+        const uint64_t vb = d_v + static_cast<uint64_t>((s * kSlotChunk) >> 4);
+        const uint32_t a = tmem + kTmemP + (i & 1) * 32;
+        mma_ts(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
+#pragma unroll
+        for (int k = 1; k < 4; ++k) mma_ts(tmem + kTmemO, a + 8 * k, vb + 128 * k, idesc_pv, 1u);
+        mma_commit(bar_addr(bars.empty[s]));
+        mma_commit(bar_addr(bars.pv_done[i & 1]));
+      };
+
+      // Poll: P V of page np once its P is written; otherwise QK^T of tile nq
+      // once its pages have landed and both warpgroups have read the scores of
+      // tile nq - 1.  The tensor pipe runs them in issue order.
+      int nq = 0, np = 0;
+      uint64_t t0 = 0;
+      uint32_t idle = 0;
+      while (ok && np < n_pages) {
+        if (np < 2 * nq && mbar_test(bar_addr(bars.p_full[np & 1]), (np >> 1) & 1)) {
+          issue_pv(np++);
+          idle = 0;
+          continue;
+        }
+        if (nq < n_tiles && mbar_test(bar_addr(bars.full[(2 * nq) % kSlots]), ((2 * nq) / kSlots) & 1) &&
+            (2 * nq + 1 >= n_pages ||
+             mbar_test(bar_addr(bars.full[(2 * nq + 1) % kSlots]), ((2 * nq + 1) / kSlots) & 1)) &&
+            (nq == 0 || mbar_test(bar_addr(bars.s_free), (nq - 1) & 1))) {
+          issue_qk(nq++);
+          idle = 0;
+          continue;
+        }
+        // bounded: give up (and make every other waiter give up) after kWaitNs
+        if (idle == 0) t0 = globaltimer_ns();
+        if ((++idle & 63u) == 0) {
+          if (*abort) {
+            ok = false;
+          } else if (globaltimer_ns() - t0 > kWaitNs) {
+            record_status(p.status, MLA_ERR_TIMEOUT);
+            *abort = 1;
+            ok = false;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
         }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
-          const uint32_t d = tmem + kTmemS + buf * 64;
-          // latent chunks 0, 1: A = query columns in TMEM (8 columns per K step of 16)
-          mma_ts(d, tmem + kTmemQ, d_k128 + so, idesc_qk, 0u);
-#pragma unroll
-          for (int k = 1; k < 8; ++k)
-            mma_ts(d, tmem + kTmemQ + 8 * k, d_k128 + so + (k >> 2) * (kPChunk >> 4) + (k & 3) * 2, idesc_qk, 1u);
-          // latent chunks 2, 3: A = query columns in shared memory
-#pragma unroll
-          for (int k = 8; k < 16; ++k)
-            mma_ss(d, d_ql + ((k - 8) >> 2) * (kQChunk >> 4) + (k & 3) * 2,
-                   d_k128 + so + (k >> 2) * (kPChunk >> 4) + (k & 3) * 2, idesc_qk, 1u);
-          // RoPE part
-          mma_ss(d, d_qr, d_k64 + so, idesc_qk, 1u);
-          mma_ss(d, d_qr + 2, d_k64 + so + 2, idesc_qk, 1u);
-          mma_commit(bar_addr(bars.s_full[buf]));
-        }
-        __syncwarp();
-        return true;
-      };
-      // O' += P(i) V(i), then page i's stage goes back to the producer.
-      auto issue_pv = [&](int i) -> bool {
-        const bool w = mbar_wait(bar_addr(bars.p_full[i & 1]), (i >> 1) & 1, p.status, abort);
-        if (!__all_sync(0xffffffffu, w)) return false;
-        tc_fence_after();
-        if (lane == 0) {
-          const uint64_t vb = d_v + static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
-          const uint32_t a = tmem + kTmemP + (i & 1) * 32;
-          mma_ts(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
-#pragma unroll
-          for (int k = 1; k < 4; ++k) mma_ts(tmem + kTmemO, a + 8 * k, vb + 128 * k, idesc_pv, 1u);
-          mma_commit(bar_addr(bars.empty[i % kStages]));
-          mma_commit(bar_addr(bars.pv_done));
-        }
-        __syncwarp();
-        return true;
-      };
-
-      // QK^T runs two pages ahead of P V: S(i + 2) only needs the softmax to have
-      // read S(i), while P V(i) needs the whole softmax of page i.
-      if (ok) ok = issue_qk(0);
-      if (ok && n_pages > 1) ok = issue_qk(1);
-      for (int i = 0; i < n_pages && ok; ++i) {
-        if (i + 2 < n_pages) ok = issue_qk(i + 2);
-        if (ok) ok = issue_pv(i);
       }
       // no tcgen05 operation may still be running when TMEM is released
-      if (lane == 0) mma_commit(bar_addr(bars.drain));
-      __syncwarp();
+      mma_commit(bar_addr(bars.drain));
       mbar_wait(bar_addr(bars.drain), 0, p.status, nullptr);
     }
+    __syncwarp();
   } else if (warp == kSignalWarp) {
     // ------------------------------------------------------------ exchange buffer recycling
     if (lane == 0) {
       for (int i = 0; i < n_pages; ++i) {
-        const int buf = i & 1;
-        if (!mbar_wait(bar_addr(bars.x_read[buf]), (i >> 1) & 1, p.status, abort)) break;
-        mbar_arrive_expect_tx(bar_addr(bars.x_full[buf]), kXTxBytes);   // armed for the buffer's next use
-        mbar_arrive_remote(mapa(bar_addr(bars.x_free[buf]), peer));      // the peer may refill it
+        const int g = i & 1;
+        if (!mbar_wait(bar_addr(bars.x_read[g]), (i >> 1) & 1, p.status, abort)) break;
+        mbar_arrive_expect_tx(bar_addr(bars.x_full[g]), kXTxBytes);   // armed for the buffer's next use
+        mbar_arrive_remote(mapa(bar_addr(bars.x_free[g]), peer));      // the peer may refill it
       }
     }
-  } else if (warp >= kExchangeWarp0) {
-    // ------------------------------------------------------------ score exchange
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;  // head
+  } else {
+    // ------------------------------------------------------------ row warpgroups
+    const int g = (warp - kRowWarp0) >> 2;  // warpgroup: pages i = g (mod 2)
+    const int quad = warp & 3;               // TMEM lane quarter this warp may access
+    const int row = quad * 32 + lane;        // head
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    float* m_slot = reinterpret_cast<float*>(smem + kOffMax) + row;
+    float2* fin = reinterpret_cast<float2*>(smem + kOffFin);
     bool ok = n_pages > 0;
     if (ok) {
-      // this CTA's first 128 latent query columns of the row into TMEM as bf16 pairs
+      // latent query columns [256r + 64g, 256r + 64g + 64) of the row into TMEM as bf16 pairs
       const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<int64_t>(bj) * kHeads + row) * kRow +
-                                                         256 * rank);
-#pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t w[32];
+                                                         256 * rank + 64 * g);
+      uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = qsrc[c0 / 4 + q];
-          w[4 * q] = v.x;
-          w[4 * q + 1] = v.y;
-          w[4 * q + 2] = v.z;
-          w[4 * q + 3] = v.w;
-        }
-        tmem_st32(tmem + lane_off + kTmemQ + c0, w);
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = qsrc[q];
+        w[4 * q] = v.x;
+        w[4 * q + 1] = v.y;
+        w[4 * q + 2] = v.z;
+        w[4 * q + 3] = v.w;
       }
+      tmem_st32(tmem + lane_off + kTmemQ + 32 * g, w);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(bars.q_tmem));
     }
-    uint8_t* xrow0 = smem + kOffX + row * kXRowBytes;
-    const uint32_t x_remote0 = mapa(smem_u32(xrow0), peer);
+    // exchange buffer g, this row: 16-byte unit q at q * 2048 + row * 16
+    uint8_t* xrow = smem + kOffX + g * kXBufBytes + row * 16;
+    const uint32_t x_remote = mapa(smem_u32(xrow), peer);
+    const uint32_t xfull_remote = mapa(bar_addr(bars.x_full[g]), peer);
+    const uint32_t s_addr = tmem + lane_off + kTmemS + 64 * g;  // this warpgroup's page of each tile
     float range_max = 0.f;
-    for (int i = 0; i < n_pages && ok; ++i) {
-      const int buf = i & 1;        // TMEM score buffer and exchange buffer
+    float m_mine = -INFINITY, l = 0.f;  // reference max this warpgroup last used, and its partial sum
+    for (int i = g; i < n_pages && ok; i += 2) {
       const uint32_t use = (i >> 1) & 1;
-      const uint32_t s_addr = tmem + lane_off + kTmemS + buf * 64;
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[buf]), use, p.status, abort));
+      const int n_valid = min(kPage, t_end - (page_begin + i) * kPage);  // visible tokens of the page
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full), use, p.status, abort));
       if (!ok) break;
       tc_fence_after();
       uint32_t mine[32];
@@ -367,147 +393,156 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
         tmem_ld32(s_addr, a);
         tmem_ld32(s_addr + 32, c);
         tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(bar_addr(bars.s_free));  // QK^T of the next tile may overwrite the buffer
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           const float x0 = __uint_as_float(a[2 * q]), x1 = __uint_as_float(a[2 * q + 1]);
           const float y0 = __uint_as_float(c[2 * q]), y1 = __uint_as_float(c[2 * q + 1]);
-          range_max = fmaxf(range_max, fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(y0), fabsf(y1))));
           mine[q] = pack_f16x2(x0 * kXScale, x1 * kXScale);
           mine[16 + q] = pack_f16x2(y0 * kXScale, y1 * kXScale);
         }
-      }
-      // send: wait until the peer has read what we sent into this buffer two pages ago
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free[buf]), use ^ 1u, p.status, abort));
-      if (!ok) break;
-      const uint32_t x_remote = x_remote0 + buf * kXBufBytes;
-      const uint32_t xfull_remote = mapa(bar_addr(bars.x_full[buf]), peer);
+        // magnitude of the visible partial scores (rows past the last token may hold anything)
+        if (n_valid == kPage) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        st_async_v4(x_remote + 16 * q, mine[4 * q], mine[4 * q + 1], mine[4 * q + 2], mine[4 * q + 3], xfull_remote);
-      // receive the peer's partial scores; both CTAs add fp16(S_0) + fp16(S_1) in fp32
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full[buf]), use, p.status, abort));
-      if (!ok) break;
-      uint32_t full0[32], full1[32];
-      {
-        const uint4* xr = reinterpret_cast<const uint4*>(xrow0 + buf * kXBufBytes);
+          for (int q = 0; q < 32; ++q)
+            range_max = fmaxf(range_max, fmaxf(fabsf(__uint_as_float(a[q])), fabsf(__uint_as_float(c[q]))));
+        } else {
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = xr[q];
-          const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int w = 4 * q + e;  // packed word index: columns 2w, 2w+1
-            const float2 a = unpack_f16x2(mine[w]);
-            const float2 c = unpack_f16x2(pw[e]);
-            const uint32_t lo = __float_as_uint((a.x + c.x) * kXUnscale);
-            const uint32_t hi = __float_as_uint((a.y + c.y) * kXUnscale);
-            if (w < 16) {
-              full0[2 * w] = lo;
-              full0[2 * w + 1] = hi;
-            } else {
-              full1[2 * (w - 16)] = lo;
-              full1[2 * (w - 16) + 1] = hi;
-            }
+          for (int q = 0; q < 32; ++q) {
+            if (q < n_valid) range_max = fmaxf(range_max, fabsf(__uint_as_float(a[q])));
+            if (q + 32 < n_valid) range_max = fmaxf(range_max, fabsf(__uint_as_float(c[q])));
           }
         }
       }
-      tmem_st32(s_addr, full0);
-      tmem_st32(s_addr + 32, full1);
+      // send: wait until the peer has read what this warpgroup sent two pages ago
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free[g]), use ^ 1u, p.status, abort));
+      if (!ok) break;
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        st_async_v4(x_remote + q * (kRowThreads * 16), mine[4 * q], mine[4 * q + 1], mine[4 * q + 2], mine[4 * q + 3],
+                    xfull_remote);
+      // receive the peer's partial scores; both CTAs add fp16(S_0) + fp16(S_1) in fp32
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full[g]), use, p.status, abort));
+      if (!ok) break;
+      float sv[64];  // S * 2^-8
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = *reinterpret_cast<const uint4*>(xrow + q * (kRowThreads * 16));
+        const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int w = 4 * q + e;  // packed word index: columns 2w, 2w+1
+          const float2 x = unpack_f16x2(mine[w]);
+          const float2 y = unpack_f16x2(pw[e]);
+          sv[2 * w] = x.x + y.x;
+          sv[2 * w + 1] = x.y + y.y;
+        }
+      }
+      mbar_arrive(bar_addr(bars.x_read[g]));  // warp 10 recycles the exchange buffer
+      // row max over the visible tokens (the scale is positive), log2 domain
+      float mx = -INFINITY;
+      if (n_valid == kPage) {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sv[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c)
+          if (c < n_valid) mx = fmaxf(mx, sv[c]);
+      }
+      mx *= kSumScaleLog2;
+      // the reference max after page i - 1 (from the other warpgroup)
+      bool rescale = false;
+      float factor = 1.f;
+      if (i == 0) {
+        m_mine = mx;
+      } else {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.hand[g ^ 1]), ((i - 1) >> 1) & 1, p.status, abort));
+        if (!ok) break;
+        const float m_prev = *m_slot;
+        if (m_prev != m_mine) {  // raised since this warpgroup's last page
+          l *= ex2_approx(m_mine - m_prev);
+          m_mine = m_prev;
+        }
+        if (mx > m_mine + kRescaleLog2) {
+          factor = ex2_approx(m_mine - mx);
+          m_mine = mx;
+          l *= factor;
+          rescale = true;
+        }
+      }
+      *m_slot = m_mine;
+      mbar_arrive(bar_addr(bars.hand[g]));  // page i + 1 may start its softmax
+      const float neg_m = -m_mine;
+      uint32_t pk[32];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        float p0 = ex2_approx(fmaf(sv[2 * c], kSumScaleLog2, neg_m));
+        float p1 = ex2_approx(fmaf(sv[2 * c + 1], kSumScaleLog2, neg_m));
+        if (2 * c >= n_valid) p0 = 0.f;
+        if (2 * c + 1 >= n_valid) p1 = 0.f;
+        pk[c] = pack_bf16x2(p0, p1);
+        sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+      }
+      l += sum;
+      if (n_valid < kPage) {
+        // Value rows past the last visible token may hold anything (NaN in
+        // unwritten slots): zero them so that P = 0 there cannot make 0 * NaN.
+        uint8_t* slot = smem + kOffRing + (i % kSlots) * kSlotChunk;
+        const int nrow = kPage - n_valid;
+        for (int v = row; v < 4 * nrow * 8; v += kRowThreads) {
+          const int c = v / (nrow * 8), r = n_valid + (v / 8) % nrow, u = v & 7;
+          *reinterpret_cast<uint4*>(slot + c * kChunkRing + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+      }
+      // O' may only be rescaled once P V(i - 1) has finished; the P buffer is
+      // free once P V(i - 2) has.
+      if (__any_sync(0xffffffffu, rescale)) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[g ^ 1]), ((i - 1) >> 1) & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + kTmemO + c0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
+          tmem_st32(tmem + lane_off + kTmemO + c0, r);
+        }
+      }
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[g]), use ^ 1u, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      tmem_st32(tmem + lane_off + kTmemP + g * 32, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar_addr(bars.s_ready[buf]));
-      // this row is done with the exchange buffer (warp 10 recycles it)
-      mbar_arrive(bar_addr(bars.x_read[buf]));
+      mbar_arrive(bar_addr(bars.p_full[g]));
     }
     // exchanged partials are fp16(S_r / 256): beyond this magnitude they overflow
     if (range_max > 1.6e7f) record_status(p.status, MLA_ERR_RANGE);
-  } else {
-    // ------------------------------------------------------------ softmax + epilogue
-    const int quad = warp & 3;
-    const int row = quad * 32 + lane;  // head
-    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int64_t out_row = (static_cast<int64_t>(bj) * p.num_splits + split) * kHeads + row;
-    float* orow = p.o_out + out_row * kLatent + rank * 256;
-    float m_ref = -INFINITY, l = 0.f;
-    bool ok = n_pages > 0;
 
+    // epilogue: combine the two warpgroups' sums, then warpgroup g writes
+    // columns [128g, 128g + 128) of this CTA's half of O' (normalised)
+    fin[g * kHeads + row] = make_float2(m_mine, l);
+    mbar_arrive(bar_addr(bars.fin));
+    ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.fin), 0, p.status, abort));
+    const int last = n_pages - 1;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[last & 1]), (last >> 1) & 1, p.status, abort));
+    tc_fence_after();
+    const int64_t out_row = (static_cast<int64_t>(bj) * p.num_splits + split) * kHeads + row;
+    float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
     if (ok) {
-      for (int i = 0; i < n_pages && ok; ++i) {
-        const int buf = i & 1;
-        const uint32_t s_addr = tmem + lane_off + kTmemS + buf * 64;
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_ready[buf]), (i >> 1) & 1, p.status, abort));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t sv[64];
-        tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_wait_ld();
-        tc_fence_before();
-        mbar_arrive(bar_addr(bars.s_free[buf]));  // the MMA issuer may overwrite this buffer
-        // raw-score row max over the visible tokens (the scale is positive)
-        const int n_valid = min(kPage, t_end - (page_begin + i) * kPage);
-        float mx = -INFINITY;
-        if (n_valid == kPage) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c < n_valid) mx = fmaxf(mx, __uint_as_float(sv[c]));
-        }
-        mx *= kScaleLog2;
-        float factor = 1.f;
-        bool rescale = false;
-        if (i == 0) {
-          m_ref = mx;
-        } else if (mx > m_ref + kRescaleLog2) {
-          factor = ex2_approx(m_ref - mx);
-          m_ref = mx;
-          rescale = true;
-        }
-        const float neg_m = -m_ref;
-        uint32_t pk[32];
-        float sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * c]), kScaleLog2, neg_m));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * c + 1]), kScaleLog2, neg_m));
-          if (2 * c >= n_valid) p0 = 0.f;
-          if (2 * c + 1 >= n_valid) p1 = 0.f;
-          pk[c] = pack_bf16x2(p0, p1);
-          sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
-        }
-        l = l * factor + sum;
-        // O' may only be touched once the previous P V has finished
-        if (i >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done), (i - 1) & 1, p.status, abort));
-          if (!ok) break;
-          tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-          for (int c0 = 0; c0 < 256; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_off + kTmemO + c0, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
-            tmem_st32(tmem + lane_off + kTmemO + c0, r);
-          }
-        }
-        tmem_st32(tmem + lane_off + kTmemP + buf * 32, pk);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar_addr(bars.p_full[buf]));
-      }
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done), (n_pages - 1) & 1, p.status, abort));
-      tc_fence_after();
-    }
-    // epilogue: this CTA's 256 columns of O' (normalised) and the row's log-sum-exp
-    if (ok) {
-      const float inv = 1.f / l;
-      for (int c0 = 0; c0 < 256; c0 += 32) {
+      const float2 f0 = fin[row], f1 = fin[kHeads + row];
+      const float m = fmaxf(f0.x, f1.x);
+      const float lt = (f0.y > 0.f ? f0.y * ex2_approx(f0.x - m) : 0.f) + (f1.y > 0.f ? f1.y * ex2_approx(f1.x - m) : 0.f);
+      const float inv = 1.f / lt;
+      for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kTmemO + c0, r);
+        tmem_ld32(tmem + lane_off + kTmemO + 128 * g + c0, r);
         tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -515,10 +550,10 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
               make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
                           __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
       }
-      if (rank == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m_ref + log2f(l)) * kLn2;
+      if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
     } else {
-      for (int c0 = 0; c0 < 256; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (rank == 0 && p.lse_out != nullptr) p.lse_out[out_row] = -INFINITY;
+      for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = -INFINITY;
     }
   }
 
