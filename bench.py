@@ -331,10 +331,9 @@ def run_ours(args, wl):
     # end to end: inputs from pinned host memory, output back to host, inside the timed region
     e2e = None
     if not args.no_e2e:
-        host_in = [x.cpu().pin_memory() for x in (s.c_new, s.k_new, s.q_nope, s.q_rope, s.prior_lens, s.kv_lens)]
-        dev_in = [s.c_new, s.k_new, s.q_nope, s.q_rope, s.prior_lens, s.kv_lens]
+        host_in = s.host_step_buffer(pin=True)   # all of this step's inputs, one packed buffer
         host_out = torch.empty(s.out.shape, dtype=s.out.dtype).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        h2d = host_in.numel()
         d2h = host_out.numel() * host_out.element_size()
         K2 = min(K, 200)
         e2e_ms = []
@@ -342,8 +341,7 @@ def run_ours(args, wl):
             flush.zero_()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            for h, d in zip(host_in, dev_in):
-                d.copy_(h, non_blocking=True)
+            s.step_buffer.copy_(host_in, non_blocking=True)
             s.step()
             host_out.copy_(s.out, non_blocking=True)
             b.record(stream)

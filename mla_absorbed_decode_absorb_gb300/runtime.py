@@ -44,8 +44,11 @@ class DecodeSession:
         self.w_uk = inp.w_uk.to(dev)
         self.w_uv = inp.w_uv.to(dev)
         self.page_table = inp.page_table.to(dev)
-        self.prior_lens = inp.prior_lens.to(dev)
-        self.kv_lens = inp.kv_lens.to(dev)
+        # this step's inputs live in one device buffer (typed views into it), so that
+        # a caller uploads them with a single copy (see host_step_buffer)
+        c_new, k_new = inp.new_tokens()
+        self._pack_step_inputs([("c_new", c_new), ("k_new", k_new), ("q_nope", inp.q_nope),
+                                ("q_rope", inp.q_rope), ("prior_lens", inp.prior_lens), ("kv_lens", inp.kv_lens)])
         self.cache = empty_cache(inp.num_pages, dev)
         zero = torch.zeros(1, dtype=torch.int32, device=dev)
         for b in range(self.B):
@@ -54,11 +57,6 @@ class DecodeSession:
                 continue
             ops.mla_append_kv(hc.to(dev)[None], hk.to(dev)[None], zero, self.page_table[b:b + 1], self.rope,
                               self.cache, stream=stream)
-        c_new, k_new = inp.new_tokens()
-        self.c_new = c_new.to(dev).contiguous()
-        self.k_new = k_new.to(dev).contiguous()
-        self.q_nope = inp.q_nope.to(dev)
-        self.q_rope = inp.q_rope.to(dev)
         self.q_abs = torch.empty(self.B, self.n_q, N_HEADS, D_ROW, dtype=torch.bfloat16, device=dev)
         self.o_latent = torch.empty(self.B, self.n_q, N_HEADS, D_LATENT, dtype=torch.float32, device=dev)
         self.lse = torch.empty(self.B, self.n_q, N_HEADS, dtype=torch.float32, device=dev)
@@ -69,6 +67,29 @@ class DecodeSession:
             self.side = torch.cuda.Stream(device=dev)
             self._forked = torch.cuda.Event()
             self._appended = torch.cuda.Event()
+
+    _ALIGN = 256
+
+    def _pack_step_inputs(self, named):
+        self._layout, off = [], 0
+        for name, t in named:
+            t = t.contiguous()
+            n = t.numel() * t.element_size()
+            self._layout.append((name, off, t.dtype, tuple(t.shape), n))
+            off = (off + n + self._ALIGN - 1) // self._ALIGN * self._ALIGN
+        self.step_buffer = torch.zeros(max(off, 1), dtype=torch.uint8, device=self.device)
+        for (name, o, dtype, shape, n), (_, t) in zip(self._layout, named):
+            view = self.step_buffer[o:o + n].view(dtype).view(shape)
+            view.copy_(t.contiguous())
+            setattr(self, name, view)
+
+    def host_step_buffer(self, pin: bool = True) -> torch.Tensor:
+        """A host copy of the packed step inputs (same layout as ``step_buffer``)."""
+        host = torch.empty(self.step_buffer.shape, dtype=torch.uint8)
+        if pin:
+            host = host.pin_memory()
+        host.copy_(self.step_buffer)
+        return host
 
     def _main(self, stream):
         if stream is None:
