@@ -167,6 +167,24 @@ def test_launch_overlap_levels_give_identical_results():
         ops.mla_set_launch_overlap(before)
 
 
+# More shapes under the automatic plan: many short sequences, ragged lengths with
+# two queries each, a uniform batch of page-aligned sequences.
+SHAPES = {
+    "many_short": W.custom("many_short", [0, 5, 63, 64, 70, 127, 128, 200] * 12, n_q=1),
+    "ragged_q2": W.custom("ragged_q2", [3000, 40, 1000, 2500, 7, 4095] * 6, n_q=2),
+    "uniform_aligned": W.custom("uniform_aligned", [2047] * 40, n_q=1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHAPES))
+def test_decode_parity_shapes(name):
+    inp = W.generate(SHAPES[name], seed=9)
+    s = run_session(inp, split_pages=0, fused_finish=False)
+    check_outputs(s, inp, range(inp.batch), heads=[0, 63, 127])
+    f = run_session(inp, split_pages=0, fused_finish=True)
+    assert np.array_equal(bits(f.out), bits(s.out))
+
+
 def test_split_count_invariance():
     """Split count changes only rounding: P is a bf16 MMA operand and each split
     rounds it against its own running max, so two split layouts differ by about
