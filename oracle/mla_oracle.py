@@ -223,6 +223,22 @@ def decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len: int, heads=None):
     return o, o_lat, lse
 
 
+def decompress_kv(c, w_uk, w_uv):
+    """The non-absorbed path's first step: per-head keys and values from the latent.
+
+    ``K[t, h] = W_UK[h] c_t`` and ``V[t, h] = W_UV[h] c_t`` ([MA] §2.2 "Non-Absorbed":
+    decompress K and V, then standard MHA; [DP] eq. (2) and the value projection)
+    for ``c [kv, d_c]`` and ``w_uk``/``w_uv [H, d_h, d_c]``; returns ``K, V [kv, H, d_h]``.
+    With the cached ``k^R`` and ``[q^C ; RoPE(q^R)]`` these feed :func:`decode_mha`'s
+    per-head attention, which is also the definition of the prefill path for any
+    number of new tokens.
+    """
+    c = np.asarray(c, np.float64)
+    k = np.einsum("tm,hdm->thd", c, np.asarray(w_uk, np.float64))
+    v = np.einsum("tm,hdm->thd", c, np.asarray(w_uv, np.float64))
+    return k, v
+
+
 def decode_absorbed(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len: int, heads=None,
                     token_range: tuple[int, int] | None = None):
     """The absorbed form in fp64, used only to cross-check the absorption identity.

@@ -162,6 +162,42 @@ def test_absorbed_equals_non_absorbed_full_dims():
         assert relerr(x, y) <= 1e-10
 
 
+def test_decompressed_keys_obey_the_absorption_identity():
+    """q^C . K[t, h] = (W_UK[h]^T q^C) . c_t (the absorbed query of absorb_query, a
+    separate code path), and V[t, h] . u = c_t . (W_UV[h]^T u), for every t and h."""
+    rng = np.random.default_rng(12)
+    n_h, kv = 4, 9
+    w_uk = rng.normal(scale=0.02, size=(n_h, 128, 512))
+    w_uv = rng.normal(scale=0.02, size=(n_h, 128, 512))
+    c = rng.normal(size=(kv, 512))
+    q_nope = rng.normal(size=(n_h, 128))
+    q_rope = rng.normal(size=(n_h, 64))
+    k, v = O.decompress_kv(c, w_uk, w_uv)
+    assert k.shape == (kv, n_h, 128) and v.shape == (kv, n_h, 128)
+    q_abs = O.absorb_query(q_nope[None], q_rope[None], w_uk, np.array([3]))[0]   # [n_h, 576]
+    lhs = np.einsum("thd,hd->th", k, q_nope)
+    rhs = c @ q_abs[:, :512].T
+    assert relerr(lhs, rhs) <= 1e-12
+    u = rng.normal(size=(n_h, 128))
+    lhs_v = np.einsum("thd,hd->th", v, u)
+    rhs_v = np.stack([c @ (w_uv[h].T @ u[h]) for h in range(n_h)], axis=1)
+    assert relerr(lhs_v, rhs_v) <= 1e-12
+    # the decompressed keys and values give decode_mha's result for a many-query chunk
+    kr = rng.normal(size=(kv, 64))
+    qn = rng.normal(size=(5, n_h, 128))
+    qr = rng.normal(size=(5, n_h, 64))
+    o, _, lse = O.decode_mha(qn, qr, w_uk, w_uv, c, kr, prior_len=kv - 5)
+    for j in range(5):
+        pos = kv - 5 + j
+        for h in range(n_h):
+            q = np.concatenate([qn[j, h], O.rope_f64(qr[j, h], pos)])
+            keys = np.concatenate([k[:pos + 1, h], kr[:pos + 1]], axis=1)
+            sc = keys @ q / np.sqrt(192.0)
+            a = np.exp(sc - sc.max())
+            assert relerr(o[j, h], (a / a.sum()) @ v[:pos + 1, h]) <= 1e-12
+            assert abs(lse[j, h] - (sc.max() + np.log(a.sum()))) <= 1e-12
+
+
 def test_softmax_rows_sum_to_one():
     rng = np.random.default_rng(5)
     p = tiny(rng, kv=7)
