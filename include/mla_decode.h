@@ -250,6 +250,49 @@ mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_page
                                   const mla_bf16* w_uv, mla_bf16* out, float* lse, cudaStream_t stream);
 
 /*
+ * The non-absorbed path, for a chunk of many new tokens (prefill / chunked
+ * prefill).  ("MLA 矩阵吸收 …" section 2.2, Non-Absorbed: decompress K = c W_UK
+ * and V = c W_UV, then standard MHA; section 6: engines switch to it when a step
+ * brings about 64 new tokens or more; "DeepSeek-MLA-Principle" section 6, the
+ * L^2 terms of prefill are ~3x smaller without absorption.)  A step on this path:
+ * mla_append_kv for the chunk, mla_decompress_kv, mla_prefill_attn; the result is
+ * the same per-head O that the absorbed path's mla_out_absorb produces.
+ *
+ * mla_decompress_kv -- K[b, h, t, :] = W_UK[h] c_t, V[b, h, t, :] = W_UV[h] c_t for
+ * the cached tokens t < kv_lens[b] of every sequence.
+ *   cache, num_pages, page_table, pt_stride: as for mla_decode_attn
+ *   kv_lens    [B] int32 tokens to decompress per sequence (<= max_kv_len)
+ *   w_uk, w_uv [128, 128, 512] bf16
+ *   k_nope, v  [B, 128, max_kv_len, 128] bf16 out (head-major).  Rows from
+ *              kv_lens[b] up to the next multiple of 128 (within max_kv_len) are
+ *              written as zeros; rows beyond that are not touched.
+ * Accumulation is float32, results rounded to bf16.  MLA_ERR_UNSUPPORTED when
+ * B * 128 * (max_kv_len + 64) does not fit in 31 bits.
+ *
+ * mla_prefill_attn -- O[b, j, h] = sum_t softmax_t(s) V[b, h, t] with
+ * s_t = [q^C ; RoPE(q^R, pos)] . [K[b, h, t] ; k^R_t] / sqrt(192), causal: query j of
+ * sequence b sits at pos = seq_lens_before[b] + j and sees tokens 0 .. pos.
+ *   q_nope     [B, n_q, 128, 128] bf16; q_rope [B, n_q, 128, 64] bf16, NOT rotated
+ *   seq_lens_before [B] int32; kv_lens [B] int32 must equal seq_lens_before + n_q
+ *   rope_table, rope_max_pos: from mla_rope_table_init (pos < rope_max_pos)
+ *   k_nope, v  as written by mla_decompress_kv (rows past kv_lens[b] up to the next
+ *              multiple of 128 must be finite)
+ *   cache ...  the cache holding the chunk (its RoPE keys k^R are read from it)
+ *   out        [B, n_q, 128, 128] bf16 out; lse [B, n_q, 128] float32 out (nullable,
+ *              natural log-sum-exp of the scaled scores)
+ * n_q is not limited to MLA_MAX_NQ here.  A sequence whose lengths are
+ * inconsistent sets MLA_ERR_BOUNDS and gets zeros.
+ */
+mla_status mla_decompress_kv(const mla_bf16* cache, int64_t num_pages, const int32_t* page_table, int pt_stride,
+                             const int32_t* kv_lens, int B, int max_kv_len, const mla_bf16* w_uk,
+                             const mla_bf16* w_uv, mla_bf16* k_nope, mla_bf16* v, cudaStream_t stream);
+mla_status mla_prefill_attn(const mla_bf16* q_nope, const mla_bf16* q_rope, const int32_t* seq_lens_before,
+                            const float* rope_table, int rope_max_pos, const mla_bf16* k_nope, const mla_bf16* v,
+                            int max_kv_len, const mla_bf16* cache, int64_t num_pages, const int32_t* page_table,
+                            int pt_stride, const int32_t* kv_lens, int B, int n_q, mla_bf16* out, float* lse,
+                            cudaStream_t stream);
+
+/*
  * mla_set_launch_overlap / mla_get_launch_overlap -- how consecutive launches
  * of this library on one stream may overlap.  (The MLA pages have no
  * counterpart; this is a launch-latency setting of the GPU runtime.)

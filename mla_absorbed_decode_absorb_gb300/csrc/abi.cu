@@ -1,5 +1,6 @@
 // The C ABI of include/mla_decode.h: argument validation, split planning,
 // the per-device status word, the RoPE table, and the launches.
+#include <limits.h>
 #include <math.h>
 #include <stdlib.h>
 
@@ -255,6 +256,44 @@ mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_page
   const float* o_part = static_cast<const float*>(workspace);
   const float* lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + plan.o_part_bytes);
   return from_cuda(launch_combine_out_absorb(o_part, lse_part, plan.num_splits, w_uv, out, lse, B, n_q, st, stream));
+}
+
+mla_status mla_decompress_kv(const mla_bf16* cache, int64_t num_pages, const int32_t* page_table, int pt_stride,
+                             const int32_t* kv_lens, int B, int max_kv_len, const mla_bf16* w_uk,
+                             const mla_bf16* w_uv, mla_bf16* k_nope, mla_bf16* v, cudaStream_t stream) {
+  if (B < 0 || max_kv_len < 0 || num_pages < 0 || pt_stride < 0) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * kHeads * (max_kv_len + kPage) > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (B == 0 || max_kv_len == 0) return MLA_OK;
+  if (!cache || !page_table || !kv_lens || !w_uk || !w_uv || !k_nope || !v) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(cache) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(k_nope) || !aligned16(v))
+    return MLA_ERR_INVALID_ARG;
+  if (pt_stride < (max_kv_len + kPage - 1) / kPage) return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_decompress_kv(cache, num_pages, page_table, pt_stride, kv_lens, B, max_kv_len, w_uk, w_uv,
+                                        k_nope, v, st, stream));
+}
+
+mla_status mla_prefill_attn(const mla_bf16* q_nope, const mla_bf16* q_rope, const int32_t* seq_lens_before,
+                            const float* rope_table, int rope_max_pos, const mla_bf16* k_nope, const mla_bf16* v,
+                            int max_kv_len, const mla_bf16* cache, int64_t num_pages, const int32_t* page_table,
+                            int pt_stride, const int32_t* kv_lens, int B, int n_q, mla_bf16* out, float* lse,
+                            cudaStream_t stream) {
+  if (B < 0 || n_q < 0 || max_kv_len < n_q || num_pages < 0 || pt_stride < 0 || rope_max_pos < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(B) * kHeads * (max_kv_len + 128) > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (B == 0 || n_q == 0) return MLA_OK;
+  if (!q_nope || !q_rope || !seq_lens_before || !rope_table || !k_nope || !v || !cache || !page_table ||
+      !kv_lens || !out)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(k_nope) || !aligned16(v) || !aligned16(cache) || !aligned16(out))
+    return MLA_ERR_INVALID_ARG;
+  if (pt_stride < (max_kv_len + kPage - 1) / kPage) return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_prefill_attn(q_nope, q_rope, seq_lens_before, rope_table, rope_max_pos, k_nope, v,
+                                       max_kv_len, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, out,
+                                       lse, st, stream));
 }
 
 mla_status mla_set_launch_overlap(int level) {

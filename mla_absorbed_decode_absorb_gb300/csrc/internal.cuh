@@ -106,6 +106,17 @@ cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, in
 cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint16_t* out,
                               int B, int n_q, int* status, cudaStream_t stream);
 
+cudaError_t launch_decompress_kv(const uint16_t* cache, int64_t num_pages, const int32_t* page_table, int pt_stride,
+                                 const int32_t* kv_lens, int B, int max_kv_len, const uint16_t* w_uk,
+                                 const uint16_t* w_uv, uint16_t* k_out, uint16_t* v_out, int* status,
+                                 cudaStream_t stream);
+
+cudaError_t launch_prefill_attn(const uint16_t* q_nope, const uint16_t* q_rope, const int32_t* seq_lens_before,
+                                const float* rope_table, int rope_max_pos, const uint16_t* k_nope,
+                                const uint16_t* v, int max_kv_len, const uint16_t* cache, int64_t num_pages,
+                                const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
+                                uint16_t* out, float* lse, int* status, cudaStream_t stream);
+
 cudaError_t launch_combine_out_absorb(const float* o_part, const float* lse_part, int num_splits,
                                       const uint16_t* w_uv, uint16_t* out, float* lse, int B, int n_q,
                                       int* status, cudaStream_t stream);

@@ -1,0 +1,390 @@
+// Non-absorbed path, step 2: causal multi-head attention of a chunk of new
+// tokens over the decompressed keys and values (the prefill / chunked-prefill form).
+//
+// "MLA 矩阵吸收 …" section 2.2 (Non-Absorbed: score = Q K^T on the decompressed
+// K, standard MHA, O = softmax(score) V) and section 6 (FlashAttention-style
+// kernel for the chunk); "DeepSeek-MLA-Principle" section 2: score =
+// [q^C ; RoPE(q^R)] . [k^C ; k^R] / sqrt(d_h + d_h^R), eqs. (2)-(10), and
+// section 6 (prefill is compute bound, the non-absorbed L^2 terms are ~3x smaller).
+//
+// One CTA per (sequence b, head h, tile of 128 new tokens).  The query tile
+// [q^C ; RoPE(q^R, pos)] (192 columns) is built in shared memory by the softmax
+// warps; per 128-key tile the producer loads, by TMA, the head's decompressed keys
+// (128 columns), the shared RoPE key of the cache (64 columns, through the page
+// table) and the values into a 2-stage ring.  S = Q K^T (M = 128 queries, N = 128
+// keys, K = 192) goes to one of two TMEM buffers, the softmax warps (one thread
+// per query) apply the causal mask and an online softmax with a lazily updated
+// reference max (O is rescaled only when a row's max grows by more than 2^8),
+// write P as bf16 into TMEM, and O += P V (N = 128, K = 128 keys) accumulates in
+// TMEM.  Query j of sequence b sits at position seq_lens_before[b] + j and sees
+// the keys 0 .. seq_lens_before[b] + j.
+#include "sm100.cuh"
+#include "tmap.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kQTile = 128;
+constexpr int kKTile = 128;
+constexpr int kStages = 2;
+constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kChunk = 128 * 128;   // 128 rows x 64 bf16 columns (SW128)
+constexpr int kOffQ = 0;            // query: 3 chunks (q^C 0-63, q^C 64-127, RoPE(q^R))
+constexpr int kStageBytes = 5 * kChunk;  // keys 2 chunks, RoPE keys 1, values 2
+constexpr int kOffStage = kOffQ + 3 * kChunk;
+constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+constexpr uint32_t kTmemO = 0;      // O: [0, 128)
+constexpr uint32_t kTmemS = 128;    // two score buffers: [128, 256), [256, 384)
+constexpr uint32_t kTmemP = 384;    // P (128 keys as bf16 pairs): [384, 448)
+constexpr float kRescaleLog2 = 8.f;
+
+struct Bars {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t q_ready;
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full;
+  uint64_t pv_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct Params {
+  const uint16_t* q_nope;
+  const uint16_t* q_rope;
+  const int32_t* seq_lens_before;
+  const float* rope;
+  const int32_t* page_table;
+  const int32_t* kv_lens;
+  uint16_t* out;
+  float* lse;
+  int* status;
+  int64_t num_pages;
+  int pt_stride;
+  int rope_max_pos;
+  int max_kv_len;
+  int n_q;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       const __grid_constant__ CUtensorMap tm_kr, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort = &bars.abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars.full[s]), 1);
+      mbar_init(smem_u32(&bars.empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars.q_ready), 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(&bars.s_full[s]), 1);
+      mbar_init(smem_u32(&bars.s_free[s]), 128);
+    }
+    mbar_init(smem_u32(&bars.p_full), 128);
+    mbar_init(smem_u32(&bars.pv_done), 1);
+    mbar_init(smem_u32(&bars.drain), 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars.tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  const int L = p.seq_lens_before[b];
+  const int kv = p.kv_lens[b];
+  const bool bad = L < 0 || kv != L + p.n_q || kv > p.max_kv_len || (kv + kPage - 1) / kPage > p.pt_stride ||
+                   L + p.n_q > p.rope_max_pos;
+  const int j0 = qt * kQTile;
+  const int j_last = min(p.n_q, j0 + kQTile) - 1;            // last query of the tile
+  const int n_kt = bad ? 0 : (L + j_last + 1 + kKTile - 1) / kKTile;  // key tiles it sees
+  if (tid == 0 && bad && qt == 0 && h == 0) record_status(p.status, MLA_ERR_BOUNDS);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_kt > 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_kr);
+      const int row0 = (b * kHeads + h) * p.max_kv_len;  // this head's rows in K and V
+      for (int kt = 0; kt < n_kt; ++kt) {
+        const int s = kt % kStages;
+        if (!mbar_wait(smem_u32(&bars.empty[s]), ((kt / kStages) & 1) ^ 1, p.status, abort)) break;
+        const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
+        const uint32_t fb = smem_u32(&bars.full[s]);
+        mbar_arrive_expect_tx(fb, kStageBytes);
+        for (int c = 0; c < 2; ++c) tma_load_2d(st + c * kChunk, &tm_k, 64 * c, row0 + kt * kKTile, fb);
+        for (int pg = 0; pg < 2; ++pg) {
+          const int tok = kt * kKTile + pg * kPage;
+          int page = 0;
+          if (tok < kv) {
+            page = p.page_table[static_cast<int64_t>(b) * p.pt_stride + tok / kPage];
+            if (page < 0 || page >= p.num_pages) {
+              record_status(p.status, MLA_ERR_BOUNDS);
+              page = 0;  // stay in bounds; the result of this tile is not meaningful
+            }
+          }
+          tma_load_2d(st + 2 * kChunk + pg * (kChunk / 2), &tm_kr, kLatent, page * kPage, fb);
+        }
+        for (int c = 0; c < 2; ++c) tma_load_2d(st + (3 + c) * kChunk, &tm_v, 64 * c, row0 + kt * kKTile, fb);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ tcgen05 issuer
+    if (lane == 0 && n_kt > 0) {
+      const uint32_t idesc_qk = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/0);
+      const uint32_t idesc_pv = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/1);
+      const uint64_t d_q = smem_desc(smem_u32(smem + kOffQ), 16, 1024, kSw128);
+      const uint64_t d_st = smem_desc(smem_u32(smem + kOffStage), 16, 1024, kSw128);           // keys (K-major)
+      const uint64_t d_v = smem_desc(smem_u32(smem + kOffStage + 3 * kChunk), kChunk, 1024, kSw128);  // values (MN-major)
+      bool ok = mbar_wait(smem_u32(&bars.q_ready), 0, p.status, abort);
+      auto issue_qk = [&](int kt) -> bool {
+        const int s = kt % kStages, buf = kt & 1;
+        bool w = mbar_wait(smem_u32(&bars.full[s]), (kt / kStages) & 1, p.status, abort);
+        w = w && mbar_wait(smem_u32(&bars.s_free[buf]), ((kt >> 1) & 1) ^ 1, p.status, abort);
+        if (!w) return false;
+        tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
+#pragma unroll
+        for (int k = 0; k < 12; ++k)  // K = 192: three 64-column chunks of four K steps
+          mma_ss(tmem + kTmemS + 128 * buf, d_q + (k >> 2) * (kChunk >> 4) + (k & 3) * 2,
+                 d_st + so + (k >> 2) * (kChunk >> 4) + (k & 3) * 2, idesc_qk, k > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bars.s_full[buf]));
+        return true;
+      };
+      auto issue_pv = [&](int kt) -> bool {
+        if (!mbar_wait(smem_u32(&bars.p_full), kt & 1, p.status, abort)) return false;
+        tc_fence_after();
+        const uint64_t vb = d_v + static_cast<uint64_t>(((kt % kStages) * kStageBytes) >> 4);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)  // K = 128 keys
+          mma_ts(tmem + kTmemO, tmem + kTmemP + 8 * k, vb + 128 * k, idesc_pv, (kt > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bars.empty[kt % kStages]));
+        mma_commit(smem_u32(&bars.pv_done));
+        return true;
+      };
+      if (ok) ok = issue_qk(0);
+      for (int kt = 0; kt < n_kt && ok; ++kt) {
+        if (kt + 1 < n_kt) ok = issue_qk(kt + 1);
+        if (ok) ok = issue_pv(kt);
+      }
+      if (!ok) {
+        record_status(p.status, MLA_ERR_TIMEOUT);
+        *abort = 1;
+      }
+      // no tcgen05 operation may still be running when TMEM is released
+      mma_commit(smem_u32(&bars.drain));
+      mbar_wait(smem_u32(&bars.drain), 0, p.status, nullptr);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax: one thread per query
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;       // query row of the tile (TMEM lane)
+    const int j = j0 + r;                 // query index in the chunk
+    const bool live = j < p.n_q;
+    const int pos = L + j;                // its position: sees keys 0 .. pos
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    // query row: [q^C ; RoPE(q^R, pos)] into the three SW128 chunks
+    {
+      const int64_t qrow = (static_cast<int64_t>(b) * p.n_q + j) * kHeads + h;
+      uint8_t* qs = smem + kOffQ;
+      if (live && !bad) {
+        const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kNope);
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+          *reinterpret_cast<uint4*>(qs + (u >> 3) * kChunk + sw128(r * 128 + (u & 7) * 16)) = qn[u];
+        const uint16_t* qr = p.q_rope + qrow * kRope;
+        const float* cs = p.rope + static_cast<int64_t>(pos) * kRope;
+        uint32_t w[32];
+#pragma unroll
+        for (int f = 0; f < kHalfRope; f += 2) {
+          float o[4];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float x1 = bf16_bits_to_f32(qr[f + e]), x2 = bf16_bits_to_f32(qr[f + e + kHalfRope]);
+            const float c = cs[f + e], sn = cs[kHalfRope + f + e];
+            o[e] = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn));
+            o[2 + e] = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn));
+          }
+          w[f / 2] = pack_bf16x2(o[0], o[1]);
+          w[16 + f / 2] = pack_bf16x2(o[2], o[3]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(qs + 2 * kChunk + sw128(r * 128 + u * 16)) =
+              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+      } else {
+        for (int u = 0; u < 24; ++u)
+          *reinterpret_cast<uint4*>(qs + (u >> 3) * kChunk + sw128(r * 128 + (u & 7) * 16)) = make_uint4(0, 0, 0, 0);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bars.q_ready));
+    }
+    constexpr float kScaleL2 = kScaleLog2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = n_kt > 0;
+    for (int kt = 0; kt < n_kt && ok; ++kt) {
+      const int buf = kt & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[buf]), (kt >> 1) & 1, p.status, abort));
+      if (!ok) break;
+      tc_fence_after();
+      // keys kt*128 + c visible to this query: c < n_vis
+      const int n_vis = live ? max(0, min(kKTile, pos + 1 - kt * kKTile)) : (kt == 0 ? 1 : 0);
+      float sv[128];
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + kTmemS + 128 * buf + c0, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) sv[c0 + c] = __uint_as_float(v[c]);
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.s_free[buf]));  // QK^T of key tile kt + 2 may overwrite the buffer
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c)
+        if (c < n_vis) mx = fmaxf(mx, sv[c]);
+      mx *= kScaleL2;
+      float factor = 1.f;
+      bool rescale = false;
+      if (m_ref == -INFINITY) {
+        m_ref = mx;  // first key tile with a visible key (or still -inf)
+      } else if (mx > m_ref + kRescaleLog2) {
+        factor = ex2_approx(m_ref - mx);
+        m_ref = mx;
+        rescale = true;
+      }
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+      uint32_t pk[64];
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        float p0 = ex2_approx(fmaf(sv[2 * c], kScaleL2, neg_m));
+        float p1 = ex2_approx(fmaf(sv[2 * c + 1], kScaleL2, neg_m));
+        if (2 * c >= n_vis) p0 = 0.f;
+        if (2 * c + 1 >= n_vis) p1 = 0.f;
+        pk[c] = pack_bf16x2(p0, p1);
+        sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+      }
+      l = l * factor + sum;
+      // O and P may only be touched once the previous P V has finished
+      if (kt > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done), (kt - 1) & 1, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_off + kTmemO + c0, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
+          tmem_st32(tmem + lane_off + kTmemO + c0, v);
+        }
+      }
+      tmem_st32(tmem + lane_off + kTmemP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tmem + lane_off + kTmemP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bars.p_full));
+    }
+    if (ok && n_kt > 0)
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done), (n_kt - 1) & 1, p.status, abort));
+    tc_fence_after();
+    // epilogue: O / l as bf16, and the natural log-sum-exp.  tcgen05.ld is a
+    // warp-wide instruction, so every lane loads and only live rows store.
+    const int64_t orow = (static_cast<int64_t>(b) * p.n_q + j) * kHeads + h;
+    uint16_t* dst = p.out + orow * kNope;
+    if (ok && n_kt > 0) {
+      const float inv = live ? 1.f / l : 0.f;
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + kTmemO + c0, v);
+        tmem_wait_ld();
+        if (live) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d4[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * inv, __uint_as_float(v[8 * q + 1]) * inv),
+                               pack_bf16x2(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv),
+                               pack_bf16x2(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv),
+                               pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
+        }
+      }
+      if (live && p.lse != nullptr) p.lse[orow] = (m_ref + log2f(l)) * kLn2;
+    } else if (live) {
+      for (int c0 = 0; c0 < 128; c0 += 8) *reinterpret_cast<uint4*>(dst + c0) = make_uint4(0, 0, 0, 0);
+      if (p.lse != nullptr) p.lse[orow] = -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+bool g_configured[64];
+
+}  // namespace
+
+cudaError_t launch_prefill_attn(const uint16_t* q_nope, const uint16_t* q_rope, const int32_t* seq_lens_before,
+                                const float* rope_table, int rope_max_pos, const uint16_t* k_nope,
+                                const uint16_t* v, int max_kv_len, const uint16_t* cache, int64_t num_pages,
+                                const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
+                                uint16_t* out, float* lse, int* status, cudaStream_t stream) {
+  if (B == 0 || n_q == 0) return cudaSuccess;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!g_configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(prefill_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBytes);
+    if (e != cudaSuccess) return e;
+    g_configured[dev] = true;
+  }
+  CUtensorMap tk, tv, tkr;
+  const uint64_t kv_rows = static_cast<uint64_t>(B) * kHeads * max_kv_len;
+  const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
+  if (!make_tmap_bf16_2d(&tk, k_nope, kv_rows, kNope, kNope, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_2d(&tv, v, kv_rows, kNope, kNope, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_2d(&tkr, cache, c_rows, kRow, kRow, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  Params prm;
+  prm.q_nope = q_nope;
+  prm.q_rope = q_rope;
+  prm.seq_lens_before = seq_lens_before;
+  prm.rope = rope_table;
+  prm.page_table = page_table;
+  prm.kv_lens = kv_lens;
+  prm.out = out;
+  prm.lse = lse;
+  prm.status = status;
+  prm.num_pages = num_pages;
+  prm.pt_stride = pt_stride;
+  prm.rope_max_pos = rope_max_pos;
+  prm.max_kv_len = max_kv_len;
+  prm.n_q = n_q;
+  dim3 grid((n_q + kQTile - 1) / kQTile, kHeads, B);
+  return launch_kernel(prefill_attn_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream, tk, tv, tkr, prm);
+}
+
+}  // namespace mla

@@ -48,6 +48,8 @@ _SIGS = {
     "mla_combine_out_absorb": ([_i, _i, _i, _i, _p, _sz, _p, _p, _p, _p, _p], _i),
     "mla_get_device_status": ([_p], _i),
     "mla_set_launch_overlap": ([_i], _i),
+    "mla_decompress_kv": ([_p, _i64, _p, _i, _p, _i, _i, _p, _p, _p, _p, _p], _i),
+    "mla_prefill_attn": ([_p, _p, _p, _p, _i, _p, _p, _i, _p, _i64, _p, _i, _p, _i, _i, _p, _p, _p], _i),
     "mla_get_launch_overlap": ([], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -57,6 +59,7 @@ for _name, (_args, _res) in _SIGS.items():
 
 MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE, MLA_ERR_CUDA, MLA_ERR_TIMEOUT, \
     MLA_ERR_BOUNDS, MLA_ERR_RANGE = range(8)
+MLA_MAX_NQ = 8  # new tokens per sequence the absorbed kernels take (MLA_MAX_NQ of the C header)
 
 
 class MLAError(RuntimeError):
@@ -232,6 +235,47 @@ def mla_combine_out_absorb(B, n_q, max_kv_len, split_pages, workspace, o_latent,
         0 if workspace is None else workspace.numel(),
         0 if o_latent is None else _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
         _dev(w_uv, "w_uv", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
+        _dev(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        0 if lse is None else _dev(lse, "lse", torch.float32, (B, n_q, N_HEADS)),
+        _stream(stream)))
+    return out
+
+
+def mla_decompress_kv(cache, page_table, kv_lens, max_kv_len, w_uk, w_uv, k_nope=None, v=None, stream=None):
+    """Non-absorbed path: per-head keys and values [B, 128, max_kv_len, 128] decompressed from the cache."""
+    B = int(kv_lens.shape[0])
+    shape = (B, N_HEADS, int(max_kv_len), D_NOPE)
+    if k_nope is None:
+        k_nope = torch.empty(shape, dtype=torch.bfloat16, device=cache.device)
+    if v is None:
+        v = torch.empty(shape, dtype=torch.bfloat16, device=cache.device)
+    _check("mla_decompress_kv", lib.mla_decompress_kv(
+        _dev(cache, "cache", torch.bfloat16), int(cache.shape[0]),
+        _dev(page_table, "page_table", torch.int32), int(page_table.shape[1]),
+        _dev(kv_lens, "kv_lens", torch.int32, (B,)), B, int(max_kv_len),
+        _dev(w_uk, "w_uk", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
+        _dev(w_uv, "w_uv", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
+        _dev(k_nope, "k_nope", torch.bfloat16, shape), _dev(v, "v", torch.bfloat16, shape), _stream(stream)))
+    return k_nope, v
+
+
+def mla_prefill_attn(q_nope, q_rope, seq_lens_before, rope, k_nope, v, cache, page_table, kv_lens,
+                     out=None, lse=None, stream=None):
+    """Non-absorbed path: causal MHA of the new tokens over the decompressed keys and values."""
+    B, n_q = q_nope.shape[:2]
+    max_kv_len = int(k_nope.shape[2])
+    if out is None:
+        out = torch.empty(B, n_q, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=q_nope.device)
+    _check("mla_prefill_attn", lib.mla_prefill_attn(
+        _dev(q_nope, "q_nope", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        _dev(q_rope, "q_rope", torch.bfloat16, (B, n_q, N_HEADS, D_ROPE)),
+        _dev(seq_lens_before, "seq_lens_before", torch.int32, (B,)),
+        _dev(rope, "rope_table", torch.float32), int(rope.shape[0]),
+        _dev(k_nope, "k_nope", torch.bfloat16, (B, N_HEADS, max_kv_len, D_NOPE)),
+        _dev(v, "v", torch.bfloat16, (B, N_HEADS, max_kv_len, D_NOPE)), max_kv_len,
+        _dev(cache, "cache", torch.bfloat16), int(cache.shape[0]),
+        _dev(page_table, "page_table", torch.int32), int(page_table.shape[1]),
+        _dev(kv_lens, "kv_lens", torch.int32, (B,)), int(B), int(n_q),
         _dev(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
         0 if lse is None else _dev(lse, "lse", torch.float32, (B, n_q, N_HEADS)),
         _stream(stream)))

@@ -18,6 +18,12 @@ step 1 runs on a side stream forked from the caller's stream and joined before
 step 3.  By default all launches stay on the caller's stream, where the
 library's programmatic dependent launch (``mla_set_launch_overlap``) lets each
 kernel's prologue overlap the previous one.
+
+A step that brings ``PREFILL_MIN_NEW_TOKENS`` (64) or more new tokens per
+sequence takes the non-absorbed path instead, as inference engines switch for
+prefill and chunked prefill: ``mla_append_kv``, ``mla_decompress_kv`` (per-head
+keys and values from the latent cache) and ``mla_prefill_attn`` (causal MHA),
+which give the same per-head output ``out``.
 """
 
 from __future__ import annotations
@@ -28,9 +34,14 @@ from . import ops
 from .workloads import D_LATENT, D_NOPE, D_ROW, N_HEADS, Inputs, empty_cache
 
 
+# New tokens per sequence from which a step takes the non-absorbed path (the
+# switch point the MLA pages give for prefill / chunked prefill).
+PREFILL_MIN_NEW_TOKENS = 64
+
+
 class DecodeSession:
     def __init__(self, inp: Inputs, device="cuda", split_pages: int | None = None, stream=None,
-                 fused_finish: bool = True, overlap_append: bool = False):
+                 fused_finish: bool = True, overlap_append: bool = False, path: str | None = None):
         self.inp = inp
         self.fused_finish = bool(fused_finish)
         self.overlap_append = bool(overlap_append)
@@ -38,6 +49,13 @@ class DecodeSession:
         wl = inp.workload
         self.B, self.n_q = wl.batch, wl.n_q
         self.split_pages = wl.split_pages if split_pages is None else int(split_pages)
+        if path is None:
+            # the absorbed kernels take up to MLA_MAX_NQ new tokens per sequence
+            small = self.n_q < PREFILL_MIN_NEW_TOKENS and self.n_q <= ops.MLA_MAX_NQ
+            path = "absorbed" if small else "non_absorbed"
+        if path not in ("absorbed", "non_absorbed"):
+            raise ValueError(f"unknown path {path!r}")
+        self.path = path
         dev = self.device
         self.max_kv_len = int(inp.kv_lens.max()) if self.B else self.n_q
         self.rope = ops.rope_table(self.max_kv_len + 1, dev, stream)
@@ -57,12 +75,18 @@ class DecodeSession:
                 continue
             ops.mla_append_kv(hc.to(dev)[None], hk.to(dev)[None], zero, self.page_table[b:b + 1], self.rope,
                               self.cache, stream=stream)
-        self.q_abs = torch.empty(self.B, self.n_q, N_HEADS, D_ROW, dtype=torch.bfloat16, device=dev)
-        self.o_latent = torch.empty(self.B, self.n_q, N_HEADS, D_LATENT, dtype=torch.float32, device=dev)
         self.lse = torch.empty(self.B, self.n_q, N_HEADS, dtype=torch.float32, device=dev)
         self.out = torch.empty(self.B, self.n_q, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=dev)
-        self.workspace = ops.alloc_workspace(self.B, self.n_q, self.max_kv_len, self.split_pages, dev)
-        self.num_splits = ops.mla_decode_num_splits(self.B, self.n_q, self.max_kv_len, self.split_pages)
+        if self.path == "absorbed":
+            self.q_abs = torch.empty(self.B, self.n_q, N_HEADS, D_ROW, dtype=torch.bfloat16, device=dev)
+            self.o_latent = torch.empty(self.B, self.n_q, N_HEADS, D_LATENT, dtype=torch.float32, device=dev)
+            self.workspace = ops.alloc_workspace(self.B, self.n_q, self.max_kv_len, self.split_pages, dev)
+            self.num_splits = ops.mla_decode_num_splits(self.B, self.n_q, self.max_kv_len, self.split_pages)
+        else:
+            kv_shape = (self.B, N_HEADS, self.max_kv_len, D_NOPE)
+            self.k_nope = torch.empty(kv_shape, dtype=torch.bfloat16, device=dev)
+            self.v = torch.empty(kv_shape, dtype=torch.bfloat16, device=dev)
+            self.num_splits = 1
         if self.overlap_append:
             self.side = torch.cuda.Stream(device=dev)
             self._forked = torch.cuda.Event()
@@ -131,7 +155,19 @@ class DecodeSession:
         ops.mla_combine_out_absorb(self.B, self.n_q, self.max_kv_len, self.split_pages, self.workspace,
                                    self.o_latent, self.w_uv, self.out, self.lse, stream=stream)
 
+    def decompress(self, stream=None):
+        if self.overlap_append:
+            self._main(stream).wait_event(self._appended)  # the cache holds the new tokens
+        ops.mla_decompress_kv(self.cache, self.page_table, self.kv_lens, self.max_kv_len, self.w_uk, self.w_uv,
+                              self.k_nope, self.v, stream=stream)
+
+    def prefill_attn(self, stream=None):
+        ops.mla_prefill_attn(self.q_nope, self.q_rope, self.prior_lens, self.rope, self.k_nope, self.v, self.cache,
+                             self.page_table, self.kv_lens, self.out, self.lse, stream=stream)
+
     def stage_names(self) -> list[str]:
+        if self.path == "non_absorbed":
+            return ["append", "decompress", "prefill_attn"]
         tail = ["finish"] if self.fused_finish else ["combine", "project_out"]
         return ["append", "absorb", "attend_partial"] + tail
 
@@ -141,6 +177,8 @@ class DecodeSession:
         return self.out
 
     def launches_per_step(self) -> int:
+        if self.path == "non_absorbed":
+            return 3
         if self.fused_finish:
             return 4
         return 4 + (1 if self.num_splits > 1 else 0)

@@ -12,6 +12,12 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a) and the built library")
 
 
+# A GPU test that has not finished after this long is stopped (with every
+# thread's stack dumped) instead of holding the device, when pytest-timeout is
+# installed; the kernels' own waits give up after 2 s.
+GPU_TEST_TIMEOUT_S = 300
+
+
 def pytest_collection_modifyitems(config, items):
     try:
         import torch
@@ -19,6 +25,10 @@ def pytest_collection_modifyitems(config, items):
     except Exception:  # pragma: no cover
         has_gpu = False
     if has_gpu:
+        if config.pluginmanager.hasplugin("timeout"):
+            for item in items:
+                if "gpu" in item.keywords and item.get_closest_marker("timeout") is None:
+                    item.add_marker(pytest.mark.timeout(GPU_TEST_TIMEOUT_S, method="thread"))
         return
     skip = pytest.mark.skip(reason="no CUDA device on this host")
     for item in items:

@@ -1,0 +1,90 @@
+"""The non-absorbed (prefill / chunked-prefill) path through the C ABI, against the oracle.
+
+mla_decompress_kv must give the oracle's per-head keys and values (bf16 outputs of
+an fp32 accumulation: within 2^-8 relative plus a small absolute floor), and
+zeros in the rows up to the next 128-token boundary; mla_prefill_attn must give
+the oracle's output O within max-abs 1e-2 and relative L2 5e-3 (as the absorbed
+path), and its log-sum-exp within 2e-2.  The same session switches to this path
+for steps of 64 or more new tokens.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import mla_oracle as O
+from mla_absorbed_decode_absorb_gb300 import workloads as W
+
+from test_gpu_parity import bits, oracle_sequence, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+O_MAX_ABS, O_REL_L2, LSE_MAX_ABS = 1e-2, 5e-3, 2e-2
+
+
+def session(inp, **kw):
+    from mla_absorbed_decode_absorb_gb300 import ops
+    from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
+    s = DecodeSession(inp, **kw)
+    s.step()
+    torch.cuda.synchronize()
+    assert ops.mla_get_device_status() == ops.MLA_OK
+    return s
+
+
+def check_prefill(s, inp, heads):
+    o_gpu = s.out.float().cpu().numpy()
+    lse_gpu = s.lse.cpu().numpy()
+    o_all, r_all = [], []
+    for b in range(inp.batch):
+        o_ref, _, lse_ref = oracle_sequence(inp, b, heads)
+        o = o_gpu[b][:, heads]
+        assert np.isfinite(o).all()
+        assert np.abs(lse_gpu[b][:, heads] - lse_ref).max() <= LSE_MAX_ABS
+        o_all.append(o), r_all.append(o_ref)
+    o, r = np.concatenate(o_all), np.concatenate(r_all)
+    assert np.abs(o - r).max() <= O_MAX_ABS, np.abs(o - r).max()
+    assert rel_l2(o, r) <= O_REL_L2, rel_l2(o, r)
+    return rel_l2(o, r)
+
+
+def test_decompress_kv_parity():
+    inp = W.generate(W.custom("decompress", [0, 63, 200, 700], n_q=64), seed=21)
+    s = session(inp)
+    assert s.path == "non_absorbed"
+    w_uk = O.bf16_bits_to_f64(bits(inp.w_uk))
+    w_uv = O.bf16_bits_to_f64(bits(inp.w_uv))
+    k_gpu = s.k_nope.float().cpu().numpy()
+    v_gpu = s.v.float().cpu().numpy()
+    heads = [0, 5, 64, 127]
+    for b in range(inp.batch):
+        c_bits, _ = (bits(x) for x in inp.sequence(b))
+        c = O.bf16_bits_to_f64(c_bits)
+        kv = c.shape[0]
+        k_ref, v_ref = O.decompress_kv(c, w_uk[heads], w_uv[heads])
+        for got, ref in ((k_gpu, k_ref), (v_gpu, v_ref)):
+            g = got[b][heads][:, :kv].transpose(1, 0, 2)
+            tol = 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max()
+            assert (np.abs(g - ref) <= tol).all(), np.abs(g - ref).max()
+            pad_end = min(s.max_kv_len, (kv + 127) // 128 * 128)
+            assert (got[b][:, kv:pad_end] == 0).all()
+
+
+@pytest.mark.parametrize("lengths,n_q", [([0, 1, 63, 500], 64), ([130, 0], 100), ([64, 1000], 129), ([300], 256)])
+def test_prefill_parity(lengths, n_q):
+    inp = W.generate(W.custom("prefill", lengths, n_q=n_q), seed=22)
+    s = session(inp)
+    assert s.path == "non_absorbed" and s.launches_per_step() == 3
+    check_prefill(s, inp, heads=[0, 77, 127])
+
+
+@pytest.mark.parametrize("n_q", [1, 4])
+def test_both_paths_agree_on_short_steps(n_q):
+    """A short step through the non-absorbed path: the oracle's answer, and
+    close to the absorbed path's (different roundings, same definition)."""
+    inp = W.generate(W.custom("both", [0, 70, 640], n_q=n_q), seed=23)
+    a = session(inp, path="absorbed")
+    n = session(inp, path="non_absorbed")
+    assert a.path == "absorbed" and n.path == "non_absorbed"
+    check_prefill(n, inp, heads=[0, 31, 127])
+    assert rel_l2(n.out.float().cpu().numpy(), a.out.float().cpu().numpy()) <= 2 * O_REL_L2
