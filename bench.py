@@ -42,6 +42,8 @@ from mla_absorbed_decode_absorb_gb300 import accounting as A  # noqa: E402
 from mla_absorbed_decode_absorb_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MLA absorbed decode µs/step, latent-cache GB/s and TFLOP/s vs GB300 roofline"
+METRIC_PREFILL = "MLA non-absorbed chunked prefill, new tokens/s and TFLOP/s vs GB300 roofline"
+PREFILL_KERNEL = "prefill attention (mla_prefill_attn)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 DOMINANT_KERNEL = "split attention (mla_decode_attn_partial)"
@@ -53,7 +55,8 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=400)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=W.DEFAULT_BENCH_WORKLOAD, choices=sorted(W.WORKLOADS))
+    p.add_argument("--workload", default=W.DEFAULT_BENCH_WORKLOAD,
+                   choices=sorted(W.WORKLOADS) + sorted(W.PREFILL_WORKLOADS))
     p.add_argument("--split-pages", type=int, default=None, help="override the workload's KV split size")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-oracle sample budget")
@@ -205,29 +208,68 @@ def oracle_sample(inp: W.Inputs, budget_s: float, max_seqs: int | None = None):
     return nbytes, t, done
 
 
+def oracle_prefill_sample(inp: W.Inputs, budget_s: float):
+    """The fp64 oracle on a bounded sample of a many-token step: the first new
+    tokens of sequence 0 on 16 heads, as many 8-token groups as the budget
+    allows; returns (new tokens scaled to all 128 heads, seconds, description)."""
+    import numpy as np
+
+    from oracle import mla_oracle as O
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    heads = list(range(16))
+    w_uk, w_uv = O.bf16_bits_to_f64(bits(inp.w_uk)), O.bf16_bits_to_f64(bits(inp.w_uv))
+    c_bits, k_bits = (bits(x) for x in inp.sequence(0))
+    kv = c_bits.shape[0]
+    c = O.bf16_bits_to_f64(c_bits)
+    kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(kv)))
+    q_nope, q_rope = O.bf16_bits_to_f64(bits(inp.q_nope[0])), O.bf16_bits_to_f64(bits(inp.q_rope[0]))
+    L = int(inp.prior_lens[0])
+    done, t = 0, 0.0
+    while done < q_nope.shape[0] and (done == 0 or t < budget_s):
+        j0 = done
+        t0 = time.perf_counter()
+        # queries j0 .. j0+7 of the chunk: the oracle's definition with the prior context shifted
+        O.decode_mha(q_nope[j0:j0 + 8], q_rope[j0:j0 + 8], w_uk, w_uv, c[:L + j0 + 8], kr[:L + j0 + 8], L + j0, heads)
+        t += time.perf_counter() - t0
+        done = min(q_nope.shape[0], j0 + 8)
+    tokens = done * len(heads) / 128
+    return tokens, t, f"first {done} new tokens of sequence 0 on 16 of 128 heads ({t:.1f} s), scaled to 128 heads"
+
+
 def run_reference(args, wl):
     rank, _, world = dist_env()
     if rank != 0:
         return 0
     inp = W.generate(wl, seed=0)
+    prefill = wl.name in W.PREFILL_WORKLOADS
+    if prefill:  # the oracle on 8 new tokens x 16 heads per step, scaled to tokens of all heads
+        sample_fn = lambda: oracle_prefill_sample(inp, 0.0)[:2]  # noqa: E731
+        sample = "8 new tokens of sequence 0 on 16 of 128 heads per step, scaled to 128 heads"
+        metric, unit, scale = METRIC_PREFILL, "tokens/s", 1.0
+    else:
+        sample_fn = lambda: oracle_sample(inp, 0.0, max_seqs=1)[:2]  # noqa: E731
+        sample = f"one sequence ({int(inp.kv_lens[0])} cached tokens, all 128 heads) of the workload per step"
+        metric, unit, scale = METRIC, "GB/s", 1e9
     for _ in range(args.warmup):
-        oracle_sample(inp, 0.0, max_seqs=1)
+        sample_fn()
     per_step = []
-    nbytes = 0
+    units = 0
     for _ in range(args.steps):
-        nb, t, _ = oracle_sample(inp, 0.0, max_seqs=1)
+        u, t = sample_fn()
         per_step.append(t)
-        nbytes = nb
+        units = u
     mean_t = sum(per_step) / len(per_step)
-    value = nbytes / mean_t / 1e9
-    sample = f"one sequence ({int(inp.kv_lens[0])} cached tokens, all 128 heads) of the workload per step"
+    value = units / mean_t / scale
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_t * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(wl, inp, world, {"sample": sample}),
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle", "sample": sample},
-        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
     return 0
@@ -275,8 +317,16 @@ def run_ours(args, wl):
     s = DecodeSession(inp, device=dev, split_pages=args.split_pages)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    step_bytes = A.step_cache_bytes(inp.kv_lens.tolist())
-    step_flops = A.step_attention_flops(inp.kv_lens.tolist(), wl.n_q)
+    kv_list = inp.kv_lens.tolist()
+    prefill = s.path == "non_absorbed"
+    step_bytes = A.step_cache_bytes(kv_list)
+    if prefill:  # the metric counts new tokens; the roofline rates the attention's FLOPs
+        step_units = wl.batch * wl.n_q
+        step_flops = A.prefill_attention_flops(kv_list, wl.n_q)
+        decompress_flops = A.decompress_flops(kv_list)
+    else:
+        step_units = step_bytes
+        step_flops = A.step_attention_flops(kv_list, wl.n_q)
 
     for _ in range(max(args.warmup, 3)):
         flush.zero_()
@@ -322,9 +372,9 @@ def run_ours(args, wl):
             e[i + 1].record(stream)
     torch.cuda.synchronize()
     per_stage = [[sev[k][i].elapsed_time(sev[k][i + 1]) for k in range(K3)] for i in range(len(stages))]
-    attn_i = stages.index("attend_partial")
+    attn_i = stages.index("prefill_attn" if prefill else "attend_partial")
     (mean_ms, attn_ms), total_bytes = reduce_over_ranks([sum(step_ms) / K, sum(per_stage[attn_i]) / K3],
-                                                       step_bytes, dev)
+                                                       step_units, dev)
     if ops.mla_get_device_status() != ops.MLA_OK:
         raise RuntimeError("device status set during the stage breakdown")
 
@@ -349,7 +399,7 @@ def run_ours(args, wl):
             if k >= 3:
                 e2e_ms.append(a.elapsed_time(b))
         (m,), _ = reduce_over_ranks([sum(e2e_ms) / len(e2e_ms)], 0, dev)
-        e2e = {"value": total_bytes / (m * 1e-3) / 1e9, "unit": "GB/s",
+        e2e = {"value": total_bytes / (m * 1e-3) / (1 if prefill else 1e9), "unit": "tokens/s" if prefill else "GB/s",
                "ms_per_step": m, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     if world > 1:
@@ -358,24 +408,32 @@ def run_ours(args, wl):
         return 0
 
     peaks, peak_src = load_peaks()
-    t_mem, bound = A.roofline_seconds(inp.kv_lens.tolist(), wl.n_q, peaks["hbm_gbs"], peaks["bf16_tflops"])
+    t_mem, bound = A.roofline_seconds(kv_list, wl.n_q, peaks["hbm_gbs"], peaks["bf16_tflops"])
     attn_s = attn_ms * 1e-3
-    if bound == "hbm":
+    if prefill:
+        t_mem, bound = (step_flops + decompress_flops) / (peaks["bf16_tflops"] * 1e12), "tensor"
+        achieved, peak, unit = step_flops / attn_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    elif bound == "hbm":
         achieved, peak, unit = step_bytes / attn_s / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = step_flops / attn_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                "traffic": profiled_traffic(wl.name), "peak_source": peak_src,
-                "kernel": DOMINANT_KERNEL, "algorithmic_bytes": step_bytes, "algorithmic_flops": step_flops}
+                "traffic": None if prefill else profiled_traffic(wl.name), "peak_source": peak_src,
+                "kernel": PREFILL_KERNEL if prefill else DOMINANT_KERNEL, "algorithmic_bytes": step_bytes,
+                "algorithmic_flops": step_flops}
 
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and prefill:
+        ntok, secs, desc = oracle_prefill_sample(inp, args.cpu_seconds)
+        cpu = {"value": ntok / secs, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
+    elif world == 1 and not args.no_cpu_baseline:
         nb, secs, nseq = oracle_sample(inp, args.cpu_seconds)
         cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{nseq} of {inp.batch} sequences, all 128 heads, fp64 non-absorbed form ({secs:.1f} s)"}
 
     line = {
-        "metric": METRIC, "value": total_bytes / (mean_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "metric": METRIC_PREFILL if prefill else METRIC,
+        "value": total_bytes / (mean_ms * 1e-3) / (1 if prefill else 1e9), "unit": "tokens/s" if prefill else "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": mean_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
@@ -384,6 +442,9 @@ def run_ours(args, wl):
         "attn_us": attn_ms * 1e3,
         "attn_tflops": step_flops / attn_s / 1e12,
         "attn_gbs": step_bytes / attn_s / 1e9,
+        "path": s.path,
+        "decompress_tflops": (decompress_flops / (1e-3 * sum(per_stage[stages.index("decompress")]) / K3) / 1e12
+                              if prefill else None),
         "stage_us": {n: 1e3 * sum(v) / K3 for n, v in zip(stages, per_stage)},
         "launch_overlap": ops.mla_get_launch_overlap(),
         "roofline_time_us": t_mem * 1e6,
@@ -400,7 +461,7 @@ def run_ours(args, wl):
 
 def main(argv=None):
     args = parse_args(argv)
-    wl = W.WORKLOADS[args.workload]
+    wl = W.WORKLOADS.get(args.workload) or W.PREFILL_WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -1,4 +1,4 @@
-"""Algorithmic byte and FLOP counts of one absorbed MLA decode step.
+"""Algorithmic byte and FLOP counts of one MLA step, on either path.
 
 These are the figures the roofline is taken against, counted from the problem
 statement, not from any kernel:
@@ -12,6 +12,12 @@ statement, not from any kernel:
   the MLA history-interaction count), i.e. 139,264 MACs = 278,528 FLOP;
 * query token ``j`` of a sequence with ``L`` prior tokens sees ``L + j + 1``
   cache tokens (causal among the new tokens).
+
+The non-absorbed path (a chunk of many new tokens) first decompresses every
+cached token into per-head keys and values, ``2 * n_h * d_h * d_c`` MACs per token
+([MA] section 2.2, K = c W_UK, V = c W_UV), then does ``n_h * (d_h + d_h^R + d_v)``
+MACs per (query token, visible token) (DeepSeek-MLA-Principle section 6, the
+non-absorbed L^2 terms: logits over 192 columns and the weighted sum over 128).
 """
 
 from __future__ import annotations
@@ -68,3 +74,27 @@ def roofline_seconds(kv_lens, n_q: int, hbm_gbs: float, tflops: float) -> tuple[
     t_mem = step_cache_bytes(kv_lens) / (hbm_gbs * 1e9)
     t_flop = step_attention_flops(kv_lens, n_q) / (tflops * 1e12)
     return (t_mem, "hbm") if t_mem >= t_flop else (t_flop, "tensor")
+
+
+def decompress_macs_per_token() -> int:
+    """K and V of one cached token for all heads: 2 * n_h * d_h * d_c."""
+    return 2 * N_HEADS * D_NOPE * D_LATENT
+
+
+def prefill_pair_macs() -> int:
+    """Non-absorbed attention per (query token, visible token): n_h * (d_h + d_h^R + d_v)."""
+    return N_HEADS * (D_NOPE + D_ROPE + D_NOPE)
+
+
+def prefill_attention_flops(kv_lens, n_q: int) -> int:
+    tot = 0
+    for n in kv_lens:
+        L = int(n) - n_q
+        pairs = n_q * (L + 1) + n_q * (n_q - 1) // 2  # sum over j of (L + j + 1)
+        tot += 2 * pairs * prefill_pair_macs()
+    return tot
+
+
+def decompress_flops(kv_lens) -> int:
+    return sum(int(n) for n in kv_lens) * 2 * decompress_macs_per_token()
+

@@ -71,6 +71,18 @@ WORKLOADS: dict[str, Workload] = {
     ]
 }
 
+# Steps with many new tokens per sequence, which take the non-absorbed path
+# (chunked prefill after a prior context, and a prompt with no prior context).
+PREFILL_WORKLOADS: dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("chunk_b4_l4096_c512", batch=4, n_q=512, context=4096,
+                 description="B=4, a chunk of 512 new tokens each after a prior context of 4096"),
+        Workload("prompt_b8_c2048", batch=8, n_q=2048, context=0,
+                 description="B=8, a 2048-token prompt each, no prior context"),
+    ]
+}
+
 DEFAULT_BENCH_WORKLOAD = "batched_b32_l4096"
 
 
