@@ -21,29 +21,29 @@
 //     hold bitwise-equal scores S = S_0 + S_1;
 //   * runs the same online softmax as its peer on that S, so both use identical
 //     P, running max and sum, and accumulates its half of O' = P c.
-// Half of the CTA's 256 latent query columns sit in TMEM (QK^T MMAs with A read
-// from TMEM), the other half and the RoPE columns in shared memory.
-//
-// Pages land in a ring of four 64-token slots stored chunk by chunk (all slots'
-// rows of one 64-column chunk are contiguous), so two consecutive slots form one
-// 128-token operand: QK^T is issued per tile of two pages with N = 128, which
-// keeps the tensor pipe at its full rate (N = 64 runs it at about half), while
-// P V stays per page (N = 256).
+// The CTA's 256 latent query columns sit in TMEM, so the latent QK^T MMAs read A
+// from TMEM and only their B operand (the page's keys) from shared memory: at
+// N = 64 that is a quarter of the shared-memory bandwidth, which leaves room
+// for the TMA writes and the score exchange (SS MMAs, which also read A from
+// shared memory, slowed down severalfold next to them).  Only the 32 RoPE query
+// columns stay in shared memory, which leaves room for a 5-stage ring of
+// half-pages.
 //
 // Warp roles: warp 0 issues TMA loads (page ids are read 32 at a time); warp 1
 // allocates TMEM and one of its threads issues tcgen05.mma, polling its
-// barriers so that P V of a page whose P is ready goes out first (it releases a
-// slot) and QK^T of a landed tile otherwise; warps 2-9 are two row warpgroups,
-// one thread per head row, and warpgroup g handles the pages i = g (mod 2), i.e.
-// the score columns [64g, 64g + 64) of each tile: it reads its partial scores
-// from TMEM, swaps them with the peer CTA, adds them, runs the softmax step and
-// writes P(i) into its own TMEM P buffer.  The two warpgroups pass only the
-// running reference max to each other, so the exchange of page i + 1 overlaps
-// the softmax of page i.  Warp 10 re-arms each exchange buffer once it has been
-// read and tells the peer (a cluster-scope release that would otherwise stall a
-// row warpgroup).  The reference max is updated lazily: O' in TMEM is rescaled
-// only when a page raises a row's max by more than 2^8; each warpgroup keeps
-// its own partial row sum relative to the max it last used.
+// barriers so that QK^T of a page whose data has landed and P V of a page whose
+// P is ready go out in whichever order they become ready (P V first, since it
+// releases a stage); warps 2-9 are two row warpgroups, one thread per head row,
+// and warpgroup g handles the pages i = g (mod 2): it reads the partial scores
+// of page i from TMEM (which frees the score buffer for QK^T of page i + 1 at
+// once), swaps them with the peer CTA, adds them, runs the softmax step and
+// writes P(i) into its own TMEM P buffer.  The two warpgroups
+// pass only the running reference max to each other, so the exchange of page
+// i + 1 overlaps the softmax of page i.  Warp 10 re-arms each exchange buffer
+// once it has been read and tells the peer (a cluster-scope release that would
+// otherwise stall a row warpgroup).  The reference max is updated lazily: O' in
+// TMEM is rescaled only when a page raises a row's max by more than 2^8; each
+// warpgroup keeps its own partial row sum relative to the max it last used.
 #include "sm100.cuh"
 #include "tmap.cuh"
 
@@ -52,7 +52,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kSlots = 4;           // 64-token page slots: two tiles of two pages
+constexpr int kStages = 5;
 constexpr int kThreads = 352;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -61,22 +61,17 @@ constexpr int kSignalWarp = 10;
 constexpr int kRowThreads = 128;    // threads of each row warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O' half: [0, 256)
-constexpr uint32_t kTmemS = 256;    // tile scores, page g of the tile in [256 + 64g, 320 + 64g)
-constexpr uint32_t kTmemP = 384;    // P of warpgroup g (64 bf16 per row = 32 columns): [384 + 32g, 416 + 32g)
-constexpr uint32_t kTmemQ = 448;    // the CTA's first 128 latent query columns as bf16 pairs: [448, 512)
+constexpr uint32_t kTmemS = 256;    // score buffer: [256, 320)
+constexpr uint32_t kTmemP = 320;    // P buffer of warpgroup g (64 bf16 per row = 32 columns): [320 + 32g, 352 + 32g)
+constexpr uint32_t kTmemQ = 384;    // the CTA's 256 latent query columns as bf16 pairs: [384, 512)
 
-constexpr int kQChunk = 128 * 128;    // 64 latent query columns x 128 heads, 128-byte rows (SW128)
-constexpr int kQRope = 128 * 64;      // 32 RoPE columns x 128 heads, 64-byte rows (SW64)
-constexpr int kQBytes = 2 * kQChunk + kQRope;  // query columns kept in shared memory
-constexpr int kSlotChunk = 64 * 128;  // one page's 64 latent columns (SW128 rows of 128 B)
-constexpr int kSlotRope = 64 * 64;    // one page's 32 RoPE columns (SW64 rows of 64 B)
-constexpr int kChunkRing = kSlots * kSlotChunk;  // stride between the four latent chunks of the ring
-constexpr int kRingBytes = 4 * kChunkRing + kSlots * kSlotRope;
-constexpr uint32_t kPageTx = 4 * kSlotChunk + kSlotRope;  // bytes of one page's TMA loads
+constexpr int kQRope = 128 * 64;      // 32 RoPE query columns x 128 heads, 64-byte rows (SW64)
+constexpr int kPChunk = 64 * 128;     // 64 latent columns x 64 tokens (SW128)
+constexpr int kPRope = 64 * 64;       // 32 RoPE columns x 64 tokens (SW64)
+constexpr int kStageBytes = 4 * kPChunk + kPRope;
 // Exchange buffer: 64 fp16 partial scores per row, stored unit-major (16-byte unit
 // q of row r at q * 2048 + r * 16), so that each warp's stores and loads of one
-// unit cover 512 contiguous bytes: whole 128-byte lines, which matters because
-// the SS MMAs of QK^T want nearly all of the shared-memory bandwidth.
+// unit cover 512 contiguous bytes: whole 128-byte lines.
 constexpr int kXBufBytes = kRowThreads * 128;
 constexpr uint32_t kXTxBytes = kXBufBytes;
 // Exchanged partial scores are fp16(S_r * 2^-8); their fp32 sum times 2^8 kScale
@@ -85,32 +80,31 @@ constexpr float kXScale = 1.f / 256.f;
 constexpr float kSumScaleLog2 = kScaleLog2 * 256.f;
 
 constexpr int kOffQ = 0;
-constexpr int kOffRing = kOffQ + kQBytes;
-constexpr int kOffRope = kOffRing + 4 * kChunkRing;
-constexpr int kOffX = kOffRing + kRingBytes;
+constexpr int kOffStage = kOffQ + kQRope;
+constexpr int kOffX = kOffStage + kStages * kStageBytes;
 constexpr int kOffBar = kOffX + 2 * kXBufBytes;
 constexpr int kOffMax = kOffBar + 256;          // per-row reference max handed between warpgroups
 constexpr int kOffFin = kOffMax + 4 * kHeads;     // per-warpgroup (max, sum) per row at the end
 constexpr int kSmemBytes = kOffFin + 8 * 2 * kHeads + 1024;  // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffRing % 1024 == 0 && kOffRope % 1024 == 0, "swizzled tiles start on 1 KB");
+static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled tiles start on 1 KB");
 
 constexpr float kRescaleLog2 = 8.f;
 
 struct Bars {
-  uint64_t full[kSlots];   // page landed in the slot
-  uint64_t empty[kSlots];  // P V of the slot's page has finished
-  uint64_t q_full;         // query columns in shared memory
-  uint64_t q_tmem;         // latent query columns in TMEM
-  uint64_t s_full;         // partial scores of the current tile are in TMEM
-  uint64_t s_free;         // both warpgroups have read them
-  uint64_t p_full[2];      // P of warpgroup g's current page is in its TMEM buffer
-  uint64_t pv_done[2];     // P V of the last page of warpgroup g has finished
-  uint64_t x_full[2];      // peer's partial scores landed in exchange buffer g
-  uint64_t x_free[2];      // peer has read our partial scores from its buffer g
-  uint64_t x_read[2];      // all rows of warpgroup g have read exchange buffer g
-  uint64_t hand[2];        // warpgroup g has published the reference max of its page
-  uint64_t fin;            // both warpgroups have published their final (max, sum)
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t q_full;      // RoPE query columns in shared memory
+  uint64_t q_tmem;      // latent query columns in TMEM
+  uint64_t s_full[2];   // partial scores of warpgroup g's current page are in the score buffer
+  uint64_t s_free[2];   // warpgroup g has read them
+  uint64_t p_full[2];   // P of warpgroup g's current page is in its TMEM buffer
+  uint64_t pv_done[2];  // P V of the last page of warpgroup g has finished
+  uint64_t x_full[2];   // peer's partial scores landed in exchange buffer g
+  uint64_t x_free[2];   // peer has read our partial scores from its buffer g
+  uint64_t x_read[2];   // all rows of warpgroup g have read exchange buffer g
+  uint64_t hand[2];     // warpgroup g has published the reference max of its page
+  uint64_t fin;         // both warpgroups have published their final (max, sum)
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -135,9 +129,8 @@ struct Params {
 __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
-                      const __grid_constant__ CUtensorMap tm_c128, const __grid_constant__ CUtensorMap tm_c64,
-                      const Params p) {
+decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_constant__ CUtensorMap tm_c128,
+                      const __grid_constant__ CUtensorMap tm_c64, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBar);
@@ -152,21 +145,21 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
   const int b = bj / p.n_q, j = bj % p.n_q;
 
   if (tid == 0) {
-    for (int s = 0; s < kSlots; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(bar_addr(bars.full[s]), 1);
       mbar_init(bar_addr(bars.empty[s]), 1);
     }
     mbar_init(bar_addr(bars.q_full), 1);
     mbar_init(bar_addr(bars.q_tmem), 2 * kRowThreads);
-    mbar_init(bar_addr(bars.s_full), 1);
-    mbar_init(bar_addr(bars.s_free), 2 * kRowThreads);
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(bar_addr(bars.p_full[g]), kRowThreads);
-      mbar_init(bar_addr(bars.pv_done[g]), 1);
-      mbar_init(bar_addr(bars.x_full[g]), 1);
-      mbar_init(bar_addr(bars.x_free[g]), 1);
-      mbar_init(bar_addr(bars.x_read[g]), kRowThreads);
-      mbar_init(bar_addr(bars.hand[g]), kRowThreads);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_addr(bars.s_full[s]), 1);
+      mbar_init(bar_addr(bars.s_free[s]), kRowThreads);
+      mbar_init(bar_addr(bars.p_full[s]), kRowThreads);
+      mbar_init(bar_addr(bars.pv_done[s]), 1);
+      mbar_init(bar_addr(bars.x_full[s]), 1);
+      mbar_init(bar_addr(bars.x_free[s]), 1);
+      mbar_init(bar_addr(bars.x_read[s]), kRowThreads);
+      mbar_init(bar_addr(bars.hand[s]), kRowThreads);
     }
     mbar_init(bar_addr(bars.fin), 2 * kRowThreads);
     mbar_init(bar_addr(bars.drain), 1);
@@ -205,17 +198,12 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
       int ids = lane < n_pages ? pt[lane] : 0;
       int ids_next = 32 + lane < n_pages ? pt[32 + lane] : 0;
       if (lane == 0) {
-        tma_prefetch_desc(&tm_q128);
         tma_prefetch_desc(&tm_q64);
         tma_prefetch_desc(&tm_c128);
         tma_prefetch_desc(&tm_c64);
-        // query columns [256r + 128, 256r + 256) and the RoPE half r into shared memory
-        const uint32_t qb = smem_u32(smem + kOffQ);
-        const int q_row = bj * kHeads;
-        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQBytes);
-        for (int c = 0; c < 2; ++c)
-          tma_load_2d(qb + c * kQChunk, &tm_q128, 256 * rank + 128 + 64 * c, q_row, bar_addr(bars.q_full));
-        tma_load_2d(qb + 2 * kQChunk, &tm_q64, kLatent + 32 * rank, q_row, bar_addr(bars.q_full));
+        // the RoPE query half r into shared memory
+        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQRope);
+        tma_load_2d(smem_u32(smem + kOffQ), &tm_q64, kLatent + 32 * rank, bj * kHeads, bar_addr(bars.q_full));
       }
       bool ok = true;
       for (int base = 0; base < n_pages && ok; base += 32) {
@@ -224,19 +212,19 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
           const int i = base + k;
           int page = __shfl_sync(0xffffffffu, ids, k);
           if (lane == 0) {
-            const int s = i % kSlots;
-            ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kSlots) & 1) ^ 1, p.status, abort);
+            const int s = i % kStages;
+            ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
             if (ok) {
               if (page < 0 || page >= p.num_pages) {
                 record_status(p.status, MLA_ERR_BOUNDS);
                 page = 0;  // stay in bounds; the result of this unit is not meaningful
               }
+              const uint32_t sb = smem_u32(smem + kOffStage + s * kStageBytes);
               const uint32_t fb = bar_addr(bars.full[s]);
-              mbar_arrive_expect_tx(fb, kPageTx);
+              mbar_arrive_expect_tx(fb, kStageBytes);
               for (int c = 0; c < 4; ++c)
-                tma_load_2d(smem_u32(smem + kOffRing + c * kChunkRing + s * kSlotChunk), &tm_c128,
-                            64 * (4 * rank + c), page * kPage, fb);
-              tma_load_2d(smem_u32(smem + kOffRope + s * kSlotRope), &tm_c64, kLatent + 32 * rank, page * kPage, fb);
+                tma_load_2d(sb + c * kPChunk, &tm_c128, 64 * (4 * rank + c), page * kPage, fb);
+              tma_load_2d(sb + 4 * kPChunk, &tm_c64, kLatent + 32 * rank, page * kPage, fb);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -249,73 +237,60 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     // ------------------------------------------------------------ tcgen05 issuer
     // One thread schedules and issues everything; the rest of the warp waits.
     if (n_pages > 0 && lane == 0) {
-      const int n_tiles = (n_pages + 1) >> 1;
-      const uint32_t idesc_qk2 = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/0);  // two-page tile
-      const uint32_t idesc_qk1 = idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);   // last tile of an odd count
+      const uint32_t idesc_qk = idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
       const uint32_t idesc_pv = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/1);
-      // Descriptors at the ring's origin; a slot, chunk or K step is a byte
-      // offset added to the start-address field (16-byte units).
-      const uint64_t d_k = smem_desc(smem_u32(smem + kOffRing), 16, 1024, kSw128);          // keys, latent
-      const uint64_t d_kr = smem_desc(smem_u32(smem + kOffRope), 16, 512, kSw64);           // keys, RoPE half
-      const uint64_t d_v = smem_desc(smem_u32(smem + kOffRing), kChunkRing, 1024, kSw128);  // values (MN-major)
-      const uint64_t d_ql = smem_desc(smem_u32(smem + kOffQ), 16, 1024, kSw128);               // query chunks 2, 3
-      const uint64_t d_qr = smem_desc(smem_u32(smem + kOffQ + 2 * kQChunk), 16, 512, kSw64);   // query RoPE half
+      // Descriptors of stage 0 and of the RoPE query columns; a stage, chunk or
+      // K step is a byte offset added to the start-address field (16-byte units).
+      const uint32_t st0 = smem_u32(smem + kOffStage);
+      const uint64_t d_k128 = smem_desc(st0, 16, 1024, kSw128);             // keys, latent chunk 0
+      const uint64_t d_k64 = smem_desc(st0 + 4 * kPChunk, 16, 512, kSw64);  // keys, RoPE half
+      const uint64_t d_v = smem_desc(st0, kPChunk, 1024, kSw128);           // values (MN-major)
+      const uint64_t d_qr = smem_desc(smem_u32(smem + kOffQ), 16, 512, kSw64);  // RoPE query half
       bool ok = mbar_wait(bar_addr(bars.q_full), 0, p.status, abort) &&
                 mbar_wait(bar_addr(bars.q_tmem), 0, p.status, abort);
 
-      // S(u) = Q K(u)^T for the tile of pages 2u, 2u + 1 (slots 2(u % 2), +1).
-      auto issue_qk = [&](int u) {
+      // S(i) = Q K(i)^T into the score buffer.
+      auto issue_qk = [&](int i) {
         tc_fence_after();
-        const int s0 = 2 * (u & 1);
-        const uint32_t idesc = 2 * u + 1 < n_pages ? idesc_qk2 : idesc_qk1;
-        const uint64_t so = static_cast<uint64_t>((s0 * kSlotChunk) >> 4);
-        const uint64_t sr = static_cast<uint64_t>((s0 * kSlotRope) >> 4);
+        const uint64_t so = static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
         const uint32_t d = tmem + kTmemS;
-        // latent chunks 0, 1: A = query columns in TMEM (8 columns per K step of 16)
-        mma_ts(d, tmem + kTmemQ, d_k + so, idesc, 0u);
+        // latent part: A = query columns in TMEM (8 columns per K step of 16)
+        mma_ts(d, tmem + kTmemQ, d_k128 + so, idesc_qk, 0u);
 #pragma unroll
-        for (int k = 1; k < 8; ++k)
-          mma_ts(d, tmem + kTmemQ + 8 * k, d_k + so + (k >> 2) * (kChunkRing >> 4) + (k & 3) * 2, idesc, 1u);
-        // latent chunks 2, 3: A = query columns in shared memory
-#pragma unroll
-        for (int k = 8; k < 16; ++k)
-          mma_ss(d, d_ql + ((k - 8) >> 2) * (kQChunk >> 4) + (k & 3) * 2,
-                 d_k + so + (k >> 2) * (kChunkRing >> 4) + (k & 3) * 2, idesc, 1u);
-        // RoPE part
-        mma_ss(d, d_qr, d_kr + sr, idesc, 1u);
-        mma_ss(d, d_qr + 2, d_kr + sr + 2, idesc, 1u);
-        mma_commit(bar_addr(bars.s_full));
+        for (int k = 1; k < 16; ++k)
+          mma_ts(d, tmem + kTmemQ + 8 * k, d_k128 + so + (k >> 2) * (kPChunk >> 4) + (k & 3) * 2, idesc_qk, 1u);
+        // RoPE part: A = query columns in shared memory
+        mma_ss(d, d_qr, d_k64 + so, idesc_qk, 1u);
+        mma_ss(d, d_qr + 2, d_k64 + so + 2, idesc_qk, 1u);
+        mma_commit(bar_addr(bars.s_full[i & 1]));
       };
-      // O' += P(i) V(i); then page i's slot goes back to the producer and
+      // O' += P(i) V(i); then page i's stage goes back to the producer and
       // warpgroup i & 1 may reuse its P buffer.
       auto issue_pv = [&](int i) {
         tc_fence_after();
-        const int s = i % kSlots;
-        const uint64_t vb = d_v + static_cast<uint64_t>((s * kSlotChunk) >> 4);
+        const uint64_t vb = d_v + static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
         const uint32_t a = tmem + kTmemP + (i & 1) * 32;
         mma_ts(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
 #pragma unroll
         for (int k = 1; k < 4; ++k) mma_ts(tmem + kTmemO, a + 8 * k, vb + 128 * k, idesc_pv, 1u);
-        mma_commit(bar_addr(bars.empty[s]));
+        mma_commit(bar_addr(bars.empty[i % kStages]));
         mma_commit(bar_addr(bars.pv_done[i & 1]));
       };
 
-      // Poll: P V of page np once its P is written; otherwise QK^T of tile nq
-      // once its pages have landed and both warpgroups have read the scores of
-      // tile nq - 1.  The tensor pipe runs them in issue order.
+      // Poll: P V of page np (< nq) once its P is written; otherwise QK^T of
+      // page nq once it has landed and the scores of page nq - 1 have been read
+      // out of the score buffer.  The tensor pipe runs them in issue order.
       int nq = 0, np = 0;
       uint64_t t0 = 0;
       uint32_t idle = 0;
       while (ok && np < n_pages) {
-        if (np < 2 * nq && mbar_test(bar_addr(bars.p_full[np & 1]), (np >> 1) & 1)) {
+        if (np < nq && mbar_test(bar_addr(bars.p_full[np & 1]), (np >> 1) & 1)) {
           issue_pv(np++);
           idle = 0;
           continue;
         }
-        if (nq < n_tiles && mbar_test(bar_addr(bars.full[(2 * nq) % kSlots]), ((2 * nq) / kSlots) & 1) &&
-            (2 * nq + 1 >= n_pages ||
-             mbar_test(bar_addr(bars.full[(2 * nq + 1) % kSlots]), ((2 * nq + 1) / kSlots) & 1)) &&
-            (nq == 0 || mbar_test(bar_addr(bars.s_free), (nq - 1) & 1))) {
+        if (nq < n_pages && mbar_test(bar_addr(bars.full[nq % kStages]), (nq / kStages) & 1) &&
+            (nq == 0 || mbar_test(bar_addr(bars.s_free[(nq - 1) & 1]), ((nq - 1) >> 1) & 1))) {
           issue_qk(nq++);
           idle = 0;
           continue;
@@ -341,10 +316,10 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     // ------------------------------------------------------------ exchange buffer recycling
     if (lane == 0) {
       for (int i = 0; i < n_pages; ++i) {
-        const int g = i & 1;
-        if (!mbar_wait(bar_addr(bars.x_read[g]), (i >> 1) & 1, p.status, abort)) break;
-        mbar_arrive_expect_tx(bar_addr(bars.x_full[g]), kXTxBytes);   // armed for the buffer's next use
-        mbar_arrive_remote(mapa(bar_addr(bars.x_free[g]), peer));      // the peer may refill it
+        const int buf = i & 1;
+        if (!mbar_wait(bar_addr(bars.x_read[buf]), (i >> 1) & 1, p.status, abort)) break;
+        mbar_arrive_expect_tx(bar_addr(bars.x_full[buf]), kXTxBytes);   // armed for the buffer's next use
+        mbar_arrive_remote(mapa(bar_addr(bars.x_free[buf]), peer));      // the peer may refill it
       }
     }
   } else {
@@ -357,34 +332,37 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
     float2* fin = reinterpret_cast<float2*>(smem + kOffFin);
     bool ok = n_pages > 0;
     if (ok) {
-      // latent query columns [256r + 64g, 256r + 64g + 64) of the row into TMEM as bf16 pairs
+      // latent query columns [256r + 128g, 256r + 128g + 128) of the row into TMEM as bf16 pairs
       const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<int64_t>(bj) * kHeads + row) * kRow +
-                                                         256 * rank + 64 * g);
-      uint32_t w[32];
+                                                         256 * rank + 128 * g);
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t w[32];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const uint4 v = qsrc[q];
-        w[4 * q] = v.x;
-        w[4 * q + 1] = v.y;
-        w[4 * q + 2] = v.z;
-        w[4 * q + 3] = v.w;
+        for (int q = 0; q < 8; ++q) {
+          const uint4 v = qsrc[8 * h + q];
+          w[4 * q] = v.x;
+          w[4 * q + 1] = v.y;
+          w[4 * q + 2] = v.z;
+          w[4 * q + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + kTmemQ + 64 * g + 32 * h, w);
       }
-      tmem_st32(tmem + lane_off + kTmemQ + 32 * g, w);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_addr(bars.q_tmem));
     }
-    // exchange buffer g, this row: 16-byte unit q at q * 2048 + row * 16
-    uint8_t* xrow = smem + kOffX + g * kXBufBytes + row * 16;
+    // exchange buffer g, this row: 16-byte unit u at (u ^ (row & 7)) * 16
+    uint8_t* xrow = smem + kOffX + g * kXBufBytes + row * 16;   // unit q of this row at q * 2048
     const uint32_t x_remote = mapa(smem_u32(xrow), peer);
     const uint32_t xfull_remote = mapa(bar_addr(bars.x_full[g]), peer);
-    const uint32_t s_addr = tmem + lane_off + kTmemS + 64 * g;  // this warpgroup's page of each tile
+    const uint32_t s_addr = tmem + lane_off + kTmemS;
     float range_max = 0.f;
     float m_mine = -INFINITY, l = 0.f;  // reference max this warpgroup last used, and its partial sum
     for (int i = g; i < n_pages && ok; i += 2) {
       const uint32_t use = (i >> 1) & 1;
       const int n_valid = min(kPage, t_end - (page_begin + i) * kPage);  // visible tokens of the page
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full), use, p.status, abort));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[g]), use, p.status, abort));
       if (!ok) break;
       tc_fence_after();
       uint32_t mine[32];
@@ -394,7 +372,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
         tmem_ld32(s_addr + 32, c);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar_addr(bars.s_free));  // QK^T of the next tile may overwrite the buffer
+        mbar_arrive(bar_addr(bars.s_free[g]));  // QK^T of page i + 1 may overwrite the buffer
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           const float x0 = __uint_as_float(a[2 * q]), x1 = __uint_as_float(a[2 * q + 1]);
@@ -489,11 +467,11 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_
       if (n_valid < kPage) {
         // Value rows past the last visible token may hold anything (NaN in
         // unwritten slots): zero them so that P = 0 there cannot make 0 * NaN.
-        uint8_t* slot = smem + kOffRing + (i % kSlots) * kSlotChunk;
+        uint8_t* stage = smem + kOffStage + (i % kStages) * kStageBytes;
         const int nrow = kPage - n_valid;
         for (int v = row; v < 4 * nrow * 8; v += kRowThreads) {
           const int c = v / (nrow * 8), r = n_valid + (v / 8) % nrow, u = v & 7;
-          *reinterpret_cast<uint4*>(slot + c * kChunkRing + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(stage + c * kPChunk + r * 128 + u * 16) = make_uint4(0, 0, 0, 0);
         }
         fence_proxy_async_smem();
       }
@@ -618,11 +596,10 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   if (units == 0) return cudaSuccess;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || !configure(dev)) return cudaErrorInvalidDevice;
-  CUtensorMap tq128, tq64, tc128, tc64;
+  CUtensorMap tq64, tc128, tc64;
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * kHeads;
   const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
-  if (!make_tmap_bf16_2d(&tq128, q_abs, q_rows, kRow, kRow, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_bf16_2d(&tc128, cache, c_rows, kRow, kRow, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
@@ -640,7 +617,7 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   prm.split_pages = plan.split_pages;
   prm.num_splits = plan.num_splits;
   return launch_kernel(decode_attn_tc_kernel, dim3(static_cast<unsigned>(2 * units)), dim3(kThreads), kSmemBytes, stream,
-                       tq128, tq64, tc128, tc64, prm);
+                       tq64, tc128, tc64, prm);
 }
 
 }  // namespace mla
