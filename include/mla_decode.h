@@ -52,7 +52,8 @@ typedef enum {
   MLA_ERR_TIMEOUT = 5,     /* (device status) a bounded wait ran out */
   MLA_ERR_BOUNDS = 6,      /* (device status) page id / position out of range */
   MLA_ERR_RANGE = 7        /* (device status) a partial attention score exceeded the
-                              kernel's exchange range (|q . row| over half a row > 1.6e7) */
+                              kernel's exchange range (|q . row| over half a row of at
+                              least 65520 * 256 = 1.677e7) or was NaN */
 } mla_status;
 
 enum {

@@ -17,8 +17,9 @@
 //     and RoPE [32r, 32r + 32), i.e. 36 KB per page instead of 72 KB;
 //   * computes the partial score over those 288 columns and swaps it with its
 //     peer through distributed shared memory; both CTAs round both partials to
-//     fp16 (scaled by 2^-8 for range) and add them in the same order, so they
-//     hold bitwise-equal scores S = S_0 + S_1;
+//     fp16 (scaled by 2^-8 for range: the query enters the MMAs pre-scaled) and
+//     add them in fp16 in the same order, so they hold bitwise-equal scores
+//     S = S_0 + S_1;
 //   * runs the same online softmax as its peer on that S, so both use identical
 //     P, running max and sum, and accumulates its half of O' = P c.
 // The CTA's 256 latent query columns sit in TMEM, so the latent QK^T MMAs read A
@@ -26,18 +27,21 @@
 // N = 64 that is a quarter of the shared-memory bandwidth, which leaves room
 // for the TMA writes and the score exchange (SS MMAs, which also read A from
 // shared memory, slowed down severalfold next to them).  Only the 32 RoPE query
-// columns stay in shared memory, which leaves room for a 5-stage ring of
-// half-pages.
+// columns stay in shared memory.  TMEM then holds O' (256 columns), the query
+// (128) and two 64-column score buffers, one per row warpgroup, so QK^T of the
+// next page never waits for the scores of the last one to be read; P goes to
+// shared memory (the A operand of P V, which reads it once per page), with a
+// 4-stage ring of half-pages beside it.
 //
 // Warp roles: warp 0 issues TMA loads (page ids are read 32 at a time); warp 1
-// allocates TMEM and one of its threads issues tcgen05.mma, polling its
-// barriers so that QK^T of a page whose data has landed and P V of a page whose
-// P is ready go out in whichever order they become ready (P V first, since it
-// releases a stage); warps 2-9 are two row warpgroups, one thread per head row,
+// allocates TMEM and one of its threads issues the QK^T MMAs, while one thread
+// of warp 11 issues the P V MMAs: an MMA issue blocks until the tensor pipe
+// takes it, so with a single issuer a ready P V waited behind a whole QK^T
+// batch (and the reverse); warps 2-9 are two row warpgroups, one thread per head row,
 // and warpgroup g handles the pages i = g (mod 2): it reads the partial scores
-// of page i from TMEM (which frees the score buffer for QK^T of page i + 1 at
-// once), swaps them with the peer CTA, adds them, runs the softmax step and
-// writes P(i) into its own TMEM P buffer.  The two warpgroups
+// of page i from its TMEM score buffer (which frees it for QK^T of page i + 2),
+// swaps them with the peer CTA, adds them, runs the softmax step and writes
+// P(i) into its own shared-memory P buffer.  The two warpgroups
 // pass only the running reference max to each other, so the exchange of page
 // i + 1 overlaps the softmax of page i.  Warp 10 re-arms each exchange buffer
 // once it has been read and tells the peer (a cluster-scope release that would
@@ -52,17 +56,17 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 5;
-constexpr int kThreads = 352;
+constexpr int kStages = 4;
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kRowWarp0 = 2;        // warps 2-5: row warpgroup 0, warps 6-9: row warpgroup 1
 constexpr int kSignalWarp = 10;
+constexpr int kPvWarp = 11;
 constexpr int kRowThreads = 128;    // threads of each row warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O' half: [0, 256)
-constexpr uint32_t kTmemS = 256;    // score buffer: [256, 320)
-constexpr uint32_t kTmemP = 320;    // P buffer of warpgroup g (64 bf16 per row = 32 columns): [320 + 32g, 352 + 32g)
+constexpr uint32_t kTmemS = 256;    // score buffer of warpgroup g: [256 + 64g, 320 + 64g)
 constexpr uint32_t kTmemQ = 384;    // the CTA's 256 latent query columns as bf16 pairs: [384, 512)
 
 constexpr int kQRope = 128 * 64;      // 32 RoPE query columns x 128 heads, 64-byte rows (SW64)
@@ -74,20 +78,25 @@ constexpr int kStageBytes = 4 * kPChunk + kPRope;
 // unit cover 512 contiguous bytes: whole 128-byte lines.
 constexpr int kXBufBytes = kRowThreads * 128;
 constexpr uint32_t kXTxBytes = kXBufBytes;
-// Exchanged partial scores are fp16(S_r * 2^-8); their fp32 sum times 2^8 kScale
-// is the scaled score, so the softmax folds 2^8 into its log2-domain scale.
-constexpr float kXScale = 1.f / 256.f;
+// Exchanged partial scores are fp16(S_r * 2^-8); their sum times 2^8 kScale is
+// the scaled score, so the softmax folds 2^8 into its log2-domain scale.  The
+// row work is done on fp16 pairs (add, max) and packed fp32 pairs (exponent
+// argument, row sum), half the instructions of scalar fp32.
 constexpr float kSumScaleLog2 = kScaleLog2 * 256.f;
 
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kOffQ + kQRope;
 constexpr int kOffX = kOffStage + kStages * kStageBytes;
-constexpr int kOffBar = kOffX + 2 * kXBufBytes;
+// P of warpgroup g: 128 rows x 64 bf16, K-major with the 128-byte swizzle (the A
+// operand of P V), row r at r * 128 with 16-byte chunk c at (c ^ (r & 7)) * 16.
+constexpr int kPBytes = kHeads * 128;
+constexpr int kOffP = kOffX + 2 * kXBufBytes;
+constexpr int kOffBar = kOffP + 2 * kPBytes;
 constexpr int kOffMax = kOffBar + 256;          // per-row reference max handed between warpgroups
 constexpr int kOffFin = kOffMax + 4 * kHeads;     // per-warpgroup (max, sum) per row at the end
 constexpr int kSmemBytes = kOffFin + 8 * 2 * kHeads + 1024;  // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0, "swizzled tiles start on 1 KB");
+static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1 KB");
 
 constexpr float kRescaleLog2 = 8.f;
 
@@ -98,14 +107,14 @@ struct Bars {
   uint64_t q_tmem;      // latent query columns in TMEM
   uint64_t s_full[2];   // partial scores of warpgroup g's current page are in the score buffer
   uint64_t s_free[2];   // warpgroup g has read them
-  uint64_t p_full[2];   // P of warpgroup g's current page is in its TMEM buffer
+  uint64_t p_full[2];   // P of warpgroup g's current page is in its P buffer (and O' rescaled)
   uint64_t pv_done[2];  // P V of the last page of warpgroup g has finished
   uint64_t x_full[2];   // peer's partial scores landed in exchange buffer g
   uint64_t x_free[2];   // peer has read our partial scores from its buffer g
   uint64_t x_read[2];   // all rows of warpgroup g have read exchange buffer g
   uint64_t hand[2];     // warpgroup g has published the reference max of its page
   uint64_t fin;         // both warpgroups have published their final (max, sum)
-  uint64_t drain;
+  uint64_t drain;       // both issuers' MMAs have finished
   uint32_t tmem_base;
   int abort;
 };
@@ -162,7 +171,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       mbar_init(bar_addr(bars.hand[s]), kRowThreads);
     }
     mbar_init(bar_addr(bars.fin), 2 * kRowThreads);
-    mbar_init(bar_addr(bars.drain), 1);
+    mbar_init(bar_addr(bars.drain), 2);
     bars.abort = 0;
     fence_mbar_init();
     // arm the first use of both exchange buffers: 16 KB of the peer's partial scores each
@@ -233,27 +242,32 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         ids_next = base + 64 + lane < n_pages ? pt[base + 64 + lane] : 0;
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ tcgen05 issuer
-    // One thread schedules and issues everything; the rest of the warp waits.
-    if (n_pages > 0 && lane == 0) {
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ------------------------------------------------------------ tcgen05 issuers
+    // One thread of warp 1 issues QK^T and one thread of warp 11 issues P V,
+    // each blocking on its own barriers, so that neither kind waits behind the
+    // other's issue (an MMA issue returns only once the tensor pipe accepts it).
+    // They touch disjoint TMEM (scores / O' and P) and a stage is released by
+    // P V of its page, which follows QK^T of that page through the softmax.
+    const uint32_t st0 = smem_u32(smem + kOffStage);
+    if (n_pages > 0 && lane == 0 && warp == kMmaWarp) {
       const uint32_t idesc_qk = idesc_bf16(128, 64, /*a_mn=*/0, /*b_mn=*/0);
-      const uint32_t idesc_pv = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/1);
       // Descriptors of stage 0 and of the RoPE query columns; a stage, chunk or
       // K step is a byte offset added to the start-address field (16-byte units).
-      const uint32_t st0 = smem_u32(smem + kOffStage);
       const uint64_t d_k128 = smem_desc(st0, 16, 1024, kSw128);             // keys, latent chunk 0
       const uint64_t d_k64 = smem_desc(st0 + 4 * kPChunk, 16, 512, kSw64);  // keys, RoPE half
-      const uint64_t d_v = smem_desc(st0, kPChunk, 1024, kSw128);           // values (MN-major)
       const uint64_t d_qr = smem_desc(smem_u32(smem + kOffQ), 16, 512, kSw64);  // RoPE query half
       bool ok = mbar_wait(bar_addr(bars.q_full), 0, p.status, abort) &&
                 mbar_wait(bar_addr(bars.q_tmem), 0, p.status, abort);
-
-      // S(i) = Q K(i)^T into the score buffer.
-      auto issue_qk = [&](int i) {
+      // S(i) = Q K(i)^T into score buffer i & 1, once page i has landed and the
+      // scores of page i - 2 have been read out of that buffer.
+      for (int i = 0; i < n_pages && ok; ++i) {
+        ok = mbar_wait(bar_addr(bars.full[i % kStages]), (i / kStages) & 1, p.status, abort);
+        if (ok && i > 1) ok = mbar_wait(bar_addr(bars.s_free[i & 1]), ((i - 2) >> 1) & 1, p.status, abort);
+        if (!ok) break;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
-        const uint32_t d = tmem + kTmemS;
+        const uint32_t d = tmem + kTmemS + 64 * (i & 1);
         // latent part: A = query columns in TMEM (8 columns per K step of 16)
         mma_ts(d, tmem + kTmemQ, d_k128 + so, idesc_qk, 0u);
 #pragma unroll
@@ -263,50 +277,27 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         mma_ss(d, d_qr, d_k64 + so, idesc_qk, 1u);
         mma_ss(d, d_qr + 2, d_k64 + so + 2, idesc_qk, 1u);
         mma_commit(bar_addr(bars.s_full[i & 1]));
-      };
-      // O' += P(i) V(i); then page i's stage goes back to the producer and
-      // warpgroup i & 1 may reuse its P buffer.
-      auto issue_pv = [&](int i) {
+      }
+    }
+    if (n_pages > 0 && lane == 0 && warp == kPvWarp) {
+      const uint32_t idesc_pv = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/1);
+      const uint64_t d_v = smem_desc(st0, kPChunk, 1024, kSw128);  // values (MN-major)
+      const uint64_t d_p = smem_desc(smem_u32(smem + kOffP), 16, 1024, kSw128);  // P of warpgroup 0 (K-major)
+      // O' += P(i) V(i) once P(i) is written; then page i's stage goes back to
+      // the producer and warpgroup i & 1 may reuse its P buffer.
+      for (int i = 0; i < n_pages; ++i) {
+        if (!mbar_wait(bar_addr(bars.p_full[i & 1]), (i >> 1) & 1, p.status, abort)) break;
         tc_fence_after();
         const uint64_t vb = d_v + static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
-        const uint32_t a = tmem + kTmemP + (i & 1) * 32;
-        mma_ts(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
+        const uint64_t a = d_p + static_cast<uint64_t>(((i & 1) * kPBytes) >> 4);
+        mma_ss(tmem + kTmemO, a, vb, idesc_pv, i > 0 ? 1u : 0u);
 #pragma unroll
-        for (int k = 1; k < 4; ++k) mma_ts(tmem + kTmemO, a + 8 * k, vb + 128 * k, idesc_pv, 1u);
+        for (int k = 1; k < 4; ++k) mma_ss(tmem + kTmemO, a + 2 * k, vb + 128 * k, idesc_pv, 1u);
         mma_commit(bar_addr(bars.empty[i % kStages]));
         mma_commit(bar_addr(bars.pv_done[i & 1]));
-      };
-
-      // Poll: P V of page np (< nq) once its P is written; otherwise QK^T of
-      // page nq once it has landed and the scores of page nq - 1 have been read
-      // out of the score buffer.  The tensor pipe runs them in issue order.
-      int nq = 0, np = 0;
-      uint64_t t0 = 0;
-      uint32_t idle = 0;
-      while (ok && np < n_pages) {
-        if (np < nq && mbar_test(bar_addr(bars.p_full[np & 1]), (np >> 1) & 1)) {
-          issue_pv(np++);
-          idle = 0;
-          continue;
-        }
-        if (nq < n_pages && mbar_test(bar_addr(bars.full[nq % kStages]), (nq / kStages) & 1) &&
-            (nq == 0 || mbar_test(bar_addr(bars.s_free[(nq - 1) & 1]), ((nq - 1) >> 1) & 1))) {
-          issue_qk(nq++);
-          idle = 0;
-          continue;
-        }
-        // bounded: give up (and make every other waiter give up) after kWaitNs
-        if (idle == 0) t0 = globaltimer_ns();
-        if ((++idle & 63u) == 0) {
-          if (*abort) {
-            ok = false;
-          } else if (globaltimer_ns() - t0 > kWaitNs) {
-            record_status(p.status, MLA_ERR_TIMEOUT);
-            *abort = 1;
-            ok = false;
-          }
-        }
       }
+    }
+    if (n_pages > 0 && lane == 0) {
       // no tcgen05 operation may still be running when TMEM is released
       mma_commit(bar_addr(bars.drain));
       mbar_wait(bar_addr(bars.drain), 0, p.status, nullptr);
@@ -332,7 +323,9 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     float2* fin = reinterpret_cast<float2*>(smem + kOffFin);
     bool ok = n_pages > 0;
     if (ok) {
-      // latent query columns [256r + 128g, 256r + 128g + 128) of the row into TMEM as bf16 pairs
+      // The query goes into the MMAs times 2^-8 (exact in bf16), so that the
+      // partial scores come out as S_r * 2^-8, the form they are exchanged in.
+      // Latent query columns [256r + 128g, 256r + 128g + 128) of the row into TMEM as bf16 pairs.
       const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<int64_t>(bj) * kHeads + row) * kRow +
                                                          256 * rank + 128 * g);
 #pragma unroll 1
@@ -341,23 +334,41 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const uint4 v = qsrc[8 * h + q];
-          w[4 * q] = v.x;
-          w[4 * q + 1] = v.y;
-          w[4 * q + 2] = v.z;
-          w[4 * q + 3] = v.w;
+          w[4 * q] = bf16x2_times_2m8(v.x);
+          w[4 * q + 1] = bf16x2_times_2m8(v.y);
+          w[4 * q + 2] = bf16x2_times_2m8(v.z);
+          w[4 * q + 3] = bf16x2_times_2m8(v.w);
         }
         tmem_st32(tmem + lane_off + kTmemQ + 64 * g + 32 * h, w);
       }
       tmem_wait_st();
+      if (g == 0) {
+        // the RoPE query columns (landed by TMA): this thread scales the 64 bytes of its row
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.q_full), 0, p.status, abort));
+        if (ok) {
+          uint4* qr = reinterpret_cast<uint4*>(smem + kOffQ + row * 64);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 v = qr[u];
+            v.x = bf16x2_times_2m8(v.x);
+            v.y = bf16x2_times_2m8(v.y);
+            v.z = bf16x2_times_2m8(v.z);
+            v.w = bf16x2_times_2m8(v.w);
+            qr[u] = v;
+          }
+          fence_proxy_async_smem();  // visible to the MMAs that read it
+        }
+      }
       tc_fence_before();
       mbar_arrive(bar_addr(bars.q_tmem));
     }
-    // exchange buffer g, this row: 16-byte unit u at (u ^ (row & 7)) * 16
-    uint8_t* xrow = smem + kOffX + g * kXBufBytes + row * 16;   // unit q of this row at q * 2048
+    // exchange buffer g, this row: 16-byte unit q at q * 2048 + row * 16
+    uint8_t* xrow = smem + kOffX + g * kXBufBytes + row * 16;
     const uint32_t x_remote = mapa(smem_u32(xrow), peer);
     const uint32_t xfull_remote = mapa(bar_addr(bars.x_full[g]), peer);
-    const uint32_t s_addr = tmem + lane_off + kTmemS;
-    float range_max = 0.f;
+    const uint32_t s_addr = tmem + lane_off + kTmemS + 64 * g;
+    uint8_t* prow = smem + kOffP + g * kPBytes + row * 128;  // this row of P
+    const uint64_t scale2 = f32x2(kSumScaleLog2, kSumScaleLog2);
     float m_mine = -INFINITY, l = 0.f;  // reference max this warpgroup last used, and its partial sum
     for (int i = g; i < n_pages && ok; i += 2) {
       const uint32_t use = (i >> 1) & 1;
@@ -365,6 +376,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[g]), use, p.status, abort));
       if (!ok) break;
       tc_fence_after();
+      // this CTA's partial scores S_r * 2^-8 as fp16 pairs: word w holds columns 2w, 2w + 1
       uint32_t mine[32];
       {
         uint32_t a[32], c[32];
@@ -372,25 +384,11 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         tmem_ld32(s_addr + 32, c);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar_addr(bars.s_free[g]));  // QK^T of page i + 1 may overwrite the buffer
+        mbar_arrive(bar_addr(bars.s_free[g]));  // QK^T of page i + 2 may overwrite the buffer
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-          const float x0 = __uint_as_float(a[2 * q]), x1 = __uint_as_float(a[2 * q + 1]);
-          const float y0 = __uint_as_float(c[2 * q]), y1 = __uint_as_float(c[2 * q + 1]);
-          mine[q] = pack_f16x2(x0 * kXScale, x1 * kXScale);
-          mine[16 + q] = pack_f16x2(y0 * kXScale, y1 * kXScale);
-        }
-        // magnitude of the visible partial scores (rows past the last token may hold anything)
-        if (n_valid == kPage) {
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            range_max = fmaxf(range_max, fmaxf(fabsf(__uint_as_float(a[q])), fabsf(__uint_as_float(c[q]))));
-        } else {
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            if (q < n_valid) range_max = fmaxf(range_max, fabsf(__uint_as_float(a[q])));
-            if (q + 32 < n_valid) range_max = fmaxf(range_max, fabsf(__uint_as_float(c[q])));
-          }
+          mine[q] = pack_f16x2(__uint_as_float(a[2 * q]), __uint_as_float(a[2 * q + 1]));
+          mine[16 + q] = pack_f16x2(__uint_as_float(c[2 * q]), __uint_as_float(c[2 * q + 1]));
         }
       }
       // send: wait until the peer has read what this warpgroup sent two pages ago
@@ -400,35 +398,39 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       for (int q = 0; q < 8; ++q)
         st_async_v4(x_remote + q * (kRowThreads * 16), mine[4 * q], mine[4 * q + 1], mine[4 * q + 2], mine[4 * q + 3],
                     xfull_remote);
-      // receive the peer's partial scores; both CTAs add fp16(S_0) + fp16(S_1) in fp32
+      // receive the peer's partial scores; both CTAs add fp16(S_0) + fp16(S_1)
+      // in fp16, in the same order, so they hold the same S * 2^-8
       ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full[g]), use, p.status, abort));
       if (!ok) break;
-      float sv[64];  // S * 2^-8
+      uint32_t sh[32];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const uint4 v = *reinterpret_cast<const uint4*>(xrow + q * (kRowThreads * 16));
-        const uint32_t pw[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int w = 4 * q + e;  // packed word index: columns 2w, 2w+1
-          const float2 x = unpack_f16x2(mine[w]);
-          const float2 y = unpack_f16x2(pw[e]);
-          sv[2 * w] = x.x + y.x;
-          sv[2 * w + 1] = x.y + y.y;
-        }
+        sh[4 * q] = hadd2(mine[4 * q], v.x);
+        sh[4 * q + 1] = hadd2(mine[4 * q + 1], v.y);
+        sh[4 * q + 2] = hadd2(mine[4 * q + 2], v.z);
+        sh[4 * q + 3] = hadd2(mine[4 * q + 3], v.w);
       }
       mbar_arrive(bar_addr(bars.x_read[g]));  // warp 10 recycles the exchange buffer
-      // row max over the visible tokens (the scale is positive), log2 domain
-      float mx = -INFINITY;
-      if (n_valid == kPage) {
+      if (n_valid < kPage) {
+        // columns past the last visible token (they may hold anything) become
+        // -inf: out of the max, and exp gives 0 for them
 #pragma unroll
-        for (int c = 0; c < 64; ++c) mx = fmaxf(mx, sv[c]);
-      } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < n_valid) mx = fmaxf(mx, sv[c]);
+        for (int w = 0; w < 32; ++w) {
+          const uint32_t lo = 2 * w < n_valid ? (sh[w] & 0x0000ffffu) : 0x0000fc00u;
+          const uint32_t hi = 2 * w + 1 < n_valid ? (sh[w] & 0xffff0000u) : 0xfc000000u;
+          sh[w] = lo | hi;
+        }
       }
-      mx *= kSumScaleLog2;
+      // row max (eight independent chains, then a tree: the same in any order), log2 domain
+      uint32_t m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = sh[k];
+#pragma unroll
+      for (int w = 8; w < 32; ++w) m8[w & 7] = hmax2(m8[w & 7], sh[w]);
+      const uint32_t mm = hmax2(hmax2(hmax2(m8[0], m8[1]), hmax2(m8[2], m8[3])), hmax2(hmax2(m8[4], m8[5]), hmax2(m8[6], m8[7])));
+      const float2 mf = unpack_f16x2(mm);
+      const float mx = fmaxf(mf.x, mf.y) * kSumScaleLog2;
       // the reference max after page i - 1 (from the other warpgroup)
       bool rescale = false;
       float factor = 1.f;
@@ -451,19 +453,23 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       }
       *m_slot = m_mine;
       mbar_arrive(bar_addr(bars.hand[g]));  // page i + 1 may start its softmax
-      const float neg_m = -m_mine;
+      // P = 2^(S * scale - m) in packed fp32 pairs; P goes to the MMA in bf16,
+      // the row sum adds the fp32 values
+      const uint64_t neg_m2 = f32x2(-m_mine, -m_mine);
       uint32_t pk[32];
-      float sum = 0.f;
+      uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        float p0 = ex2_approx(fmaf(sv[2 * c], kSumScaleLog2, neg_m));
-        float p1 = ex2_approx(fmaf(sv[2 * c + 1], kSumScaleLog2, neg_m));
-        if (2 * c >= n_valid) p0 = 0.f;
-        if (2 * c + 1 >= n_valid) p1 = 0.f;
-        pk[c] = pack_bf16x2(p0, p1);
-        sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+      for (int w = 0; w < 32; ++w) {
+        const float2 sf = unpack_f16x2(sh[w]);
+        const float2 e = f32x2_split(fma_f32x2(f32x2(sf.x, sf.y), scale2, neg_m2));
+        const float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
+        pk[w] = pack_bf16x2(p0, p1);
+        s4[w & 3] = add_f32x2(s4[w & 3], f32x2(p0, p1));
       }
-      l += sum;
+      {
+        const float2 a = f32x2_split(add_f32x2(add_f32x2(s4[0], s4[1]), add_f32x2(s4[2], s4[3])));
+        l += a.x + a.y;
+      }
       if (n_valid < kPage) {
         // Value rows past the last visible token may hold anything (NaN in
         // unwritten slots): zero them so that P = 0 there cannot make 0 * NaN.
@@ -475,8 +481,17 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         }
         fence_proxy_async_smem();
       }
-      // O' may only be rescaled once P V(i - 1) has finished; the P buffer is
-      // free once P V(i - 2) has.
+      // The P buffer is free once P V(i - 2) has finished; O' may only be
+      // rescaled once P V(i - 1) has.
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[g]), use ^ 1u, p.status, abort));
+        if (!ok) break;
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      fence_proxy_async_smem();  // visible to the P V MMAs
       if (__any_sync(0xffffffffu, rescale)) {
         ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[g ^ 1]), ((i - 1) >> 1) & 1, p.status, abort));
         if (!ok) break;
@@ -489,19 +504,14 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
           for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
           tmem_st32(tmem + lane_off + kTmemO + c0, r);
         }
+        tmem_wait_st();
+        tc_fence_before();
       }
-      if (i >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[g]), use ^ 1u, p.status, abort));
-        if (!ok) break;
-        tc_fence_after();
-      }
-      tmem_st32(tmem + lane_off + kTmemP + g * 32, pk);
-      tmem_wait_st();
-      tc_fence_before();
       mbar_arrive(bar_addr(bars.p_full[g]));
     }
-    // exchanged partials are fp16(S_r / 256): beyond this magnitude they overflow
-    if (range_max > 1.6e7f) record_status(p.status, MLA_ERR_RANGE);
+    // Exchanged partials are fp16(S_r / 256): one beyond |S_r| = 65520 * 256
+    // (or a NaN) becomes infinite or NaN and leaves the row's max or sum non-finite.
+    if (ok && g < n_pages && !(isfinite(l) && isfinite(m_mine))) record_status(p.status, MLA_ERR_RANGE);
 
     // epilogue: combine the two warpgroups' sums, then warpgroup g writes
     // columns [128g, 128g + 128) of this CTA's half of O' (normalised)
