@@ -99,6 +99,11 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1 KB");
 
 constexpr float kRescaleLog2 = 8.f;
+// Output staging at the end: warpgroup g's 128 x 128 fp32 tile of O' as four
+// 32-column boxes in the ring (idle by then).
+constexpr int kOBoxBytes = 128 * 128;
+constexpr int kOTileBytes = 4 * kOBoxBytes;
+static_assert(2 * kOTileBytes <= kStages * kStageBytes, "output staging fits in the ring");
 
 struct Bars {
   uint64_t full[kStages];
@@ -117,6 +122,7 @@ struct Bars {
   uint64_t drain;       // both issuers' MMAs have finished
   uint32_t tmem_base;
   int abort;
+  int wg_bad[2];        // a row of warpgroup g has no valid result: it writes zeros
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
@@ -139,7 +145,8 @@ __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b);
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_constant__ CUtensorMap tm_c128,
-                      const __grid_constant__ CUtensorMap tm_c64, const Params p) {
+                      const __grid_constant__ CUtensorMap tm_c64, const __grid_constant__ CUtensorMap tm_o,
+                      const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBar);
@@ -173,6 +180,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     mbar_init(bar_addr(bars.fin), 2 * kRowThreads);
     mbar_init(bar_addr(bars.drain), 2);
     bars.abort = 0;
+    bars.wg_bad[0] = bars.wg_bad[1] = 0;
     fence_mbar_init();
     // arm the first use of both exchange buffers: 16 KB of the peer's partial scores each
     mbar_arrive_expect_tx(bar_addr(bars.x_full[0]), kXTxBytes);
@@ -522,24 +530,43 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[last & 1]), (last >> 1) & 1, p.status, abort));
     tc_fence_after();
     const int64_t out_row = (static_cast<int64_t>(bj) * p.num_splits + split) * kHeads + row;
-    float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
-    if (ok) {
+    // One decision per warpgroup: its 128 x 128 tile of O' is staged in the
+    // (now idle) ring and stored by TMA, or, if any of its rows has no valid
+    // result, the warpgroup writes zeros directly.
+    if (!ok && lane == 0) bars.wg_bad[g] = 1;
+    named_barrier_sync(1 + g, kRowThreads);
+    if (*reinterpret_cast<volatile int*>(&bars.wg_bad[g]) == 0) {
       const float2 f0 = fin[row], f1 = fin[kHeads + row];
       const float m = fmaxf(f0.x, f1.x);
       const float lt = (f0.y > 0.f ? f0.y * ex2_approx(f0.x - m) : 0.f) + (f1.y > 0.f ? f1.y * ex2_approx(f1.x - m) : 0.f);
       const float inv = 1.f / lt;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      // four boxes of 32 fp32 columns x 128 rows, 128-byte swizzle: row r at
+      // r * 128, 16-byte chunk c at (c ^ (r & 7)) * 16
+      uint8_t* tile = smem + kOffStage + g * kOTileBytes;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
         uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kTmemO + 128 * g + c0, r);
+        tmem_ld32(tmem + lane_off + kTmemO + 128 * g + 32 * k, r);
         tmem_wait_ld();
+        uint8_t* brow = tile + k * kOBoxBytes + row * 128;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float4*>(orow + c0 + 4 * q) =
-              make_float4(__uint_as_float(r[4 * q]) * inv, __uint_as_float(r[4 * q + 1]) * inv,
-                          __uint_as_float(r[4 * q + 2]) * inv, __uint_as_float(r[4 * q + 3]) * inv);
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4*>(brow + ((c ^ (row & 7)) << 4)) =
+              make_float4(__uint_as_float(r[4 * c]) * inv, __uint_as_float(r[4 * c + 1]) * inv,
+                          __uint_as_float(r[4 * c + 2]) * inv, __uint_as_float(r[4 * c + 3]) * inv);
       }
+      fence_proxy_async_smem();  // visible to the TMA store
       if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
+      named_barrier_sync(1 + g, kRowThreads);
+      if (row == 0) {
+        const int32_t y0 = static_cast<int32_t>(out_row);  // row 0 of the unit
+        for (int k = 0; k < 4; ++k)
+          tma_store_2d(&tm_o, smem_u32(tile + k * kOBoxBytes), static_cast<int32_t>(rank * 256 + 128 * g + 32 * k), y0);
+        bulk_commit_group();
+        bulk_wait_all();
+      }
     } else {
+      float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
       for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
       if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = -INFINITY;
     }
@@ -606,12 +633,14 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   if (units == 0) return cudaSuccess;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || !configure(dev)) return cudaErrorInvalidDevice;
-  CUtensorMap tq64, tc128, tc64;
+  CUtensorMap tq64, tc128, tc64, to;
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * kHeads;
   const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
   if (!make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_bf16_2d(&tc128, cache, c_rows, kRow, kRow, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+      !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_tmap_f32_2d(&to, o_out, static_cast<uint64_t>(units) * kHeads, kLatent, kLatent, 32, 128,
+                        CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   Params prm;
   prm.page_table = page_table;
@@ -627,7 +656,7 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   prm.split_pages = plan.split_pages;
   prm.num_splits = plan.num_splits;
   return launch_kernel(decode_attn_tc_kernel, dim3(static_cast<unsigned>(2 * units)), dim3(kThreads), kSmemBytes, stream,
-                       tq64, tc128, tc64, prm);
+                       tq64, tc128, tc64, to, prm);
 }
 
 }  // namespace mla
