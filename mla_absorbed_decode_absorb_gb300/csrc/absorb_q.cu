@@ -9,10 +9,12 @@
 // computes D[m, t] = sum_d W_UK[h][d][m] * q_nope[t][h][d] for 128 latent
 // columns m (M = 128) and up to 256 query tokens t (N).  A = W_UK[h] is
 // MN-major (m contiguous), B = q_nope rows are K-major (d contiguous); both are
-// staged into shared memory in the 128-byte-swizzled canonical layouts, one MMA
+// staged into shared memory in the 128-byte-swizzled canonical layouts (A by
+// two TMA boxes of 64 m x 128 d, B by 16-byte asynchronous copies), one MMA
 // chain of 8 x (K = 16) accumulates into TMEM, and four warps read their 32
 // TMEM lanes back (lane = m, column = token) and store bf16.
 #include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
@@ -36,10 +38,11 @@ __host__ __device__ inline uint32_t tmem_cols_for(int nb) {
   return c;
 }
 __host__ __device__ inline int smem_bytes_for(int T) { return kSmemA + 2 * tile_tokens(T) * 128 + 1024 + 64; }
+constexpr uint32_t kWaitBarOffset = 16;  // weight barrier after the MMA barrier and the TMEM slot
 
 __global__ void __launch_bounds__(kThreads)
-absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restrict__ q_rope,
-                   const int32_t* __restrict__ lens, const uint16_t* __restrict__ w_uk,
+absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t* __restrict__ q_nope, const uint16_t* __restrict__ q_rope,
+                   const int32_t* __restrict__ lens,
                    const float* __restrict__ rope, int rope_max_pos, uint16_t* __restrict__ q_abs,
                    int T, int n_q, int* status, bool weights_early) {
   extern __shared__ uint8_t smem_raw[];
@@ -51,6 +54,7 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
   const uint32_t tmem_cols = tmem_cols_for(nb);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sB + 2 * nb * 128);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* wbar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(bar) + kWaitBarOffset);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = blockIdx.x * kMTile;
@@ -59,26 +63,25 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
   const int nt = min(kNMax, T - t0);
   const int npad = (nt + 15) & ~15;
 
-  // A: W_UK[h][d][m0 .. m0+128) -> two MN-major chunks of 64 columns, rows d;
-  // B: q_nope[t0 + t][h][0 .. 128) -> two K-major chunks of 64, rows t (zero past nt).
-  // Asynchronous 16-byte copies, all in flight at once; the weights may be
-  // requested before the previous kernel of the stream has finished.
+  // A: W_UK[h][d][m0 .. m0+128) -> two MN-major chunks of 64 columns, rows d,
+  // by TMA (the weights may be requested before the previous kernel of the
+  // stream has finished); B: q_nope[t0 + t][h][0 .. 128) -> two K-major chunks
+  // of 64, rows t (zero past nt), by 16-byte asynchronous copies.
   auto load_w = [&]() {
-    const uint4* wsrc = reinterpret_cast<const uint4*>(w_uk + (static_cast<int64_t>(h) * kNope) * kLatent + m0);
-#pragma unroll 4
-    for (int v = tid; v < kNope * 16; v += kThreads) {
-      const int d = v >> 4, u = v & 15, c = u >> 3;
-      cp_async16(smem_u32(sA + c * kAChunk + sw128(d * 128 + (u & 7) * 16)), wsrc + d * (kLatent / 8) + u);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(smem_u32(wbar), kSmemA);
+      for (int c = 0; c < 2; ++c) tma_load_2d(smem_u32(sA + c * kAChunk), &tm_w, m0 + 64 * c, h * kNope, smem_u32(wbar));
     }
   };
+  if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    mbar_init(smem_u32(wbar), 1);
+    fence_mbar_init();
+  }
   if (weights_early) load_w();
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), tmem_cols);
     tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(smem_u32(bar), 1);
-    fence_mbar_init();
   }
   grid_dep_wait();
   grid_dep_launch();
@@ -116,7 +119,10 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (tid == 0) {
+  bool wok = true;
+  if (tid == 0) wok = mbar_wait(smem_u32(wbar), 0, status);  // the weight tile has landed
+  if (tid == 0 && wok) {
+    tc_fence_after();
     const uint32_t idesc = idesc_bf16(128, npad, /*a_mn=*/1, /*b_mn=*/0);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
@@ -127,6 +133,7 @@ absorb_q_tc_kernel(const uint16_t* __restrict__ q_nope, const uint16_t* __restri
     }
     mma_commit(smem_u32(bar));
   }
+  if (tid == 0 && !wok) mbar_arrive(smem_u32(bar));  // no MMA: release the waiters (the result is flagged)
   const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), 0, status));
   tc_fence_after();
 
@@ -164,9 +171,14 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  // W_UK as a [128 * 128, 512] matrix: box 64 columns x 128 rows, 128-byte swizzle
+  CUtensorMap tw;
+  if (!make_tmap_bf16_2d(&tw, w_uk, static_cast<uint64_t>(kHeads) * kNope, kLatent, kLatent, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   dim3 grid(kLatent / kMTile, kHeads, (T + kNMax - 1) / kNMax);
-  return launch_kernel(absorb_q_tc_kernel, grid, dim3(kThreads), smem_bytes_for(T), stream, q_nope, q_rope,
-                       seq_lens_before, w_uk, rope_table, rope_max_pos, q_abs, T, n_q, status, launch_overlap() >= 2);
+  return launch_kernel(absorb_q_tc_kernel, grid, dim3(kThreads), smem_bytes_for(T), stream, tw, q_nope, q_rope,
+                       seq_lens_before, rope_table, rope_max_pos, q_abs, T, n_q, status, launch_overlap() >= 2);
 }
 
 }  // namespace mla

@@ -11,12 +11,13 @@
 // tcgen05 version, operands swapped so the large side is M: per head h the CTA
 // computes D[d, t] = sum_m W_UV[h][d][m] * O'[t][h][m] with the 128 output
 // dimensions d as M and up to 64 query tokens as N.  Both operands are K-major
-// (m contiguous).  All of W_UV[h] (128 KB) is requested at once with 16-byte
-// asynchronous copies; while it is in flight the CTA builds O' (merging the
+// (m contiguous).  All of W_UV[h] (128 KB) is requested at once, as eight TMA
+// boxes of 64 m x 128 d; while it is in flight the CTA builds O' (merging the
 // splits in float32 with the same operations, in the same order, as the
 // stand-alone merge kernel) and rounds it to bf16 into shared memory.  One
 // chain of 32 MMAs (K = 16 each) accumulates in TMEM.
 #include "sm100.cuh"
+#include "tmap.cuh"
 
 namespace mla {
 namespace {
@@ -27,7 +28,6 @@ constexpr int kNMax = 64;                          // query tokens per CTA
 constexpr int kThreads = 256;
 constexpr int kChunk = 128 * 128;                  // 128 rows x 64 m (128 B), SW128
 constexpr int kSmemA = (kLatent / 64) * kChunk;    // W_UV[h]: 8 chunks, 128 KB
-constexpr int kSmemB = (kLatent / 64) * kNMax * 128;  // O' bf16: 8 chunks of up to 64 rows, 64 KB
 
 // Tokens of the widest tile (rounded up to the MMA's N granularity of 16), and
 // the TMEM columns for its fp32 accumulator (a power of two, at least 32).
@@ -41,7 +41,7 @@ constexpr int kTableSplits = 128;  // merge weights kept in shared memory up to 
 __host__ __device__ inline int smem_bytes_for(int T, int num_splits) {
   const int nb = tile_tokens(T);
   const int table = num_splits <= kTableSplits ? nb * num_splits : 0;
-  return kSmemA + (kLatent / 64) * nb * 128 + 16 + 4 * (2 * kNMax + table) + 1024;
+  return kSmemA + (kLatent / 64) * nb * 128 + 24 + 4 * (2 * kNMax + table) + 1024;
 }
 
 // src: O' rows; with src_lse == nullptr, row (t, h) is src[(t * 128 + h) * 512]
@@ -49,8 +49,8 @@ __host__ __device__ inline int smem_bytes_for(int T, int num_splits) {
 // with log-sum-exps src_lse[(t * S + s) * 128 + h] are merged first, and the
 // merged log-sum-exp goes to lse_out[t * 128 + h] (if non-null).
 __global__ void __launch_bounds__(kThreads, 1)
-out_absorb_tc_kernel(const float* __restrict__ src, const float* __restrict__ src_lse, int num_splits,
-                     const uint16_t* __restrict__ w_uv, uint16_t* __restrict__ out, float* __restrict__ lse_out,
+out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ src,
+                     const float* __restrict__ src_lse, int num_splits, uint16_t* __restrict__ out, float* __restrict__ lse_out,
                      int T, int* status, bool weights_early) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -59,8 +59,9 @@ out_absorb_tc_kernel(const float* __restrict__ src, const float* __restrict__ sr
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSmemA;
   uint64_t* bar = reinterpret_cast<uint64_t*>(sB + (kLatent / 64) * nb * 128);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 1);
-  float* s_max = reinterpret_cast<float*>(bar + 2);  // per token: max_s lse_s
+  uint64_t* wbar = bar + 1;                          // W_UV[h] has landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 2);
+  float* s_max = reinterpret_cast<float*>(bar + 3);  // per token: max_s lse_s
   float* s_inv = s_max + kNMax;                      // per token: 1 / sum_s exp(lse_s - max)
   float* s_w = s_inv + kNMax;                        // [token][split] weights (table mode)
 
@@ -71,53 +72,58 @@ out_absorb_tc_kernel(const float* __restrict__ src, const float* __restrict__ sr
   const int npad = (nt + 15) & ~15;
   const int64_t S = num_splits;
 
-  // A: W_UV[h][d][0 .. 512) -> 8 K-major chunks of 64 m, rows d (all in flight
-  // at once; possibly requested before the previous kernel has finished)
+  // A: W_UV[h][d][0 .. 512) -> 8 K-major chunks of 64 m, rows d, by TMA (all in
+  // flight at once; possibly requested before the previous kernel has finished)
   auto load_w = [&]() {
-    const uint4* wsrc = reinterpret_cast<const uint4*>(w_uv + static_cast<int64_t>(h) * kNope * kLatent);
-#pragma unroll 4
-    for (int v = tid; v < kNope * (kLatent / 8); v += kThreads) {
-      const int d = v >> 6, u = v & 63;  // 16-byte unit u of row d: chunk u / 8
-      cp_async16(smem_u32(sA + (u >> 3) * kChunk + sw128(d * 128 + (u & 7) * 16)), wsrc + v);
+    if (tid == 0) {
+      mbar_arrive_expect_tx(smem_u32(wbar), kSmemA);
+      for (int c = 0; c < kLatent / 64; ++c)
+        tma_load_2d(smem_u32(sA + c * kChunk), &tm_w, 64 * c, h * kNope, smem_u32(wbar));
     }
   };
+  if (tid == 0) {
+    mbar_init(smem_u32(bar), 1);
+    mbar_init(smem_u32(wbar), 1);
+    fence_mbar_init();
+  }
   if (weights_early) load_w();
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), tmem_cols);
     tmem_relinquish();
-  }
-  if (tid == 0) {
-    mbar_init(smem_u32(bar), 1);
-    fence_mbar_init();
   }
   grid_dep_wait();
   grid_dep_launch();
   if (!weights_early) load_w();
   // Merge weights: w[t][s] = exp(lse_s - max_s lse_s) (-1 marks an empty split,
   // which is skipped), kept in shared memory for up to kTableSplits splits.
+  // They are computed once the first split rows are in flight (the row loads
+  // do not depend on them), so the two round trips to memory overlap.
   const bool table = num_splits <= kTableSplits;
-  if (src_lse != nullptr && tid < nt) {
-    const float* ls = src_lse + (static_cast<int64_t>(t0 + tid) * S) * kHeads + h;
-    float m = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, ls[s * kHeads]);
-    float z = 0.f;
-    if (m != -INFINITY)
-      for (int s = 0; s < num_splits; ++s) {
-        const float l = ls[s * kHeads];
-        const float w = l == -INFINITY ? -1.f : expf(l - m);
-        if (w >= 0.f) z += w;
-        if (table) s_w[tid * num_splits + s] = w;
-      }
-    s_max[tid] = m;
-    s_inv[tid] = 1.f / z;
-    if (lse_out != nullptr) lse_out[static_cast<int64_t>(t0 + tid) * kHeads + h] = m == -INFINITY ? m : m + logf(z);
-  }
-  __syncthreads();
+  auto merge_weights = [&]() {
+    if (tid < nt) {
+      const float* ls = src_lse + (static_cast<int64_t>(t0 + tid) * S) * kHeads + h;
+      float m = -INFINITY;
+      for (int s = 0; s < num_splits; ++s) m = fmaxf(m, ls[s * kHeads]);
+      float z = 0.f;
+      if (m != -INFINITY)
+        for (int s = 0; s < num_splits; ++s) {
+          const float l = ls[s * kHeads];
+          const float w = l == -INFINITY ? -1.f : expf(l - m);
+          if (w >= 0.f) z += w;
+          if (table) s_w[tid * num_splits + s] = w;
+        }
+      s_max[tid] = m;
+      s_inv[tid] = 1.f / z;
+      if (lse_out != nullptr) lse_out[static_cast<int64_t>(t0 + tid) * kHeads + h] = m == -INFINITY ? m : m + logf(z);
+    }
+    __syncthreads();
+  };
+  bool weights_ready = src_lse == nullptr;
 
   // B: O'[t0 + t][h][0 .. 512) rounded to bf16: 8 K-major chunks of 64, rows t
   // (zero past nt).  Thread (tq, u) = (tid / 64, tid % 64) builds 16-byte unit u
-  // (8 consecutive m) of tokens t = tq + 4i, 8 tokens at a time, so that each
-  // split's 16 loads are in flight together.
+  // (8 consecutive m) of tokens t = tq + 4i, 8 tokens at a time; the rows of
+  // two splits (32 loads) are in flight together.
   const int u = tid & 63, tq = tid >> 6;
   for (int i0 = 0; i0 < npad / 4; i0 += 8) {
     float4 a[8], b[8];
@@ -134,36 +140,47 @@ out_absorb_tc_kernel(const float* __restrict__ src, const float* __restrict__ sr
         }
       }
     } else {
-      for (int s = 0; s < num_splits; ++s) {
-        float4 x[8], y[8];
-        float w[8];
+      for (int s0 = 0; s0 < num_splits; s0 += 2) {
+        float4 x[2][8], y[2][8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int t = tq + 4 * (i0 + k);
-          w[k] = -1.f;
-          x[k] = y[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (t < nt && s_max[t] != -INFINITY) {
-            const int64_t r = (static_cast<int64_t>(t0 + t) * S + s) * kHeads + h;
-            if (table) {
-              w[k] = s_w[t * num_splits + s];
-            } else {
-              const float l = src_lse[r];
-              w[k] = l == -INFINITY ? -1.f : expf(l - s_max[t]);
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int t = tq + 4 * (i0 + k);
+            x[j][k] = y[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < nt && s0 + j < num_splits) {
+              const int64_t r = (static_cast<int64_t>(t0 + t) * S + s0 + j) * kHeads + h;
+              const float4* p = reinterpret_cast<const float4*>(src + r * kLatent) + 2 * u;
+              x[j][k] = p[0];
+              y[j][k] = p[1];
             }
-            const float4* p = reinterpret_cast<const float4*>(src + r * kLatent) + 2 * u;
-            x[k] = p[0];
-            y[k] = p[1];
           }
+        if (!weights_ready) {
+          merge_weights();
+          weights_ready = true;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (w[k] >= 0.f) {
-            a[k].x = fmaf(w[k], x[k].x, a[k].x); a[k].y = fmaf(w[k], x[k].y, a[k].y);
-            a[k].z = fmaf(w[k], x[k].z, a[k].z); a[k].w = fmaf(w[k], x[k].w, a[k].w);
-            b[k].x = fmaf(w[k], y[k].x, b[k].x); b[k].y = fmaf(w[k], y[k].y, b[k].y);
-            b[k].z = fmaf(w[k], y[k].z, b[k].z); b[k].w = fmaf(w[k], y[k].w, b[k].w);
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int t = tq + 4 * (i0 + k);
+            const int s = s0 + j;
+            float w = -1.f;
+            if (t < nt && s < num_splits && s_max[t] != -INFINITY) {
+              if (table) {
+                w = s_w[t * num_splits + s];
+              } else {
+                const float l = src_lse[(static_cast<int64_t>(t0 + t) * S + s) * kHeads + h];
+                w = l == -INFINITY ? -1.f : expf(l - s_max[t]);
+              }
+            }
+            if (w >= 0.f) {
+              a[k].x = fmaf(w, x[j][k].x, a[k].x); a[k].y = fmaf(w, x[j][k].y, a[k].y);
+              a[k].z = fmaf(w, x[j][k].z, a[k].z); a[k].w = fmaf(w, x[j][k].w, a[k].w);
+              b[k].x = fmaf(w, y[j][k].x, b[k].x); b[k].y = fmaf(w, y[j][k].y, b[k].y);
+              b[k].z = fmaf(w, y[j][k].z, b[k].z); b[k].w = fmaf(w, y[j][k].w, b[k].w);
+            }
           }
-        }
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -184,14 +201,16 @@ out_absorb_tc_kernel(const float* __restrict__ src, const float* __restrict__ sr
                        pack_bf16x2(b[k].z, b[k].w));
     }
   }
-  cp_async_wait_all();
   fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (tid == 0) {
+  bool wok = true;
+  if (tid == 0) wok = mbar_wait(smem_u32(wbar), 0, status);  // W_UV[h] has landed
+  if (tid == 0 && wok) {
+    tc_fence_after();
     const uint32_t idesc = idesc_bf16(128, npad, /*a_mn=*/0, /*b_mn=*/0);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
 #pragma unroll
@@ -202,6 +221,7 @@ out_absorb_tc_kernel(const float* __restrict__ src, const float* __restrict__ sr
     }
     mma_commit(smem_u32(bar));
   }
+  if (tid == 0 && !wok) mbar_arrive(smem_u32(bar));  // no MMA: release the waiters (the result is flagged)
   const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(bar), 0, status));
   tc_fence_after();
 
@@ -225,9 +245,224 @@ out_absorb_tc_kernel(const float* __restrict__ src, const float* __restrict__ sr
   if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
+// ------------------------------------------------------------------ streamed variant
+// For up to kTMaxSplits splits the O' rows come in by TMA as well: a plain
+// load of 128 KB per CTA is limited by what L1 can hold in flight next to the
+// 128 KB of W_UV in shared memory, while a TMA box lands in shared memory
+// directly.  Per CTA (head h, up to kTTokens tokens): W_UV[h] as 8 boxes; the
+// rows (token t, split s) of latent chunk k (64 m) as one box of up to 64 rows
+// through a 3-slot ring; 8 combine warps merge chunk k (same fp32 operations
+// in the same order as the stand-alone merge) into bf16 chunk k of B, and
+// warp 8 issues the chunk's 4 MMAs as soon as it is written, then refills the
+// slot.  The merge of chunk k + 1 overlaps the MMAs of chunk k.
+constexpr int kTTokens = 32;                   // tokens per CTA (at most)
+constexpr int kTBoxRows = 64;                  // O' rows (token x split) per box
+constexpr int kTStages = 3;
+constexpr int kTBoxBytes = 64 * 4 * kTBoxRows;  // 16 KB
+constexpr int kTThreads = 288;                 // warps 0-7 merge, warp 8 loads and issues MMAs
+constexpr int kTMaxSplits = 16;
+constexpr int kTSmemB = (kLatent / 64) * kTTokens * 128;  // 32 KB
+
+struct TBars {
+  uint64_t w_full;
+  uint64_t p_full[kTStages];
+  uint64_t b_full[kLatent / 64];  // chunk k of B written (and box k read) by all 256 merge threads
+  uint64_t mma_done;
+  uint32_t tmem_slot;
+};
+constexpr int kTOffB = kSmemA;
+constexpr int kTOffRing = kTOffB + kTSmemB;
+constexpr int kTOffBars = kTOffRing + kTStages * kTBoxBytes;
+constexpr int kTOffTab = kTOffBars + 256;
+constexpr int kTSmemBytes = kTOffTab + 4 * (kTTokens * kTMaxSplits + 2 * kTTokens) + 1024;
+static_assert(sizeof(TBars) <= 256, "barrier block");
+static_assert(kTSmemBytes <= 232448, "shared memory budget");
+
+// Tokens per CTA for S splits: whole tokens' rows fit one box.
+__host__ __device__ inline int t_tile(int S) { return min(kTTokens, kTBoxRows / S); }
+
+__global__ void __launch_bounds__(kTThreads, 1)
+out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_p,
+                         const float* __restrict__ src_lse, int num_splits, uint16_t* __restrict__ out,
+                         float* __restrict__ lse_out, int T, int* status, bool weights_early) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kTOffB;
+  uint8_t* ring = smem + kTOffRing;
+  TBars& bars = *reinterpret_cast<TBars*>(smem + kTOffBars);
+  float* s_w = reinterpret_cast<float*>(smem + kTOffTab);  // [token][split] merge weights
+  float* s_inv = s_w + kTTokens * kTMaxSplits;            // per token: 1 / sum_s w
+  float* s_max = s_inv + kTTokens;                        // per token: max_s lse_s
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = num_splits;
+  const int ntile = t_tile(S);
+  const int h = blockIdx.x;
+  const int t0 = blockIdx.y * ntile;
+  const int nt = min(ntile, T - t0);
+  const int npad = (nt + 15) & ~15;
+  const uint32_t tmem_cols = 32;  // npad <= 32
+  const bool merge = src_lse != nullptr;
+
+  auto load_w = [&]() {
+    mbar_arrive_expect_tx(smem_u32(&bars.w_full), kSmemA);
+    for (int c = 0; c < kLatent / 64; ++c)
+      tma_load_2d(smem_u32(sA + c * kChunk), &tm_w, 64 * c, h * kNope, smem_u32(&bars.w_full));
+  };
+  // box k: rows (t0 + t) * S + s, t < ntile, columns [64k, 64k + 64) of head h
+  auto load_p = [&](int k) {
+    const int slot = k % kTStages;
+    mbar_arrive_expect_tx(smem_u32(&bars.p_full[slot]), 256u * ntile * S);  // the whole box, rows past T * S as zeros
+    tma_load_3d(smem_u32(ring + slot * kTBoxBytes), &tm_p, 64 * k, h, t0 * S, smem_u32(&bars.p_full[slot]));
+  };
+
+  if (tid == 256) {
+    mbar_init(smem_u32(&bars.w_full), 1);
+    for (int i = 0; i < kTStages; ++i) mbar_init(smem_u32(&bars.p_full[i]), 1);
+    for (int i = 0; i < kLatent / 64; ++i) mbar_init(smem_u32(&bars.b_full[i]), 256);
+    mbar_init(smem_u32(&bars.mma_done), 1);
+    fence_mbar_init();
+    if (weights_early) load_w();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(&bars.tmem_slot), tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  if (warp == 8) {
+    // ------------------------------------------------ loads and MMAs
+    if (lane == 0) {
+      if (!weights_early) load_w();
+      for (int k = 0; k < kTStages; ++k) load_p(k);
+      bool ok = mbar_wait(smem_u32(&bars.w_full), 0, status);
+      const uint32_t idesc = idesc_bf16(128, npad, /*a_mn=*/0, /*b_mn=*/0);
+      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+      for (int k = 0; k < kLatent / 64 && ok; ++k) {
+        ok = mbar_wait(smem_u32(&bars.b_full[k]), 0, status);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t ad = smem_desc(a0 + k * kChunk + q * 32, 16, 1024, kSw128);
+          const uint64_t bd = smem_desc(b0 + k * npad * 128 + q * 32, 16, 1024, kSw128);
+          mma_ss(tmem, ad, bd, idesc, (k | q) ? 1u : 0u);
+        }
+        if (k + kTStages < kLatent / 64) load_p(k + kTStages);  // box k has been read
+      }
+      if (ok) mma_commit(smem_u32(&bars.mma_done));
+      else mbar_arrive(smem_u32(&bars.mma_done));  // no result: release the epilogue (the status is set)
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ merge: thread (t, u) = 8 m of token t
+    const int t = tid >> 3, u = tid & 7;
+    if (merge && tid < nt) {
+      const float* ls = src_lse + (static_cast<int64_t>(t0 + tid) * S) * kHeads + h;
+      float m = -INFINITY;
+      for (int s = 0; s < S; ++s) m = fmaxf(m, ls[s * kHeads]);
+      float z = 0.f;
+      if (m != -INFINITY)
+        for (int s = 0; s < S; ++s) {
+          const float l = ls[s * kHeads];
+          const float w = l == -INFINITY ? -1.f : expf(l - m);
+          if (w >= 0.f) z += w;
+          s_w[tid * S + s] = w;
+        }
+      s_max[tid] = m;
+      s_inv[tid] = 1.f / z;
+      if (lse_out != nullptr) lse_out[static_cast<int64_t>(t0 + tid) * kHeads + h] = m == -INFINITY ? m : m + logf(z);
+    }
+    named_barrier_sync(1, 256);
+    const bool live = t < nt && (!merge || s_max[t] != -INFINITY);
+    for (int k = 0; k < kLatent / 64; ++k) {
+      const int slot = k % kTStages;
+      mbar_wait(smem_u32(&bars.p_full[slot]), (k / kTStages) & 1, status);
+      if (t < npad) {
+        float a[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] = 0.f;
+        if (live) {
+          const uint8_t* box = ring + slot * kTBoxBytes;
+          for (int s = 0; s < S; ++s) {
+            const float w = merge ? s_w[t * S + s] : 1.f;
+            if (w >= 0.f) {
+              const float4* r = reinterpret_cast<const float4*>(box + (t * S + s) * 256 + u * 32);
+              const float4 x = r[0], y = r[1];
+              a[0] = fmaf(w, x.x, a[0]); a[1] = fmaf(w, x.y, a[1]); a[2] = fmaf(w, x.z, a[2]); a[3] = fmaf(w, x.w, a[3]);
+              a[4] = fmaf(w, y.x, a[4]); a[5] = fmaf(w, y.y, a[5]); a[6] = fmaf(w, y.z, a[6]); a[7] = fmaf(w, y.w, a[7]);
+            }
+          }
+          if (merge) {
+            const float inv = s_inv[t];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a[e] *= inv;
+          }
+        }
+        *reinterpret_cast<uint4*>(sB + k * npad * 128 + sw128(t * 128 + u * 16)) =
+            make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bars.b_full[k]));
+    }
+    // ------------------------------------------------ epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 32 (d),
+    // columns (tokens) of half w / 4
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.mma_done), 0, status));
+    tc_fence_after();
+    if (ok) {
+      const int d = (warp & 3) * 32 + lane;
+      const uint32_t row_addr = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+      for (int c0 = (warp >> 2) * 16; c0 < npad; c0 += 32) {
+        uint32_t r[16];
+        tmem_ld16(row_addr + c0, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int tt = c0 + i;
+          if (tt < nt) out[(static_cast<int64_t>(t0 + tt) * kHeads + h) * kNope + d] = f32_to_bf16_bits(__uint_as_float(r[i]));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) tmem_dealloc(tmem, tmem_cols);
+}
+
+cudaError_t launch_stream(const float* src, const float* src_lse, int num_splits, const uint16_t* w_uv, uint16_t* out,
+                          float* lse_out, int T, int* status, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(out_absorb_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  CUtensorMap tw, tp;
+  const int S = num_splits;
+  const int ntile = t_tile(S);
+  // W_UV as a [128 * 128, 512] matrix: box 64 columns x 128 rows, 128-byte swizzle;
+  // O' rows as [T * S][128 heads][512]: box 64 columns x 1 head x (ntile * S) rows
+  if (!make_tmap_bf16_2d(&tw, w_uv, static_cast<uint64_t>(kHeads) * kNope, kLatent, kLatent, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_f32_3d(&tp, src, kLatent, kHeads, static_cast<uint64_t>(T) * S, kLatent * 4ull,
+                        static_cast<uint64_t>(kHeads) * kLatent * 4ull, 64, 1, static_cast<uint32_t>(ntile * S)))
+    return cudaErrorInvalidValue;
+  dim3 grid(kHeads, (T + ntile - 1) / ntile);
+  return launch_kernel(out_absorb_stream_kernel, grid, dim3(kTThreads), kTSmemBytes, stream, tw, tp, src_lse,
+                       num_splits, out, lse_out, T, status, launch_overlap() >= 2);
+}
+
 cudaError_t launch(const float* src, const float* src_lse, int num_splits, const uint16_t* w_uv, uint16_t* out,
                    float* lse_out, int T, int* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
+  if (num_splits <= kTMaxSplits && (reinterpret_cast<uintptr_t>(src) & 15u) == 0)
+    return launch_stream(src, src_lse, num_splits, w_uv, out, lse_out, T, status, stream);
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(out_absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -235,9 +470,14 @@ cudaError_t launch(const float* src, const float* src_lse, int num_splits, const
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  // W_UV as a [128 * 128, 512] matrix: box 64 columns x 128 rows, 128-byte swizzle
+  CUtensorMap tw;
+  if (!make_tmap_bf16_2d(&tw, w_uv, static_cast<uint64_t>(kHeads) * kNope, kLatent, kLatent, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   dim3 grid(kHeads, (T + kNMax - 1) / kNMax);
-  return launch_kernel(out_absorb_tc_kernel, grid, dim3(kThreads), smem_bytes_for(T, num_splits), stream, src,
-                       src_lse, num_splits, w_uv, out, lse_out, T, status, launch_overlap() >= 2);
+  return launch_kernel(out_absorb_tc_kernel, grid, dim3(kThreads), smem_bytes_for(T, num_splits), stream, tw, src,
+                       src_lse, num_splits, out, lse_out, T, status, launch_overlap() >= 2);
 }
 
 }  // namespace
