@@ -47,6 +47,7 @@ PREFILL_KERNEL = "prefill attention (mla_prefill_attn)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 DOMINANT_KERNEL = "split attention (mla_decode_attn_partial)"
+DOMINANT_KERNEL_FP8 = "split attention over the FP8 cache (mla_decode_attn_fp8_partial)"
 
 
 def parse_args(argv=None):
@@ -56,7 +57,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=W.DEFAULT_BENCH_WORKLOAD,
-                   choices=sorted(W.WORKLOADS) + sorted(W.PREFILL_WORKLOADS))
+                   choices=sorted(W.WORKLOADS) + sorted(W.PREFILL_WORKLOADS) + sorted(W.FP8_WORKLOADS))
     p.add_argument("--split-pages", type=int, default=None, help="override the workload's KV split size")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-oracle sample budget")
@@ -199,12 +200,19 @@ def oracle_sample(inp: W.Inputs, budget_s: float, max_seqs: int | None = None):
         q_nope, q_rope = O.bf16_bits_to_f64(bits(inp.q_nope[b])), O.bf16_bits_to_f64(bits(inp.q_rope[b]))
         t0 = time.perf_counter()
         kv = c_bits.shape[0]
-        c = O.bf16_bits_to_f64(c_bits)
-        kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(kv)))
+        if inp.workload.cache_format == "fp8":
+            pages = (kv + 63) // 64
+            img = (np.full((pages, 64, 512), 0x7F, np.uint8), np.full((pages, 64), np.nan, np.float32),
+                   np.full((pages, 64, 64), 0x7E00, np.uint16))
+            img = O.append_kv_fp8(*img, c_bits[None], k_bits[None], [0], np.arange(pages)[None])
+            c, kr = O.gather_sequence_fp8(*img, np.arange(pages), kv)
+        else:
+            c = O.bf16_bits_to_f64(c_bits)
+            kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(kv)))
         O.decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, int(inp.prior_lens[b]))
         t += time.perf_counter() - t0
         done += 1
-        nbytes += kv * A.cache_bytes_per_token()
+        nbytes += kv * A.cache_bytes_per_token(cache_format=inp.workload.cache_format)
         if t >= budget_s:
             break
     return nbytes, t, done
@@ -330,7 +338,8 @@ def run_ours(args, wl):
         torch.sum(flush_r, dim=0, out=flush_sink)
     kv_list = inp.kv_lens.tolist()
     prefill = s.path == "non_absorbed"
-    step_bytes = A.step_cache_bytes(kv_list)
+    fp8 = wl.cache_format == "fp8"
+    step_bytes = A.step_cache_bytes(kv_list, wl.cache_format)
     if prefill:  # the metric counts new tokens; the roofline rates the attention's FLOPs
         step_units = wl.batch * wl.n_q
         step_flops = A.prefill_attention_flops(kv_list, wl.n_q)
@@ -430,7 +439,8 @@ def run_ours(args, wl):
         achieved, peak, unit = step_flops / attn_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                 "traffic": None if prefill else profiled_traffic(wl.name), "peak_source": peak_src,
-                "kernel": PREFILL_KERNEL if prefill else DOMINANT_KERNEL, "algorithmic_bytes": step_bytes,
+                "kernel": PREFILL_KERNEL if prefill else (DOMINANT_KERNEL_FP8 if fp8 else DOMINANT_KERNEL),
+                "algorithmic_bytes": step_bytes,
                 "algorithmic_flops": step_flops}
 
     cpu = None
@@ -446,7 +456,7 @@ def run_ours(args, wl):
         "metric": METRIC_PREFILL if prefill else METRIC,
         "value": total_bytes / (mean_ms * 1e-3) / (1 if prefill else 1e9), "unit": "tokens/s" if prefill else "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": mean_ms,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16" if fp8 else "bf16",
         "data": "synthetic",
         "config": workload_config(wl, inp, world, {"split_pages": s.split_pages, "num_splits": s.num_splits}),
         "us_per_step": mean_ms * 1e3,
@@ -472,7 +482,7 @@ def run_ours(args, wl):
 
 def main(argv=None):
     args = parse_args(argv)
-    wl = W.WORKLOADS.get(args.workload) or W.PREFILL_WORKLOADS[args.workload]
+    wl = W.WORKLOADS.get(args.workload) or W.PREFILL_WORKLOADS.get(args.workload) or W.FP8_WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -183,6 +183,48 @@ mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
                               float* o_latent, float* lse, cudaStream_t stream);
 
 /*
+ * FP8 latent cache.  The pages list FP8 (one byte per value) among the cache
+ * precisions, with a scaling strategy ("DeepSeek-MLA-Principle" section 7,
+ * mixed precision such as FP16/BF16/FP8 with scaling; "DeepSeek MLA 架构详解",
+ * the KV-cache memory formula with p_bytes = 1 for FP8), without fixing a
+ * format.  This library's format, per token t at page p, slot k:
+ *   cache_c8    [num_pages, 64, 512] uint8    OCP FP8 E4M3 codes of c_t / s_t
+ *   cache_scale [num_pages, 64]      float32  s_t = max(amax_t / 448, 2^-10)
+ *   cache_kr    [num_pages, 64, 64]  float16  (bits) k^R_t / s_t
+ * where amax_t is the largest |c_t[i]| of the token's bf16 latent, 448 the
+ * largest finite E4M3 value and k^R_t the rotated key of mla_append_kv.  644
+ * bytes per token instead of 1152.  The attention works on the dequantised
+ * values c_t = s_t E4M3(code) and k^R_t = s_t f16(stored).
+ *
+ * mla_append_kv_fp8 -- mla_append_kv for this format.  Each value passes the
+ * same float32 steps (so the image is reproducible bit for bit): amax of the
+ * bf16 inputs; s_t = max(amax / 448, 2^-10) with one IEEE division; each code
+ * = E4M3(c_i / s_t), one IEEE division, then nearest even with saturation at
+ * +-448; the key r is rotated as in mla_append_kv (float32, separately rounded
+ * products and sums) and stored as f16(r / s_t), one IEEE division, nearest
+ * even.  Arguments, placement and errors are those of mla_append_kv.
+ *
+ * mla_decode_attn_fp8_partial -- mla_decode_attn_partial over this format:
+ * same outputs, workspace, split plan and errors (combine and the fused
+ * finish calls take its partials unchanged).  Partial scores are exchanged as
+ * fp16 of (score over half a row) / 256 as in the bf16 kernel, and P reaches
+ * the P V MMA as f16(p_t s_t): a page whose p_t s_t exceeds 65504 (s_t above
+ * 255, i.e. a latent value beyond about 114000) overflows.  The query is
+ * converted to float16 (exact for 2^-14 <= |q| <= 65504).
+ */
+mla_status mla_append_kv_fp8(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
+                             const int32_t* seq_lens_before, const int32_t* page_table,
+                             int pt_stride, const float* rope_table, int rope_max_pos,
+                             uint8_t* cache_c8, float* cache_scale, uint16_t* cache_kr,
+                             int64_t num_pages, int B, int n_new, cudaStream_t stream);
+mla_status mla_decode_attn_fp8_partial(const mla_bf16* q_abs, const uint8_t* cache_c8,
+                                       const float* cache_scale, const uint16_t* cache_kr,
+                                       int64_t num_pages, const int32_t* page_table, int pt_stride,
+                                       const int32_t* kv_lens, int B, int n_q, int max_kv_len,
+                                       int split_pages, void* workspace, size_t workspace_bytes,
+                                       float* o_latent, float* lse, cudaStream_t stream);
+
+/*
  * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate
  * device memory.  (The MLA pages have no counterpart to this call; it exists for
  * deployment.)  Some callers may not call cudaMalloc when they run a decode

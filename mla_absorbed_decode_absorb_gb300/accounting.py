@@ -36,7 +36,13 @@ def mha_cache_scalars_per_token() -> int:
     return 2 * N_HEADS * D_NOPE
 
 
-def cache_bytes_per_token(dtype_bytes: int = BF16_BYTES) -> int:
+# The FP8 latent cache: 512 one-byte E4M3 codes, one float32 scale, 64 float16 key values.
+FP8_CACHE_BYTES_PER_TOKEN = D_LATENT + 4 + 2 * D_ROPE
+
+
+def cache_bytes_per_token(dtype_bytes: int = BF16_BYTES, cache_format: str = "bf16") -> int:
+    if cache_format == "fp8":
+        return FP8_CACHE_BYTES_PER_TOKEN
     return cache_scalars_per_token() * dtype_bytes
 
 
@@ -54,9 +60,9 @@ def flops_per_token_pair() -> int:
     return 2 * mla_history_macs(1)
 
 
-def step_cache_bytes(kv_lens) -> int:
+def step_cache_bytes(kv_lens, cache_format: str = "bf16") -> int:
     """Cache bytes one decode step reads: every cached token once per sequence."""
-    return sum(int(n) for n in kv_lens) * cache_bytes_per_token()
+    return sum(int(n) for n in kv_lens) * cache_bytes_per_token(cache_format=cache_format)
 
 
 def step_attention_flops(kv_lens, n_q: int) -> int:

@@ -149,6 +149,55 @@ mla_status mla_append_kv(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
                                     rope_table, rope_max_pos, cache, num_pages, B, n_new, st, stream));
 }
 
+mla_status mla_append_kv_fp8(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
+                             const int32_t* seq_lens_before, const int32_t* page_table,
+                             int pt_stride, const float* rope_table, int rope_max_pos,
+                             uint8_t* cache_c8, float* cache_scale, uint16_t* cache_kr,
+                             int64_t num_pages, int B, int n_new, cudaStream_t stream) {
+  if (B < 0 || n_new < 0) return MLA_ERR_INVALID_ARG;
+  if (B == 0 || n_new == 0) return MLA_OK;
+  if (!c_kv_new || !k_pe_new || !seq_lens_before || !page_table || !rope_table || !cache_c8 || !cache_scale ||
+      !cache_kr)
+    return MLA_ERR_INVALID_ARG;
+  if (pt_stride < 1 || rope_max_pos < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c_kv_new) || !aligned16(cache_c8)) return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_append_kv_fp8(c_kv_new, k_pe_new, seq_lens_before, page_table, pt_stride, rope_table,
+                                        rope_max_pos, cache_c8, cache_scale, cache_kr, num_pages, B, n_new, st,
+                                        stream));
+}
+
+mla_status mla_decode_attn_fp8_partial(const mla_bf16* q_abs, const uint8_t* cache_c8, const float* cache_scale,
+                                       const uint16_t* cache_kr, int64_t num_pages, const int32_t* page_table,
+                                       int pt_stride, const int32_t* kv_lens, int B, int n_q, int max_kv_len,
+                                       int split_pages, void* workspace, size_t workspace_bytes,
+                                       float* o_latent, float* lse, cudaStream_t stream) {
+  SplitPlan plan;
+  if (!make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_abs || !cache_c8 || !cache_scale || !cache_kr || !page_table || !kv_lens || !o_latent || num_pages < 1 ||
+      pt_stride < 1)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_abs) || !aligned16(cache_c8) || !aligned16(cache_scale) || !aligned16(cache_kr) ||
+      !aligned16(o_latent))
+    return MLA_ERR_INVALID_ARG;
+  if (plan.workspace_bytes > 0 && (workspace == nullptr || workspace_bytes < plan.workspace_bytes ||
+                                   !aligned16(workspace)))
+    return MLA_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  float* o_out = o_latent;
+  float* lse_out = lse;
+  if (plan.num_splits > 1) {
+    o_out = static_cast<float*>(workspace);
+    lse_out = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.o_part_bytes);
+  }
+  return from_cuda(launch_decode_partial_fp8(q_abs, cache_c8, cache_scale, cache_kr, num_pages, page_table,
+                                             pt_stride, kv_lens, B, n_q, max_kv_len, plan, o_out, lse_out, st,
+                                             stream));
+}
+
 mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope,
                         const int32_t* seq_lens_before, const mla_bf16* w_uk,
                         const float* rope_table, int rope_max_pos, mla_bf16* q_abs,

@@ -100,6 +100,18 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   const SplitPlan& plan, float* o_out, float* lse_out,
                                   int* status, cudaStream_t stream);
 
+cudaError_t launch_decode_partial_fp8(const uint16_t* q_abs, const uint8_t* cache_c8, const float* cache_scale,
+                                      const uint16_t* cache_kr, int64_t num_pages, const int32_t* page_table,
+                                      int pt_stride, const int32_t* kv_lens, int B, int n_q, int max_kv_len,
+                                      const SplitPlan& plan, float* o_out, float* lse_out, int* status,
+                                      cudaStream_t stream);
+
+cudaError_t launch_append_kv_fp8(const uint16_t* c_kv_new, const uint16_t* k_pe_new,
+                                 const int32_t* seq_lens_before, const int32_t* page_table,
+                                 int pt_stride, const float* rope_table, int rope_max_pos,
+                                 uint8_t* c8, float* scale, uint16_t* kr, int64_t num_pages, int B, int n_new,
+                                 int* status, cudaStream_t stream);
+
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream);
 

@@ -122,6 +122,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// Contiguous global -> shared copy of `bytes` (a multiple of 16, both addresses
+// 16-byte aligned), completing its bytes of transaction on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // 3-D tiled load of the box at (x, y, z) into shared memory.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                                             uint32_t bar) {
@@ -195,6 +203,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | (1u << 7)                              // A format: bf16
          | (1u << 10)                             // B format: bf16
          | (static_cast<uint32_t>(a_mn) << 15)    // A major
+         | (static_cast<uint32_t>(b_mn) << 16)    // B major
+         | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
+}
+
+// Instruction descriptor, kind::f16 with f16 A/B and fp32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                                // D format: f32
+         | (static_cast<uint32_t>(a_mn) << 15)    // A major (A, B format 0: f16)
          | (static_cast<uint32_t>(b_mn) << 16)    // B major
          | (static_cast<uint32_t>(N >> 3) << 17)  // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
@@ -350,6 +367,11 @@ __device__ __forceinline__ float2 f32x2_split(uint64_t v) {
 __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {

@@ -51,6 +51,8 @@ _SIGS = {
     "mla_decompress_kv": ([_p, _i64, _p, _i, _p, _i, _i, _p, _p, _p, _p, _p], _i),
     "mla_prefill_attn": ([_p, _p, _p, _p, _i, _p, _p, _i, _p, _i64, _p, _i, _p, _i, _i, _p, _p, _p], _i),
     "mla_get_launch_overlap": ([], _i),
+    "mla_append_kv_fp8": ([_p, _p, _p, _p, _i, _p, _i, _p, _p, _p, _i64, _i, _i, _p], _i),
+    "mla_decode_attn_fp8_partial": ([_p, _p, _p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -129,6 +131,56 @@ def mla_append_kv(c_kv_new, k_pe_new, seq_lens_before, page_table, rope, cache, 
         raise ValueError("cache must be [num_pages, 64, 576]")
     _check("mla_append_kv", lib.mla_append_kv(*args))
     return cache
+
+
+def fp8_cache_empty(num_pages, device, fill_code=0x7F):
+    """An FP8 latent cache: (E4M3 codes [P, 64, 512] uint8, scales [P, 64] f32, keys [P, 64, 64] f16).
+
+    Unwritten slots hold ``fill_code`` (0x7F is E4M3 NaN), NaN scales and NaN keys.
+    """
+    c8 = torch.full((num_pages, 64, D_LATENT), fill_code, dtype=torch.uint8, device=device)
+    scale = torch.full((num_pages, 64), float("nan"), dtype=torch.float32, device=device)
+    kr = torch.full((num_pages, 64, D_ROPE), float("nan"), dtype=torch.float16, device=device)
+    return c8, scale, kr
+
+
+def mla_append_kv_fp8(c_kv_new, k_pe_new, seq_lens_before, page_table, rope, cache_fp8, stream=None):
+    c8, scale, kr = cache_fp8
+    B, n_new = c_kv_new.shape[:2]
+    P = int(c8.shape[0])
+    if page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages]")
+    _check("mla_append_kv_fp8", lib.mla_append_kv_fp8(
+        _dev(c_kv_new, "c_kv_new", torch.bfloat16, (B, n_new, D_LATENT)),
+        _dev(k_pe_new, "k_pe_new", torch.bfloat16, (B, n_new, D_ROPE)),
+        _dev(seq_lens_before, "seq_lens_before", torch.int32, (B,)),
+        _dev(page_table, "page_table", torch.int32), int(page_table.shape[1]),
+        _dev(rope, "rope_table", torch.float32), int(rope.shape[0]),
+        _dev(c8, "cache_c8", torch.uint8, (P, 64, D_LATENT)),
+        _dev(scale, "cache_scale", torch.float32, (P, 64)),
+        _dev(kr, "cache_kr", torch.float16, (P, 64, D_ROPE)),
+        P, int(B), int(n_new), _stream(stream)))
+    return cache_fp8
+
+
+def mla_decode_attn_fp8_partial(q_abs, cache_fp8, page_table, kv_lens, n_q, max_kv_len, split_pages, workspace,
+                                o_latent, lse=None, stream=None):
+    c8, scale, kr = cache_fp8
+    B = kv_lens.shape[0]
+    P = int(c8.shape[0])
+    _check("mla_decode_attn_fp8_partial", lib.mla_decode_attn_fp8_partial(
+        _dev(q_abs, "q_abs", torch.bfloat16, (B, n_q, N_HEADS, D_ROW)),
+        _dev(c8, "cache_c8", torch.uint8, (P, 64, D_LATENT)),
+        _dev(scale, "cache_scale", torch.float32, (P, 64)),
+        _dev(kr, "cache_kr", torch.float16, (P, 64, D_ROPE)),
+        P, _dev(page_table, "page_table", torch.int32), int(page_table.shape[1]),
+        _dev(kv_lens, "kv_lens", torch.int32, (B,)),
+        int(B), int(n_q), int(max_kv_len), int(split_pages),
+        0 if workspace is None else _dev(workspace, "workspace", torch.uint8),
+        0 if workspace is None else workspace.numel(),
+        _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
+        0 if lse is None else _dev(lse, "lse", torch.float32, (B, n_q, N_HEADS)),
+        _stream(stream)))
 
 
 def mla_absorb_q(q_nope, q_rope, seq_lens_before, w_uk, rope, q_abs=None, stream=None):

@@ -19,6 +19,10 @@ step 3.  By default all launches stay on the caller's stream, where the
 library's programmatic dependent launch (``mla_set_launch_overlap``) lets each
 kernel's prologue overlap the previous one.
 
+With the workload's ``cache_format`` "fp8" the cache is the FP8 latent cache
+(E4M3 codes with one scale per token) and steps 1 and 3 are
+``mla_append_kv_fp8`` and ``mla_decode_attn_fp8_partial``; the rest is unchanged.
+
 A step that brings ``PREFILL_MIN_NEW_TOKENS`` (64) or more new tokens per
 sequence takes the non-absorbed path instead, as inference engines switch for
 prefill and chunked prefill: ``mla_append_kv``, ``mla_decompress_kv`` (per-head
@@ -43,6 +47,9 @@ class DecodeSession:
     def __init__(self, inp: Inputs, device="cuda", split_pages: int | None = None, stream=None,
                  fused_finish: bool = True, overlap_append: bool = False, path: str | None = None):
         self.inp = inp
+        self.cache_format = inp.workload.cache_format
+        if self.cache_format not in ("bf16", "fp8"):
+            raise ValueError(f"unknown cache format {self.cache_format!r}")
         self.fused_finish = bool(fused_finish)
         self.overlap_append = bool(overlap_append)
         self.device = torch.device(device)
@@ -56,6 +63,8 @@ class DecodeSession:
         if path not in ("absorbed", "non_absorbed"):
             raise ValueError(f"unknown path {path!r}")
         self.path = path
+        if self.cache_format == "fp8" and path != "absorbed":
+            raise ValueError("the FP8 latent cache is read by the absorbed path only")
         dev = self.device
         self.max_kv_len = int(inp.kv_lens.max()) if self.B else self.n_q
         self.rope = ops.rope_table(self.max_kv_len + 1, dev, stream)
@@ -67,14 +76,22 @@ class DecodeSession:
         c_new, k_new = inp.new_tokens()
         self._pack_step_inputs([("c_new", c_new), ("k_new", k_new), ("q_nope", inp.q_nope),
                                 ("q_rope", inp.q_rope), ("prior_lens", inp.prior_lens), ("kv_lens", inp.kv_lens)])
-        self.cache = empty_cache(inp.num_pages, dev)
+        if self.cache_format == "fp8":
+            self.cache = None
+            self.cache_fp8 = ops.fp8_cache_empty(inp.num_pages, dev)
+        else:
+            self.cache = empty_cache(inp.num_pages, dev)
         zero = torch.zeros(1, dtype=torch.int32, device=dev)
         for b in range(self.B):
             hc, hk = inp.history(b)
             if hc.shape[0] == 0:
                 continue
-            ops.mla_append_kv(hc.to(dev)[None], hk.to(dev)[None], zero, self.page_table[b:b + 1], self.rope,
-                              self.cache, stream=stream)
+            if self.cache_format == "fp8":
+                ops.mla_append_kv_fp8(hc.to(dev)[None], hk.to(dev)[None], zero, self.page_table[b:b + 1],
+                                      self.rope, self.cache_fp8, stream=stream)
+            else:
+                ops.mla_append_kv(hc.to(dev)[None], hk.to(dev)[None], zero, self.page_table[b:b + 1], self.rope,
+                                  self.cache, stream=stream)
         self.lse = torch.empty(self.B, self.n_q, N_HEADS, dtype=torch.float32, device=dev)
         self.out = torch.empty(self.B, self.n_q, N_HEADS, D_NOPE, dtype=torch.bfloat16, device=dev)
         if self.path == "absorbed":
@@ -128,8 +145,12 @@ class DecodeSession:
             self._forked.record(self._main(stream))
             self.side.wait_event(self._forked)
             stream = self.side
-        ops.mla_append_kv(self.c_new, self.k_new, self.prior_lens, self.page_table, self.rope, self.cache,
-                          stream=stream)
+        if self.cache_format == "fp8":
+            ops.mla_append_kv_fp8(self.c_new, self.k_new, self.prior_lens, self.page_table, self.rope,
+                                  self.cache_fp8, stream=stream)
+        else:
+            ops.mla_append_kv(self.c_new, self.k_new, self.prior_lens, self.page_table, self.rope, self.cache,
+                              stream=stream)
         if self.overlap_append:
             self._appended.record(self.side)
 
@@ -140,9 +161,14 @@ class DecodeSession:
     def attend_partial(self, stream=None):
         if self.overlap_append:
             self._main(stream).wait_event(self._appended)  # the cache holds the new tokens
-        ops.mla_decode_attn_partial(self.q_abs, self.cache, self.page_table, self.kv_lens, self.n_q,
-                                    self.max_kv_len, self.split_pages, self.workspace, self.o_latent,
-                                    self.lse, stream=stream)
+        if self.cache_format == "fp8":
+            ops.mla_decode_attn_fp8_partial(self.q_abs, self.cache_fp8, self.page_table, self.kv_lens, self.n_q,
+                                            self.max_kv_len, self.split_pages, self.workspace, self.o_latent,
+                                            self.lse, stream=stream)
+        else:
+            ops.mla_decode_attn_partial(self.q_abs, self.cache, self.page_table, self.kv_lens, self.n_q,
+                                        self.max_kv_len, self.split_pages, self.workspace, self.o_latent,
+                                        self.lse, stream=stream)
 
     def combine(self, stream=None):
         ops.mla_decode_combine(self.B, self.n_q, self.max_kv_len, self.split_pages, self.workspace,

@@ -52,6 +52,7 @@ class Workload:
     lengths: tuple[int, ...] | None = None  # explicit L_b (edge-case workloads)
     split_pages: int = 0                  # prescribed KV split size in pages (0 = auto)
     description: str = ""
+    cache_format: str = "bf16"            # "bf16" (576 bf16 per token) or "fp8" (E4M3 latent, see ops)
 
 
 # The five workloads of the benchmark, named by what they are.
@@ -83,13 +84,23 @@ PREFILL_WORKLOADS: dict[str, Workload] = {
     ]
 }
 
+# The batched decode over the FP8 latent cache (644 bytes per token instead of 1152).
+FP8_WORKLOADS: dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("batched_b32_l4096_fp8", batch=32, n_q=1, context=4096, cache_format="fp8",
+                 description="B=32, 1 new token each, uniform prior context 4096, FP8 latent cache"),
+    ]
+}
+
 DEFAULT_BENCH_WORKLOAD = "batched_b32_l4096"
 
 
-def custom(name: str, lengths, n_q: int = 1, split_pages: int = 0) -> Workload:
+def custom(name: str, lengths, n_q: int = 1, split_pages: int = 0, cache_format: str = "bf16") -> Workload:
     """A workload with explicit prior lengths (parity and edge-case tests)."""
     lengths = tuple(int(x) for x in lengths)
-    return Workload(name, batch=len(lengths), n_q=n_q, lengths=lengths, split_pages=split_pages)
+    return Workload(name, batch=len(lengths), n_q=n_q, lengths=lengths, split_pages=split_pages,
+                    cache_format=cache_format)
 
 
 def scaled(wl: Workload, batch: int | None = None, context: int | None = None) -> Workload:
@@ -98,7 +109,8 @@ def scaled(wl: Workload, batch: int | None = None, context: int | None = None) -
         wl.name + "_scaled", batch=batch or wl.batch, n_q=wl.n_q,
         context=context if context is not None else wl.context,
         ragged=None if context is not None else wl.ragged,
-        lengths=None, split_pages=wl.split_pages, description="scaled " + wl.description)
+        lengths=None, split_pages=wl.split_pages, description="scaled " + wl.description,
+        cache_format=wl.cache_format)
 
 
 @dataclass

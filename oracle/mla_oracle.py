@@ -116,6 +116,11 @@ def rope_key_bf16_bits(k_pe_bits, pos) -> np.ndarray:
     then rounded to bf16 (nearest even):
     ``r1 = (x1*c) - (x2*s)``, ``r2 = (x2*c) + (x1*s)``.
     """
+    return f32_to_bf16_bits(rope_key_f32(k_pe_bits, pos))
+
+
+def rope_key_f32(k_pe_bits, pos) -> np.ndarray:
+    """The float32 rotated key of :func:`rope_key_bf16_bits` before its bf16 rounding."""
     x = bf16_bits_to_f32(k_pe_bits)
     pos = np.asarray(pos, dtype=np.int64)
     half = x.shape[-1] // 2
@@ -125,7 +130,7 @@ def rope_key_bf16_bits(k_pe_bits, pos) -> np.ndarray:
     x1, x2 = x[..., :half], x[..., half:]
     r1 = np.subtract(np.multiply(x1, c, dtype=np.float32), np.multiply(x2, s, dtype=np.float32), dtype=np.float32)
     r2 = np.add(np.multiply(x2, c, dtype=np.float32), np.multiply(x1, s, dtype=np.float32), dtype=np.float32)
-    return f32_to_bf16_bits(np.concatenate([r1, r2], axis=-1))
+    return np.concatenate([r1, r2], axis=-1)
 
 
 # --------------------------------------------------------------------------- paged cache
@@ -162,6 +167,120 @@ def gather_sequence(cache_bits, page_table_row, kv_len: int, d_c: int = 512):
     pages = np.asarray(page_table_row, dtype=np.int64)[t // PAGE]
     rows = np.asarray(cache_bits, dtype=np.uint16)[pages, t % PAGE]
     return bf16_bits_to_f64(rows[:, :d_c]), bf16_bits_to_f64(rows[:, d_c:])
+
+
+# --------------------------------------------------------------------------- FP8 latent cache
+# The pages name FP8 (one byte per value) among the precisions for the cache and
+# for "mixed precision with a scaling strategy" ([DP] §7, training and
+# inference; [N1] "标准 KV Cache 的显存瓶颈", p_bytes = 1 for FP8) but fix no
+# format.  Reading taken here: the 512 latent values of a token are stored as
+# OCP FP8 E4M3 codes of c / s with one float32 scale s per token,
+# s = max(amax / 448, 2^-10) (448 is E4M3's largest finite value; the floor keeps
+# the stored RoPE key in range); the rotated key is stored as float16 of
+# k^R / s, so that both parts of the score carry the same factor 1 / s.  The
+# attention then works on the dequantised values c = s * E4M3(code) and
+# k^R = s * f16(stored).
+
+E4M3_MAX = 448.0
+FP8_SCALE_FLOOR = 2.0 ** -10
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Value of E4M3 codes as float64: sign bit, 4 exponent bits (bias 7), 3 mantissa bits.
+
+    Exponent field 0 is subnormal (m / 8 * 2^-6); S.1111.111 is NaN; there are no
+    infinities, so S.1111.110 = 448 is the largest finite magnitude.
+    """
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+    return sign * mag
+
+
+@lru_cache(maxsize=1)
+def _e4m3_positive_grid():
+    codes = np.arange(0x7F, dtype=np.uint8)          # 0x00 .. 0x7E: every finite non-negative value
+    return codes, e4m3_decode(codes)
+
+
+def f32_to_e4m3_codes(x) -> np.ndarray:
+    """Round float32 values to E4M3, to nearest with ties to the even code, saturating at +-448.
+
+    Brute force over the 127 finite non-negative codes: the nearest value wins;
+    on a tie the code with an even last mantissa bit.  NaN maps to 0x7F.
+    """
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    codes, vals = _e4m3_positive_grid()
+    a = np.minimum(np.abs(x), E4M3_MAX)
+    d = np.abs(a[..., None] - vals)                   # [..., 127]
+    best = d.min(axis=-1, keepdims=True)
+    cand = d == best
+    # among tied candidates (at most two adjacent codes) prefer the even code
+    even = (codes & 1) == 0
+    pick = np.where(cand & even, 1, 0) + np.where(cand, 1, 0)   # 2: tied and even, 1: tied
+    idx = pick.argmax(axis=-1)
+    out = codes[idx].astype(np.uint8)
+    out = np.where(np.signbit(x), out | 0x80, out).astype(np.uint8)   # the sign is kept, also on zero
+    out = np.where(np.isnan(x), np.uint8(0x7F), out)
+    return out.astype(np.uint8)
+
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    """Round float32 to IEEE binary16 (nearest even, overflow to infinity); bit patterns."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def fp8_token_scale(c_bits) -> np.ndarray:
+    """Per-token scale ``s = max(amax / 448, 2^-10)`` in float32 (one IEEE division)."""
+    c = bf16_bits_to_f32(c_bits)
+    amax = np.abs(c).max(axis=-1).astype(np.float32)
+    s = np.divide(amax, np.float32(E4M3_MAX), dtype=np.float32)
+    return np.maximum(s, np.float32(FP8_SCALE_FLOOR)).astype(np.float32)
+
+
+def append_kv_fp8(c8, scale, kr, c_kv_new_bits, k_pe_new_bits, seq_lens_before, page_table):
+    """Append n_new tokens per sequence to an FP8 paged cache (returns new images).
+
+    Images: ``c8 [P, 64, 512]`` uint8 E4M3 codes, ``scale [P, 64]`` float32,
+    ``kr [P, 64, 64]`` uint16 float16 bits.  Token placement as :func:`append_kv`.
+    Per token: ``s`` by :func:`fp8_token_scale`; code_i = E4M3(float32(c_i / s))
+    (one IEEE division each, then :func:`f32_to_e4m3_codes`); the stored key is
+    f16(float32(r / s)) for the float32 rotated key ``r`` of :func:`rope_key_f32`.
+    """
+    c8 = np.array(c8, dtype=np.uint8, copy=True)
+    scale = np.array(scale, dtype=np.float32, copy=True)
+    kr = np.array(kr, dtype=np.uint16, copy=True)
+    c_new = np.asarray(c_kv_new_bits, dtype=np.uint16)
+    k_new = np.asarray(k_pe_new_bits, dtype=np.uint16)
+    B, n_new, d_c = c_new.shape
+    if B == 0 or n_new == 0:
+        return c8, scale, kr
+    lens = np.asarray(seq_lens_before, dtype=np.int64)
+    pt = np.asarray(page_table, dtype=np.int64)
+    pos = lens[:, None] + np.arange(n_new)[None, :]
+    pages = np.take_along_axis(pt, pos // PAGE, axis=1)
+    slots = pos % PAGE
+    s = fp8_token_scale(c_new)                                     # [B, n]
+    q = np.divide(bf16_bits_to_f32(c_new), s[..., None], dtype=np.float32)
+    c8[pages, slots] = f32_to_e4m3_codes(q)
+    scale[pages, slots] = s
+    r = rope_key_f32(k_new.reshape(B * n_new, -1), pos.reshape(-1)).reshape(B, n_new, -1)
+    kr[pages, slots] = f32_to_f16_bits(np.divide(r, s[..., None], dtype=np.float32))
+    return c8, scale, kr
+
+
+def gather_sequence_fp8(c8, scale, kr, page_table_row, kv_len: int):
+    """Dequantised tokens 0..kv_len-1 of one sequence in float64: (c = s E4M3(code), k^R = s f16(stored))."""
+    t = np.arange(kv_len)
+    pages = np.asarray(page_table_row, dtype=np.int64)[t // PAGE]
+    slots = t % PAGE
+    s = np.asarray(scale, dtype=np.float32)[pages, slots].astype(np.float64)[:, None]
+    c = s * e4m3_decode(np.asarray(c8, dtype=np.uint8)[pages, slots])
+    k = s * np.asarray(kr, dtype=np.uint16)[pages, slots].view(np.float16).astype(np.float64)
+    return c, k
 
 
 # --------------------------------------------------------------------------- attention

@@ -414,3 +414,104 @@ def test_planted_mistakes(monkeypatch):
     def mha_off_by_one(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len, heads=None):
         return O.decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len - 1, heads)
     assert not check_two_tokens(decode=mha_off_by_one)
+
+
+# ------------------------------------------------------------------------ FP8 latent cache
+def test_e4m3_decode_follows_the_format():
+    """Values of E4M3 codes from the format's definition (bias 7, 3 mantissa bits,
+    subnormals, no infinities, S.1111.111 NaN), cross-checked with torch's float8_e4m3fn."""
+    codes = np.arange(256, dtype=np.uint8)
+    v = O.e4m3_decode(codes)
+    assert v[0x38] == 1.0 and v[0x39] == 1.125 and v[0x7E] == 448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x07] == 7 * 2.0 ** -9 and v[0x01] == 2.0 ** -9
+    assert v[0xB8] == -1.0 and v[0xFE] == -448.0 and v[0x80] == 0.0 and np.signbit(v[0x80])
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF]) and np.isnan(v).sum() == 2
+    assert np.all(np.diff(v[:0x7F]) > 0)           # codes 0x00 .. 0x7E are in increasing order
+    t = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(v), np.isnan(t))
+    assert np.array_equal(v[~np.isnan(v)], t[~np.isnan(t)])
+
+
+def test_e4m3_encode_rounds_to_nearest_even_and_saturates():
+    cases = [(1.0625, 0x38), (1.1875, 0x3A), (1.0626, 0x39), (448.0, 0x7E), (464.0, 0x7E), (1e6, 0x7E),
+             (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02), (2.0 ** -9, 0x01), (-1.0, 0xB8), (-1e6, 0xFE),
+             (0.0, 0x00), (-0.0, 0x80), (240.0, 0x77), (248.0, 0x78)]
+    x = np.array([v for v, _ in cases], dtype=np.float32)
+    assert O.f32_to_e4m3_codes(x).tolist() == [c for _, c in cases]
+    assert O.f32_to_e4m3_codes(np.array([np.nan], np.float32))[0] == 0x7F
+    finite = np.arange(0x7F, dtype=np.uint8)        # every finite code round-trips, both signs
+    assert np.array_equal(O.f32_to_e4m3_codes(O.e4m3_decode(finite).astype(np.float32)), finite)
+    neg = (finite | 0x80).astype(np.uint8)
+    assert np.array_equal(O.f32_to_e4m3_codes(O.e4m3_decode(neg).astype(np.float32)), neg)
+    rng = np.random.default_rng(11)
+    y = (rng.standard_normal(50000) * np.exp2(rng.integers(-12, 9, 50000))).astype(np.float32)
+    y = np.clip(y, -448, 448).astype(np.float32)
+    ref = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.f32_to_e4m3_codes(y), ref)
+
+
+def _fp8_images(P):
+    return (np.full((P, 64, 512), 0x7F, np.uint8), np.full((P, 64), np.nan, np.float32),
+            np.full((P, 64, 64), 0x7E00, np.uint16))
+
+
+def test_fp8_append_stores_within_the_format_bounds():
+    """Placement as the bf16 append; the scale is max(amax / 448, 2^-10); the largest
+    latent value maps to +-448 exactly; every dequantised value is within half an E4M3
+    step; the stored key gives back k^R within half an f16 step; other slots untouched."""
+    rng = np.random.default_rng(12)
+    B, n, P = 4, 3, 12
+    c = rng.standard_normal((B, n, 512)).astype(np.float32)
+    c[1, 0] = 0.0                     # an all-zero latent: the scale floor
+    c[2, 1] *= 1e-4                   # tiny latent: the floor again, codes below 448
+    c[3, 2] *= 300.0                  # large latent
+    c_bits = O.f32_to_bf16_bits(c)
+    k_bits = O.f32_to_bf16_bits(rng.standard_normal((B, n, 64)).astype(np.float32))
+    lens = np.array([0, 62, 64, 125])
+    pt = rng.permutation(P).reshape(B, 3)
+    c8, sc, kr = O.append_kv_fp8(*_fp8_images(P), c_bits, k_bits, lens, pt)
+    cv = O.bf16_bits_to_f64(c_bits)
+    written = np.zeros((P, 64), bool)
+    for b in range(B):
+        for j in range(n):
+            pos = lens[b] + j
+            pg, sl = pt[b, pos // 64], pos % 64
+            written[pg, sl] = True
+            amax = np.abs(cv[b, j]).max()
+            s = np.float32(max(np.float32(amax) / np.float32(448.0), np.float32(2.0 ** -10)))
+            assert sc[pg, sl] == s
+            deq = float(s) * O.e4m3_decode(c8[pg, sl])
+            step = np.where(np.abs(cv[b, j]) / s >= 2.0 ** -6, np.abs(cv[b, j]) * 2.0 ** -4, float(s) * 2.0 ** -10)
+            assert np.all(np.abs(deq - cv[b, j]) <= step * (1 + 1e-6))
+            if amax / 448 >= 2.0 ** -10:
+                assert np.abs(O.e4m3_decode(c8[pg, sl])).max() == 448.0
+            r = O.rope_key_f32(k_bits[b, j][None], np.array([pos]))[0].astype(np.float64)
+            kd = float(s) * kr[pg, sl].view(np.float16).astype(np.float64)
+            assert np.all(np.abs(kd - r) <= np.abs(r) * 2.0 ** -11 * (1 + 1e-6) + float(s) * 2.0 ** -25)
+    assert np.all(c8[~written] == 0x7F) and np.all(np.isnan(sc[~written])) and np.all(kr[~written] == 0x7E00)
+    assert sc[pt[1, 0], 62] == np.float32(2.0 ** -10) and np.all(c8[pt[1, 0], 62] == 0)
+
+
+def test_fp8_cache_attention_stays_near_the_bf16_result():
+    """The definition on the dequantised FP8 cache against the same on the bf16 cache:
+    the latent output moves by the quantisation error (about 2^-5 relative per value,
+    averaged over the attended tokens), the log-sum-exp by a few hundredths."""
+    rng = np.random.default_rng(13)
+    H, kv = 4, 200
+    c = rng.standard_normal((kv, 512)).astype(np.float32)
+    k_pe = rng.standard_normal((kv, 64)).astype(np.float32)
+    c_bits, k_bits = O.f32_to_bf16_bits(c), O.f32_to_bf16_bits(k_pe)
+    pt = np.arange(4)[None]
+    c8, sc, kr = O.append_kv_fp8(*_fp8_images(4), c_bits[None], k_bits[None], [0], pt)
+    cq, kq = O.gather_sequence_fp8(c8, sc, kr, pt[0], kv)
+    cb = O.bf16_bits_to_f64(c_bits)
+    kb = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(kv)))
+    q_nope = rng.standard_normal((1, H, 128))
+    q_rope = rng.standard_normal((1, H, 64))
+    w_uk = rng.standard_normal((H, 128, 512)) * 0.02
+    w_uv = rng.standard_normal((H, 128, 512)) * 0.02
+    o8, lat8, lse8 = O.decode_mha(q_nope, q_rope, w_uk, w_uv, cq, kq, kv - 1)
+    ob, latb, lseb = O.decode_mha(q_nope, q_rope, w_uk, w_uv, cb, kb, kv - 1)
+    rel = np.linalg.norm(lat8 - latb) / np.linalg.norm(latb)
+    assert 1e-4 < rel < 4e-2, rel
+    assert np.abs(lse8 - lseb).max() < 5e-2
