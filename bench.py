@@ -42,6 +42,7 @@ from mla_absorbed_decode_absorb_gb300 import accounting as A  # noqa: E402
 from mla_absorbed_decode_absorb_gb300 import workloads as W  # noqa: E402
 
 METRIC = "MLA absorbed decode µs/step, latent-cache GB/s and TFLOP/s vs GB300 roofline"
+METRIC_LAYER = "MLA decode layer (projections + absorbed attention) µs/step, HBM GB/s of weights and cache"
 METRIC_PREFILL = "MLA non-absorbed chunked prefill, new tokens/s and TFLOP/s vs GB300 roofline"
 PREFILL_KERNEL = "prefill attention (mla_prefill_attn)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -57,7 +58,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=W.DEFAULT_BENCH_WORKLOAD,
-                   choices=sorted(W.WORKLOADS) + sorted(W.PREFILL_WORKLOADS) + sorted(W.FP8_WORKLOADS))
+                   choices=sorted(W.WORKLOADS) + sorted(W.PREFILL_WORKLOADS) + sorted(W.FP8_WORKLOADS)
+                   + sorted(W.LAYER_WORKLOADS))
     p.add_argument("--split-pages", type=int, default=None, help="override the workload's KV split size")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-oracle sample budget")
@@ -218,6 +220,33 @@ def oracle_sample(inp: W.Inputs, budget_s: float, max_seqs: int | None = None):
     return nbytes, t, done
 
 
+def oracle_layer_sample(li, budget_s: float, max_seqs=None):
+    """The fp64 layer oracle on whole sequences until ``budget_s`` is spent; returns
+    (sequences done, seconds).  A step of the workload costs B times one sequence."""
+    import numpy as np
+
+    from oracle import mla_oracle as O
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    f64 = lambda t: O.bf16_bits_to_f64(bits(t))  # noqa: E731
+    inp = li.base
+    ws = [f64(w) for w in (li.w_dkv, li.w_kr, li.w_dq, li.w_uq, li.w_qr)]
+    w_uk, w_uv, w_o = f64(inp.w_uk), f64(inp.w_uv), f64(li.w_o)
+    done, t = 0, 0.0
+    for b in range(inp.batch if max_seqs is None else min(max_seqs, inp.batch)):
+        hc, hk = inp.history(b)
+        L = int(inp.prior_lens[b])
+        t0 = time.perf_counter()
+        kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(bits(hk), np.arange(L)))
+        O.decode_layer(f64(li.x[b]), *ws, w_uk, w_uv, w_o, f64(hc), kr, L)
+        t += time.perf_counter() - t0
+        done += 1
+        if t >= budget_s:
+            break
+    return done, t
+
+
 def oracle_prefill_sample(inp: W.Inputs, budget_s: float):
     """The fp64 oracle on a bounded sample of a many-token step: the first new
     tokens of sequence 0 on 16 heads, as many 8-token groups as the budget
@@ -259,6 +288,16 @@ def run_reference(args, wl):
         sample_fn = lambda: oracle_prefill_sample(inp, 0.0)[:2]  # noqa: E731
         sample = "8 new tokens of sequence 0 on 16 of 128 heads per step, scaled to 128 heads"
         metric, unit, scale = METRIC_PREFILL, "tokens/s", 1.0
+    elif wl.d_model > 0:  # one sequence through the layer oracle per step, a step costing B of them
+        li = W.generate_layer(wl, seed=0)
+        inp = li.base
+        units_step = A.step_cache_bytes(inp.kv_lens.tolist()) + A.layer_weight_bytes(wl.d_model)
+
+        def sample_fn():
+            _, t = oracle_layer_sample(li, 0.0, max_seqs=1)
+            return units_step, t * inp.batch
+        sample = f"one sequence of the layer workload per step, a step costing {inp.batch} of them"
+        metric, unit, scale = METRIC_LAYER, "GB/s", 1e9
     else:
         sample_fn = lambda: oracle_sample(inp, 0.0, max_seqs=1)[:2]  # noqa: E731
         sample = f"one sequence ({int(inp.kv_lens[0])} cached tokens, all 128 heads) of the workload per step"
@@ -310,7 +349,7 @@ def run_ours(args, wl):
     import torch.distributed as dist
 
     from mla_absorbed_decode_absorb_gb300 import ops
-    from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
+    from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession, LayerSession
 
     rank, local_rank, world = dist_env()
     torch.cuda.set_device(local_rank)
@@ -323,8 +362,14 @@ def run_ours(args, wl):
             dist.barrier()
 
     ops.mla_set_launch_overlap(args.launch_overlap)
-    inp = W.generate(wl, seed=rank)
-    s = DecodeSession(inp, device=dev, split_pages=args.split_pages)
+    layer = wl.d_model > 0
+    if layer:
+        li = W.generate_layer(wl, seed=rank)
+        inp = li.base
+        s = LayerSession(li, device=dev, split_pages=args.split_pages)
+    else:
+        inp = W.generate(wl, seed=rank)
+        s = DecodeSession(inp, device=dev, split_pages=args.split_pages)
     stream = torch.cuda.current_stream()
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -345,7 +390,7 @@ def run_ours(args, wl):
         step_flops = A.prefill_attention_flops(kv_list, wl.n_q)
         decompress_flops = A.decompress_flops(kv_list)
     else:
-        step_units = step_bytes
+        step_units = step_bytes + (A.layer_weight_bytes(wl.d_model) if layer else 0)
         step_flops = A.step_attention_flops(kv_list, wl.n_q)
 
     for _ in range(max(args.warmup, 3)):
@@ -447,13 +492,19 @@ def run_ours(args, wl):
     if world == 1 and not args.no_cpu_baseline and prefill:
         ntok, secs, desc = oracle_prefill_sample(inp, args.cpu_seconds)
         cpu = {"value": ntok / secs, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
+    elif world == 1 and not args.no_cpu_baseline and layer:
+        nseq, secs = oracle_layer_sample(li, args.cpu_seconds)
+        cpu = {"value": step_units / (secs / nseq * inp.batch) / 1e9, "unit": "GB/s", "cores": blas_threads(),
+               "kind": "oracle",
+               "sample": f"{nseq} of {inp.batch} sequences through the fp64 layer ({secs:.1f} s), a step costing "
+                         f"{inp.batch} sequences"}
     elif world == 1 and not args.no_cpu_baseline:
         nb, secs, nseq = oracle_sample(inp, args.cpu_seconds)
         cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{nseq} of {inp.batch} sequences, all 128 heads, fp64 non-absorbed form ({secs:.1f} s)"}
 
     line = {
-        "metric": METRIC_PREFILL if prefill else METRIC,
+        "metric": METRIC_PREFILL if prefill else (METRIC_LAYER if layer else METRIC),
         "value": total_bytes / (mean_ms * 1e-3) / (1 if prefill else 1e9), "unit": "tokens/s" if prefill else "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": mean_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16" if fp8 else "bf16",
@@ -482,7 +533,8 @@ def run_ours(args, wl):
 
 def main(argv=None):
     args = parse_args(argv)
-    wl = W.WORKLOADS.get(args.workload) or W.PREFILL_WORKLOADS.get(args.workload) or W.FP8_WORKLOADS[args.workload]
+    wl = (W.WORKLOADS.get(args.workload) or W.PREFILL_WORKLOADS.get(args.workload)
+          or W.FP8_WORKLOADS.get(args.workload) or W.LAYER_WORKLOADS[args.workload])
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -183,6 +183,27 @@ mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
                               float* o_latent, float* lse, cudaStream_t stream);
 
 /*
+ * mla_linear -- y = x W^T for a few tokens: the projections around the
+ * attention ("DeepSeek MLA 架构详解", decode listing: W_DKV, W_KR, W_DQ, W_UQ,
+ * W_QR and W_O are linear layers without bias; "DeepSeek-MLA-Principle"
+ * section 2 table for their shapes).
+ *
+ *   x  [T, K] bf16, 1 <= T <= MLA_LINEAR_MAX_T, K a multiple of 64
+ *   w  [N, K] bf16 (the nn.Linear weight layout: one row per output), N >= 1
+ *   y  [T, N] bf16 out: y[t][n] = bf16(sum_k x[t][k] w[n][k]), fp32 accumulation
+ *   workspace: mla_linear_workspace_size bytes (0 when K is not split), 16-byte
+ *              aligned, caller-owned; its contents are scratch.
+ *
+ * K is split over CTAs when the output alone would not cover the GPU; the
+ * split partials are then added in a fixed order by a second kernel, so the
+ * result does not depend on timing.  x and w need 16-byte-aligned bases.
+ */
+#define MLA_LINEAR_MAX_T 256
+mla_status mla_linear_workspace_size(int T, int K, int N, size_t* bytes);
+mla_status mla_linear(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * FP8 latent cache.  The pages list FP8 (one byte per value) among the cache
  * precisions, with a scaling strategy ("DeepSeek-MLA-Principle" section 7,
  * mixed precision such as FP16/BF16/FP8 with scaling; "DeepSeek MLA 架构详解",

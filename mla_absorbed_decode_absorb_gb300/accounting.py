@@ -104,3 +104,12 @@ def prefill_attention_flops(kv_lens, n_q: int) -> int:
 def decompress_flops(kv_lens) -> int:
     return sum(int(n) for n in kv_lens) * 2 * decompress_macs_per_token()
 
+
+
+def layer_weight_bytes(d_model: int, d_q_latent: int = 1536) -> int:
+    """bf16 bytes of every weight one decode-layer step reads once: W_DKV, W_KR, W_DQ,
+    W_UQ, W_QR, W_O ([N1] decode listing) and W_UK, W_UV."""
+    hd = N_HEADS * D_NOPE
+    elems = (D_LATENT + D_ROPE + d_q_latent) * d_model + (hd + N_HEADS * D_ROPE) * d_q_latent + d_model * hd \
+        + 2 * N_HEADS * D_NOPE * D_LATENT
+    return elems * BF16_BYTES

@@ -198,6 +198,23 @@ mla_status mla_decode_attn_fp8_partial(const mla_bf16* q_abs, const uint8_t* cac
                                              stream));
 }
 
+mla_status mla_linear_workspace_size(int T, int K, int N, size_t* bytes) {
+  if (bytes == nullptr || T < 1 || T > MLA_LINEAR_MAX_T || K < 64 || K % 64 != 0 || N < 1) return MLA_ERR_INVALID_ARG;
+  *bytes = linear_workspace_bytes(T, K, N);
+  return MLA_OK;
+}
+
+mla_status mla_linear(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+  if (T < 1 || T > MLA_LINEAR_MAX_T || K < 64 || K % 64 != 0 || N < 1) return MLA_ERR_INVALID_ARG;
+  if (!x || !w || !y || !aligned16(x) || !aligned16(w)) return MLA_ERR_INVALID_ARG;
+  const size_t need = linear_workspace_bytes(T, K, N);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return MLA_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_linear(x, w, y, T, K, N, static_cast<float*>(workspace), st, stream));
+}
+
 mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope,
                         const int32_t* seq_lens_before, const mla_bf16* w_uk,
                         const float* rope_table, int rope_max_pos, mla_bf16* q_abs,

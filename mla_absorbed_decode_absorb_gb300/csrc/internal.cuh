@@ -112,6 +112,11 @@ cudaError_t launch_append_kv_fp8(const uint16_t* c_kv_new, const uint16_t* k_pe_
                                  uint8_t* c8, float* scale, uint16_t* kr, int64_t num_pages, int B, int n_new,
                                  int* status, cudaStream_t stream);
 
+int linear_num_splits(int T, int K, int N);
+size_t linear_workspace_bytes(int T, int K, int N);
+cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, float* part,
+                          int* status, cudaStream_t stream);
+
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream);
 

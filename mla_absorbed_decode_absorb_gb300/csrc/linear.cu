@@ -1,0 +1,226 @@
+// y[T, N] = x[T, K] W[N, K]^T for a few tokens (T <= 256): the projections of
+// the MLA layer around the attention ("DeepSeek MLA 架构详解", decode listing:
+// W_DKV, W_KR, W_DQ, W_UQ, W_QR and W_O are nn.Linear layers; "DeepSeek-MLA-
+// Principle" section 2 table, the dimension changes 7168 -> 512, 7168 -> 64,
+// 7168 -> 1536, 1536 -> 128 x 128, 1536 -> 128 x 64 and 16384 -> 7168).
+//
+// With T this small the work is streaming W once from HBM.  Operands are
+// swapped so the weight is the M = 128 side of the tcgen05 MMA: one CTA owns
+// 128 output features and a range of K, and streams its W tile and the matching
+// columns of x through a TMA ring (128-byte swizzle, 64 K per stage), one
+// thread issuing 4 MMAs (K = 16) per stage into a TMEM accumulator of T
+// columns.  K is split over CTAs so that the grid covers the GPU; a split
+// launch writes fp32 partials and a second kernel adds them in split order.
+#include "sm100.cuh"
+#include "tmap.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kKB = 64;           // K per stage
+constexpr int kThreads = 128;     // warp 0: TMA, warp 1: MMA; all four: epilogue
+constexpr int kWBox = 128 * 128;  // 128 W rows x 64 K (bf16)
+constexpr int kSmemBudget = 200 * 1024;
+
+__host__ __device__ inline int pad16(int t) { return (t + 15) & ~15; }
+__host__ __device__ inline int stage_bytes(int tp) { return kWBox + tp * 128; }
+__host__ __device__ inline int num_stages(int tp) { return min(8, kSmemBudget / stage_bytes(tp)); }
+__host__ __device__ inline uint32_t tmem_cols_for(int tp) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(tp)) c <<= 1;
+  return c;
+}
+inline int smem_bytes_for(int tp) { return num_stages(tp) * stage_bytes(tp) + 256 + 1024; }
+
+struct LinParams {
+  uint16_t* y;        // [T, N] bf16 (no split)
+  float* part;        // [ksplit, T, N] fp32 (split)
+  int* status;
+  int T, K, N;
+  int kb_per_split;   // K blocks of 64 per CTA
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                 const LinParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tp = pad16(p.T);
+  const int S = num_stages(tp);
+  const int SB = stage_bytes(tp);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
+  uint64_t* empty = full + 8;
+  uint64_t* done = empty + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  const uint32_t tmem_cols = tmem_cols_for(tp);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * 128;
+  const int kb0 = blockIdx.y * p.kb_per_split;
+  const int nkb = min(p.kb_per_split, p.K / kKB - kb0);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    mbar_init(smem_u32(done), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  grid_dep_wait();
+  grid_dep_launch();
+
+  if (warp == 0 && lane == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    for (int i = 0; i < nkb; ++i) {
+      const int s = i % S;
+      if (!mbar_wait(smem_u32(&empty[s]), ((i / S) & 1) ^ 1, p.status)) break;
+      uint8_t* st = smem + s * SB;
+      mbar_arrive_expect_tx(smem_u32(&full[s]), SB);
+      const int k = (kb0 + i) * kKB;
+      tma_load_2d(smem_u32(st), &tm_w, k, n0, smem_u32(&full[s]));
+      tma_load_2d(smem_u32(st + kWBox), &tm_x, k, 0, smem_u32(&full[s]));
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA issuer
+    const uint32_t idesc = idesc_bf16(128, tp, /*a_mn=*/0, /*b_mn=*/0);
+    bool ok = true;
+    for (int i = 0; i < nkb && ok; ++i) {
+      const int s = i % S;
+      ok = mbar_wait(smem_u32(&full[s]), (i / S) & 1, p.status);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t a0 = smem_u32(smem + s * SB), b0 = a0 + kWBox;
+#pragma unroll
+      for (int q = 0; q < kKB / 16; ++q)
+        mma_ss(tmem, smem_desc(a0 + q * 32, 16, 1024, kSw128), smem_desc(b0 + q * 32, 16, 1024, kSw128), idesc,
+               (i | q) ? 1u : 0u);
+      mma_commit(smem_u32(&empty[s]));
+    }
+    if (ok) mma_commit(smem_u32(done));
+    else mbar_arrive(smem_u32(done));  // no result (the status is set): release the epilogue
+  }
+  __syncwarp();
+
+  // -------------------------------------------------------------------- epilogue
+  // TMEM lane = output feature n0 + 32 warp + lane, column = token
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done), 0, p.status));
+  tc_fence_after();
+  const int n = n0 + warp * 32 + lane;
+  const uint32_t row_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  if (ok && nkb > 0) {
+    for (int c0 = 0; c0 < tp; c0 += 16) {
+      uint32_t r[16];
+      tmem_ld16(row_addr + c0, r);
+      tmem_wait_ld();
+      if (n < p.N) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = c0 + i;
+          if (t < p.T) {
+            if (gridDim.y == 1)
+              p.y[static_cast<int64_t>(t) * p.N + n] = f32_to_bf16_bits(__uint_as_float(r[i]));
+            else
+              p.part[(static_cast<int64_t>(blockIdx.y) * p.T + t) * p.N + n] = __uint_as_float(r[i]);
+          }
+        }
+      }
+    }
+  } else if (n < p.N) {
+    for (int t = 0; t < p.T; ++t) {
+      if (gridDim.y == 1)
+        p.y[static_cast<int64_t>(t) * p.N + n] = 0;
+      else
+        p.part[(static_cast<int64_t>(blockIdx.y) * p.T + t) * p.N + n] = 0.f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+}
+
+// y[t, n] = bf16(sum over splits s in order of part[s, t, n])
+__global__ void __launch_bounds__(256)
+linear_reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, int64_t elems, int ksplit) {
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < elems;
+       e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float a = 0.f;
+    for (int s = 0; s < ksplit; ++s) a += part[s * elems + e];
+    y[e] = f32_to_bf16_bits(a);
+  }
+}
+
+int g_sms = 0;
+
+}  // namespace
+
+// K split so that tiles x splits covers about two waves of the GPU, each split
+// keeping at least 4 K blocks of 64.
+int linear_num_splits(int T, int K, int N) {
+  (void)T;
+  if (g_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || g_sms <= 0) g_sms = 148;
+  }
+  const int tiles = (N + 127) / 128;
+  const int kbs = K / kKB;
+  int split = max(1, (2 * g_sms) / tiles);
+  split = min(split, max(1, kbs / 4));
+  const int per = (kbs + split - 1) / split;
+  return (kbs + per - 1) / per;  // no empty split
+}
+
+size_t linear_workspace_bytes(int T, int K, int N) {
+  const int split = linear_num_splits(T, K, N);
+  return split > 1 ? static_cast<size_t>(split) * T * N * sizeof(float) : 0;
+}
+
+cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, float* part,
+                          int* status, cudaStream_t stream) {
+  const int tp = pad16(T);
+  static bool configured = false;
+  if (!configured) {
+    int most = 0;
+    for (int t = 16; t <= 256; t += 16) most = max(most, smem_bytes_for(t));
+    cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  const int split = linear_num_splits(T, K, N);
+  const int kbs = K / kKB;
+  CUtensorMap tx, tw;
+  if (!make_tmap_bf16_2d(&tx, x, T, K, K, kKB, tp, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_2d(&tw, w, N, K, K, kKB, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  LinParams prm;
+  prm.y = y;
+  prm.part = part;
+  prm.status = status;
+  prm.T = T;
+  prm.K = K;
+  prm.N = N;
+  prm.kb_per_split = (kbs + split - 1) / split;
+  cudaError_t e = launch_kernel(linear_tc_kernel, dim3((N + 127) / 128, split), dim3(kThreads), smem_bytes_for(tp),
+                                stream, tx, tw, prm);
+  if (e != cudaSuccess || split == 1) return e;
+  const int64_t elems = static_cast<int64_t>(T) * N;
+  const int64_t want = (elems + 255) / 256;
+  const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+  return launch_kernel(linear_reduce_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const float*>(part), y,
+                       elems, split);
+}
+
+}  // namespace mla

@@ -51,6 +51,8 @@ _SIGS = {
     "mla_decompress_kv": ([_p, _i64, _p, _i, _p, _i, _i, _p, _p, _p, _p, _p], _i),
     "mla_prefill_attn": ([_p, _p, _p, _p, _i, _p, _p, _i, _p, _i64, _p, _i, _p, _i, _i, _p, _p, _p], _i),
     "mla_get_launch_overlap": ([], _i),
+    "mla_linear_workspace_size": ([_i, _i, _i, ctypes.POINTER(_sz)], _i),
+    "mla_linear": ([_p, _p, _p, _i, _i, _i, _p, _sz, _p], _i),
     "mla_append_kv_fp8": ([_p, _p, _p, _p, _i, _p, _i, _p, _p, _p, _i64, _i, _i, _p], _i),
     "mla_decode_attn_fp8_partial": ([_p, _p, _p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
 }
@@ -131,6 +133,37 @@ def mla_append_kv(c_kv_new, k_pe_new, seq_lens_before, page_table, rope, cache, 
         raise ValueError("cache must be [num_pages, 64, 576]")
     _check("mla_append_kv", lib.mla_append_kv(*args))
     return cache
+
+
+MLA_LINEAR_MAX_T = 256
+
+
+def mla_linear_workspace_size(T, K, N) -> int:
+    n = _sz(0)
+    _check("mla_linear_workspace_size", lib.mla_linear_workspace_size(int(T), int(K), int(N), ctypes.byref(n)))
+    return int(n.value)
+
+
+def alloc_linear_workspace(T, K, N, device):
+    n = mla_linear_workspace_size(T, K, N)
+    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mla_linear(x, w, y=None, workspace=None, stream=None):
+    """``y [T, N] = x [T, K] w [N, K]^T`` in bf16 (fp32 accumulation)."""
+    T, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty(T, N, dtype=torch.bfloat16, device=x.device)
+    need = mla_linear_workspace_size(T, K, N)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check("mla_linear", lib.mla_linear(
+        _dev(x, "x", torch.bfloat16, (T, K)), _dev(w, "w", torch.bfloat16, (N, K)),
+        _dev(y, "y", torch.bfloat16, (T, N)), int(T), int(K), int(N),
+        0 if not need else _dev(workspace, "workspace", torch.uint8), 0 if not need else workspace.numel(),
+        _stream(stream)))
+    return y
 
 
 def fp8_cache_empty(num_pages, device, fill_code=0x7F):

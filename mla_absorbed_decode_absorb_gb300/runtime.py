@@ -208,3 +208,85 @@ class DecodeSession:
         if self.fused_finish:
             return 4
         return 4 + (1 if self.num_splits > 1 else 0)
+
+
+class LayerSession:
+    """One MLA decode layer from the hidden state, as in the pages' decode listing
+    ("DeepSeek MLA 架构详解", forward_decode), on top of a :class:`DecodeSession`:
+
+    1. ``proj_kv``: c_kv = x W_DKV^T and k_pe = x W_KR^T, written straight into the
+       decode session's step inputs (so the append stores this step's projections);
+    2. ``proj_q``: c_q = x W_DQ^T, then q^C = c_q W_UQ^T and q^R = c_q W_QR^T into
+       the step's query inputs;
+    3. the decode session's append, absorb_q, split attention and fused finish,
+       which give the per-head output O;
+    4. ``proj_out``: y = O W_O^T, the layer's output [B, n_q, d_model].
+
+    Every projection is one ``mla_linear`` (plus its split-sum kernel when K is
+    split).  The history of every sequence is in the cache before the first step.
+    """
+
+    def __init__(self, li, device="cuda", split_pages: int | None = None, stream=None):
+        self.li = li
+        dev = torch.device(device)
+        self.device = dev
+        self.dec = DecodeSession(li.base, device=dev, split_pages=split_pages, stream=stream)
+        d = self.dec
+        self.T = d.B * d.n_q
+        self.d_model = li.workload.d_model
+        self.x = li.x.to(dev).reshape(self.T, self.d_model)
+        self.w_dkv, self.w_kr, self.w_dq = li.w_dkv.to(dev), li.w_kr.to(dev), li.w_dq.to(dev)
+        self.w_uq, self.w_qr, self.w_o = li.w_uq.to(dev), li.w_qr.to(dev), li.w_o.to(dev)
+        self.c_q = torch.empty(self.T, self.w_dq.shape[0], dtype=torch.bfloat16, device=dev)
+        self.y = torch.empty(self.T, self.d_model, dtype=torch.bfloat16, device=dev)
+        # step inputs of the decode session, viewed as [tokens, features]
+        self._c_new = d.c_new.view(self.T, -1)
+        self._k_new = d.k_new.view(self.T, -1)
+        self._q_nope = d.q_nope.view(self.T, -1)
+        self._q_rope = d.q_rope.view(self.T, -1)
+        shapes = [(self.w_dkv, self.d_model), (self.w_kr, self.d_model), (self.w_dq, self.d_model),
+                  (self.w_uq, self.c_q.shape[1]), (self.w_qr, self.c_q.shape[1]), (self.w_o, d.out[0].numel() // d.n_q)]
+        need = max(ops.mla_linear_workspace_size(self.T, k, w.shape[0]) for w, k in shapes)
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        # a layer step's input is the hidden state, its result the layer output
+        self.step_buffer = self.x
+        self.out = self.y
+
+    def host_step_buffer(self, pin: bool = True) -> torch.Tensor:
+        host = torch.empty(self.x.shape, dtype=self.x.dtype)
+        if pin:
+            host = host.pin_memory()
+        host.copy_(self.x)
+        return host
+
+    def proj_kv(self, stream=None):
+        ops.mla_linear(self.x, self.w_dkv, self._c_new, self.ws, stream)
+        ops.mla_linear(self.x, self.w_kr, self._k_new, self.ws, stream)
+
+    def proj_q(self, stream=None):
+        ops.mla_linear(self.x, self.w_dq, self.c_q, self.ws, stream)
+        ops.mla_linear(self.c_q, self.w_uq, self._q_nope, self.ws, stream)
+        ops.mla_linear(self.c_q, self.w_qr, self._q_rope, self.ws, stream)
+
+    def proj_out(self, stream=None):
+        ops.mla_linear(self.dec.out.view(self.T, -1), self.w_o, self.y, self.ws, stream)
+
+    def stage_names(self) -> list[str]:
+        return ["proj_kv", "proj_q"] + self.dec.stage_names() + ["proj_out"]
+
+    def __getattr__(self, name):
+        # the decode stages (append, absorb, attend_partial, finish, ...) run on the decode session
+        return getattr(self.__dict__["dec"], name)
+
+    def step(self, stream=None):
+        for name in self.stage_names():
+            getattr(self, name)(stream)
+        return self.y
+
+    def launches_per_step(self) -> int:
+        n = self.dec.launches_per_step()
+        d = self.d_model
+        for w, k in [(self.w_dkv, d), (self.w_kr, d), (self.w_dq, d), (self.w_uq, self.c_q.shape[1]),
+                     (self.w_qr, self.c_q.shape[1]), (self.w_o, self.w_o.shape[1])]:
+            n += 1 + (1 if ops.mla_linear_workspace_size(self.T, k, w.shape[0]) else 0)
+        return n

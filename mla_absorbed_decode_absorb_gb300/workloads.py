@@ -53,6 +53,7 @@ class Workload:
     split_pages: int = 0                  # prescribed KV split size in pages (0 = auto)
     description: str = ""
     cache_format: str = "bf16"            # "bf16" (576 bf16 per token) or "fp8" (E4M3 latent, see ops)
+    d_model: int = 0                      # > 0: the whole layer from the hidden state (see LayerInputs)
 
 
 # The five workloads of the benchmark, named by what they are.
@@ -90,6 +91,19 @@ FP8_WORKLOADS: dict[str, Workload] = {
     for w in [
         Workload("batched_b32_l4096_fp8", batch=32, n_q=1, context=4096, cache_format="fp8",
                  description="B=32, 1 new token each, uniform prior context 4096, FP8 latent cache"),
+    ]
+}
+
+# The whole decode layer from the hidden state: the projections of the pages'
+# decode listing around the absorbed attention, hidden size 7168 (DeepSeek-V3).
+D_MODEL = 7168
+D_Q_LATENT = 1536
+LAYER_WORKLOADS: dict[str, Workload] = {
+    w.name: w
+    for w in [
+        Workload("layer_b32_l4096", batch=32, n_q=1, context=4096, d_model=D_MODEL,
+                 description="decode layer from the hidden state (d_model 7168): B=32, 1 new token each, "
+                             "uniform prior context 4096"),
     ]
 }
 
@@ -223,3 +237,41 @@ def empty_cache(num_pages: int, device="cpu") -> torch.Tensor:
     """A page pool ``[num_pages, 64, 576]`` bf16 filled with the NaN sentinel."""
     t = torch.full((num_pages, PAGE, D_ROW), CACHE_SENTINEL_BITS, dtype=torch.int16, device=device)
     return t.view(torch.bfloat16)
+
+
+@dataclass
+class LayerInputs:
+    """The decode-layer inputs: the hidden state of the new tokens and the six
+    projection weights (nn.Linear layout [out, in]), next to the attention inputs
+    (history, page table, W_UK, W_UV) of :class:`Inputs`, whose own new-token
+    latent rows and queries the layer replaces by its projections."""
+
+    base: Inputs
+    x: torch.Tensor          # [B, n_q, d_model]
+    w_dkv: torch.Tensor      # [512, d_model]
+    w_kr: torch.Tensor       # [64, d_model]
+    w_dq: torch.Tensor       # [1536, d_model]
+    w_uq: torch.Tensor       # [128 * 128, 1536]
+    w_qr: torch.Tensor       # [128 * 64, 1536]
+    w_o: torch.Tensor        # [d_model, 128 * 128]
+
+    @property
+    def workload(self) -> Workload:
+        return self.base.workload
+
+
+def generate_layer(wl: Workload, seed: int = 0) -> LayerInputs:
+    """:func:`generate` for the attention inputs, then (second generator, seed + 1)
+    the hidden state ~ N(0, 1) and weights ~ N(0, 1 / fan_in), rounded to bf16."""
+    base = generate(wl, seed)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 1)
+    d = wl.d_model
+    B, n_q = wl.batch, wl.n_q
+
+    def w(n_out, n_in):
+        return _bf16(torch.randn(n_out, n_in, generator=g) / math.sqrt(n_in))
+    return LayerInputs(base=base, x=_bf16(torch.randn(B, n_q, d, generator=g)),
+                       w_dkv=w(D_LATENT, d), w_kr=w(D_ROPE, d), w_dq=w(D_Q_LATENT, d),
+                       w_uq=w(N_HEADS * D_NOPE, D_Q_LATENT), w_qr=w(N_HEADS * D_ROPE, D_Q_LATENT),
+                       w_o=w(d, N_HEADS * D_NOPE))

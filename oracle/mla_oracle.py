@@ -420,6 +420,48 @@ def out_absorb(o_lat, w_uv):
     return np.einsum("...hm,hdm->...hd", np.asarray(o_lat, np.float64), np.asarray(w_uv, np.float64))
 
 
+def linear(x, w):
+    """``y = x W^T`` in fp64 for ``x [..., K]`` and an nn.Linear weight ``w [N, K]``
+    ([N1] decode listing: the W_DKV, W_KR, W_DQ, W_UQ, W_QR and W_O projections)."""
+    return np.asarray(x, np.float64) @ np.asarray(w, np.float64).T
+
+
+def decode_layer(x, w_dkv, w_kr, w_dq, w_uq, w_qr, w_uk, w_uv, w_o, c_hist, kr_hist, prior_len: int,
+                 cache_bf16_rows: bool = True):
+    """One sequence's decode layer from the hidden state ([N1] forward_decode).
+
+    ``x [n_q, d_model]`` is the hidden state of the ``n_q`` new tokens at positions
+    ``prior_len + j``; ``c_hist [prior_len, 512]`` and ``kr_hist [prior_len, 64]``
+    (rotated) are the cached history.  Steps, in the listing's order:
+    1. ``c^KV = x W_DKV^T`` and ``k^R = RoPE(x W_KR^T, pos)``, appended to the cache
+       (as the bf16 rows the cache format holds, with the fixed RoPE recipe of
+       :func:`rope_key_bf16_bits`, when ``cache_bf16_rows``);
+    2. ``c^Q = x W_DQ^T``, ``q^C = c^Q W_UQ^T`` and ``q^R = c^Q W_QR^T`` per head;
+    3-5. the attention of :func:`decode_mha` (per-head output O);
+    then ``y = O W_O^T`` over the concatenated heads.
+    Returns ``(y [n_q, d_model], O [n_q, H, d_v])``; everything else in fp64.
+    """
+    x = np.asarray(x, np.float64)
+    n_q = x.shape[0]
+    c_new = linear(x, w_dkv)
+    k_new = linear(x, w_kr)
+    pos = prior_len + np.arange(n_q)
+    if cache_bf16_rows:
+        c_new = bf16_bits_to_f64(f32_to_bf16_bits(c_new.astype(np.float32)))
+        kr_new = bf16_bits_to_f64(rope_key_bf16_bits(f32_to_bf16_bits(k_new.astype(np.float32)), pos))
+    else:
+        kr_new = rope_f64(k_new, pos)
+    c = np.concatenate([np.asarray(c_hist, np.float64).reshape(-1, c_new.shape[1]), c_new])
+    kr = np.concatenate([np.asarray(kr_hist, np.float64).reshape(-1, kr_new.shape[1]), kr_new])
+    c_q = linear(x, w_dq)
+    H, d_h, _ = np.asarray(w_uk).shape
+    q_nope = linear(c_q, w_uq).reshape(n_q, H, d_h)
+    q_rope = linear(c_q, w_qr).reshape(n_q, H, -1)
+    o, _, _ = decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len)
+    y = linear(o.reshape(n_q, -1), w_o)
+    return y, o
+
+
 def absorb_query(q_nope, q_rope, w_uk, pos):
     """``[W_UK[h]^T q^C ; RoPE(q^R, pos)]`` per head: the 576-wide absorbed query in fp64.
 

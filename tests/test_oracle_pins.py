@@ -515,3 +515,38 @@ def test_fp8_cache_attention_stays_near_the_bf16_result():
     rel = np.linalg.norm(lat8 - latb) / np.linalg.norm(latb)
     assert 1e-4 < rel < 4e-2, rel
     assert np.abs(lse8 - lseb).max() < 5e-2
+
+
+# ------------------------------------------------------------------------ decode layer
+def test_linear_is_x_times_w_transposed():
+    """y[t, n] = sum_k x[t, k] w[n, k] by explicit loops on a non-square case."""
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((3, 5))
+    w = rng.standard_normal((4, 5))
+    ref = np.array([[sum(x[t, k] * w[n, k] for k in range(5)) for n in range(4)] for t in range(3)])
+    assert np.allclose(O.linear(x, w), ref, rtol=1e-14, atol=1e-14)
+
+
+def test_decode_layer_single_token_closed_form():
+    """A first token attends only to itself (alpha = 1), so the per-head output is
+    W_UV[h] c with c = W_DKV x, and the layer output is its concatenation times W_O^T,
+    whatever the query side."""
+    rng = np.random.default_rng(22)
+    d, dc, dr, dq, H, dh = 16, 8, 4, 6, 2, 4
+    x = rng.standard_normal((1, d))
+    w_dkv, w_kr, w_dq = rng.standard_normal((dc, d)), rng.standard_normal((dr, d)), rng.standard_normal((dq, d))
+    w_uq, w_qr = rng.standard_normal((H * dh, dq)), rng.standard_normal((H * dr, dq))
+    w_uk, w_uv = rng.standard_normal((H, dh, dc)), rng.standard_normal((H, dh, dc))
+    w_o = rng.standard_normal((d, H * dh))
+    y, o = O.decode_layer(x, w_dkv, w_kr, w_dq, w_uq, w_qr, w_uk, w_uv, w_o, np.zeros((0, dc)), np.zeros((0, dr)), 0,
+                          cache_bf16_rows=False)
+    c = w_dkv @ x[0]
+    o_ref = np.stack([w_uv[h] @ c for h in range(H)])
+    assert np.allclose(o[0], o_ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(y[0], w_o @ o_ref.reshape(-1), rtol=1e-12, atol=1e-12)
+    # the query side matters once there are two tokens: changing W_UQ changes the output
+    hist_c, hist_k = rng.standard_normal((1, dc)), rng.standard_normal((1, dr))
+    y1, _ = O.decode_layer(x, w_dkv, w_kr, w_dq, w_uq, w_qr, w_uk, w_uv, w_o, hist_c, hist_k, 1, cache_bf16_rows=False)
+    y2, _ = O.decode_layer(x, w_dkv, w_kr, w_dq, 2 * w_uq, w_qr, w_uk, w_uv, w_o, hist_c, hist_k, 1,
+                           cache_bf16_rows=False)
+    assert np.abs(y1 - y2).max() > 1e-6
