@@ -291,7 +291,7 @@ def run_reference(args, wl):
     elif wl.d_model > 0:  # one sequence through the layer oracle per step, a step costing B of them
         li = W.generate_layer(wl, seed=0)
         inp = li.base
-        units_step = A.step_cache_bytes(inp.kv_lens.tolist()) + A.layer_weight_bytes(wl.d_model)
+        units_step = A.step_cache_bytes(inp.kv_lens.tolist()) + A.layer_weight_bytes(wl.d_model, fold=wl.fold)
 
         def sample_fn():
             _, t = oracle_layer_sample(li, 0.0, max_seqs=1)
@@ -366,7 +366,7 @@ def run_ours(args, wl):
     if layer:
         li = W.generate_layer(wl, seed=rank)
         inp = li.base
-        s = LayerSession(li, device=dev, split_pages=args.split_pages)
+        s = LayerSession(li, device=dev, split_pages=args.split_pages, fold=wl.fold)
     else:
         inp = W.generate(wl, seed=rank)
         s = DecodeSession(inp, device=dev, split_pages=args.split_pages)
@@ -390,7 +390,7 @@ def run_ours(args, wl):
         step_flops = A.prefill_attention_flops(kv_list, wl.n_q)
         decompress_flops = A.decompress_flops(kv_list)
     else:
-        step_units = step_bytes + (A.layer_weight_bytes(wl.d_model) if layer else 0)
+        step_units = step_bytes + (A.layer_weight_bytes(wl.d_model, fold=wl.fold) if layer else 0)
         step_flops = A.step_attention_flops(kv_list, wl.n_q)
 
     for _ in range(max(args.warmup, 3)):

@@ -202,6 +202,32 @@ mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
 mla_status mla_linear_workspace_size(int T, int K, int N, size_t* bytes);
 mla_status mla_linear(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N,
                       void* workspace, size_t workspace_bytes, cudaStream_t stream);
+/*
+ * mla_linear_strided -- mla_linear writing y[t][n] to
+ *   y[t * y_ld + (n / seg) * seg_ld + n % seg]
+ * (N a multiple of seg, seg_ld >= seg, y_ld >= (N / seg) * seg_ld): e.g. the
+ * latent half of q_abs [T, 128, 576] with seg = 512, seg_ld = 576, y_ld = 128 * 576.
+ */
+mla_status mla_linear_strided(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N,
+                              int64_t y_ld, int seg, int seg_ld, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Weight pre-folds ("DeepSeek-MLA-Principle", key absorption: when q^C = W_UQ c^Q
+ * the two linear maps combine, q~ = (W_UK[h])^T W_UQ[h] c^Q; "DeepSeek MLA 架构详解":
+ * W_UV folded into the output projection, W^OV[h] = W^O[h] W_UV[h], d x d_c).
+ * With the folded weights the query's latent half is one mla_linear_strided of
+ * c^Q into q_abs, and the layer output one mla_linear of the merged latent
+ * output O' (as bf16) with W^OV.  Two helpers complete those steps:
+ *
+ * mla_rope_q -- the RoPE half of q_abs alone: q_abs[t, h, 512:576] =
+ *   RoPE(q_rope[t, h], seq_lens_before[b] + j), the float32 recipe of
+ *   mla_absorb_q, bit for bit; arguments as mla_absorb_q.
+ * mla_f32_to_bf16 -- dst[i] = bf16(src[i]) (nearest even), n elements.
+ */
+mla_status mla_rope_q(const mla_bf16* q_rope, const int32_t* seq_lens_before, const float* rope_table,
+                      int rope_max_pos, mla_bf16* q_abs, int B, int n_q, cudaStream_t stream);
+mla_status mla_f32_to_bf16(const float* src, mla_bf16* dst, int64_t n, cudaStream_t stream);
 
 /*
  * FP8 latent cache.  The pages list FP8 (one byte per value) among the cache

@@ -106,10 +106,15 @@ def decompress_flops(kv_lens) -> int:
 
 
 
-def layer_weight_bytes(d_model: int, d_q_latent: int = 1536) -> int:
+def layer_weight_bytes(d_model: int, d_q_latent: int = 1536, fold: bool = False) -> int:
     """bf16 bytes of every weight one decode-layer step reads once: W_DKV, W_KR, W_DQ,
-    W_UQ, W_QR, W_O ([N1] decode listing) and W_UK, W_UV."""
+    W_UQ, W_QR, W_O ([N1] decode listing) and W_UK, W_UV; with the pre-folds, W_DKV,
+    W_KR, W_DQ, W_QK [n_h d_c, d_c'], W_QR and W_OV [d_model, n_h d_c]."""
     hd = N_HEADS * D_NOPE
-    elems = (D_LATENT + D_ROPE + d_q_latent) * d_model + (hd + N_HEADS * D_ROPE) * d_q_latent + d_model * hd \
-        + 2 * N_HEADS * D_NOPE * D_LATENT
+    head_in = (D_LATENT + D_ROPE + d_q_latent) * d_model
+    if fold:
+        elems = head_in + N_HEADS * D_LATENT * d_q_latent + N_HEADS * D_ROPE * d_q_latent \
+            + d_model * N_HEADS * D_LATENT
+    else:
+        elems = head_in + (hd + N_HEADS * D_ROPE) * d_q_latent + d_model * hd + 2 * N_HEADS * D_NOPE * D_LATENT
     return elems * BF16_BYTES

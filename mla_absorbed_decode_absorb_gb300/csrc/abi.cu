@@ -204,15 +204,37 @@ mla_status mla_linear_workspace_size(int T, int K, int N, size_t* bytes) {
   return MLA_OK;
 }
 
-mla_status mla_linear(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N, void* workspace,
-                      size_t workspace_bytes, cudaStream_t stream) {
+mla_status mla_linear_strided(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N, int64_t y_ld,
+                              int seg, int seg_ld, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (T < 1 || T > MLA_LINEAR_MAX_T || K < 64 || K % 64 != 0 || N < 1) return MLA_ERR_INVALID_ARG;
   if (!x || !w || !y || !aligned16(x) || !aligned16(w)) return MLA_ERR_INVALID_ARG;
+  if (seg < 1 || N % seg != 0 || seg_ld < seg || y_ld < static_cast<int64_t>(N / seg) * seg_ld) return MLA_ERR_INVALID_ARG;
   const size_t need = linear_workspace_bytes(T, K, N);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return MLA_ERR_WORKSPACE;
   int* st = status_ptr();
   if (st == nullptr) return MLA_ERR_CUDA;
-  return from_cuda(launch_linear(x, w, y, T, K, N, static_cast<float*>(workspace), st, stream));
+  return from_cuda(launch_linear(x, w, y, T, K, N, y_ld, seg, seg_ld, static_cast<float*>(workspace), st, stream));
+}
+
+mla_status mla_linear(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N, void* workspace,
+                      size_t workspace_bytes, cudaStream_t stream) {
+  return mla_linear_strided(x, w, y, T, K, N, N, N, N, workspace, workspace_bytes, stream);
+}
+
+mla_status mla_rope_q(const mla_bf16* q_rope, const int32_t* seq_lens_before, const float* rope_table,
+                      int rope_max_pos, mla_bf16* q_abs, int B, int n_q, cudaStream_t stream) {
+  if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!q_rope || !seq_lens_before || !rope_table || !q_abs || rope_max_pos < 1) return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_rope_q(q_rope, seq_lens_before, rope_table, rope_max_pos, q_abs, B, n_q, st, stream));
+}
+
+mla_status mla_f32_to_bf16(const float* src, mla_bf16* dst, int64_t n, cudaStream_t stream) {
+  if (n < 0 || (n > 0 && (!src || !dst))) return MLA_ERR_INVALID_ARG;
+  if (n == 0) return MLA_OK;
+  return from_cuda(launch_f32_to_bf16(src, dst, n, stream));
 }
 
 mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope,

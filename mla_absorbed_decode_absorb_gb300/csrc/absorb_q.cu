@@ -157,7 +157,44 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t* __r
   if (warp == 0) tmem_dealloc(tmem, tmem_cols);
 }
 
+// The RoPE half of q_abs alone (q_abs[t, h, 512:576] = RoPE(q_rope[t, h], pos_t)),
+// for callers that produce the latent half by other means (the query-side
+// weight fold); the same float32 recipe as above, one thread per (t, h, f).
+__global__ void __launch_bounds__(256)
+rope_q_kernel(const uint16_t* __restrict__ q_rope, const int32_t* __restrict__ lens, const float* __restrict__ rope,
+              int rope_max_pos, uint16_t* __restrict__ q_abs, int T, int n_q, int* status) {
+  grid_dep_wait();
+  grid_dep_launch();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<int64_t>(T) * kHeads * kHalfRope) return;
+  const int f = static_cast<int>(i % kHalfRope);
+  const int64_t th = i / kHalfRope;  // t * 128 + h
+  const int t = static_cast<int>(th / kHeads);
+  const int b = t / n_q, j = t % n_q;
+  const int64_t pos = static_cast<int64_t>(lens[b]) + j;
+  uint16_t* row = q_abs + th * kRow + kLatent;
+  if (pos < 0 || pos >= rope_max_pos) {
+    record_status(status, MLA_ERR_BOUNDS);
+    row[f] = row[f + kHalfRope] = 0;
+    return;
+  }
+  const uint16_t* x = q_rope + th * kRope;
+  const float x1 = bf16_bits_to_f32(x[f]), x2 = bf16_bits_to_f32(x[f + kHalfRope]);
+  const float c = rope[pos * kRope + f], sn = rope[pos * kRope + kHalfRope + f];
+  row[f] = f32_to_bf16_bits(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn)));
+  row[f + kHalfRope] = f32_to_bf16_bits(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn)));
+}
+
 }  // namespace
+
+cudaError_t launch_rope_q(const uint16_t* q_rope, const int32_t* seq_lens_before, const float* rope_table,
+                          int rope_max_pos, uint16_t* q_abs, int B, int n_q, int* status, cudaStream_t stream) {
+  const int T = B * n_q;
+  if (T == 0) return cudaSuccess;
+  const int64_t n = static_cast<int64_t>(T) * kHeads * kHalfRope;
+  return launch_kernel(rope_q_kernel, dim3(static_cast<unsigned>((n + 255) / 256)), dim3(256), 0, stream, q_rope,
+                       seq_lens_before, rope_table, rope_max_pos, q_abs, T, n_q, status);
+}
 
 cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
                             const int32_t* seq_lens_before, const uint16_t* w_uk,

@@ -45,7 +45,24 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
   if (lse != nullptr && threadIdx.x == 0) lse[row] = m == -INFINITY ? m : m + logf(z);
 }
 
+// dst[i] = bf16(src[i]), nearest even (the merged latent output as a bf16 GEMM operand)
+__global__ void __launch_bounds__(256)
+f32_to_bf16_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, int64_t n) {
+  grid_dep_wait();
+  grid_dep_launch();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    dst[i] = f32_to_bf16_bits(src[i]);
+}
+
 }  // namespace
+
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t want = (n + 255) / 256;
+  return launch_kernel(f32_to_bf16_kernel, dim3(static_cast<unsigned>(want < 8192 ? want : 8192)), dim3(256), 0,
+                       stream, src, dst, n);
+}
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream) {

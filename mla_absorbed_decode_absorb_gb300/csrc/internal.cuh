@@ -114,8 +114,11 @@ cudaError_t launch_append_kv_fp8(const uint16_t* c_kv_new, const uint16_t* k_pe_
 
 int linear_num_splits(int T, int K, int N);
 size_t linear_workspace_bytes(int T, int K, int N);
-cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, float* part,
-                          int* status, cudaStream_t stream);
+cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, int64_t y_ld,
+                          int seg, int seg_ld, float* part, int* status, cudaStream_t stream);
+cudaError_t launch_rope_q(const uint16_t* q_rope, const int32_t* seq_lens_before, const float* rope_table,
+                          int rope_max_pos, uint16_t* q_abs, int B, int n_q, int* status, cudaStream_t stream);
+cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, cudaStream_t stream);
 
 cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream);

@@ -35,12 +35,18 @@ __host__ __device__ inline uint32_t tmem_cols_for(int tp) {
 inline int smem_bytes_for(int tp) { return num_stages(tp) * stage_bytes(tp) + 256 + 1024; }
 
 struct LinParams {
-  uint16_t* y;        // [T, N] bf16 (no split)
+  uint16_t* y;        // bf16 out (no split): element (t, n) at t * y_ld + (n / seg) * seg_ld + n % seg
   float* part;        // [ksplit, T, N] fp32 (split)
   int* status;
   int T, K, N;
   int kb_per_split;   // K blocks of 64 per CTA
+  int64_t y_ld;
+  int seg, seg_ld;
 };
+
+__device__ __forceinline__ int64_t y_index(const LinParams& p, int t, int n) {
+  return static_cast<int64_t>(t) * p.y_ld + static_cast<int64_t>(n / p.seg) * p.seg_ld + n % p.seg;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -129,7 +135,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
           const int t = c0 + i;
           if (t < p.T) {
             if (gridDim.y == 1)
-              p.y[static_cast<int64_t>(t) * p.N + n] = f32_to_bf16_bits(__uint_as_float(r[i]));
+              p.y[y_index(p, t, n)] = f32_to_bf16_bits(__uint_as_float(r[i]));
             else
               p.part[(static_cast<int64_t>(blockIdx.y) * p.T + t) * p.N + n] = __uint_as_float(r[i]);
           }
@@ -139,7 +145,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   } else if (n < p.N) {
     for (int t = 0; t < p.T; ++t) {
       if (gridDim.y == 1)
-        p.y[static_cast<int64_t>(t) * p.N + n] = 0;
+        p.y[y_index(p, t, n)] = 0;
       else
         p.part[(static_cast<int64_t>(blockIdx.y) * p.T + t) * p.N + n] = 0.f;
     }
@@ -149,16 +155,17 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   if (warp == 1) tmem_dealloc(tmem, tmem_cols);
 }
 
-// y[t, n] = bf16(sum over splits s in order of part[s, t, n])
+// y(t, n) = bf16(sum over splits s in order of part[s, t, n])
 __global__ void __launch_bounds__(256)
-linear_reduce_kernel(const float* __restrict__ part, uint16_t* __restrict__ y, int64_t elems, int ksplit) {
+linear_reduce_kernel(const float* __restrict__ part, const LinParams p, int ksplit) {
   grid_dep_wait();
   grid_dep_launch();
+  const int64_t elems = static_cast<int64_t>(p.T) * p.N;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < elems;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float a = 0.f;
     for (int s = 0; s < ksplit; ++s) a += part[s * elems + e];
-    y[e] = f32_to_bf16_bits(a);
+    p.y[y_index(p, static_cast<int>(e / p.N), static_cast<int>(e % p.N))] = f32_to_bf16_bits(a);
   }
 }
 
@@ -188,8 +195,8 @@ size_t linear_workspace_bytes(int T, int K, int N) {
   return split > 1 ? static_cast<size_t>(split) * T * N * sizeof(float) : 0;
 }
 
-cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, float* part,
-                          int* status, cudaStream_t stream) {
+cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, int64_t y_ld,
+                          int seg, int seg_ld, float* part, int* status, cudaStream_t stream) {
   const int tp = pad16(T);
   static bool configured = false;
   if (!configured) {
@@ -213,14 +220,17 @@ cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int
   prm.K = K;
   prm.N = N;
   prm.kb_per_split = (kbs + split - 1) / split;
+  prm.y_ld = y_ld;
+  prm.seg = seg;
+  prm.seg_ld = seg_ld;
   cudaError_t e = launch_kernel(linear_tc_kernel, dim3((N + 127) / 128, split), dim3(kThreads), smem_bytes_for(tp),
                                 stream, tx, tw, prm);
   if (e != cudaSuccess || split == 1) return e;
   const int64_t elems = static_cast<int64_t>(T) * N;
   const int64_t want = (elems + 255) / 256;
   const int blocks = static_cast<int>(want < 4096 ? want : 4096);
-  return launch_kernel(linear_reduce_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const float*>(part), y,
-                       elems, split);
+  return launch_kernel(linear_reduce_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const float*>(part), prm,
+                       split);
 }
 
 }  // namespace mla

@@ -53,6 +53,9 @@ _SIGS = {
     "mla_get_launch_overlap": ([], _i),
     "mla_linear_workspace_size": ([_i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_linear": ([_p, _p, _p, _i, _i, _i, _p, _sz, _p], _i),
+    "mla_linear_strided": ([_p, _p, _p, _i, _i, _i, _i64, _i, _i, _p, _sz, _p], _i),
+    "mla_rope_q": ([_p, _p, _p, _i, _p, _i, _i, _p], _i),
+    "mla_f32_to_bf16": ([_p, _p, _i64, _p], _i),
     "mla_append_kv_fp8": ([_p, _p, _p, _p, _i, _p, _i, _p, _p, _p, _i64, _i, _i, _p], _i),
     "mla_decode_attn_fp8_partial": ([_p, _p, _p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
 }
@@ -164,6 +167,44 @@ def mla_linear(x, w, y=None, workspace=None, stream=None):
         0 if not need else _dev(workspace, "workspace", torch.uint8), 0 if not need else workspace.numel(),
         _stream(stream)))
     return y
+
+
+def mla_linear_strided(x, w, y, y_ld, seg, seg_ld, workspace=None, stream=None):
+    """``mla_linear`` writing element (t, n) to ``y.flatten()[t*y_ld + (n//seg)*seg_ld + n%seg]``."""
+    T, K = x.shape
+    N = w.shape[0]
+    need = mla_linear_workspace_size(T, K, N)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    if y.dtype != torch.bfloat16 or not y.is_cuda:
+        raise TypeError("y must be a CUDA bf16 tensor")
+    extent = y.untyped_storage().nbytes() // y.element_size() - y.storage_offset()
+    if (T - 1) * y_ld + (N // seg - 1) * seg_ld + seg > extent:
+        raise ValueError("y's storage is too small for the strided output")
+    _check("mla_linear_strided", lib.mla_linear_strided(
+        _dev(x, "x", torch.bfloat16, (T, K)), _dev(w, "w", torch.bfloat16, (N, K)), y.data_ptr(),
+        int(T), int(K), int(N), int(y_ld), int(seg), int(seg_ld),
+        0 if not need else _dev(workspace, "workspace", torch.uint8), 0 if not need else workspace.numel(),
+        _stream(stream)))
+    return y
+
+
+def mla_rope_q(q_rope, seq_lens_before, rope, q_abs, stream=None):
+    B, n_q = q_rope.shape[:2]
+    _check("mla_rope_q", lib.mla_rope_q(
+        _dev(q_rope, "q_rope", torch.bfloat16, (B, n_q, N_HEADS, D_ROPE)),
+        _dev(seq_lens_before, "seq_lens_before", torch.int32, (B,)),
+        _dev(rope, "rope_table", torch.float32), int(rope.shape[0]),
+        _dev(q_abs, "q_abs", torch.bfloat16, (B, n_q, N_HEADS, D_ROW)), int(B), int(n_q), _stream(stream)))
+    return q_abs
+
+
+def mla_f32_to_bf16(src, dst, stream=None):
+    if src.numel() != dst.numel():
+        raise ValueError("src and dst sizes differ")
+    _check("mla_f32_to_bf16", lib.mla_f32_to_bf16(
+        _dev(src, "src", torch.float32), _dev(dst, "dst", torch.bfloat16), int(src.numel()), _stream(stream)))
+    return dst
 
 
 def fp8_cache_empty(num_pages, device, fill_code=0x7F):

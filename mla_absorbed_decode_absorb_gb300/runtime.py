@@ -224,10 +224,20 @@ class LayerSession:
 
     Every projection is one ``mla_linear`` (plus its split-sum kernel when K is
     split).  The history of every sequence is in the cache before the first step.
+
+    With ``fold=True`` the layer uses the weight pre-folds of the pages ("DeepSeek-
+    MLA-Principle", key absorption: q~ = (W_UK[h])^T W_UQ[h] c^Q; "DeepSeek MLA
+    架构详解": W^OV[h] = W^O[h] W_UV[h]), prepared once by ``mla_linear`` calls:
+    ``proj_q`` writes the query's latent half straight into q_abs (one strided
+    linear of c^Q with W_QK [128 * 512, 1536]) and its RoPE half by ``mla_rope_q``
+    (no absorb_q); after the attention the merged latent output O' is rounded to
+    bf16 and ``proj_out`` is one linear with W_OV [d_model, 128 * 512] (no W_UV
+    step).  The folded weights are 201 MB and 940 MB against 66 MB and 252 MB.
     """
 
-    def __init__(self, li, device="cuda", split_pages: int | None = None, stream=None):
+    def __init__(self, li, device="cuda", split_pages: int | None = None, stream=None, fold: bool = False):
         self.li = li
+        self.fold = bool(fold)
         dev = torch.device(device)
         self.device = dev
         self.dec = DecodeSession(li.base, device=dev, split_pages=split_pages, stream=stream)
@@ -251,6 +261,37 @@ class LayerSession:
         # a layer step's input is the hidden state, its result the layer output
         self.step_buffer = self.x
         self.out = self.y
+        if self.fold:
+            self._prepare_folds(stream)
+
+    def _prepare_folds(self, stream=None):
+        """W_QK[(h, m), c] = sum_d W_UK[h, d, m] W_UQ[h*128 + d, c] and
+        W_OV[j, (h, m)] = sum_d W_O[j, h*128 + d] W_UV[h, d, m], each by mla_linear calls
+        (K = d_h = 128; row blocks of at most 256)."""
+        d = self.dec
+        H, dh, dc = d.w_uk.shape
+        dev = self.device
+        dq = self.w_uq.shape[1]
+        self.w_qk = torch.empty(H * dc, dq, dtype=torch.bfloat16, device=dev)
+        self.w_ov = torch.empty(self.d_model, H * dc, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(16, max(ops.mla_linear_workspace_size(256, dh, n) for n in (dq, dc))),
+                         dtype=torch.uint8, device=dev)
+        for h in range(H):
+            uk_t = d.w_uk[h].t().contiguous()                          # [512, 128]
+            uq_t = self.w_uq[h * dh:(h + 1) * dh].t().contiguous()      # [1536, 128]
+            for r0 in range(0, dc, 256):
+                ops.mla_linear(uk_t[r0:r0 + 256], uq_t, self.w_qk[h * dc + r0:h * dc + r0 + 256], ws, stream)
+            o_blk = self.w_o[:, h * dh:(h + 1) * dh].contiguous()       # [d_model, 128]
+            uv_t = d.w_uv[h].t().contiguous()                           # [512, 128]
+            for r0 in range(0, self.d_model, 256):
+                rows = min(256, self.d_model - r0)
+                ops.mla_linear_strided(o_blk[r0:r0 + rows], uv_t, self.w_ov[r0:, h * dc:], H * dc, dc, dc, ws,
+                                       stream)
+        self.o_lat_bf16 = torch.empty(self.T, H * dc, dtype=torch.bfloat16, device=dev)
+        need = max(ops.mla_linear_workspace_size(self.T, dq, H * dc),
+                   ops.mla_linear_workspace_size(self.T, H * dc, self.d_model))
+        if need > self.ws.numel():
+            self.ws = torch.empty(need, dtype=torch.uint8, device=dev)
 
     def host_step_buffer(self, pin: bool = True) -> torch.Tensor:
         host = torch.empty(self.x.shape, dtype=self.x.dtype)
@@ -265,13 +306,27 @@ class LayerSession:
 
     def proj_q(self, stream=None):
         ops.mla_linear(self.x, self.w_dq, self.c_q, self.ws, stream)
+        if self.fold:
+            d = self.dec
+            ops.mla_linear_strided(self.c_q, self.w_qk, d.q_abs, N_HEADS * D_ROW, D_LATENT, D_ROW, self.ws, stream)
+            ops.mla_linear(self.c_q, self.w_qr, self._q_rope, self.ws, stream)
+            ops.mla_rope_q(d.q_rope, d.prior_lens, d.rope, d.q_abs, stream=stream)
+            return
         ops.mla_linear(self.c_q, self.w_uq, self._q_nope, self.ws, stream)
         ops.mla_linear(self.c_q, self.w_qr, self._q_rope, self.ws, stream)
 
+    def to_bf16(self, stream=None):
+        ops.mla_f32_to_bf16(self.dec.o_latent, self.o_lat_bf16, stream=stream)
+
     def proj_out(self, stream=None):
+        if self.fold:
+            ops.mla_linear(self.o_lat_bf16, self.w_ov, self.y, self.ws, stream)
+            return
         ops.mla_linear(self.dec.out.view(self.T, -1), self.w_o, self.y, self.ws, stream)
 
     def stage_names(self) -> list[str]:
+        if self.fold:
+            return ["proj_kv", "proj_q", "append", "attend_partial", "combine", "to_bf16", "proj_out"]
         return ["proj_kv", "proj_q"] + self.dec.stage_names() + ["proj_out"]
 
     def __getattr__(self, name):
@@ -284,9 +339,16 @@ class LayerSession:
         return self.y
 
     def launches_per_step(self) -> int:
-        n = self.dec.launches_per_step()
         d = self.d_model
-        for w, k in [(self.w_dkv, d), (self.w_kr, d), (self.w_dq, d), (self.w_uq, self.c_q.shape[1]),
-                     (self.w_qr, self.c_q.shape[1]), (self.w_o, self.w_o.shape[1])]:
+        dq = self.c_q.shape[1]
+        if self.fold:
+            n = 2 + (1 if self.dec.num_splits > 1 else 0) + 1 + 1   # append, attention, combine, to_bf16, rope_q
+            lin = [(self.w_dkv, d), (self.w_kr, d), (self.w_dq, d), (self.w_qk, dq), (self.w_qr, dq),
+                   (self.w_ov, self.w_ov.shape[1])]
+        else:
+            n = self.dec.launches_per_step()
+            lin = [(self.w_dkv, d), (self.w_kr, d), (self.w_dq, d), (self.w_uq, dq), (self.w_qr, dq),
+                   (self.w_o, self.w_o.shape[1])]
+        for w, k in lin:
             n += 1 + (1 if ops.mla_linear_workspace_size(self.T, k, w.shape[0]) else 0)
         return n

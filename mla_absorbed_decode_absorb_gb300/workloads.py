@@ -54,6 +54,7 @@ class Workload:
     description: str = ""
     cache_format: str = "bf16"            # "bf16" (576 bf16 per token) or "fp8" (E4M3 latent, see ops)
     d_model: int = 0                      # > 0: the whole layer from the hidden state (see LayerInputs)
+    fold: bool = False                    # the layer with the weight pre-folds (W_QK, W_OV)
 
 
 # The five workloads of the benchmark, named by what they are.
@@ -104,6 +105,8 @@ LAYER_WORKLOADS: dict[str, Workload] = {
         Workload("layer_b32_l4096", batch=32, n_q=1, context=4096, d_model=D_MODEL,
                  description="decode layer from the hidden state (d_model 7168): B=32, 1 new token each, "
                              "uniform prior context 4096"),
+        Workload("layer_b32_l4096_fold", batch=32, n_q=1, context=4096, d_model=D_MODEL, fold=True,
+                 description="the same decode layer with the weight pre-folds W_UK^T W_UQ and W_O W_UV"),
     ]
 }
 

@@ -75,3 +75,36 @@ def test_layer_full_size_sampled():
     li = W.generate_layer(W.LAYER_WORKLOADS["layer_b32_l4096"], seed=0)
     s = run_layer(li)
     check_layer(s, li, [0, li.workload.batch - 1])
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_layer_fold_parity_small(name):
+    """The weight pre-folds (W_UK^T W_UQ into the query, W_O W_UV into the output) give
+    the same layer: one more bf16 rounding (of the folded weights and of O') than the
+    unfolded path, the same tolerance."""
+    li = W.generate_layer(SMALL[name], seed=6)
+    s = run_layer(li, fold=True)
+    y = s.y.float().cpu().numpy().reshape(li.workload.batch, li.workload.n_q, -1)
+    ys, yr = [], []
+    for b in range(li.workload.batch):
+        y_ref, _ = oracle_layer(li, b)
+        ys.append(y[b]), yr.append(y_ref)
+    assert rel_l2(np.concatenate(ys), np.concatenate(yr)) <= Y_REL_L2, rel_l2(np.concatenate(ys), np.concatenate(yr))
+
+
+def test_fold_weights_match_their_definition():
+    """W_QK[(h, m), c] = sum_d W_UK[h, d, m] W_UQ[h*128 + d, c] and
+    W_OV[j, (h, m)] = sum_d W_O[j, h*128 + d] W_UV[h, d, m], on sampled heads."""
+    li = W.generate_layer(SMALL["edges"], seed=7)
+    s = run_layer(li, fold=True)
+    wqk = s.w_qk.float().cpu().numpy()
+    wov = s.w_ov.float().cpu().numpy()
+    w_uk, w_uv = f64(li.base.w_uk), f64(li.base.w_uv)
+    w_uq, w_o = f64(li.w_uq), f64(li.w_o)
+    for h in (0, 77, 127):
+        ref_qk = w_uk[h].T @ w_uq[h * 128:(h + 1) * 128]
+        ref_ov = w_o[:, h * 128:(h + 1) * 128] @ w_uv[h]
+        got_qk = wqk[h * 512:(h + 1) * 512]
+        got_ov = wov[:, h * 512:(h + 1) * 512]
+        assert np.abs(got_qk - ref_qk).max() <= 2.0 ** -8 * np.abs(ref_qk).max() + 1e-6
+        assert np.abs(got_ov - ref_ov).max() <= 2.0 ** -8 * np.abs(ref_ov).max() + 1e-6
