@@ -231,7 +231,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       // this CTA's 288 columns of a page into L2
       auto prefetch = [&](int page) {
         if (page < 0 || page >= p.num_pages) return;
-        for (int c = 0; c < 4; ++c) tma_prefetch_l2_2d(&tm_c128, 64 * (4 * rank + c), page * kPage);
+        tma_prefetch_l2_3d(&tm_c128, 0, page * kPage, 4 * rank);
         tma_prefetch_l2_2d(&tm_c64, kLatent + 32 * rank, page * kPage);
       };
       for (int q = kStages; q < min(kL2Ahead, n_pages); ++q) {
@@ -258,8 +258,8 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
               const uint32_t sb = smem_u32(smem + kOffStage + s * kStageBytes);
               const uint32_t fb = bar_addr(bars.full[s]);
               mbar_arrive_expect_tx(fb, kStageBytes);
-              for (int c = 0; c < 4; ++c)
-                tma_load_2d(sb + c * kPChunk, &tm_c128, 64 * (4 * rank + c), page * kPage, fb);
+              // the CTA's four 64-column chunks of the page in one box: (64 columns, 64 tokens, 4 chunks)
+              tma_load_3d(sb, &tm_c128, 0, page * kPage, 4 * rank, fb);
               tma_load_2d(sb + 4 * kPChunk, &tm_c64, kLatent + 32 * rank, page * kPage, fb);
             }
           }
@@ -656,7 +656,7 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * kHeads;
   const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
   if (!make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_tmap_bf16_2d(&tc128, cache, c_rows, kRow, kRow, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_chunks(&tc128, cache, c_rows, kRow, 64, 4) ||
       !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_f32_2d(&to, o_out, static_cast<uint64_t>(units) * kHeads, kLatent, kLatent, 32, 128,
                         CU_TENSOR_MAP_SWIZZLE_128B))

@@ -38,6 +38,24 @@ inline bool make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A bf16 matrix [rows, row_elems] seen as 64-column chunks: dims (64 columns,
+// rows, chunks) with strides (row_elems * 2 B, 128 B), box (64, box_rows,
+// box_chunks), 128-byte swizzle.  One box lands as box_chunks consecutive
+// [box_rows x 128 B] swizzled tiles, chunk-major, as box_chunks separate 2-D
+// boxes of 64 columns would.
+inline bool make_tmap_bf16_chunks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                                  uint32_t box_rows, uint32_t box_chunks) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {64, rows, row_elems / 64};
+  const cuuint64_t strides[2] = {row_elems * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, box_chunks};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-major byte matrix [rows, cols] with `row_stride` bytes between rows.
 inline bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride,
                             uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
