@@ -26,13 +26,15 @@ constexpr int kSmemBudget = 200 * 1024;
 
 __host__ __device__ inline int pad16(int t) { return (t + 15) & ~15; }
 __host__ __device__ inline int stage_bytes(int tp) { return kWBox + tp * 128; }
-__host__ __device__ inline int num_stages(int tp) { return min(8, kSmemBudget / stage_bytes(tp)); }
+constexpr int kMaxStages = 12;
+__host__ __device__ inline int num_stages(int tp) { return min(kMaxStages, kSmemBudget / stage_bytes(tp)); }
 __host__ __device__ inline uint32_t tmem_cols_for(int tp) {
   uint32_t c = 32;
   while (c < static_cast<uint32_t>(tp)) c <<= 1;
   return c;
 }
 inline int smem_bytes_for(int tp) { return num_stages(tp) * stage_bytes(tp) + 256 + 1024; }
+static_assert((2 * kMaxStages + 1) * 8 + 4 <= 256, "barrier block");
 
 struct LinParams {
   uint16_t* y;        // bf16 out (no split): element (t, n) at t * y_ld + (n / seg) * seg_ld + n % seg
@@ -57,8 +59,8 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   const int S = num_stages(tp);
   const int SB = stage_bytes(tp);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
-  uint64_t* empty = full + 8;
-  uint64_t* done = empty + 8;
+  uint64_t* empty = full + kMaxStages;
+  uint64_t* done = empty + kMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
   const uint32_t tmem_cols = tmem_cols_for(tp);
 
@@ -173,8 +175,9 @@ int g_sms = 0;
 
 }  // namespace
 
-// K split so that tiles x splits covers about two waves of the GPU, each split
-// keeping at least 4 K blocks of 64.
+// K split so that tiles x splits fills one wave of the GPU (one CTA per SM),
+// each split keeping at least 4 K blocks of 64: a second, partial wave of short
+// weight streams cost more than it overlapped (W_O, K = 16384: 60.9 -> 55.4 us).
 int linear_num_splits(int T, int K, int N) {
   (void)T;
   if (g_sms == 0) {
@@ -184,7 +187,10 @@ int linear_num_splits(int T, int K, int N) {
   }
   const int tiles = (N + 127) / 128;
   const int kbs = K / kKB;
-  int split = max(1, (2 * g_sms) / tiles);
+  int split = max(1, g_sms / tiles);
+  // long weight streams (over 128 K blocks per split in one wave) keep a second wave
+  // busy: W_OV, K = 65536, streamed faster in two (166 against 183 us)
+  if (kbs / split > 128) split = max(1, (2 * g_sms) / tiles);
   split = min(split, max(1, kbs / 4));
   const int per = (kbs + split - 1) / split;
   return (kbs + per - 1) / per;  // no empty split
