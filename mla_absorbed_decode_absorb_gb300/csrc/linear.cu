@@ -165,8 +165,17 @@ linear_reduce_kernel(const float* __restrict__ part, const LinParams p, int kspl
   const int64_t elems = static_cast<int64_t>(p.T) * p.N;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < elems;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    // the loads of eight splits are in flight together; the sum keeps split order
     float a = 0.f;
-    for (int s = 0; s < ksplit; ++s) a += part[s * elems + e];
+    int s = 0;
+    for (; s + 8 <= ksplit; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = part[(s + q) * elems + e];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a += v[q];
+    }
+    for (; s < ksplit; ++s) a += part[s * elems + e];
     p.y[y_index(p, static_cast<int>(e / p.N), static_cast<int>(e % p.N))] = f32_to_bf16_bits(a);
   }
 }
