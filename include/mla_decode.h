@@ -137,6 +137,27 @@ mla_status mla_absorb_q(const mla_bf16* q_nope, const mla_bf16* q_rope,
                         int B, int n_q, cudaStream_t stream);
 
 /*
+ * mla_append_absorb_q -- mla_append_kv(c_kv_new, k_pe_new, ..., cache, B, n_new = n_q)
+ * and mla_absorb_q(q_nope, q_rope, ..., q_abs, B, n_q) in one launch.
+ * (The same two steps as above: "DeepSeek MLA 架构详解" decode listing steps 1
+ *  and 3.)  The query side reads nothing the append writes, so the rows are
+ * written by warps of the absorbed-query kernel; the cache image and q_abs are
+ * bit for bit those of the two separate calls.  Arguments as in those calls,
+ * with n_new = n_q; the constraints of both apply (16-byte aligned c_kv_new,
+ * cache, q_nope, q_rope, w_uk, q_abs; 1 <= n_q <= MLA_MAX_NQ), and a token out
+ * of range sets MLA_ERR_BOUNDS exactly as in mla_append_kv.  A decode step that
+ * uses it launches one kernel fewer, and the attention that follows waits for
+ * one grid instead of two.
+ */
+mla_status mla_append_absorb_q(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
+                               const mla_bf16* q_nope, const mla_bf16* q_rope,
+                               const int32_t* seq_lens_before, const int32_t* page_table,
+                               int pt_stride, const mla_bf16* w_uk,
+                               const float* rope_table, int rope_max_pos,
+                               mla_bf16* cache, int64_t num_pages, mla_bf16* q_abs,
+                               int B, int n_q, cudaStream_t stream);
+
+/*
  * Split-KV attention over the paged latent cache.
  * ("DeepSeek-MLA-Principle" section 2: score = q.k / sqrt(d_h + d_h^R), softmax,
  *  eq. (10); the absorbed score Q'_nope c^T + Q_rope k_rope^T of "MLA 矩阵吸收 …"

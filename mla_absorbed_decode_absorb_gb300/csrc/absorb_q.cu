@@ -13,6 +13,11 @@
 // two TMA boxes of 64 m x 128 d, B by 16-byte asynchronous copies), one MMA
 // chain of 8 x (K = 16) accumulates into TMEM, and four warps read their 32
 // TMEM lanes back (lane = m, column = token) and store bf16.
+//
+// The same launch may also write the step's new cache rows (the append): the
+// query side does not read them, so one launch replaces two and the attention
+// waits for one grid instead of two.  Warp 0 of CTA k appends tokens k, k + grid, ...
+#include "append_row.cuh"
 #include "sm100.cuh"
 #include "tmap.cuh"
 
@@ -44,7 +49,7 @@ __global__ void __launch_bounds__(kThreads)
 absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t* __restrict__ q_nope, const uint16_t* __restrict__ q_rope,
                    const int32_t* __restrict__ lens,
                    const float* __restrict__ rope, int rope_max_pos, uint16_t* __restrict__ q_abs,
-                   int T, int n_q, int* status, bool weights_early) {
+                   int T, int n_q, int* status, bool weights_early, const AppendArgs ap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -86,6 +91,13 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t* __r
   grid_dep_wait();
   grid_dep_launch();
   if (!weights_early) load_w();
+  if (ap.cache != nullptr && warp == 0) {
+    const int64_t ncta = static_cast<int64_t>(gridDim.x) * gridDim.y * gridDim.z;
+    const int64_t tokens = static_cast<int64_t>(ap.B) * ap.n_new;
+    for (int64_t tok = (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x; tok < tokens;
+         tok += ncta)
+      append_token_bf16(ap, tok, lane, status);
+  }
   for (int v = tid; v < npad * 16; v += kThreads) {
     const int t = v >> 4, u = v & 15, c = u >> 3;
     uint8_t* dst = sB + c * npad * 128 + sw128(t * 128 + (u & 7) * 16);
@@ -196,12 +208,12 @@ cudaError_t launch_rope_q(const uint16_t* q_rope, const int32_t* seq_lens_before
                        seq_lens_before, rope_table, rope_max_pos, q_abs, T, n_q, status);
 }
 
-cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
-                            const int32_t* seq_lens_before, const uint16_t* w_uk,
-                            const float* rope_table, int rope_max_pos, uint16_t* q_abs,
-                            int B, int n_q, int* status, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_absorb(const uint16_t* q_nope, const uint16_t* q_rope, const int32_t* seq_lens_before,
+                          const uint16_t* w_uk, const float* rope_table, int rope_max_pos, uint16_t* q_abs, int B,
+                          int n_q, const AppendArgs& ap, int* status, cudaStream_t stream) {
   const int T = B * n_q;
-  if (T == 0) return cudaSuccess;
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(absorb_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -215,7 +227,31 @@ cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
     return cudaErrorInvalidValue;
   dim3 grid(kLatent / kMTile, kHeads, (T + kNMax - 1) / kNMax);
   return launch_kernel(absorb_q_tc_kernel, grid, dim3(kThreads), smem_bytes_for(T), stream, tw, q_nope, q_rope,
-                       seq_lens_before, rope_table, rope_max_pos, q_abs, T, n_q, status, launch_overlap() >= 2);
+                       seq_lens_before, rope_table, rope_max_pos, q_abs, T, n_q, status, launch_overlap() >= 2, ap);
+}
+
+}  // namespace
+
+cudaError_t launch_absorb_q(const uint16_t* q_nope, const uint16_t* q_rope,
+                            const int32_t* seq_lens_before, const uint16_t* w_uk,
+                            const float* rope_table, int rope_max_pos, uint16_t* q_abs,
+                            int B, int n_q, int* status, cudaStream_t stream) {
+  if (B * n_q == 0) return cudaSuccess;
+  AppendArgs none{};
+  return launch_absorb(q_nope, q_rope, seq_lens_before, w_uk, rope_table, rope_max_pos, q_abs, B, n_q, none, status,
+                       stream);
+}
+
+cudaError_t launch_append_absorb_q(const uint16_t* c_kv_new, const uint16_t* k_pe_new, const uint16_t* q_nope,
+                                   const uint16_t* q_rope, const int32_t* seq_lens_before, const int32_t* page_table,
+                                   int pt_stride, const uint16_t* w_uk, const float* rope_table, int rope_max_pos,
+                                   uint16_t* cache, int64_t num_pages, uint16_t* q_abs, int B, int n_q, int* status,
+                                   cudaStream_t stream) {
+  if (B * n_q == 0) return cudaSuccess;
+  const AppendArgs ap{c_kv_new, k_pe_new, seq_lens_before, page_table, pt_stride, rope_table, rope_max_pos,
+                      cache, num_pages, B, n_q};
+  return launch_absorb(q_nope, q_rope, seq_lens_before, w_uk, rope_table, rope_max_pos, q_abs, B, n_q, ap, status,
+                       stream);
 }
 
 }  // namespace mla

@@ -13,9 +13,10 @@ four ABI calls with no allocation:
 
 With ``fused_finish=False`` step 4 is the two separate calls
 ``mla_decode_combine`` (which also writes the merged O' to ``o_latent``) and
-``mla_out_absorb``.  Steps 1 and 2 are independent; with ``overlap_append``
-step 1 runs on a side stream forked from the caller's stream and joined before
-step 3.  By default all launches stay on the caller's stream, where the
+``mla_out_absorb``.  Steps 1 and 2 are independent: by default
+(``fused_prologue``, bf16 cache) they are the one call ``mla_append_absorb_q``,
+so a step is three launches; with ``overlap_append`` step 1 runs on a side
+stream forked from the caller's stream and joined before step 3.  By default all launches stay on the caller's stream, where the
 library's programmatic dependent launch (``mla_set_launch_overlap``) lets each
 kernel's prologue overlap the previous one.
 
@@ -45,7 +46,8 @@ PREFILL_MIN_NEW_TOKENS = 64
 
 class DecodeSession:
     def __init__(self, inp: Inputs, device="cuda", split_pages: int | None = None, stream=None,
-                 fused_finish: bool = True, overlap_append: bool = False, path: str | None = None):
+                 fused_finish: bool = True, overlap_append: bool = False, path: str | None = None,
+                 fused_prologue: bool = True):
         self.inp = inp
         self.cache_format = inp.workload.cache_format
         if self.cache_format not in ("bf16", "fp8"):
@@ -65,6 +67,9 @@ class DecodeSession:
         self.path = path
         if self.cache_format == "fp8" and path != "absorbed":
             raise ValueError("the FP8 latent cache is read by the absorbed path only")
+        # append + absorb_q as one launch (bf16 cache, both on the caller's stream)
+        self.fused_prologue = (bool(fused_prologue) and path == "absorbed" and self.cache_format == "bf16"
+                               and not self.overlap_append)
         dev = self.device
         self.max_kv_len = int(inp.kv_lens.max()) if self.B else self.n_q
         self.rope = ops.rope_table(self.max_kv_len + 1, dev, stream)
@@ -158,6 +163,10 @@ class DecodeSession:
         ops.mla_absorb_q(self.q_nope, self.q_rope, self.prior_lens, self.w_uk, self.rope, self.q_abs,
                          stream=stream)
 
+    def append_absorb(self, stream=None):
+        ops.mla_append_absorb_q(self.c_new, self.k_new, self.q_nope, self.q_rope, self.prior_lens, self.page_table,
+                                self.w_uk, self.rope, self.cache, self.q_abs, stream=stream)
+
     def attend_partial(self, stream=None):
         if self.overlap_append:
             self._main(stream).wait_event(self._appended)  # the cache holds the new tokens
@@ -195,7 +204,8 @@ class DecodeSession:
         if self.path == "non_absorbed":
             return ["append", "decompress", "prefill_attn"]
         tail = ["finish"] if self.fused_finish else ["combine", "project_out"]
-        return ["append", "absorb", "attend_partial"] + tail
+        head = ["append_absorb"] if self.fused_prologue else ["append", "absorb"]
+        return head + ["attend_partial"] + tail
 
     def step(self, stream=None):
         for name in self.stage_names():
@@ -205,9 +215,10 @@ class DecodeSession:
     def launches_per_step(self) -> int:
         if self.path == "non_absorbed":
             return 3
+        n = 3 if self.fused_prologue else 4
         if self.fused_finish:
-            return 4
-        return 4 + (1 if self.num_splits > 1 else 0)
+            return n
+        return n + (1 if self.num_splits > 1 else 0)
 
 
 class LayerSession:

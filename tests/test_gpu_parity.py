@@ -142,6 +142,19 @@ def test_append_on_side_stream_matches_in_order():
     assert np.array_equal(bits(a.out), bits(b.out))
 
 
+@pytest.mark.parametrize("lens,n_q", [([10, 64, 333], 3), ([0, 63, 127, 4000], 1), ([5, 200], 4)])
+def test_fused_append_absorb_matches_separate_calls(lens, n_q):
+    """mla_append_absorb_q writes the cache rows and q_abs of mla_append_kv followed
+    by mla_absorb_q, bit for bit (and so the step's outputs)."""
+    inp = W.generate(W.custom("prologue", lens, n_q=n_q), seed=11)
+    a = run_session(inp, fused_prologue=True)
+    b = run_session(inp, fused_prologue=False)
+    assert a.stage_names()[0] == "append_absorb" and b.stage_names()[:2] == ["append", "absorb"]
+    assert a.launches_per_step() == b.launches_per_step() - 1
+    for x, y in [(a.cache, b.cache), (a.q_abs, b.q_abs), (a.out, b.out)]:
+        assert np.array_equal(bits(x), bits(y))
+
+
 def test_launch_overlap_levels_give_identical_results():
     """Programmatic dependent launch only moves prologues (and, at level 2, the
     weight reads) ahead of the previous kernel's completion: same bits."""
