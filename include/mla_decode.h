@@ -279,12 +279,25 @@ mla_status mla_f32_to_bf16(const float* src, mla_bf16* dst, int64_t n, cudaStrea
  * the P V MMA as f16(p_t s_t): a page whose p_t s_t exceeds 65504 (s_t above
  * 255, i.e. a latent value beyond about 114000) overflows.  The query is
  * converted to float16 (exact for 2^-14 <= |q| <= 65504).
+ *
+ * mla_append_absorb_q_fp8 -- mla_append_absorb_q with this format: the rows of
+ * mla_append_kv_fp8 (n_new = n_q) and the q_abs of mla_absorb_q in one launch,
+ * bit for bit those of the two separate calls; arguments and errors of both
+ * (16-byte aligned c_kv_new, cache_c8, q_nope, q_rope, w_uk, q_abs).
  */
 mla_status mla_append_kv_fp8(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
                              const int32_t* seq_lens_before, const int32_t* page_table,
                              int pt_stride, const float* rope_table, int rope_max_pos,
                              uint8_t* cache_c8, float* cache_scale, uint16_t* cache_kr,
                              int64_t num_pages, int B, int n_new, cudaStream_t stream);
+mla_status mla_append_absorb_q_fp8(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
+                                   const mla_bf16* q_nope, const mla_bf16* q_rope,
+                                   const int32_t* seq_lens_before, const int32_t* page_table,
+                                   int pt_stride, const mla_bf16* w_uk,
+                                   const float* rope_table, int rope_max_pos,
+                                   uint8_t* cache_c8, float* cache_scale, uint16_t* cache_kr,
+                                   int64_t num_pages, mla_bf16* q_abs, int B, int n_q,
+                                   cudaStream_t stream);
 mla_status mla_decode_attn_fp8_partial(const mla_bf16* q_abs, const uint8_t* cache_c8,
                                        const float* cache_scale, const uint16_t* cache_kr,
                                        int64_t num_pages, const int32_t* page_table, int pt_stride,

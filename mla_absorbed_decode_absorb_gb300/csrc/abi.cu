@@ -276,6 +276,30 @@ mla_status mla_append_absorb_q(const mla_bf16* c_kv_new, const mla_bf16* k_pe_ne
                                           stream));
 }
 
+mla_status mla_append_absorb_q_fp8(const mla_bf16* c_kv_new, const mla_bf16* k_pe_new,
+                                   const mla_bf16* q_nope, const mla_bf16* q_rope,
+                                   const int32_t* seq_lens_before, const int32_t* page_table,
+                                   int pt_stride, const mla_bf16* w_uk,
+                                   const float* rope_table, int rope_max_pos,
+                                   uint8_t* cache_c8, float* cache_scale, uint16_t* cache_kr,
+                                   int64_t num_pages, mla_bf16* q_abs, int B, int n_q,
+                                   cudaStream_t stream) {
+  if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ) return MLA_ERR_INVALID_ARG;
+  if (B == 0) return MLA_OK;
+  if (!c_kv_new || !k_pe_new || !q_nope || !q_rope || !seq_lens_before || !page_table || !w_uk || !rope_table ||
+      !cache_c8 || !cache_scale || !cache_kr || !q_abs)
+    return MLA_ERR_INVALID_ARG;
+  if (pt_stride < 1 || rope_max_pos < 1 || num_pages < 1) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c_kv_new) || !aligned16(cache_c8) || !aligned16(q_nope) || !aligned16(q_rope) || !aligned16(w_uk) ||
+      !aligned16(q_abs))
+    return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_append_absorb_q_fp8(c_kv_new, k_pe_new, q_nope, q_rope, seq_lens_before, page_table,
+                                              pt_stride, w_uk, rope_table, rope_max_pos, cache_c8, cache_scale,
+                                              cache_kr, num_pages, q_abs, B, n_q, st, stream));
+}
+
 mla_status mla_decode_workspace_size(int B, int n_q, int max_kv_len, int split_pages, size_t* bytes) {
   SplitPlan plan;
   if (bytes == nullptr || !make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;

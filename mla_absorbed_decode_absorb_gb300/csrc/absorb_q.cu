@@ -91,12 +91,16 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t* __r
   grid_dep_wait();
   grid_dep_launch();
   if (!weights_early) load_w();
-  if (ap.cache != nullptr && warp == 0) {
+  if ((ap.cache != nullptr || ap.c8 != nullptr) && warp == 0) {
     const int64_t ncta = static_cast<int64_t>(gridDim.x) * gridDim.y * gridDim.z;
     const int64_t tokens = static_cast<int64_t>(ap.B) * ap.n_new;
     for (int64_t tok = (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x; tok < tokens;
-         tok += ncta)
-      append_token_bf16(ap, tok, lane, status);
+         tok += ncta) {
+      if (ap.cache != nullptr)
+        append_token_bf16(ap, tok, lane, status);
+      else
+        append_token_fp8(ap, tok, lane, status);
+    }
   }
   for (int v = tid; v < npad * 16; v += kThreads) {
     const int t = v >> 4, u = v & 15, c = u >> 3;
@@ -250,6 +254,19 @@ cudaError_t launch_append_absorb_q(const uint16_t* c_kv_new, const uint16_t* k_p
   if (B * n_q == 0) return cudaSuccess;
   const AppendArgs ap{c_kv_new, k_pe_new, seq_lens_before, page_table, pt_stride, rope_table, rope_max_pos,
                       cache, num_pages, B, n_q};
+  return launch_absorb(q_nope, q_rope, seq_lens_before, w_uk, rope_table, rope_max_pos, q_abs, B, n_q, ap, status,
+                       stream);
+}
+
+cudaError_t launch_append_absorb_q_fp8(const uint16_t* c_kv_new, const uint16_t* k_pe_new, const uint16_t* q_nope,
+                                       const uint16_t* q_rope, const int32_t* seq_lens_before,
+                                       const int32_t* page_table, int pt_stride, const uint16_t* w_uk,
+                                       const float* rope_table, int rope_max_pos, uint8_t* c8, float* scale,
+                                       uint16_t* kr, int64_t num_pages, uint16_t* q_abs, int B, int n_q, int* status,
+                                       cudaStream_t stream) {
+  if (B * n_q == 0) return cudaSuccess;
+  const AppendArgs ap{c_kv_new, k_pe_new, seq_lens_before, page_table, pt_stride, rope_table, rope_max_pos,
+                      nullptr, num_pages, B, n_q, c8, scale, kr};
   return launch_absorb(q_nope, q_rope, seq_lens_before, w_uk, rope_table, rope_max_pos, q_abs, B, n_q, ap, status,
                        stream);
 }

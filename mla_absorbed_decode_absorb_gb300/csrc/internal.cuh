@@ -71,6 +71,13 @@ cudaError_t launch_append_absorb_q(const uint16_t* c_kv_new, const uint16_t* k_p
                                    int pt_stride, const uint16_t* w_uk, const float* rope_table, int rope_max_pos,
                                    uint16_t* cache, int64_t num_pages, uint16_t* q_abs, int B, int n_q, int* status,
                                    cudaStream_t stream);
+// The same with the FP8 latent cache (the rows as mla_append_kv_fp8 writes them).
+cudaError_t launch_append_absorb_q_fp8(const uint16_t* c_kv_new, const uint16_t* k_pe_new, const uint16_t* q_nope,
+                                       const uint16_t* q_rope, const int32_t* seq_lens_before,
+                                       const int32_t* page_table, int pt_stride, const uint16_t* w_uk,
+                                       const float* rope_table, int rope_max_pos, uint8_t* c8, float* scale,
+                                       uint16_t* kr, int64_t num_pages, uint16_t* q_abs, int B, int n_q, int* status,
+                                       cudaStream_t stream);
 
 // Clusters of the attention kernel that fit on the current device at once.
 int decode_cluster_slots();

@@ -40,6 +40,7 @@ _SIGS = {
     "mla_append_kv": ([_p, _p, _p, _p, _i, _p, _i, _p, _i64, _i, _i, _p], _i),
     "mla_absorb_q": ([_p, _p, _p, _p, _p, _i, _p, _i, _i, _p], _i),
     "mla_append_absorb_q": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _p, _i64, _p, _i, _i, _p], _i),
+    "mla_append_absorb_q_fp8": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _p, _p, _p, _i64, _p, _i, _i, _p], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_decode_num_splits": ([_i, _i, _i, _i, ctypes.POINTER(_i)], _i),
     "mla_decode_attn": ([_p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
@@ -294,6 +295,32 @@ def mla_append_absorb_q(c_kv_new, k_pe_new, q_nope, q_rope, seq_lens_before, pag
         _dev(q_abs, "q_abs", torch.bfloat16, (B, n_q, N_HEADS, D_ROW)),
         int(B), int(n_q), _stream(stream)))
     return cache, q_abs
+
+
+def mla_append_absorb_q_fp8(c_kv_new, k_pe_new, q_nope, q_rope, seq_lens_before, page_table, w_uk, rope,
+                            cache_fp8, q_abs, stream=None):
+    """mla_append_kv_fp8 and mla_absorb_q in one launch (n_new = n_q)."""
+    B, n_q = q_nope.shape[:2]
+    c8, scale, kr = cache_fp8
+    P = int(c8.shape[0])
+    if page_table.dim() != 2 or page_table.shape[0] != B:
+        raise ValueError("page_table must be [B, max_pages]")
+    _check("mla_append_absorb_q_fp8", lib.mla_append_absorb_q_fp8(
+        _dev(c_kv_new, "c_kv_new", torch.bfloat16, (B, n_q, D_LATENT)),
+        _dev(k_pe_new, "k_pe_new", torch.bfloat16, (B, n_q, D_ROPE)),
+        _dev(q_nope, "q_nope", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        _dev(q_rope, "q_rope", torch.bfloat16, (B, n_q, N_HEADS, D_ROPE)),
+        _dev(seq_lens_before, "seq_lens_before", torch.int32, (B,)),
+        _dev(page_table, "page_table", torch.int32), int(page_table.shape[1]),
+        _dev(w_uk, "w_uk", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
+        _dev(rope, "rope_table", torch.float32), int(rope.shape[0]),
+        _dev(c8, "cache_c8", torch.uint8, (P, 64, D_LATENT)),
+        _dev(scale, "cache_scale", torch.float32, (P, 64)),
+        _dev(kr, "cache_kr", torch.float16, (P, 64, D_ROPE)),
+        P,
+        _dev(q_abs, "q_abs", torch.bfloat16, (B, n_q, N_HEADS, D_ROW)),
+        int(B), int(n_q), _stream(stream)))
+    return cache_fp8, q_abs
 
 
 def mla_decode_workspace_size(B: int, n_q: int, max_kv_len: int, split_pages: int = 0) -> int:

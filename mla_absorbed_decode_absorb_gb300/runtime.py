@@ -14,7 +14,7 @@ four ABI calls with no allocation:
 With ``fused_finish=False`` step 4 is the two separate calls
 ``mla_decode_combine`` (which also writes the merged O' to ``o_latent``) and
 ``mla_out_absorb``.  Steps 1 and 2 are independent: by default
-(``fused_prologue``, bf16 cache) they are the one call ``mla_append_absorb_q``,
+(``fused_prologue``) they are the one call ``mla_append_absorb_q`` (or its FP8 form),
 so a step is three launches; with ``overlap_append`` step 1 runs on a side
 stream forked from the caller's stream and joined before step 3.  By default all launches stay on the caller's stream, where the
 library's programmatic dependent launch (``mla_set_launch_overlap``) lets each
@@ -67,9 +67,8 @@ class DecodeSession:
         self.path = path
         if self.cache_format == "fp8" and path != "absorbed":
             raise ValueError("the FP8 latent cache is read by the absorbed path only")
-        # append + absorb_q as one launch (bf16 cache, both on the caller's stream)
-        self.fused_prologue = (bool(fused_prologue) and path == "absorbed" and self.cache_format == "bf16"
-                               and not self.overlap_append)
+        # append + absorb_q as one launch (both on the caller's stream)
+        self.fused_prologue = bool(fused_prologue) and path == "absorbed" and not self.overlap_append
         dev = self.device
         self.max_kv_len = int(inp.kv_lens.max()) if self.B else self.n_q
         self.rope = ops.rope_table(self.max_kv_len + 1, dev, stream)
@@ -164,8 +163,13 @@ class DecodeSession:
                          stream=stream)
 
     def append_absorb(self, stream=None):
-        ops.mla_append_absorb_q(self.c_new, self.k_new, self.q_nope, self.q_rope, self.prior_lens, self.page_table,
-                                self.w_uk, self.rope, self.cache, self.q_abs, stream=stream)
+        if self.cache_format == "fp8":
+            ops.mla_append_absorb_q_fp8(self.c_new, self.k_new, self.q_nope, self.q_rope, self.prior_lens,
+                                        self.page_table, self.w_uk, self.rope, self.cache_fp8, self.q_abs,
+                                        stream=stream)
+        else:
+            ops.mla_append_absorb_q(self.c_new, self.k_new, self.q_nope, self.q_rope, self.prior_lens,
+                                    self.page_table, self.w_uk, self.rope, self.cache, self.q_abs, stream=stream)
 
     def attend_partial(self, stream=None):
         if self.overlap_append:

@@ -95,6 +95,19 @@ def test_fp8_decode_parity_small(name, split_pages):
     check_outputs_fp8(s, inp, oracle_fp8_images(inp), range(inp.batch))
 
 
+def test_fp8_fused_append_absorb_matches_separate_calls():
+    """mla_append_absorb_q_fp8 writes the cache image and q_abs of mla_append_kv_fp8
+    followed by mla_absorb_q, bit for bit."""
+    inp = W.generate(SMALL["mtp_q4"], seed=12)
+    a = run_session(inp, fused_prologue=True)
+    b = run_session(inp, fused_prologue=False)
+    assert a.stage_names()[0] == "append_absorb" and b.stage_names()[:2] == ["append", "absorb"]
+    for x, y in zip(gpu_images(a), gpu_images(b)):
+        assert np.array_equal(x.view(np.uint8), y.view(np.uint8))
+    assert np.array_equal(bits(a.q_abs), bits(b.q_abs))
+    assert np.array_equal(bits(a.out), bits(b.out))
+
+
 def test_fp8_decode_full_size_sampled():
     """The FP8 benchmark workload at full size, in the bench's launch configuration:
     sampled sequences (first, middle, last) on sampled heads."""
