@@ -11,7 +11,8 @@ Printed (rank 0, one JSON line): ``value`` = latent-cache bytes the step reads
 divided by the mean step time (device time from CUDA events on the launching
 stream, L2 flushed before every step, inputs resident in HBM).  ``e2e`` repeats
 the measurement through the same calls with the step's inputs copied from
-pinned host memory and the output copied back inside the timed region.
+pinned host memory and the output copied back inside the timed region (both
+by ``mla_copy_async``: the GPU's own loads and stores over the host link).
 ``roofline`` rates the split-attention kernel against the measured HBM copy
 bandwidth (or dense bf16 peak when FLOPs bind).  ``cpu_baseline`` times the
 fp64 CPU oracle on a bounded sample of the same workload.
@@ -470,9 +471,9 @@ def run_ours(args, wl):
             flush_l2()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
-            s.step_buffer.copy_(host_in, non_blocking=True)
+            s.upload(host_in)
             s.step()
-            host_out.copy_(s.out, non_blocking=True)
+            s.download(host_out)
             b.record(stream)
             b.synchronize()
             if k >= 3:

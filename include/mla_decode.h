@@ -417,6 +417,24 @@ mla_status mla_prefill_attn(const mla_bf16* q_nope, const mla_bf16* q_rope, cons
                             cudaStream_t stream);
 
 /*
+ * mla_copy_async -- copy `bytes` from src to dst with the GPU's own loads and
+ * stores, as one kernel of this library on `stream`.  (The MLA pages have no
+ * counterpart; this moves a step's inputs and outputs.)  Each of dst and src
+ * is device memory of the current device, managed memory, or pinned host
+ * memory mapped into the device's address space (cudaHostAlloc /
+ * cudaHostRegister on a unified-address system: on an NVLink-C2C machine the
+ * GPU reads and writes it at link speed); the whole range [p, p + bytes) must
+ * lie inside one such allocation, and the two ranges must not overlap, else
+ * MLA_ERR_INVALID_ARG (pageable host memory is refused).  Any alignment (16-
+ * byte aligned pointers take the vector path).  Ordered on the stream like the
+ * other calls and part of the launch-overlap chain (mla_set_launch_overlap):
+ * at level 2 a host-memory source is read before the previous kernel of the
+ * stream has completed, so the caller must not change it after enqueueing.
+ * bytes == 0 does nothing.
+ */
+mla_status mla_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream);
+
+/*
  * mla_set_launch_overlap / mla_get_launch_overlap -- how consecutive launches
  * of this library on one stream may overlap.  (The MLA pages have no
  * counterpart; this is a launch-latency setting of the GPU runtime.)
@@ -430,7 +448,8 @@ mla_status mla_prefill_attn(const mla_bf16* q_nope, const mla_bf16* q_rope, cons
  *   2  as 1, and the weight matrices w_uk (mla_absorb_q) and w_uv
  *      (mla_out_absorb, mla_combine_out_absorb) are read BEFORE the previous
  *      kernel has completed.  Only valid while no work still running on the
- *      stream writes those weights (fixed inference weights).
+ *      stream writes those weights (fixed inference weights).  Likewise
+ *      mla_copy_async reads a host-memory source before that point.
  *
  * The level is process-wide and read at each launch.  MLA_ERR_INVALID_ARG for a
  * level outside 0..2.  A launch whose predecessor on the stream is not a kernel

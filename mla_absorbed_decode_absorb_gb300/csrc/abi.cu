@@ -8,6 +8,9 @@
 #include <mutex>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "internal.cuh"
 
 // Per-device fault word written by the kernels (first code wins).
@@ -47,6 +50,47 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 mla_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// The device address of [p, p + bytes) if the current device can address all of
+// it: device memory of this device, managed memory, or pinned host memory
+// mapped into the device's address space (`host` is then set).
+bool device_view(const void* p, size_t bytes, void** out, bool* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  *host = false;
+  switch (a.type) {
+    case cudaMemoryTypeDevice:
+      if (a.device != current_device()) return false;
+      break;
+    case cudaMemoryTypeManaged:
+      break;
+    case cudaMemoryTypeHost:
+      *host = true;
+      break;
+    default:
+      return false;  // pageable host memory
+  }
+  if (a.devicePointer == nullptr) return false;
+  *out = a.devicePointer;
+  // the whole range lies inside the one allocation
+  static PFN_cuMemGetAddressRange_v3020 range = nullptr;
+  if (range == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 3020, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
+  }
+  CUdeviceptr base = 0;
+  size_t size = 0;
+  if (range(&base, &size, reinterpret_cast<CUdeviceptr>(*out)) != CUDA_SUCCESS) return false;
+  const uintptr_t start = reinterpret_cast<uintptr_t>(*out);
+  return start >= base && bytes <= size && start - base <= size - bytes;
+}
 
 // Split-KV partition.  Automatic choice: the split count s per (sequence,
 // query) that minimises waves(s) * (pages per split + 3), where a wave is as
@@ -298,6 +342,17 @@ mla_status mla_append_absorb_q_fp8(const mla_bf16* c_kv_new, const mla_bf16* k_p
   return from_cuda(launch_append_absorb_q_fp8(c_kv_new, k_pe_new, q_nope, q_rope, seq_lens_before, page_table,
                                               pt_stride, w_uk, rope_table, rope_max_pos, cache_c8, cache_scale,
                                               cache_kr, num_pages, q_abs, B, n_q, st, stream));
+}
+
+mla_status mla_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
+  if (bytes == 0) return MLA_OK;
+  if (dst == nullptr || src == nullptr) return MLA_ERR_INVALID_ARG;
+  void *d = nullptr, *s = nullptr;
+  bool d_host = false, s_host = false;
+  if (!device_view(dst, bytes, &d, &d_host) || !device_view(src, bytes, &s, &s_host)) return MLA_ERR_INVALID_ARG;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(d), b = reinterpret_cast<uintptr_t>(s);
+  if (a < b + bytes && b < a + bytes) return MLA_ERR_INVALID_ARG;  // overlapping ranges
+  return from_cuda(launch_copy(d, s, bytes, s_host, stream));
 }
 
 mla_status mla_decode_workspace_size(int B, int n_q, int max_kv_len, int split_pages, size_t* bytes) {

@@ -108,6 +108,10 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 }
 int* device_status_word();
 
+// SM-driven copy of `bytes` from src to dst, both device-addressable (csrc/copy.cu);
+// `src_is_host`: the source is host memory, which no kernel writes.
+cudaError_t launch_copy(void* dst, const void* src, size_t bytes, bool src_is_host, cudaStream_t stream);
+
 cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   int64_t num_pages, const int32_t* page_table, int pt_stride,
                                   const int32_t* kv_lens, int B, int n_q, int max_kv_len,

@@ -40,6 +40,7 @@ _SIGS = {
     "mla_append_kv": ([_p, _p, _p, _p, _i, _p, _i, _p, _i64, _i, _i, _p], _i),
     "mla_absorb_q": ([_p, _p, _p, _p, _p, _i, _p, _i, _i, _p], _i),
     "mla_append_absorb_q": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _p, _i64, _p, _i, _i, _p], _i),
+    "mla_copy_async": ([_p, _p, _sz, _p], _i),
     "mla_append_absorb_q_fp8": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _p, _p, _p, _i64, _p, _i, _i, _p], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_decode_num_splits": ([_i, _i, _i, _i, ctypes.POINTER(_i)], _i),
@@ -321,6 +322,23 @@ def mla_append_absorb_q_fp8(c_kv_new, k_pe_new, q_nope, q_rope, seq_lens_before,
         _dev(q_abs, "q_abs", torch.bfloat16, (B, n_q, N_HEADS, D_ROW)),
         int(B), int(n_q), _stream(stream)))
     return cache_fp8, q_abs
+
+
+def mla_copy(dst: torch.Tensor, src: torch.Tensor, stream=None):
+    """dst <- src (same number of bytes, both contiguous) with mla_copy_async: device
+    tensors of the current device or pinned (page-locked) host tensors."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.type == "cpu" and not t.is_pinned():
+            raise ValueError(f"{name} is pageable host memory: pin it (tensor.pin_memory())")
+    nbytes = dst.numel() * dst.element_size()
+    if nbytes != src.numel() * src.element_size():
+        raise ValueError("dst and src differ in size")
+    _check("mla_copy_async", lib.mla_copy_async(dst.data_ptr(), src.data_ptr(), nbytes, _stream(stream)))
+    return dst
 
 
 def mla_decode_workspace_size(B: int, n_q: int, max_kv_len: int, split_pages: int = 0) -> int:

@@ -136,6 +136,15 @@ class DecodeSession:
         host.copy_(self.step_buffer)
         return host
 
+    def upload(self, host_in: torch.Tensor, stream=None):
+        """This step's inputs from a pinned host buffer laid out as ``host_step_buffer``:
+        one ``mla_copy_async`` (SM loads over the host link, in the launch-overlap chain)."""
+        ops.mla_copy(self.step_buffer, host_in, stream)
+
+    def download(self, host_out: torch.Tensor, stream=None):
+        """The step's output ``out`` into a pinned host buffer of the same size."""
+        ops.mla_copy(host_out, self.out, stream)
+
     def _main(self, stream):
         if stream is None:
             return torch.cuda.current_stream(self.device)
@@ -314,6 +323,12 @@ class LayerSession:
             host = host.pin_memory()
         host.copy_(self.x)
         return host
+
+    def upload(self, host_in: torch.Tensor, stream=None):
+        ops.mla_copy(self.x, host_in, stream)
+
+    def download(self, host_out: torch.Tensor, stream=None):
+        ops.mla_copy(host_out, self.y, stream)
 
     def proj_kv(self, stream=None):
         ops.mla_linear(self.x, self.w_dkv, self._c_new, self.ws, stream)
