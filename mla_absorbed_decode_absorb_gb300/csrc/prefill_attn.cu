@@ -9,14 +9,17 @@
 //
 // One CTA per (sequence b, head h, tile of 128 new tokens).  The query tile
 // [q^C ; RoPE(q^R, pos)] (192 columns) is built in shared memory by the softmax
-// warps; per 128-key tile the producer loads, by TMA, the head's decompressed keys
-// (128 columns), the shared RoPE key of the cache (64 columns, through the page
-// table) and the values into a 2-stage ring.  S = Q K^T (M = 128 queries, N = 128
-// keys, K = 192) goes to one of two TMEM buffers, the softmax warps (one thread
-// per query) apply the causal mask and an online softmax with a lazily updated
-// reference max (O is rescaled only when a row's max grows by more than 2^8),
-// write P as bf16 into TMEM, and O += P V (N = 128, K = 128 keys) accumulates in
-// TMEM.  Query j of sequence b sits at position seq_lens_before[b] + j and sees
+// warps; per 128-key tile one producer warp loads, by TMA, the head's
+// decompressed keys (128 columns) and the shared RoPE key of the cache (64
+// columns, through the page table, whose entries it reads 32 at a time) into a
+// 2-stage key ring, and another the values into a 2-stage value ring: a key
+// stage is free again as soon as its S = Q K^T has been computed, so the next
+// keys load while the softmax runs.  S (M = 128 queries, N = 128 keys, K = 192)
+// goes to one of two TMEM buffers, the softmax warps (one thread per query)
+// apply the causal mask and an online softmax with a lazily updated reference
+// max (O is rescaled only when a row's max grows by more than 2^8), write P as
+// bf16 into one of two TMEM buffers (so P of the next tile never waits for P V
+// of this one), and O += P V (N = 128, K = 128 keys) accumulates in TMEM.  Query j of sequence b sits at position seq_lens_before[b] + j and sees
 // the keys 0 .. seq_lens_before[b] + j.
 #include "sm100.cuh"
 #include "tmap.cuh"
@@ -29,31 +32,39 @@ using namespace sm100;
 constexpr int kQTile = 128;
 constexpr int kKTile = 128;
 constexpr int kStages = 2;
-constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+// warp 0 key TMA, warp 1 QK^T issuer, warps 2-5 softmax, warp 6 value TMA, warp 7 P V issuer
+constexpr int kThreads = 256;
+constexpr int kVWarp = 6;
+constexpr int kPvWarp = 7;
 constexpr int kChunk = 128 * 128;   // 128 rows x 64 bf16 columns (SW128)
 constexpr int kOffQ = 0;            // query: 3 chunks (q^C 0-63, q^C 64-127, RoPE(q^R))
-constexpr int kStageBytes = 5 * kChunk;  // keys 2 chunks, RoPE keys 1, values 2
-constexpr int kOffStage = kOffQ + 3 * kChunk;
-constexpr int kOffBar = kOffStage + kStages * kStageBytes;
+constexpr int kKStageBytes = 3 * kChunk;  // keys 2 chunks, RoPE keys 1
+constexpr int kVStageBytes = 2 * kChunk;  // values 2 chunks
+constexpr int kOffK = kOffQ + 3 * kChunk;
+constexpr int kOffV = kOffK + kStages * kKStageBytes;
+constexpr int kOffBar = kOffV + kStages * kVStageBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemO = 0;      // O: [0, 128)
 constexpr uint32_t kTmemS = 128;    // two score buffers: [128, 256), [256, 384)
-constexpr uint32_t kTmemP = 384;    // P (128 keys as bf16 pairs): [384, 448)
+constexpr uint32_t kTmemP = 384;    // two P buffers (128 keys as bf16 pairs): [384, 448), [448, 512)
 constexpr float kRescaleLog2 = 8.f;
 
 struct Bars {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t kfull[kStages];
+  uint64_t kempty[kStages];
+  uint64_t vfull[kStages];
+  uint64_t vempty[kStages];
   uint64_t q_ready;
   uint64_t s_full[2];
   uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t pv_done;
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 256, "barrier block");
 
 struct Params {
   const uint16_t* q_nope;
@@ -84,17 +95,19 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bars.full[s]), 1);
-      mbar_init(smem_u32(&bars.empty[s]), 1);
+      mbar_init(smem_u32(&bars.kfull[s]), 1);
+      mbar_init(smem_u32(&bars.kempty[s]), 1);
+      mbar_init(smem_u32(&bars.vfull[s]), 1);
+      mbar_init(smem_u32(&bars.vempty[s]), 1);
     }
     mbar_init(smem_u32(&bars.q_ready), 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.s_full[s]), 1);
       mbar_init(smem_u32(&bars.s_free[s]), 128);
+      mbar_init(smem_u32(&bars.p_full[s]), 128);
+      mbar_init(smem_u32(&bars.pv_done[s]), 1);
     }
-    mbar_init(smem_u32(&bars.p_full), 128);
-    mbar_init(smem_u32(&bars.pv_done), 1);
-    mbar_init(smem_u32(&bars.drain), 1);
+    mbar_init(smem_u32(&bars.drain), 2);  // both issuers
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -119,72 +132,107 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
   if (tid == 0 && bad && qt == 0 && h == 0) record_status(p.status, MLA_ERR_BOUNDS);
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_kt > 0) {
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
-      tma_prefetch_desc(&tm_kr);
-      const int row0 = (b * kHeads + h) * p.max_kv_len;  // this head's rows in K and V
-      for (int kt = 0; kt < n_kt; ++kt) {
-        const int s = kt % kStages;
-        if (!mbar_wait(smem_u32(&bars.empty[s]), ((kt / kStages) & 1) ^ 1, p.status, abort)) break;
-        const uint32_t st = smem_u32(smem + kOffStage + s * kStageBytes);
-        const uint32_t fb = smem_u32(&bars.full[s]);
-        mbar_arrive_expect_tx(fb, kStageBytes);
-        for (int c = 0; c < 2; ++c) tma_load_2d(st + c * kChunk, &tm_k, 64 * c, row0 + kt * kKTile, fb);
-        for (int pg = 0; pg < 2; ++pg) {
-          const int tok = kt * kKTile + pg * kPage;
-          int page = 0;
-          if (tok < kv) {
-            page = p.page_table[static_cast<int64_t>(b) * p.pt_stride + tok / kPage];
-            if (page < 0 || page >= p.num_pages) {
-              record_status(p.status, MLA_ERR_BOUNDS);
-              page = 0;  // stay in bounds; the result of this tile is not meaningful
+    // ------------------------------------------------------------ key TMA producer
+    if (n_kt > 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_kr);
+      }
+      const int row0 = (b * kHeads + h) * p.max_kv_len;  // this head's rows in K
+      const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride;
+      const int n_pg = (kv + kPage - 1) / kPage;         // pages holding the sequence (<= pt_stride)
+      int ids = 0;
+      bool ok = true;
+      for (int kt = 0; kt < n_kt && ok; ++kt) {
+        if ((kt & 15) == 0) {  // the page ids of key tiles kt .. kt + 15, one per lane
+          const int q = 2 * kt + lane;
+          ids = q < n_pg ? pt[q] : 0;
+        }
+        const int pg0 = __shfl_sync(0xffffffffu, ids, (2 * kt) & 31);
+        const int pg1 = __shfl_sync(0xffffffffu, ids, (2 * kt + 1) & 31);
+        if (lane == 0) {
+          const int s = kt % kStages;
+          ok = mbar_wait(smem_u32(&bars.kempty[s]), ((kt / kStages) & 1) ^ 1, p.status, abort);
+          if (ok) {
+            const uint32_t st = smem_u32(smem + kOffK + s * kKStageBytes);
+            const uint32_t fb = smem_u32(&bars.kfull[s]);
+            mbar_arrive_expect_tx(fb, kKStageBytes);
+            for (int c = 0; c < 2; ++c) tma_load_2d(st + c * kChunk, &tm_k, 64 * c, row0 + kt * kKTile, fb);
+            for (int pg = 0; pg < 2; ++pg) {
+              const int tok = kt * kKTile + pg * kPage;
+              int page = pg == 0 ? pg0 : pg1;
+              if (tok >= kv) {
+                page = 0;  // past the sequence: masked, any page will do
+              } else if (page < 0 || page >= p.num_pages) {
+                record_status(p.status, MLA_ERR_BOUNDS);
+                page = 0;  // stay in bounds; the result of this tile is not meaningful
+              }
+              tma_load_2d(st + 2 * kChunk + pg * (kChunk / 2), &tm_kr, kLatent, page * kPage, fb);
             }
           }
-          tma_load_2d(st + 2 * kChunk + pg * (kChunk / 2), &tm_kr, kLatent, page * kPage, fb);
         }
-        for (int c = 0; c < 2; ++c) tma_load_2d(st + (3 + c) * kChunk, &tm_v, 64 * c, row0 + kt * kKTile, fb);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ tcgen05 issuer
+  } else if (warp == kVWarp) {
+    // ------------------------------------------------------------ value TMA producer
+    if (lane == 0 && n_kt > 0) {
+      tma_prefetch_desc(&tm_v);
+      const int row0 = (b * kHeads + h) * p.max_kv_len;  // this head's rows in V
+      for (int kt = 0; kt < n_kt; ++kt) {
+        const int s = kt % kStages;
+        if (!mbar_wait(smem_u32(&bars.vempty[s]), ((kt / kStages) & 1) ^ 1, p.status, abort)) break;
+        const uint32_t st = smem_u32(smem + kOffV + s * kVStageBytes);
+        const uint32_t fb = smem_u32(&bars.vfull[s]);
+        mbar_arrive_expect_tx(fb, kVStageBytes);
+        for (int c = 0; c < 2; ++c) tma_load_2d(st + c * kChunk, &tm_v, 64 * c, row0 + kt * kKTile, fb);
+      }
+    }
+  } else if (warp == 1 || warp == kPvWarp) {
+    // ------------------------------------------------------------ tcgen05 issuers
+    // One thread issues QK^T and another P V: an MMA issue returns only once the
+    // tensor pipe takes it, so with one issuer QK^T of the next key tile waited
+    // behind P V of the previous one (and that behind its P).
     if (lane == 0 && n_kt > 0) {
       const uint32_t idesc_qk = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/0);
       const uint32_t idesc_pv = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/1);
       const uint64_t d_q = smem_desc(smem_u32(smem + kOffQ), 16, 1024, kSw128);
-      const uint64_t d_st = smem_desc(smem_u32(smem + kOffStage), 16, 1024, kSw128);           // keys (K-major)
-      const uint64_t d_v = smem_desc(smem_u32(smem + kOffStage + 3 * kChunk), kChunk, 1024, kSw128);  // values (MN-major)
+      const uint64_t d_k = smem_desc(smem_u32(smem + kOffK), 16, 1024, kSw128);           // keys (K-major)
+      const uint64_t d_v = smem_desc(smem_u32(smem + kOffV), kChunk, 1024, kSw128);       // values (MN-major)
       bool ok = mbar_wait(smem_u32(&bars.q_ready), 0, p.status, abort);
       auto issue_qk = [&](int kt) -> bool {
         const int s = kt % kStages, buf = kt & 1;
-        bool w = mbar_wait(smem_u32(&bars.full[s]), (kt / kStages) & 1, p.status, abort);
+        bool w = mbar_wait(smem_u32(&bars.kfull[s]), (kt / kStages) & 1, p.status, abort);
         w = w && mbar_wait(smem_u32(&bars.s_free[buf]), ((kt >> 1) & 1) ^ 1, p.status, abort);
         if (!w) return false;
         tc_fence_after();
-        const uint64_t so = static_cast<uint64_t>((s * kStageBytes) >> 4);
+        const uint64_t so = static_cast<uint64_t>((s * kKStageBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < 12; ++k)  // K = 192: three 64-column chunks of four K steps
           mma_ss(tmem + kTmemS + 128 * buf, d_q + (k >> 2) * (kChunk >> 4) + (k & 3) * 2,
-                 d_st + so + (k >> 2) * (kChunk >> 4) + (k & 3) * 2, idesc_qk, k > 0 ? 1u : 0u);
+                 d_k + so + (k >> 2) * (kChunk >> 4) + (k & 3) * 2, idesc_qk, k > 0 ? 1u : 0u);
+        mma_commit(smem_u32(&bars.kempty[s]));   // the key stage may be refilled
         mma_commit(smem_u32(&bars.s_full[buf]));
         return true;
       };
       auto issue_pv = [&](int kt) -> bool {
-        if (!mbar_wait(smem_u32(&bars.p_full), kt & 1, p.status, abort)) return false;
+        const int s = kt % kStages, buf = kt & 1;
+        bool w = mbar_wait(smem_u32(&bars.p_full[buf]), (kt >> 1) & 1, p.status, abort);
+        w = w && mbar_wait(smem_u32(&bars.vfull[s]), (kt / kStages) & 1, p.status, abort);
+        if (!w) return false;
         tc_fence_after();
-        const uint64_t vb = d_v + static_cast<uint64_t>(((kt % kStages) * kStageBytes) >> 4);
+        const uint64_t vb = d_v + static_cast<uint64_t>((s * kVStageBytes) >> 4);
 #pragma unroll
         for (int k = 0; k < 8; ++k)  // K = 128 keys
-          mma_ts(tmem + kTmemO, tmem + kTmemP + 8 * k, vb + 128 * k, idesc_pv, (kt > 0 || k > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&bars.empty[kt % kStages]));
-        mma_commit(smem_u32(&bars.pv_done));
+          mma_ts(tmem + kTmemO, tmem + kTmemP + 64 * buf + 8 * k, vb + 128 * k, idesc_pv, (kt > 0 || k > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&bars.vempty[s]));
+        mma_commit(smem_u32(&bars.pv_done[buf]));
         return true;
       };
-      if (ok) ok = issue_qk(0);
-      for (int kt = 0; kt < n_kt && ok; ++kt) {
-        if (kt + 1 < n_kt) ok = issue_qk(kt + 1);
-        if (ok) ok = issue_pv(kt);
+      if (warp == 1) {
+        for (int kt = 0; kt < n_kt && ok; ++kt) ok = issue_qk(kt);
+      } else {
+        for (int kt = 0; kt < n_kt && ok; ++kt) ok = issue_pv(kt);
       }
       if (!ok) {
         record_status(p.status, MLA_ERR_TIMEOUT);
@@ -250,20 +298,32 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       // keys kt*128 + c visible to this query: c < n_vis
       const int n_vis = live ? max(0, min(kKTile, pos + 1 - kt * kKTile)) : (kt == 0 ? 1 : 0);
       float sv[128];
+      {
+        uint32_t v[4][32];  // all four loads in flight, one wait
 #pragma unroll
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kTmemS + 128 * buf + c0, v);
+        for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + kTmemS + 128 * buf + 32 * q, v[q]);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) sv[c0 + c] = __uint_as_float(v[c]);
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int c = 0; c < 32; ++c) sv[32 * q + c] = __uint_as_float(v[q][c]);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.s_free[buf]));  // QK^T of key tile kt + 2 may overwrite the buffer
-      float mx = -INFINITY;
+      // row max over the visible columns: eight independent chains (one warp per
+      // SM sub-partition leaves no other warp to hide a 128-long dependent chain)
+      float m8[8];
 #pragma unroll
-      for (int c = 0; c < 128; ++c)
-        if (c < n_vis) mx = fmaxf(mx, sv[c]);
+      for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+      if (n_vis >= kKTile) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c < n_vis) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+      }
+      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       mx *= kScaleL2;
       float factor = 1.f;
       bool rescale = false;
@@ -275,25 +335,37 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
         rescale = true;
       }
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+      // P = 2^(S scale - m): exponent arguments on packed fp32 pairs; the row sum
+      // adds the bf16-rounded P that P V uses, in four independent pair chains
       uint32_t pk[64];
-      float sum = 0.f;
+      const uint64_t scale2 = f32x2(kScaleL2, kScaleL2), negm2 = f32x2(neg_m, neg_m);
+      uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        float p0 = ex2_approx(fmaf(sv[2 * c], kScaleL2, neg_m));
-        float p1 = ex2_approx(fmaf(sv[2 * c + 1], kScaleL2, neg_m));
+        const float2 e = f32x2_split(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), scale2, negm2));
+        float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
         if (2 * c >= n_vis) p0 = 0.f;
         if (2 * c + 1 >= n_vis) p1 = 0.f;
         pk[c] = pack_bf16x2(p0, p1);
-        sum += __uint_as_float(pk[c] << 16) + __uint_as_float(pk[c] & 0xffff0000u);
+        s4[c & 3] = add_f32x2(s4[c & 3], f32x2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u)));
       }
+      const float2 s2 = f32x2_split(add_f32x2(add_f32x2(s4[0], s4[1]), add_f32x2(s4[2], s4[3])));
+      const float sum = s2.x + s2.y;
       l = l * factor + sum;
-      // O and P may only be touched once the previous P V has finished
-      if (kt > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done), (kt - 1) & 1, p.status, abort));
+      // P buffer kt & 1 is free once P V(kt - 2) has finished; O may only be
+      // rescaled once P V(kt - 1) has
+      if (kt >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done[buf]), ((kt - 2) >> 1) & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, rescale)) {
+        if (kt >= 1) {
+          ok = __all_sync(0xffffffffu,
+                          mbar_wait(smem_u32(&bars.pv_done[buf ^ 1]), ((kt - 1) >> 1) & 1, p.status, abort));
+          if (!ok) break;
+          tc_fence_after();
+        }
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + kTmemO + c0, v);
@@ -303,14 +375,15 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
           tmem_st32(tmem + lane_off + kTmemO + c0, v);
         }
       }
-      tmem_st32(tmem + lane_off + kTmemP, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tmem + lane_off + kTmemP + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st32(tmem + lane_off + kTmemP + 64 * buf, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tmem_st32(tmem + lane_off + kTmemP + 64 * buf + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars.p_full));
+      mbar_arrive(smem_u32(&bars.p_full[buf]));
     }
     if (ok && n_kt > 0)
-      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.pv_done), (n_kt - 1) & 1, p.status, abort));
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(smem_u32(&bars.pv_done[(n_kt - 1) & 1]), ((n_kt - 1) >> 1) & 1, p.status, abort));
     tc_fence_after();
     // epilogue: O / l as bf16, and the natural log-sum-exp.  tcgen05.ld is a
     // warp-wide instruction, so every lane loads and only live rows store.
