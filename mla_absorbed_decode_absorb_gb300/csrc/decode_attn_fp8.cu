@@ -19,12 +19,14 @@
 // and give P V the operand P_t s_t, so that O' = sum_t p_t s_t E4M3(code_t).
 //
 // Pipeline per CTA (cluster of two, CTA r owns latent columns [256r, 256r+256)
-// as in the bf16 kernel): warp 0 loads each page's 16 KB of codes, 4 KB of
-// key and 256 B of scales by TMA into a 2-slot landing ring; warps 12-15 widen
-// the codes into a 3-slot ring of float16 stages (the landing slot is free again
-// right away, so the float16 stage's life does not include the load latency);
-// warp 1 issues QK^T, warp 2 P V, warp 3 recycles the exchange buffers, and
-// warps 4-11 are the two row warpgroups.  Score exchange, lazy reference max,
+// as in the bf16 kernel): warps 12-15 read each page's 16 KB of codes and 64
+// scales straight from global memory into registers (issued before they wait
+// for the stage; they run up to three pages ahead of the MMAs) and widen the
+// codes into a 4-slot ring of float16 stages; warp 0
+// loads the page's 4 KB of key by TMA into the stage (its layout is the
+// stage's) and pulls the next page's codes into L2; warp 1 issues QK^T, warp 2
+// P V, warp 3 recycles the exchange buffers, and warps 4-11 are the two row
+// warpgroups.  Without a landing ring for the codes, four float16 stages fit.  Score exchange, lazy reference max,
 // packed softmax arithmetic, TMEM layout and epilogue follow the bf16 kernel.
 #include <cuda_fp16.h>
 
@@ -36,8 +38,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kStages = 3;          // float16 stages the MMAs read
-constexpr int kF8Stages = 2;        // landing slots of the loads
+constexpr int kStages = 4;          // float16 stages the MMAs read
 constexpr int kThreads = 512;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -55,13 +56,6 @@ constexpr int kQRope = 128 * 64;      // 32 RoPE query columns x 128 heads, 64-b
 constexpr int kPChunk = 64 * 128;     // 64 latent columns x 64 tokens, f16 (SW128)
 constexpr int kPRope = 64 * 64;       // 32 RoPE columns x 64 tokens, f16 (SW64)
 constexpr int kStageBytes = 4 * kPChunk + kPRope;
-// landing slot: four boxes of 64 codes x 64 tokens (64-byte swizzle), the key
-// box (as in the stage), 64 scales
-constexpr int kF8Chunk = 64 * 64;
-constexpr int kF8OffKey = 4 * kF8Chunk;
-constexpr int kF8OffScale = kF8OffKey + kPRope;
-constexpr uint32_t kF8TxBytes = kF8OffScale + 64 * 4;
-constexpr int kF8SlotBytes = 21 * 1024;
 constexpr int kXBufBytes = kRowThreads * 128;
 constexpr uint32_t kXTxBytes = kXBufBytes;
 constexpr float kSumScaleLog2 = kScaleLog2 * 256.f;
@@ -69,29 +63,24 @@ constexpr int kPBytes = kHeads * 128;
 
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kOffQ + kQRope;
-constexpr int kOffF8 = kOffStage + kStages * kStageBytes;
-constexpr int kOffX = kOffF8 + kF8Stages * kF8SlotBytes;
+constexpr int kOffX = kOffStage + kStages * kStageBytes;
 constexpr int kOffP = kOffX + 2 * kXBufBytes;
 constexpr int kOffSc = kOffP + 2 * kPBytes;     // per stage: 64 x s_t / 256, then 64 x s_t
 constexpr int kOffBar = kOffSc + kStages * 512;
 constexpr int kOffMax = kOffBar + 256;          // per-row reference max handed between warpgroups
 constexpr int kSmemBytes = kOffMax + 4 * kHeads + 1024;  // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffF8 % 1024 == 0 && kF8SlotBytes % 1024 == 0 &&
-                  kOffX % 1024 == 0 && kOffP % 1024 == 0,
+static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffX % 1024 == 0 && kOffP % 1024 == 0,
               "swizzled tiles start on 1 KB");
-static_assert(kF8TxBytes <= kF8SlotBytes, "landing slot");
 
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kOBoxBytes = 128 * 128;
 constexpr int kOTileBytes = 4 * kOBoxBytes;
-static_assert(2 * kOTileBytes <= kOffX - kOffStage, "output staging fits in the stages and landing slots");
+static_assert(2 * kOTileBytes <= kOffX - kOffStage, "output staging fits in the stages");
 
 struct Bars {
-  uint64_t full[kStages];       // float16 stage written by the dequantisation warpgroup
+  uint64_t full[kStages];       // float16 stage written (128 dequantisation threads) and its key landed
   uint64_t empty[kStages];      // P V of the stage's page has finished
-  uint64_t f8_full[kF8Stages];  // landing slot loaded
-  uint64_t f8_empty[kF8Stages]; // landing slot widened
   uint64_t q_full;
   uint64_t q_tmem;
   uint64_t s_full[2];
@@ -115,6 +104,7 @@ struct Params {
   const int32_t* kv_lens;
   const uint16_t* q_abs;
   const float* scale;          // [num_pages * 64]
+  const uint8_t* c8;           // [num_pages * 64, 512] E4M3 codes
   float* o_out;
   float* lse_out;
   int* status;
@@ -163,12 +153,8 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar_addr(bars.full[s]), kRowThreads);  // the 128 dequantisation threads
+      mbar_init(bar_addr(bars.full[s]), kRowThreads + 1);  // the 128 dequantisation threads + the key's load
       mbar_init(bar_addr(bars.empty[s]), 1);
-    }
-    for (int s = 0; s < kF8Stages; ++s) {
-      mbar_init(bar_addr(bars.f8_full[s]), 1);
-      mbar_init(bar_addr(bars.f8_empty[s]), kRowThreads);
     }
     mbar_init(bar_addr(bars.q_full), 1);
     mbar_init(bar_addr(bars.q_tmem), 2 * kRowThreads);
@@ -211,7 +197,7 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
   if (tid == 0 && bad && rank == 0) record_status(p.status, MLA_ERR_BOUNDS);
 
   if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ loads into the landing slots
+    // ------------------------------------------------------------ keys into the stages, codes into L2
     if (n_pages > 0) {
       const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride + page_begin;
       int ids = lane < n_pages ? pt[lane] : 0;
@@ -229,21 +215,24 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
         for (int k = 0; k < cnt && ok; ++k) {
           const int i = base + k;
           int page = __shfl_sync(0xffffffffu, ids, k);
+          const int ahead_a = __shfl_sync(0xffffffffu, ids, (k + 1) & 31);
+          const int ahead_b = __shfl_sync(0xffffffffu, ids_next, (k + 1) & 31);
           if (lane == 0) {
-            const int s = i % kF8Stages;
-            ok = mbar_wait(bar_addr(bars.f8_empty[s]), ((i / kF8Stages) & 1) ^ 1, p.status, abort);
+            // the codes of the page after this one into L2, for the dequantisation warps' loads
+            const int ahead = k + 1 < 32 ? ahead_a : ahead_b;
+            if (i + 1 < n_pages && ahead >= 0 && ahead < p.num_pages)
+              for (int c = 0; c < 4; ++c) tma_prefetch_l2_2d(&tm_c8, 64 * (4 * rank + c), ahead * kPage);
+            const int s = i % kStages;
+            ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
             if (ok) {
               if (page < 0 || page >= p.num_pages) {
                 record_status(p.status, MLA_ERR_BOUNDS);
                 page = 0;
               }
-              uint8_t* slot = smem + kOffF8 + s * kF8SlotBytes;
-              const uint32_t fb = bar_addr(bars.f8_full[s]);
-              mbar_arrive_expect_tx(fb, kF8TxBytes);
-              for (int c = 0; c < 4; ++c)
-                tma_load_2d(smem_u32(slot + c * kF8Chunk), &tm_c8, 64 * (4 * rank + c), page * kPage, fb);
-              tma_load_2d(smem_u32(slot + kF8OffKey), &tm_kr, 32 * rank, page * kPage, fb);
-              bulk_load(smem_u32(slot + kF8OffScale), p.scale + static_cast<int64_t>(page) * kPage, 64 * 4, fb);
+              uint8_t* stage = smem + kOffStage + s * kStageBytes;
+              const uint32_t fb = bar_addr(bars.full[s]);
+              mbar_arrive_expect_tx(fb, kPRope);
+              tma_load_2d(smem_u32(stage + 4 * kPChunk), &tm_kr, 32 * rank, page * kPage, fb);
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -254,21 +243,44 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
     }
   } else if (warp >= kDqWarp0) {
     // ------------------------------------------------------------ codes -> float16 stages
+    // Thread dt reads the 16-code pieces q = dt + 128 r (r < 8) of the CTA's 16 KB of
+    // the page: token t = q / 16, codes [16 (q % 16), +16) of its 256 columns, i.e.
+    // float16 chunk c = (q % 16) / 4, units 2 ((q % 16) % 4) and + 1 of row t (128-byte
+    // swizzle: unit u of row t at t * 128 + (u ^ (t & 7)) * 16).  A warp's loads cover
+    // two tokens' 256 contiguous bytes each.
     const int dt = tid - kDqWarp0 * 32;  // 0..127
+    const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride + page_begin;
+    int ids = lane < n_pages ? pt[lane] : 0;
+    int ids_next = 32 + lane < n_pages ? pt[32 + lane] : 0;
+    uint4 cur[8];
+    float sc_cur = 0.f;
+    int base = 0;  // the first page of the ids / ids_next window
     for (int i = 0; i < n_pages; ++i) {
-      const int s8 = i % kF8Stages, s = i % kStages;
-      if (!mbar_wait(bar_addr(bars.f8_full[s8]), (i / kF8Stages) & 1, p.status, abort)) break;
-      if (!mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort)) break;
-      const uint8_t* slot = smem + kOffF8 + s8 * kF8SlotBytes;
+      if (i - base == 32) {  // slide the page-id window
+        base += 32;
+        ids = ids_next;
+        ids_next = base + 32 + lane < n_pages ? pt[base + 32 + lane] : 0;
+      }
+      int pg = __shfl_sync(0xffffffffu, ids, i - base);
+      if (pg < 0 || pg >= p.num_pages) pg = 0;  // out of range: reported by the producer
+      {
+        const uint8_t* src = p.c8 + static_cast<int64_t>(pg) * kPage * kLatent + 256 * rank;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          const int q = dt + 128 * r;
+          cur[r] = *reinterpret_cast<const uint4*>(src + (q >> 4) * kLatent + (q & 15) * 16);
+        }
+        sc_cur = dt < 64 ? p.scale[static_cast<int64_t>(pg) * kPage + dt] : 0.f;
+      }
+      const int s = i % kStages;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort)))
+        break;
       uint8_t* stage = smem + kOffStage + s * kStageBytes;
-      // chunk c, token t, 16-code unit u: codes at t * 64 + (u ^ ((t >> 1) & 3)) * 16 (64-byte
-      // swizzle); float16 at t * 128 + ((2u + h) ^ (t & 7)) * 16, h = 0, 1 (128-byte swizzle)
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const int item = r * 128 + dt;          // 1024 items: 4 chunks x 64 tokens x 4 units
-        const int c = item >> 8, t = (item >> 2) & 63, u = item & 3;
-        const uint4 v = *reinterpret_cast<const uint4*>(slot + c * kF8Chunk + t * 64 + ((u ^ ((t >> 1) & 3)) << 4));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const int q = dt + 128 * r;
+        const int t = q >> 4, c = (q & 15) >> 2, u = q & 3;
+        const uint32_t w[4] = {cur[r].x, cur[r].y, cur[r].z, cur[r].w};
         uint32_t h[8];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -279,20 +291,12 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
         *reinterpret_cast<uint4*>(row + (((2 * u) ^ (t & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
         *reinterpret_cast<uint4*>(row + (((2 * u + 1) ^ (t & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
       }
-      // the key box has the stage's layout already: copy its 4 KB
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int off = (r * 128 + dt) * 16;
-        *reinterpret_cast<uint4*>(stage + 4 * kPChunk + off) = *reinterpret_cast<const uint4*>(slot + kF8OffKey + off);
-      }
       if (dt < 64) {
-        const float st = reinterpret_cast<const float*>(slot + kF8OffScale)[dt];
         float* sc = reinterpret_cast<float*>(smem + kOffSc + s * 512);
-        sc[dt] = st * (1.f / 256.f);  // exact
-        sc[64 + dt] = st;
+        sc[dt] = sc_cur * (1.f / 256.f);  // exact
+        sc[64 + dt] = sc_cur;
       }
       fence_proxy_async_smem();  // the stage is read by the MMAs
-      mbar_arrive(bar_addr(bars.f8_empty[s8]));
       mbar_arrive(bar_addr(bars.full[s]));
     }
   } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -659,6 +663,7 @@ cudaError_t launch_decode_partial_fp8(const uint16_t* q_abs, const uint8_t* cach
   prm.kv_lens = kv_lens;
   prm.q_abs = q_abs;
   prm.scale = cache_scale;
+  prm.c8 = cache_c8;
   prm.o_out = o_out;
   prm.lse_out = lse_out;
   prm.status = status;
