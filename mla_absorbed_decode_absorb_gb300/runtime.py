@@ -2,8 +2,8 @@
 
 A :class:`DecodeSession` owns (as torch tensors) the weights, the paged cache
 with each sequence's history already appended, the page table, the RoPE table,
-the step's inputs and every output/workspace buffer, so that a step is just the
-four ABI calls with no allocation:
+the step's inputs and every output/workspace buffer, so that a step is just
+these ABI calls with no allocation (three launches with the defaults below):
 
 1. ``mla_append_kv``           -- write this step's n_q tokens into the cache;
 2. ``mla_absorb_q``            -- ``q_abs = [q^C W_UK ; RoPE(q^R)]``;
