@@ -11,8 +11,10 @@ Printed (rank 0, one JSON line): ``value`` = latent-cache bytes the step reads
 divided by the mean step time (device time from CUDA events on the launching
 stream, L2 flushed before every step, inputs resident in HBM).  ``e2e`` repeats
 the measurement through the same calls with the step's inputs copied from
-pinned host memory and the output copied back inside the timed region (both
-by ``mla_copy_async``: the GPU's own loads and stores over the host link).
+pinned host memory and the output copied back inside the timed region (the
+upload by ``mla_copy_async``, the GPU's own loads over the host link; the
+decode step's out-projection stores its result straight into the pinned
+host buffer, other steps download it with ``mla_copy_async``).
 ``roofline`` rates the split-attention kernel against the measured HBM copy
 bandwidth (or dense bf16 peak when FLOPs bind).  ``cpu_baseline`` times the
 fp64 CPU oracle on a bounded sample of the same workload.
@@ -472,8 +474,7 @@ def run_ours(args, wl):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             s.upload(host_in)
-            s.step()
-            s.download(host_out)
+            s.step(host_out=host_out)
             b.record(stream)
             b.synchronize()
             if k >= 3:

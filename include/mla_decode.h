@@ -340,7 +340,10 @@ mla_status mla_decode_attn_noalloc(const mla_bf16* q_abs, const mla_bf16* cache,
  *
  *   o_latent [B, n_q, 128, 512] float32 (from mla_decode_attn)
  *   w_uv     [128, 128, 512] bf16   W_UV[h][d][m]
- *   out      [B, n_q, 128, 128] bf16 out
+ *   out      [B, n_q, 128, 128] bf16 out: device memory, or pinned host memory
+ *            mapped into the device's address space (the kernel then stores the
+ *            result across the host link itself: no separate download); 16-byte
+ *            aligned; pageable host memory gives MLA_ERR_INVALID_ARG
  *
  * o_latent is rounded to bf16 before the product; accumulation is float32.
  */
@@ -359,7 +362,8 @@ mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16*
  *   o_latent   [B, n_q, 128, 512] float32: read only when the plan has a single
  *              split (mla_decode_attn_partial then wrote the final O' there)
  *   w_uv       [128, 128, 512] bf16   W_UV[h][d][m]
- *   out        [B, n_q, 128, 128] bf16 out
+ *   out        [B, n_q, 128, 128] bf16 out: device memory or mapped pinned host
+ *              memory, as in mla_out_absorb
  *   lse        [B, n_q, 128] float32 out (nullable), written only when there is
  *              more than one split (otherwise the partial call already wrote it)
  *

@@ -344,6 +344,23 @@ mla_status mla_append_absorb_q_fp8(const mla_bf16* c_kv_new, const mla_bf16* k_p
                                               cache_kr, num_pages, q_abs, B, n_q, st, stream));
 }
 
+// An output buffer that may be pinned host memory: its device address (the
+// kernels store to it across the host link), or the pointer itself for device
+// memory.  False for pageable host memory or a range outside the allocation.
+bool output_view(void* p, size_t bytes, void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeUnregistered) {
+    *out = p;
+    return true;
+  }
+  bool host = false;
+  return device_view(p, bytes, out, &host);
+}
+
 mla_status mla_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
   if (bytes == 0) return MLA_OK;
   if (dst == nullptr || src == nullptr) return MLA_ERR_INVALID_ARG;
@@ -426,10 +443,12 @@ mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16*
   if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ) return MLA_ERR_INVALID_ARG;
   if (B == 0) return MLA_OK;
   if (!o_latent || !w_uv || !out) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(o_latent) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  void* od = nullptr;
+  if (!output_view(out, static_cast<size_t>(B) * n_q * kHeads * kNope * 2, &od)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_latent) || !aligned16(w_uv) || !aligned16(od)) return MLA_ERR_INVALID_ARG;
   int* st = status_ptr();
   if (st == nullptr) return MLA_ERR_CUDA;
-  return from_cuda(launch_out_absorb(o_latent, w_uv, out, B, n_q, st, stream));
+  return from_cuda(launch_out_absorb(o_latent, w_uv, static_cast<uint16_t*>(od), B, n_q, st, stream));
 }
 
 mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_pages,
@@ -439,13 +458,17 @@ mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_page
   if (!make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
   if (B == 0) return MLA_OK;
   if (plan.num_splits == 1) return mla_out_absorb(o_latent, w_uv, out, B, n_q, stream);
-  if (!w_uv || !out || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  if (!w_uv || !out) return MLA_ERR_INVALID_ARG;
+  void* od = nullptr;
+  if (!output_view(out, static_cast<size_t>(B) * n_q * kHeads * kNope * 2, &od)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(w_uv) || !aligned16(od)) return MLA_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return MLA_ERR_WORKSPACE;
   int* st = status_ptr();
   if (st == nullptr) return MLA_ERR_CUDA;
   const float* o_part = static_cast<const float*>(workspace);
   const float* lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + plan.o_part_bytes);
-  return from_cuda(launch_combine_out_absorb(o_part, lse_part, plan.num_splits, w_uv, out, lse, B, n_q, st, stream));
+  return from_cuda(launch_combine_out_absorb(o_part, lse_part, plan.num_splits, w_uv, static_cast<uint16_t*>(od), lse,
+                                             B, n_q, st, stream));
 }
 
 mla_status mla_decompress_kv(const mla_bf16* cache, int64_t num_pages, const int32_t* page_table, int pt_stride,

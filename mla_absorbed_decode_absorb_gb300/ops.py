@@ -95,6 +95,18 @@ def _stream(stream) -> int:
     return int(stream)
 
 
+def _dev_or_pinned(t: torch.Tensor, name: str, dtype, shape=None) -> int:
+    """An output the kernels may store to across the host link: a CUDA tensor, or a
+    pinned (page-locked) host tensor."""
+    if isinstance(t, torch.Tensor) and t.device.type == "cpu":
+        if not t.is_pinned():
+            raise ValueError(f"{name} is pageable host memory: pin it (tensor.pin_memory())")
+        if t.dtype != dtype or not t.is_contiguous() or (shape is not None and tuple(t.shape) != tuple(shape)):
+            raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {shape}")
+        return t.data_ptr()
+    return _dev(t, name, dtype, shape)
+
+
 def _dev(t: torch.Tensor, name: str, dtype, shape=None) -> int:
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
@@ -414,7 +426,7 @@ def mla_out_absorb(o_latent, w_uv, out=None, stream=None):
     _check("mla_out_absorb", lib.mla_out_absorb(
         _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
         _dev(w_uv, "w_uv", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
-        _dev(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        _dev_or_pinned(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
         int(B), int(n_q), _stream(stream)))
     return out
 
@@ -430,7 +442,7 @@ def mla_combine_out_absorb(B, n_q, max_kv_len, split_pages, workspace, o_latent,
         0 if workspace is None else workspace.numel(),
         0 if o_latent is None else _dev(o_latent, "o_latent", torch.float32, (B, n_q, N_HEADS, D_LATENT)),
         _dev(w_uv, "w_uv", torch.bfloat16, (N_HEADS, D_NOPE, D_LATENT)),
-        _dev(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
+        _dev_or_pinned(out, "out", torch.bfloat16, (B, n_q, N_HEADS, D_NOPE)),
         0 if lse is None else _dev(lse, "lse", torch.float32, (B, n_q, N_HEADS)),
         _stream(stream)))
     return out

@@ -196,12 +196,13 @@ class DecodeSession:
         ops.mla_decode_combine(self.B, self.n_q, self.max_kv_len, self.split_pages, self.workspace,
                                self.o_latent, self.lse, stream=stream)
 
-    def project_out(self, stream=None):
-        ops.mla_out_absorb(self.o_latent, self.w_uv, self.out, stream=stream)
+    def project_out(self, stream=None, out=None):
+        ops.mla_out_absorb(self.o_latent, self.w_uv, self.out if out is None else out, stream=stream)
 
-    def finish(self, stream=None):
+    def finish(self, stream=None, out=None):
         ops.mla_combine_out_absorb(self.B, self.n_q, self.max_kv_len, self.split_pages, self.workspace,
-                                   self.o_latent, self.w_uv, self.out, self.lse, stream=stream)
+                                   self.o_latent, self.w_uv, self.out if out is None else out, self.lse,
+                                   stream=stream)
 
     def decompress(self, stream=None):
         if self.overlap_append:
@@ -220,9 +221,20 @@ class DecodeSession:
         head = ["append_absorb"] if self.fused_prologue else ["append", "absorb"]
         return head + ["attend_partial"] + tail
 
-    def step(self, stream=None):
-        for name in self.stage_names():
+    def step(self, stream=None, host_out: torch.Tensor | None = None):
+        """One decode step; with ``host_out`` (pinned host memory, the shape of ``out``)
+        the result lands there: the out-projection stores it across the host link
+        itself, or (other paths) a download follows."""
+        names = self.stage_names()
+        for name in names[:-1]:
             getattr(self, name)(stream)
+        if host_out is not None and names[-1] in ("finish", "project_out"):
+            getattr(self, names[-1])(stream, out=host_out)
+            return host_out
+        getattr(self, names[-1])(stream)
+        if host_out is not None:
+            self.download(host_out, stream)
+            return host_out
         return self.out
 
     def launches_per_step(self) -> int:
@@ -363,9 +375,12 @@ class LayerSession:
         # the decode stages (append, absorb, attend_partial, finish, ...) run on the decode session
         return getattr(self.__dict__["dec"], name)
 
-    def step(self, stream=None):
+    def step(self, stream=None, host_out: torch.Tensor | None = None):
         for name in self.stage_names():
             getattr(self, name)(stream)
+        if host_out is not None:
+            self.download(host_out, stream)
+            return host_out
         return self.y
 
     def launches_per_step(self) -> int:

@@ -40,6 +40,16 @@ def test_copy_device_and_host(n, offset):
     assert ops.mla_get_device_status() == ops.MLA_OK
 
 
+def test_out_projection_refuses_pageable_output():
+    from mla_absorbed_decode_absorb_gb300 import ops
+    o = torch.zeros(1, 1, 128, 512, dtype=torch.float32, device="cuda")
+    w = torch.zeros(128, 128, 512, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        ops.mla_out_absorb(o, w, torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16))
+    pageable = torch.zeros(1, 1, 128, 128, dtype=torch.bfloat16)
+    assert ops.lib.mla_out_absorb(o.data_ptr(), w.data_ptr(), pageable.data_ptr(), 1, 1, 0) == ops.MLA_ERR_INVALID_ARG
+
+
 def test_copy_refusals():
     from mla_absorbed_decode_absorb_gb300 import ops
     dev = torch.zeros(256, dtype=torch.uint8, device="cuda")
@@ -76,5 +86,16 @@ def test_step_through_host_buffers(level):
         torch.cuda.synchronize()
         assert ops.mla_get_device_status() == ops.MLA_OK
         assert torch.equal(host_out.view(torch.int16), ref.out.cpu().view(torch.int16))
+        # the out-projection storing straight into the pinned buffer
+        host_out.zero_()
+        for fused in (True, False):
+            t = DecodeSession(inp, fused_finish=fused)
+            t.step_buffer.zero_()
+            t.upload(host_in)
+            assert t.step(host_out=host_out) is host_out
+            torch.cuda.synchronize()
+            assert ops.mla_get_device_status() == ops.MLA_OK
+            assert torch.equal(host_out.view(torch.int16), ref.out.cpu().view(torch.int16))
+            host_out.zero_()
     finally:
         ops.mla_set_launch_overlap(before)
