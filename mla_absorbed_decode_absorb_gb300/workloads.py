@@ -83,6 +83,9 @@ PREFILL_WORKLOADS: dict[str, Workload] = {
                  description="B=4, a chunk of 512 new tokens each after a prior context of 4096"),
         Workload("prompt_b8_c2048", batch=8, n_q=2048, context=0,
                  description="B=8, a 2048-token prompt each, no prior context"),
+        Workload("chunk_b1_l4096_c512", batch=1, n_q=512, context=4096,
+                 description="B=1, a chunk of 512 new tokens after 4096 (the chunk case at the size "
+                             "a full counter capture handles)"),
     ]
 }
 
