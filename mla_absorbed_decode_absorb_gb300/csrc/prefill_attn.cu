@@ -32,10 +32,13 @@ using namespace sm100;
 constexpr int kQTile = 128;
 constexpr int kKTile = 128;
 constexpr int kStages = 2;
-// warp 0 key TMA, warp 1 QK^T issuer, warps 2-5 softmax, warp 6 value TMA, warp 7 P V issuer
-constexpr int kThreads = 256;
-constexpr int kVWarp = 6;
-constexpr int kPvWarp = 7;
+// warp 0 key TMA, warp 1 QK^T issuer, warps 2-9 softmax (two per query row),
+// warp 10 value TMA, warp 11 P V issuer
+constexpr int kThreads = 384;
+constexpr int kSoftWarp0 = 2;
+constexpr int kVWarp = 10;
+constexpr int kPvWarp = 11;
+constexpr int kSoftThreads = 256;
 constexpr int kChunk = 128 * 128;   // 128 rows x 64 bf16 columns (SW128)
 constexpr int kOffQ = 0;            // query: 3 chunks (q^C 0-63, q^C 64-127, RoPE(q^R))
 constexpr int kKStageBytes = 3 * kChunk;  // keys 2 chunks, RoPE keys 1
@@ -43,7 +46,8 @@ constexpr int kVStageBytes = 2 * kChunk;  // values 2 chunks
 constexpr int kOffK = kOffQ + 3 * kChunk;
 constexpr int kOffV = kOffK + kStages * kKStageBytes;
 constexpr int kOffBar = kOffV + kStages * kVStageBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kOffHx = kOffBar + 256;           // half-row maxima [4][2][128], then row sums [2][128]
+constexpr int kSmemBytes = kOffHx + 4 * (4 * 2 * 128 + 2 * 128) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 constexpr uint32_t kTmemO = 0;      // O: [0, 128)
 constexpr uint32_t kTmemS = 128;    // two score buffers: [128, 256), [256, 384)
@@ -60,6 +64,8 @@ struct Bars {
   uint64_t s_free[2];
   uint64_t p_full[2];
   uint64_t pv_done[2];
+  uint64_t hx[2];      // both halves of every row have published their half-row max
+  uint64_t fin;        // both halves have published their row sums
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -103,11 +109,13 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
     mbar_init(smem_u32(&bars.q_ready), 128);
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.s_full[s]), 1);
-      mbar_init(smem_u32(&bars.s_free[s]), 128);
-      mbar_init(smem_u32(&bars.p_full[s]), 128);
+      mbar_init(smem_u32(&bars.s_free[s]), kSoftThreads);
+      mbar_init(smem_u32(&bars.p_full[s]), kSoftThreads);
+      mbar_init(smem_u32(&bars.hx[s]), kSoftThreads);
       mbar_init(smem_u32(&bars.pv_done[s]), 1);
     }
     mbar_init(smem_u32(&bars.drain), 2);  // both issuers
+    mbar_init(smem_u32(&bars.fin), kSoftThreads);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -244,15 +252,23 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax: one thread per query
+    // ------------------------------------------------------------ softmax: two threads per query
+    // Thread (row r, half hf) owns the key columns [64 hf, 64 hf + 64) of every key
+    // tile and the output columns [64 hf, 64 hf + 64): the two halves of a row sit
+    // in warps w and w + 4 (same TMEM lanes, same SM sub-partition), so one's
+    // exponentials overlap the other's loads and waits.  They swap their half-row
+    // maxima through shared memory and take identical decisions from them.
     const int quad = warp & 3;
+    const int hf = (warp - kSoftWarp0) >> 2;
     const int r = quad * 32 + lane;       // query row of the tile (TMEM lane)
     const int j = j0 + r;                 // query index in the chunk
     const bool live = j < p.n_q;
     const int pos = L + j;                // its position: sees keys 0 .. pos
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    // query row: [q^C ; RoPE(q^R, pos)] into the three SW128 chunks
-    {
+    float* hmax = reinterpret_cast<float*>(smem + kOffHx);  // [4 tiles][2 halves][128 rows]
+    float* fin = hmax + 4 * 2 * kQTile;                      // [2 halves][128 rows]
+    // query row: [q^C ; RoPE(q^R, pos)] into the three SW128 chunks (half 0)
+    if (hf == 0) {
       const int64_t qrow = (static_cast<int64_t>(b) * p.n_q + j) * kHeads + h;
       uint8_t* qs = smem + kOffQ;
       if (live && !bad) {
@@ -288,6 +304,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       mbar_arrive(smem_u32(&bars.q_ready));
     }
     constexpr float kScaleL2 = kScaleLog2;
+    const int c_off = 64 * hf;            // this thread's first key column of a tile
     float m_ref = -INFINITY, l = 0.f;
     bool ok = n_kt > 0;
     for (int kt = 0; kt < n_kt && ok; ++kt) {
@@ -295,35 +312,43 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.s_full[buf]), (kt >> 1) & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after();
-      // keys kt*128 + c visible to this query: c < n_vis
+      // keys kt*128 + c visible to this query: c < n_vis; this thread's columns c_off + c, c < n_mine
       const int n_vis = live ? max(0, min(kKTile, pos + 1 - kt * kKTile)) : (kt == 0 ? 1 : 0);
-      float sv[128];
+      const int n_mine = max(0, min(64, n_vis - c_off));
+      float sv[64];
       {
-        uint32_t v[4][32];  // all four loads in flight, one wait
+        uint32_t v[2][32];  // both loads in flight, one wait
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + kTmemS + 128 * buf + 32 * q, v[q]);
+        for (int q = 0; q < 2; ++q) tmem_ld32(tmem + lane_off + kTmemS + 128 * buf + c_off + 32 * q, v[q]);
         tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
 #pragma unroll
           for (int c = 0; c < 32; ++c) sv[32 * q + c] = __uint_as_float(v[q][c]);
       }
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.s_free[buf]));  // QK^T of key tile kt + 2 may overwrite the buffer
-      // row max over the visible columns: eight independent chains (one warp per
-      // SM sub-partition leaves no other warp to hide a 128-long dependent chain)
+      // half-row max in eight independent chains, then the row max from both halves
       float m8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
-      if (n_vis >= kKTile) {
+      if (n_mine >= 64) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+        for (int c = 0; c < 64; ++c) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
       } else {
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c < n_vis) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
+        for (int c = 0; c < 64; ++c)
+          if (c < n_mine) m8[c & 7] = fmaxf(m8[c & 7], sv[c]);
       }
-      float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mh = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // the slot of tile kt is written again at tile kt + 4, after P V(kt) (which needs
+      // the partner's P of tile kt, written after it read this value) has finished
+      float* hx = hmax + (kt & 3) * 2 * kQTile;
+      hx[hf * kQTile + r] = mh;
+      mbar_arrive(smem_u32(&bars.hx[buf]));
+      ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.hx[buf]), (kt >> 1) & 1, p.status, abort));
+      if (!ok) break;
+      float mx = fmaxf(mh, hx[(hf ^ 1) * kQTile + r]);
       mx *= kScaleL2;
       float factor = 1.f;
       bool rescale = false;
@@ -337,21 +362,20 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
       // P = 2^(S scale - m): exponent arguments on packed fp32 pairs; the row sum
       // adds the bf16-rounded P that P V uses, in four independent pair chains
-      uint32_t pk[64];
+      uint32_t pk[32];
       const uint64_t scale2 = f32x2(kScaleL2, kScaleL2), negm2 = f32x2(neg_m, neg_m);
       uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const float2 e = f32x2_split(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), scale2, negm2));
         float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
-        if (2 * c >= n_vis) p0 = 0.f;
-        if (2 * c + 1 >= n_vis) p1 = 0.f;
+        if (2 * c >= n_mine) p0 = 0.f;
+        if (2 * c + 1 >= n_mine) p1 = 0.f;
         pk[c] = pack_bf16x2(p0, p1);
         s4[c & 3] = add_f32x2(s4[c & 3], f32x2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u)));
       }
       const float2 s2 = f32x2_split(add_f32x2(add_f32x2(s4[0], s4[1]), add_f32x2(s4[2], s4[3])));
-      const float sum = s2.x + s2.y;
-      l = l * factor + sum;
+      l = l * factor + (s2.x + s2.y);
       // P buffer kt & 1 is free once P V(kt - 2) has finished; O may only be
       // rescaled once P V(kt - 1) has
       if (kt >= 2) {
@@ -366,17 +390,16 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
           if (!ok) break;
           tc_fence_after();
         }
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           uint32_t v[32];
-          tmem_ld32(tmem + lane_off + kTmemO + c0, v);
+          tmem_ld32(tmem + lane_off + kTmemO + c_off + c0, v);
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) * factor);
-          tmem_st32(tmem + lane_off + kTmemO + c0, v);
+          tmem_st32(tmem + lane_off + kTmemO + c_off + c0, v);
         }
       }
-      tmem_st32(tmem + lane_off + kTmemP + 64 * buf, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tmem + lane_off + kTmemP + 64 * buf + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tmem_st32(tmem + lane_off + kTmemP + 64 * buf + 32 * hf, pk);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(smem_u32(&bars.p_full[buf]));
@@ -384,16 +407,21 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
     if (ok && n_kt > 0)
       ok = __all_sync(0xffffffffu,
                       mbar_wait(smem_u32(&bars.pv_done[(n_kt - 1) & 1]), ((n_kt - 1) >> 1) & 1, p.status, abort));
+    // the row sum from both halves (both rescaled against the same reference max)
+    fin[hf * kQTile + r] = l;
+    mbar_arrive(smem_u32(&bars.fin));
+    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.fin), 0, p.status, abort)) && ok;
+    const float lt = fin[r] + fin[kQTile + r];
     tc_fence_after();
-    // epilogue: O / l as bf16, and the natural log-sum-exp.  tcgen05.ld is a
-    // warp-wide instruction, so every lane loads and only live rows store.
+    // epilogue: O / l as bf16 (this thread's 64 columns), and the natural log-sum-exp.
+    // tcgen05.ld is a warp-wide instruction, so every lane loads and only live rows store.
     const int64_t orow = (static_cast<int64_t>(b) * p.n_q + j) * kHeads + h;
-    uint16_t* dst = p.out + orow * kNope;
+    uint16_t* dst = p.out + orow * kNope + c_off;
     if (ok && n_kt > 0) {
-      const float inv = live ? 1.f / l : 0.f;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
+      const float inv = live ? 1.f / lt : 0.f;
+      for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + kTmemO + c0, v);
+        tmem_ld32(tmem + lane_off + kTmemO + c_off + c0, v);
         tmem_wait_ld();
         if (live) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
@@ -405,10 +433,10 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
                                pack_bf16x2(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv));
         }
       }
-      if (live && p.lse != nullptr) p.lse[orow] = (m_ref + log2f(l)) * kLn2;
+      if (live && hf == 0 && p.lse != nullptr) p.lse[orow] = (m_ref + log2f(lt)) * kLn2;
     } else if (live) {
-      for (int c0 = 0; c0 < 128; c0 += 8) *reinterpret_cast<uint4*>(dst + c0) = make_uint4(0, 0, 0, 0);
-      if (p.lse != nullptr) p.lse[orow] = -INFINITY;
+      for (int c0 = 0; c0 < 64; c0 += 8) *reinterpret_cast<uint4*>(dst + c0) = make_uint4(0, 0, 0, 0);
+      if (hf == 0 && p.lse != nullptr) p.lse[orow] = -INFINITY;
     }
   }
   tc_fence_before();
