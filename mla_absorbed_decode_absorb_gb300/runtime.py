@@ -44,6 +44,28 @@ from .workloads import D_LATENT, D_NOPE, D_ROW, N_HEADS, Inputs, empty_cache
 PREFILL_MIN_NEW_TOKENS = 64
 
 
+class StepGraph:
+    """A session's step captured once into a CUDA graph (the session's buffers are
+    fixed, so every replay runs the same kernels on the current step inputs)."""
+
+    def __init__(self, session, warmup: int = 2):
+        self.session = session
+        self.stream = torch.cuda.Stream(device=session.device)
+        self.stream.wait_stream(torch.cuda.current_stream(session.device))
+        with torch.cuda.stream(self.stream):
+            for _ in range(warmup):  # lazy one-time setup (attributes, tables) outside the capture
+                session.step(self.stream)
+        torch.cuda.current_stream(session.device).wait_stream(self.stream)
+        torch.cuda.synchronize(session.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.stream):
+            session.step(self.stream)
+
+    def replay(self):
+        self.graph.replay()
+        return self.session.out
+
+
 class DecodeSession:
     def __init__(self, inp: Inputs, device="cuda", split_pages: int | None = None, stream=None,
                  fused_finish: bool = True, overlap_append: bool = False, path: str | None = None,
@@ -236,6 +258,12 @@ class DecodeSession:
             self.download(host_out, stream)
             return host_out
         return self.out
+
+    def capture(self, warmup: int = 2) -> "StepGraph":
+        """The decode step (its launches and their programmatic dependencies) captured
+        as one CUDA graph: ``replay()`` then costs one launch call on the host instead of
+        one per kernel, which is what bounds short steps issued back to back."""
+        return StepGraph(self, warmup)
 
     def launches_per_step(self) -> int:
         if self.path == "non_absorbed":

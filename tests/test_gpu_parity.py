@@ -155,6 +155,40 @@ def test_fused_append_absorb_matches_separate_calls(lens, n_q):
         assert np.array_equal(bits(x), bits(y))
 
 
+@pytest.mark.parametrize("level", [0, 2])
+def test_graph_replay_matches_eager_steps(level):
+    """A step captured as a CUDA graph gives the eager step's bits, and picks up new
+    step inputs written into the session's buffers between replays."""
+    from mla_absorbed_decode_absorb_gb300 import ops
+    before = ops.mla_get_launch_overlap()
+    ops.mla_set_launch_overlap(level)
+    try:
+        inp = W.generate(W.custom("graph", [5, 700, 4000], n_q=2), seed=14)
+        s = run_session(inp)
+        eager = bits(s.out).copy()
+        g = s.capture()
+        s.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert ops.mla_get_device_status() == ops.MLA_OK
+        assert np.array_equal(bits(s.out), eager)
+        # new step inputs through the same graph, against an eager step on them
+        gen = torch.Generator().manual_seed(15)
+        for t in (s.q_nope, s.q_rope, s.c_new, s.k_new):
+            t.copy_((torch.randn(t.shape, generator=gen) * 0.5).to(t.dtype))
+        g.replay()
+        torch.cuda.synchronize()
+        assert ops.mla_get_device_status() == ops.MLA_OK
+        replayed = (bits(s.q_abs).copy(), bits(s.out).copy())
+        assert not np.array_equal(replayed[1], eager)
+        s.step()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(s.q_abs), replayed[0])
+        assert np.array_equal(bits(s.out), replayed[1])
+    finally:
+        ops.mla_set_launch_overlap(before)
+
+
 def test_launch_overlap_levels_give_identical_results():
     """Programmatic dependent launch only moves prologues (and, at level 2, the
     weight reads) ahead of the previous kernel's completion: same bits."""
