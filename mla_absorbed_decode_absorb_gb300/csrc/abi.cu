@@ -75,16 +75,17 @@ bool device_view(const void* p, size_t bytes, void** out, bool* host) {
   }
   if (a.devicePointer == nullptr) return false;
   *out = a.devicePointer;
-  // the whole range lies inside the one allocation
-  static PFN_cuMemGetAddressRange_v3020 range = nullptr;
-  if (range == nullptr) {
+  // the whole range lies inside the one allocation (the driver entry point is looked
+  // up once; a function-local static is initialised once even under concurrent calls)
+  static const PFN_cuMemGetAddressRange_v3020 range = []() -> PFN_cuMemGetAddressRange_v3020 {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 3020, cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || fn == nullptr)
-      return false;
-    range = reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
-  }
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuMemGetAddressRange_v3020>(fn);
+  }();
+  if (range == nullptr) return false;
   CUdeviceptr base = 0;
   size_t size = 0;
   if (range(&base, &size, reinterpret_cast<CUdeviceptr>(*out)) != CUDA_SUCCESS) return false;

@@ -218,11 +218,13 @@ cudaError_t launch_absorb(const uint16_t* q_nope, const uint16_t* q_rope, const 
                           const uint16_t* w_uk, const float* rope_table, int rope_max_pos, uint16_t* q_abs, int B,
                           int n_q, const AppendArgs& ap, int* status, cudaStream_t stream) {
   const int T = B * n_q;
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[kMaxDevicesLocal] = {};  // the attribute is per device
+  const int dev_ = current_device_index();
+  if (dev_ < 0) return cudaErrorInvalidDevice;
+  if (!configured[dev_]) {
     cudaError_t e = cudaFuncSetAttribute(absorb_q_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev_] = true;
   }
   // W_UK as a [128 * 128, 512] matrix: box 64 columns x 128 rows, 128-byte swizzle
   CUtensorMap tw;

@@ -91,6 +91,15 @@ bool split_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan
 // kernel); 2 as 1, and weight matrices are also read before grid_dep_wait().
 int launch_overlap();
 
+// The current device as an index into per-device tables of at most
+// kMaxDevicesLocal entries, or -1.
+constexpr int kMaxDevicesLocal = 64;
+inline int current_device_index() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesLocal) return -1;
+  return dev;
+}
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                           Args... args) {

@@ -213,13 +213,15 @@ size_t linear_workspace_bytes(int T, int K, int N) {
 cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, int64_t y_ld,
                           int seg, int seg_ld, float* part, int* status, cudaStream_t stream) {
   const int tp = pad16(T);
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[kMaxDevicesLocal] = {};  // the attribute is per device
+  const int dev_ = current_device_index();
+  if (dev_ < 0) return cudaErrorInvalidDevice;
+  if (!configured[dev_]) {
     int most = 0;
     for (int t = 16; t <= 256; t += 16) most = max(most, smem_bytes_for(t));
     cudaError_t e = cudaFuncSetAttribute(linear_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, most);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev_] = true;
   }
   const int split = linear_num_splits(T, K, N);
   const int kbs = K / kKB;

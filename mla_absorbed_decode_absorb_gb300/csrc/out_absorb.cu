@@ -437,11 +437,13 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
 
 cudaError_t launch_stream(const float* src, const float* src_lse, int num_splits, const uint16_t* w_uv, uint16_t* out,
                           float* lse_out, int T, int* status, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[kMaxDevicesLocal] = {};  // the attribute is per device
+  const int dev_ = current_device_index();
+  if (dev_ < 0) return cudaErrorInvalidDevice;
+  if (!configured[dev_]) {
     cudaError_t e = cudaFuncSetAttribute(out_absorb_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmemBytes);
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev_] = true;
   }
   CUtensorMap tw, tp;
   const int S = num_splits;
@@ -463,12 +465,14 @@ cudaError_t launch(const float* src, const float* src_lse, int num_splits, const
   if (T == 0) return cudaSuccess;
   if (num_splits <= kTMaxSplits && (reinterpret_cast<uintptr_t>(src) & 15u) == 0)
     return launch_stream(src, src_lse, num_splits, w_uv, out, lse_out, T, status, stream);
-  static bool configured = false;
-  if (!configured) {
+  static bool configured[kMaxDevicesLocal] = {};  // the attribute is per device
+  const int dev_ = current_device_index();
+  if (dev_ < 0) return cudaErrorInvalidDevice;
+  if (!configured[dev_]) {
     cudaError_t e = cudaFuncSetAttribute(out_absorb_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smem_bytes_for(kNMax, kTableSplits));
     if (e != cudaSuccess) return e;
-    configured = true;
+    configured[dev_] = true;
   }
   // W_UV as a [128 * 128, 512] matrix: box 64 columns x 128 rows, 128-byte swizzle
   CUtensorMap tw;
