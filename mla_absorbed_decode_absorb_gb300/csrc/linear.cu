@@ -19,13 +19,16 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kKB = 64;           // K per stage
+// A stage holds kBoxes consecutive 64-wide K boxes of the CTA's 128 weight rows
+// (and of x): the weight rows are read kBoxes * 128 contiguous bytes at a time.
+constexpr int kBoxes = 2;
+constexpr int kKB = 64 * kBoxes;  // K per stage
 constexpr int kThreads = 128;     // warp 0: TMA, warp 1: MMA; all four: epilogue
 constexpr int kWBox = 128 * 128;  // 128 W rows x 64 K (bf16)
 constexpr int kSmemBudget = 200 * 1024;
 
 __host__ __device__ inline int pad16(int t) { return (t + 15) & ~15; }
-__host__ __device__ inline int stage_bytes(int tp) { return kWBox + tp * 128; }
+__host__ __device__ inline int stage_bytes(int tp) { return kBoxes * (kWBox + tp * 128); }
 constexpr int kMaxStages = 12;
 __host__ __device__ inline int num_stages(int tp) { return min(kMaxStages, kSmemBudget / stage_bytes(tp)); }
 __host__ __device__ inline uint32_t tmem_cols_for(int tp) {
@@ -67,7 +70,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * 128;
   const int kb0 = blockIdx.y * p.kb_per_split;
-  const int nkb = min(p.kb_per_split, p.K / kKB - kb0);
+  const int nkb = min(p.kb_per_split, (p.K + kKB - 1) / kKB - kb0);  // K past the end reads as zeros
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
@@ -96,8 +99,10 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
       uint8_t* st = smem + s * SB;
       mbar_arrive_expect_tx(smem_u32(&full[s]), SB);
       const int k = (kb0 + i) * kKB;
-      tma_load_2d(smem_u32(st), &tm_w, k, n0, smem_u32(&full[s]));
-      tma_load_2d(smem_u32(st + kWBox), &tm_x, k, 0, smem_u32(&full[s]));
+      for (int bx = 0; bx < kBoxes; ++bx) {
+        tma_load_2d(smem_u32(st + bx * kWBox), &tm_w, k + 64 * bx, n0, smem_u32(&full[s]));
+        tma_load_2d(smem_u32(st + kBoxes * kWBox + bx * tp * 128), &tm_x, k + 64 * bx, 0, smem_u32(&full[s]));
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA issuer
@@ -108,11 +113,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
       ok = mbar_wait(smem_u32(&full[s]), (i / S) & 1, p.status);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t a0 = smem_u32(smem + s * SB), b0 = a0 + kWBox;
+      const uint32_t a0 = smem_u32(smem + s * SB), b0 = a0 + kBoxes * kWBox;
 #pragma unroll
       for (int q = 0; q < kKB / 16; ++q)
-        mma_ss(tmem, smem_desc(a0 + q * 32, 16, 1024, kSw128), smem_desc(b0 + q * 32, 16, 1024, kSw128), idesc,
-               (i | q) ? 1u : 0u);
+        mma_ss(tmem, smem_desc(a0 + (q >> 2) * kWBox + (q & 3) * 32, 16, 1024, kSw128),
+               smem_desc(b0 + (q >> 2) * tp * 128 + (q & 3) * 32, 16, 1024, kSw128), idesc, (i | q) ? 1u : 0u);
       mma_commit(smem_u32(&empty[s]));
     }
     if (ok) mma_commit(smem_u32(done));
@@ -185,7 +190,7 @@ int g_sms = 0;
 }  // namespace
 
 // K split so that tiles x splits fills one wave of the GPU (one CTA per SM),
-// each split keeping at least 4 K blocks of 64: a second, partial wave of short
+// each split keeping at least 256 of K: a second, partial wave of short
 // weight streams cost more than it overlapped (W_O, K = 16384: 60.9 -> 55.4 us).
 int linear_num_splits(int T, int K, int N) {
   (void)T;
@@ -195,12 +200,12 @@ int linear_num_splits(int T, int K, int N) {
     if (cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || g_sms <= 0) g_sms = 148;
   }
   const int tiles = (N + 127) / 128;
-  const int kbs = K / kKB;
+  const int kbs = (K + kKB - 1) / kKB;
   int split = max(1, g_sms / tiles);
   // long weight streams (over 128 K blocks per split in one wave) keep a second wave
   // busy: W_OV, K = 65536, streamed faster in two (166 against 183 us)
   if (kbs / split > 128) split = max(1, (2 * g_sms) / tiles);
-  split = min(split, max(1, kbs / 4));
+  split = min(split, max(1, kbs / (4 / kBoxes)));  // at least 256 K per split
   const int per = (kbs + split - 1) / split;
   return (kbs + per - 1) / per;  // no empty split
 }
@@ -224,10 +229,10 @@ cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int
     configured[dev_] = true;
   }
   const int split = linear_num_splits(T, K, N);
-  const int kbs = K / kKB;
+  const int kbs = (K + kKB - 1) / kKB;
   CUtensorMap tx, tw;
-  if (!make_tmap_bf16_2d(&tx, x, T, K, K, kKB, tp, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_bf16_2d(&tw, w, N, K, K, kKB, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!make_tmap_bf16_2d(&tx, x, T, K, K, 64, tp, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_2d(&tw, w, N, K, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   LinParams prm;
   prm.y = y;
