@@ -232,6 +232,20 @@ mla_status mla_linear(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, 
 mla_status mla_linear_strided(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, int K, int N,
                               int64_t y_ld, int seg, int seg_ld, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
+/*
+ * mla_linear_pair -- two projections of the same x in one launch: y0 = x W0^T
+ * [T, N0] and y1 = x W1^T [T, N1], each as mla_linear computes it (fp32
+ * accumulation; K may be split differently from two separate calls, which
+ * only reorders the fp32 sums).  For the pairs of the decode
+ * listing that share their input, W_DKV and W_KR of the hidden state: a launch
+ * and a split-K sum fewer than two calls, which matters when the weights are
+ * small and the projections latency-bound.  workspace: mla_linear_pair_workspace_size
+ * bytes (0 when K is not split).  Arguments and errors otherwise as mla_linear.
+ */
+mla_status mla_linear_pair_workspace_size(int T, int K, int N0, int N1, size_t* bytes);
+mla_status mla_linear_pair(const mla_bf16* x, int T, int K, const mla_bf16* w0, int N0, mla_bf16* y0,
+                           const mla_bf16* w1, int N1, mla_bf16* y1, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
 
 /*
  * Weight pre-folds ("DeepSeek-MLA-Principle", key absorption: when q^C = W_UQ c^Q

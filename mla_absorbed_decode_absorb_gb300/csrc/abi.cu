@@ -266,6 +266,25 @@ mla_status mla_linear(const mla_bf16* x, const mla_bf16* w, mla_bf16* y, int T, 
   return mla_linear_strided(x, w, y, T, K, N, N, N, N, workspace, workspace_bytes, stream);
 }
 
+mla_status mla_linear_pair_workspace_size(int T, int K, int N0, int N1, size_t* bytes) {
+  if (bytes == nullptr || T < 1 || T > MLA_LINEAR_MAX_T || K < 64 || K % 64 != 0 || N0 < 1 || N1 < 1)
+    return MLA_ERR_INVALID_ARG;
+  *bytes = linear_workspace_bytes(T, K, N0, N1);
+  return MLA_OK;
+}
+
+mla_status mla_linear_pair(const mla_bf16* x, int T, int K, const mla_bf16* w0, int N0, mla_bf16* y0,
+                           const mla_bf16* w1, int N1, mla_bf16* y1, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  if (T < 1 || T > MLA_LINEAR_MAX_T || K < 64 || K % 64 != 0 || N0 < 1 || N1 < 1) return MLA_ERR_INVALID_ARG;
+  if (!x || !w0 || !y0 || !w1 || !y1 || !aligned16(x) || !aligned16(w0) || !aligned16(w1)) return MLA_ERR_INVALID_ARG;
+  const size_t need = linear_workspace_bytes(T, K, N0, N1);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))) return MLA_ERR_WORKSPACE;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_linear_pair(x, w0, y0, N0, w1, y1, N1, T, K, static_cast<float*>(workspace), st, stream));
+}
+
 mla_status mla_rope_q(const mla_bf16* q_rope, const int32_t* seq_lens_before, const float* rope_table,
                       int rope_max_pos, mla_bf16* q_abs, int B, int n_q, cudaStream_t stream) {
   if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ) return MLA_ERR_INVALID_ARG;

@@ -140,9 +140,11 @@ cudaError_t launch_append_kv_fp8(const uint16_t* c_kv_new, const uint16_t* k_pe_
                                  int* status, cudaStream_t stream);
 
 int linear_num_splits(int T, int K, int N);
-size_t linear_workspace_bytes(int T, int K, int N);
+size_t linear_workspace_bytes(int T, int K, int N, int N1 = 0);
 cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, int64_t y_ld,
                           int seg, int seg_ld, float* part, int* status, cudaStream_t stream);
+cudaError_t launch_linear_pair(const uint16_t* x, const uint16_t* w0, uint16_t* y0, int N0, const uint16_t* w1,
+                               uint16_t* y1, int N1, int T, int K, float* part, int* status, cudaStream_t stream);
 cudaError_t launch_rope_q(const uint16_t* q_rope, const int32_t* seq_lens_before, const float* rope_table,
                           int rope_max_pos, uint16_t* q_abs, int B, int n_q, int* status, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, cudaStream_t stream);

@@ -39,13 +39,17 @@ __host__ __device__ inline uint32_t tmem_cols_for(int tp) {
 inline int smem_bytes_for(int tp) { return num_stages(tp) * stage_bytes(tp) + 256 + 1024; }
 static_assert((2 * kMaxStages + 1) * 8 + 4 <= 256, "barrier block");
 
+// One or two projections of the same x: CTAs [0, tiles0) compute y = x W^T with
+// N outputs, CTAs [tiles0, ..) y1 = x W1^T with N1 outputs (N1 = 0: one projection).
 struct LinParams {
   uint16_t* y;        // bf16 out (no split): element (t, n) at t * y_ld + (n / seg) * seg_ld + n % seg
-  float* part;        // [ksplit, T, N] fp32 (split)
+  uint16_t* y1;       // second projection's bf16 out: element (t, n) at t * y1_ld + n
+  float* part;        // [ksplit, T, N + N1] fp32 (split)
   int* status;
-  int T, K, N;
-  int kb_per_split;   // K blocks of 64 per CTA
-  int64_t y_ld;
+  int T, K, N, N1;
+  int tiles0;         // 128-row tiles of the first projection
+  int kb_per_split;   // K blocks of kKB per CTA
+  int64_t y_ld, y1_ld;
   int seg, seg_ld;
 };
 
@@ -55,7 +59,7 @@ __device__ __forceinline__ int64_t y_index(const LinParams& p, int t, int n) {
 
 __global__ void __launch_bounds__(kThreads, 1)
 linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                 const LinParams p) {
+                 const __grid_constant__ CUtensorMap tm_w1, const LinParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tp = pad16(p.T);
@@ -68,7 +72,11 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   const uint32_t tmem_cols = tmem_cols_for(tp);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * 128;
+  const bool second = static_cast<int>(blockIdx.x) >= p.tiles0;  // this CTA's projection
+  const CUtensorMap* tw = second ? &tm_w1 : &tm_w;
+  const int n0 = (static_cast<int>(blockIdx.x) - (second ? p.tiles0 : 0)) * 128;
+  const int Ng = second ? p.N1 : p.N;
+  const int ncol = second ? p.N + n0 : n0;  // column of the partials' row [N + N1]
   const int kb0 = blockIdx.y * p.kb_per_split;
   const int nkb = min(p.kb_per_split, (p.K + kKB - 1) / kKB - kb0);  // K past the end reads as zeros
 
@@ -100,7 +108,7 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
       mbar_arrive_expect_tx(smem_u32(&full[s]), SB);
       const int k = (kb0 + i) * kKB;
       for (int bx = 0; bx < kBoxes; ++bx) {
-        tma_load_2d(smem_u32(st + bx * kWBox), &tm_w, k + 64 * bx, n0, smem_u32(&full[s]));
+        tma_load_2d(smem_u32(st + bx * kWBox), tw, k + 64 * bx, n0, smem_u32(&full[s]));
         tma_load_2d(smem_u32(st + kBoxes * kWBox + bx * tp * 128), &tm_x, k + 64 * bx, 0, smem_u32(&full[s]));
       }
     }
@@ -130,32 +138,31 @@ linear_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
   const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(done), 0, p.status));
   tc_fence_after();
   const int n = n0 + warp * 32 + lane;
+  const int64_t ntot = p.N + p.N1;
   const uint32_t row_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  auto put = [&](int t, float v) {
+    if (gridDim.y > 1)
+      p.part[(static_cast<int64_t>(blockIdx.y) * p.T + t) * ntot + ncol + warp * 32 + lane] = v;
+    else if (second)
+      p.y1[static_cast<int64_t>(t) * p.y1_ld + n] = f32_to_bf16_bits(v);
+    else
+      p.y[y_index(p, t, n)] = f32_to_bf16_bits(v);
+  };
   if (ok && nkb > 0) {
     for (int c0 = 0; c0 < tp; c0 += 16) {
       uint32_t r[16];
       tmem_ld16(row_addr + c0, r);
       tmem_wait_ld();
-      if (n < p.N) {
+      if (n < Ng) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int t = c0 + i;
-          if (t < p.T) {
-            if (gridDim.y == 1)
-              p.y[y_index(p, t, n)] = f32_to_bf16_bits(__uint_as_float(r[i]));
-            else
-              p.part[(static_cast<int64_t>(blockIdx.y) * p.T + t) * p.N + n] = __uint_as_float(r[i]);
-          }
+          if (t < p.T) put(t, __uint_as_float(r[i]));
         }
       }
     }
-  } else if (n < p.N) {
-    for (int t = 0; t < p.T; ++t) {
-      if (gridDim.y == 1)
-        p.y[y_index(p, t, n)] = 0;
-      else
-        p.part[(static_cast<int64_t>(blockIdx.y) * p.T + t) * p.N + n] = 0.f;
-    }
+  } else if (n < Ng) {
+    for (int t = 0; t < p.T; ++t) put(t, 0.f);
   }
   tc_fence_before();
   __syncthreads();
@@ -167,7 +174,8 @@ __global__ void __launch_bounds__(256)
 linear_reduce_kernel(const float* __restrict__ part, const LinParams p, int ksplit) {
   grid_dep_wait();
   grid_dep_launch();
-  const int64_t elems = static_cast<int64_t>(p.T) * p.N;
+  const int64_t ntot = p.N + p.N1;
+  const int64_t elems = static_cast<int64_t>(p.T) * ntot;
   for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < elems;
        e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     // the loads of eight splits are in flight together; the sum keeps split order
@@ -181,7 +189,11 @@ linear_reduce_kernel(const float* __restrict__ part, const LinParams p, int kspl
       for (int q = 0; q < 8; ++q) a += v[q];
     }
     for (; s < ksplit; ++s) a += part[s * elems + e];
-    p.y[y_index(p, static_cast<int>(e / p.N), static_cast<int>(e % p.N))] = f32_to_bf16_bits(a);
+    const int t = static_cast<int>(e / ntot), c = static_cast<int>(e % ntot);
+    if (c < p.N)
+      p.y[y_index(p, t, c)] = f32_to_bf16_bits(a);
+    else
+      p.y1[static_cast<int64_t>(t) * p.y1_ld + (c - p.N)] = f32_to_bf16_bits(a);
   }
 }
 
@@ -210,13 +222,17 @@ int linear_num_splits(int T, int K, int N) {
   return (kbs + per - 1) / per;  // no empty split
 }
 
-size_t linear_workspace_bytes(int T, int K, int N) {
-  const int split = linear_num_splits(T, K, N);
-  return split > 1 ? static_cast<size_t>(split) * T * N * sizeof(float) : 0;
+size_t linear_workspace_bytes(int T, int K, int N, int N1) {
+  const int tiles = (N + 127) / 128 + (N1 + 127) / 128;
+  const int split = linear_num_splits(T, K, 128 * tiles);
+  return split > 1 ? static_cast<size_t>(split) * T * (N + N1) * sizeof(float) : 0;
 }
 
-cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, int64_t y_ld,
-                          int seg, int seg_ld, float* part, int* status, cudaStream_t stream) {
+namespace {
+
+cudaError_t launch_linear_any(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, int64_t y_ld,
+                              int seg, int seg_ld, const uint16_t* w1, uint16_t* y1, int N1, int64_t y1_ld,
+                              float* part, int* status, cudaStream_t stream) {
   const int tp = pad16(T);
   static bool configured[kMaxDevicesLocal] = {};  // the attribute is per device
   const int dev_ = current_device_index();
@@ -228,31 +244,53 @@ cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int
     if (e != cudaSuccess) return e;
     configured[dev_] = true;
   }
-  const int split = linear_num_splits(T, K, N);
+  const int tiles0 = (N + 127) / 128, tiles = tiles0 + (N1 + 127) / 128;
+  const int split = linear_num_splits(T, K, 128 * tiles);
   const int kbs = (K + kKB - 1) / kKB;
-  CUtensorMap tx, tw;
+  CUtensorMap tx, tw, tw1;
   if (!make_tmap_bf16_2d(&tx, x, T, K, K, 64, tp, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16_2d(&tw, w, N, K, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  if (N1 > 0) {
+    if (!make_tmap_bf16_2d(&tw1, w1, N1, K, K, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+  } else {
+    tw1 = tw;  // not read
+  }
   LinParams prm;
   prm.y = y;
+  prm.y1 = y1;
   prm.part = part;
   prm.status = status;
   prm.T = T;
   prm.K = K;
   prm.N = N;
+  prm.N1 = N1;
+  prm.tiles0 = tiles0;
   prm.kb_per_split = (kbs + split - 1) / split;
   prm.y_ld = y_ld;
+  prm.y1_ld = y1_ld;
   prm.seg = seg;
   prm.seg_ld = seg_ld;
-  cudaError_t e = launch_kernel(linear_tc_kernel, dim3((N + 127) / 128, split), dim3(kThreads), smem_bytes_for(tp),
-                                stream, tx, tw, prm);
+  cudaError_t e = launch_kernel(linear_tc_kernel, dim3(tiles, split), dim3(kThreads), smem_bytes_for(tp), stream, tx,
+                                tw, tw1, prm);
   if (e != cudaSuccess || split == 1) return e;
-  const int64_t elems = static_cast<int64_t>(T) * N;
+  const int64_t elems = static_cast<int64_t>(T) * (N + N1);
   const int64_t want = (elems + 255) / 256;
   const int blocks = static_cast<int>(want < 4096 ? want : 4096);
   return launch_kernel(linear_reduce_kernel, dim3(blocks), dim3(256), 0, stream, static_cast<const float*>(part), prm,
                        split);
+}
+
+}  // namespace
+
+cudaError_t launch_linear(const uint16_t* x, const uint16_t* w, uint16_t* y, int T, int K, int N, int64_t y_ld,
+                          int seg, int seg_ld, float* part, int* status, cudaStream_t stream) {
+  return launch_linear_any(x, w, y, T, K, N, y_ld, seg, seg_ld, nullptr, nullptr, 0, 0, part, status, stream);
+}
+
+cudaError_t launch_linear_pair(const uint16_t* x, const uint16_t* w0, uint16_t* y0, int N0, const uint16_t* w1,
+                               uint16_t* y1, int N1, int T, int K, float* part, int* status, cudaStream_t stream) {
+  return launch_linear_any(x, w0, y0, T, K, N0, N0, N0, N0, w1, y1, N1, N1, part, status, stream);
 }
 
 }  // namespace mla

@@ -56,6 +56,8 @@ _SIGS = {
     "mla_get_launch_overlap": ([], _i),
     "mla_linear_workspace_size": ([_i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_linear": ([_p, _p, _p, _i, _i, _i, _p, _sz, _p], _i),
+    "mla_linear_pair_workspace_size": ([_i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
+    "mla_linear_pair": ([_p, _i, _i, _p, _i, _p, _p, _i, _p, _p, _sz, _p], _i),
     "mla_linear_strided": ([_p, _p, _p, _i, _i, _i, _i64, _i, _i, _p, _sz, _p], _i),
     "mla_rope_q": ([_p, _p, _p, _i, _p, _i, _i, _p], _i),
     "mla_f32_to_bf16": ([_p, _p, _i64, _p], _i),
@@ -165,6 +167,33 @@ def mla_linear_workspace_size(T, K, N) -> int:
 def alloc_linear_workspace(T, K, N, device):
     n = mla_linear_workspace_size(T, K, N)
     return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mla_linear_pair_workspace_size(T: int, K: int, N0: int, N1: int) -> int:
+    out = _sz(0)
+    _check("mla_linear_pair_workspace_size",
+           lib.mla_linear_pair_workspace_size(int(T), int(K), int(N0), int(N1), ctypes.byref(out)))
+    return int(out.value)
+
+
+def mla_linear_pair(x, w0, w1, y0=None, y1=None, workspace=None, stream=None):
+    """``y0 = x w0^T`` and ``y1 = x w1^T`` in one launch."""
+    T, K = x.shape
+    N0, N1 = w0.shape[0], w1.shape[0]
+    if y0 is None:
+        y0 = torch.empty(T, N0, dtype=torch.bfloat16, device=x.device)
+    if y1 is None:
+        y1 = torch.empty(T, N1, dtype=torch.bfloat16, device=x.device)
+    need = mla_linear_pair_workspace_size(T, K, N0, N1)
+    if need and (workspace is None or workspace.numel() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _check("mla_linear_pair", lib.mla_linear_pair(
+        _dev(x, "x", torch.bfloat16, (T, K)), int(T), int(K),
+        _dev(w0, "w0", torch.bfloat16, (N0, K)), int(N0), _dev(y0, "y0", torch.bfloat16, (T, N0)),
+        _dev(w1, "w1", torch.bfloat16, (N1, K)), int(N1), _dev(y1, "y1", torch.bfloat16, (T, N1)),
+        0 if not need else _dev(workspace, "workspace", torch.uint8), 0 if not need else workspace.numel(),
+        _stream(stream)))
+    return y0, y1
 
 
 def mla_linear(x, w, y=None, workspace=None, stream=None):

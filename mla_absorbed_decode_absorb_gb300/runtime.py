@@ -321,6 +321,8 @@ class LayerSession:
         shapes = [(self.w_dkv, self.d_model), (self.w_kr, self.d_model), (self.w_dq, self.d_model),
                   (self.w_uq, self.c_q.shape[1]), (self.w_qr, self.c_q.shape[1]), (self.w_o, d.out[0].numel() // d.n_q)]
         need = max(ops.mla_linear_workspace_size(self.T, k, w.shape[0]) for w, k in shapes)
+        need = max(need, ops.mla_linear_pair_workspace_size(self.T, self.d_model, self.w_dkv.shape[0],
+                                                            self.w_kr.shape[0]))
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
         # a layer step's input is the hidden state, its result the layer output
         self.step_buffer = self.x
@@ -371,8 +373,8 @@ class LayerSession:
         ops.mla_copy(host_out, self.y, stream)
 
     def proj_kv(self, stream=None):
-        ops.mla_linear(self.x, self.w_dkv, self._c_new, self.ws, stream)
-        ops.mla_linear(self.x, self.w_kr, self._k_new, self.ws, stream)
+        # W_DKV and W_KR read the same hidden state: one launch
+        ops.mla_linear_pair(self.x, self.w_dkv, self.w_kr, self._c_new, self._k_new, self.ws, stream)
 
     def proj_q(self, stream=None):
         ops.mla_linear(self.x, self.w_dq, self.c_q, self.ws, stream)
@@ -416,12 +418,12 @@ class LayerSession:
         dq = self.c_q.shape[1]
         if self.fold:
             n = 2 + (1 if self.dec.num_splits > 1 else 0) + 1 + 1   # append, attention, combine, to_bf16, rope_q
-            lin = [(self.w_dkv, d), (self.w_kr, d), (self.w_dq, d), (self.w_qk, dq), (self.w_qr, dq),
-                   (self.w_ov, self.w_ov.shape[1])]
+            lin = [(self.w_dq, d), (self.w_qk, dq), (self.w_qr, dq), (self.w_ov, self.w_ov.shape[1])]
         else:
             n = self.dec.launches_per_step()
-            lin = [(self.w_dkv, d), (self.w_kr, d), (self.w_dq, d), (self.w_uq, dq), (self.w_qr, dq),
-                   (self.w_o, self.w_o.shape[1])]
+            lin = [(self.w_dq, d), (self.w_uq, dq), (self.w_qr, dq), (self.w_o, self.w_o.shape[1])]
         for w, k in lin:
             n += 1 + (1 if ops.mla_linear_workspace_size(self.T, k, w.shape[0]) else 0)
+        # W_DKV and W_KR in one launch (plus its split-K sum)
+        n += 1 + (1 if ops.mla_linear_pair_workspace_size(self.T, d, self.w_dkv.shape[0], self.w_kr.shape[0]) else 0)
         return n
