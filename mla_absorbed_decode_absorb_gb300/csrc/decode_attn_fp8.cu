@@ -589,6 +589,7 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
       // four boxes of 32 fp32 columns x 128 rows, 128-byte swizzle: row r at
       // r * 128, 16-byte chunk c at (c ^ (r & 7)) * 16
       uint8_t* tile = smem + kOffStage + g * kOTileBytes;
+      const int32_t y0 = static_cast<int32_t>(out_row) - row;  // row 0 of the unit
 #pragma unroll 1
       for (int k = 0; k < 4; ++k) {
         uint32_t r[32];
@@ -600,17 +601,15 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
           *reinterpret_cast<float4*>(brow + ((c ^ (row & 7)) << 4)) =
               make_float4(__uint_as_float(r[4 * c]) * inv, __uint_as_float(r[4 * c + 1]) * inv,
                           __uint_as_float(r[4 * c + 2]) * inv, __uint_as_float(r[4 * c + 3]) * inv);
-      }
-      fence_proxy_async_smem();  // visible to the TMA store
-      if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
-      named_barrier_sync(1 + g, kRowThreads);
-      if (row == 0) {
-        const int32_t y0 = static_cast<int32_t>(out_row);  // row 0 of the unit
-        for (int k = 0; k < 4; ++k)
+        fence_proxy_async_smem();  // visible to the TMA store
+        named_barrier_sync(1 + g, kRowThreads);
+        if (row == 0) {  // each box goes out as soon as it is staged
           tma_store_2d(&tm_o, smem_u32(tile + k * kOBoxBytes), static_cast<int32_t>(rank * 256 + 128 * g + 32 * k), y0);
-        bulk_commit_group();
-        bulk_wait_all();
+          bulk_commit_group();
+        }
       }
+      if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
+      if (row == 0) bulk_wait_all();
     } else {
       float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
       for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
