@@ -435,6 +435,17 @@ mla_status mla_prefill_attn(const mla_bf16* q_nope, const mla_bf16* q_rope, cons
                             cudaStream_t stream);
 
 /*
+ * mla_selftest_wait_timeout -- exercises the failure path of the bounded waits
+ * every kernel uses (no counterpart on the MLA pages).  One warp waits on an
+ * mbarrier that nothing completes; after limit_ns nanoseconds (1 .. 2e9) of
+ * %globaltimer the wait gives up, MLA_ERR_TIMEOUT is recorded in the device
+ * status word and the kernel returns: the context stays usable and the next
+ * mla_get_device_status reports (and clears) the code.  Nothing faults, traps
+ * or hangs.  Asynchronous on `stream`.
+ */
+mla_status mla_selftest_wait_timeout(int64_t limit_ns, cudaStream_t stream);
+
+/*
  * mla_copy_async -- copy `bytes` from src to dst with the GPU's own loads and
  * stores, as one kernel of this library on `stream`.  (The MLA pages have no
  * counterpart; this moves a step's inputs and outputs.)  Each of dst and src

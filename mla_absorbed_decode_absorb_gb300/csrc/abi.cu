@@ -381,6 +381,13 @@ bool output_view(void* p, size_t bytes, void** out) {
   return device_view(p, bytes, out, &host);
 }
 
+mla_status mla_selftest_wait_timeout(int64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns < 1 || limit_ns > 2000000000ll) return MLA_ERR_INVALID_ARG;
+  int* st = status_ptr();
+  if (st == nullptr) return MLA_ERR_CUDA;
+  return from_cuda(launch_wait_timeout(st, static_cast<uint64_t>(limit_ns), stream));
+}
+
 mla_status mla_copy_async(void* dst, const void* src, size_t bytes, cudaStream_t stream) {
   if (bytes == 0) return MLA_OK;
   if (dst == nullptr || src == nullptr) return MLA_ERR_INVALID_ARG;

@@ -121,6 +121,9 @@ int* device_status_word();
 // `src_is_host`: the source is host memory, which no kernel writes.
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, bool src_is_host, cudaStream_t stream);
 
+// One warp waiting on an mbarrier nothing completes, given up after limit_ns (csrc/selftest.cu).
+cudaError_t launch_wait_timeout(int* status, uint64_t limit_ns, cudaStream_t stream);
+
 cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   int64_t num_pages, const int32_t* page_table, int pt_stride,
                                   const int32_t* kv_lens, int B, int n_q, int max_kv_len,

@@ -69,14 +69,15 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // Bounded wait for phase `parity` of `bar` to complete.  `abort` (optional,
 // shared by the CTA) makes every other waiter give up too once one has timed out.
 template <bool kClusterScope>
-__device__ __forceinline__ bool mbar_wait_impl(uint32_t bar, uint32_t parity, int* status, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_impl(uint32_t bar, uint32_t parity, int* status, volatile int* abort,
+                                               uint64_t limit_ns = kWaitNs) {
   if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (kClusterScope ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (abort != nullptr && *abort) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         record_status(status, MLA_ERR_TIMEOUT);
         if (abort != nullptr) *abort = 1;
         return false;

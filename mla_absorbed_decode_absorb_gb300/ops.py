@@ -41,6 +41,7 @@ _SIGS = {
     "mla_absorb_q": ([_p, _p, _p, _p, _p, _i, _p, _i, _i, _p], _i),
     "mla_append_absorb_q": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _p, _i64, _p, _i, _i, _p], _i),
     "mla_copy_async": ([_p, _p, _sz, _p], _i),
+    "mla_selftest_wait_timeout": ([_i64, _p], _i),
     "mla_append_absorb_q_fp8": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _p, _p, _p, _i64, _p, _i, _i, _p], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_decode_num_splits": ([_i, _i, _i, _i, ctypes.POINTER(_i)], _i),

@@ -265,6 +265,24 @@ def test_out_of_range_page_is_reported():
     assert ops.mla_get_device_status() == ops.MLA_OK
 
 
+def test_wait_timeout_is_reported_and_context_survives():
+    """A bounded wait on a barrier nothing completes gives up, reports MLA_ERR_TIMEOUT
+    through the status word, and later work on the same context is unaffected."""
+    from mla_absorbed_decode_absorb_gb300 import ops
+    import time
+    assert ops.mla_get_device_status() == ops.MLA_OK
+    t0 = time.perf_counter()
+    assert ops.lib.mla_selftest_wait_timeout(20_000_000, 0) == ops.MLA_OK   # 20 ms
+    torch.cuda.synchronize()
+    assert 0.015 < time.perf_counter() - t0 < 1.0
+    assert ops.mla_get_device_status() == ops.MLA_ERR_TIMEOUT
+    assert ops.mla_get_device_status() == ops.MLA_OK  # read-and-clear
+    assert ops.lib.mla_selftest_wait_timeout(0, 0) == ops.MLA_ERR_INVALID_ARG
+    inp = W.generate(W.custom("after_timeout", [100, 64], n_q=1), seed=16)
+    s = run_session(inp)  # asserts a clean status itself
+    check_outputs(s, inp, range(inp.batch))
+
+
 def test_invalid_arguments_raise():
     from mla_absorbed_decode_absorb_gb300 import ops
     x = torch.zeros(1, 1, 512, dtype=torch.float32, device="cuda")
