@@ -249,30 +249,36 @@ out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __re
 // For up to kTMaxSplits splits the O' rows come in by TMA as well: a plain
 // load of 128 KB per CTA is limited by what L1 can hold in flight next to the
 // 128 KB of W_UV in shared memory, while a TMA box lands in shared memory
-// directly.  Per CTA (head h, up to kTTokens tokens): W_UV[h] as 8 boxes; the
-// rows (token t, split s) of latent chunk k (64 m) as one box of up to 64 rows
-// through a 3-slot ring; 8 combine warps merge chunk k (same fp32 operations
-// in the same order as the stand-alone merge) into bf16 chunk k of B, and
-// warp 8 issues the chunk's 4 MMAs as soon as it is written, then refills the
-// slot.  The merge of chunk k + 1 overlaps the MMAs of chunk k.
+// directly.  Per CTA (head h, up to kTTokens tokens), latent chunk k (64 m)
+// travels through a 5-slot ring as W_UV[h]'s chunk k (a 64 m x 128 d box) and the
+// rows (token t, split s) of O' (one box of up to 64 rows): the first five
+// weight chunks are requested before the previous kernel has finished (where
+// the launch allows) and the last three pulled into L2, so that the O' of five
+// chunks is in flight at once (two round trips to L2 for the tile, where a
+// 3-slot ring of O' beside all of W_UV needed three).  8 combine warps merge
+// chunk k (same fp32 operations in the same order as the stand-alone merge) into
+// bf16 chunk k of B, and warp 8 issues the chunk's 4 MMAs as soon as it is
+// written, then refills the slot once they have finished.
 constexpr int kTTokens = 32;                   // tokens per CTA (at most)
 constexpr int kTBoxRows = 64;                  // O' rows (token x split) per box
-constexpr int kTStages = 3;
+constexpr int kTStages = 5;
 constexpr int kTBoxBytes = 64 * 4 * kTBoxRows;  // 16 KB
+constexpr int kTSlotBytes = kChunk + kTBoxBytes;  // W_UV chunk, then the O' box
 constexpr int kTThreads = 288;                 // warps 0-7 merge, warp 8 loads and issues MMAs
 constexpr int kTMaxSplits = 16;
 constexpr int kTSmemB = (kLatent / 64) * kTTokens * 128;  // 32 KB
 
 struct TBars {
-  uint64_t w_full;
-  uint64_t p_full[kTStages];
+  uint64_t w_full[kTStages];      // the slot's weight chunk has landed
+  uint64_t p_full[kTStages];      // the slot's O' box has landed
+  uint64_t s_free[kTStages];      // the MMAs of the slot's chunk have finished (its weights are read)
   uint64_t b_full[kLatent / 64];  // chunk k of B written (and box k read) by all 256 merge threads
   uint64_t mma_done;
   uint32_t tmem_slot;
 };
-constexpr int kTOffB = kSmemA;
-constexpr int kTOffRing = kTOffB + kTSmemB;
-constexpr int kTOffBars = kTOffRing + kTStages * kTBoxBytes;
+constexpr int kTOffRing = 0;
+constexpr int kTOffB = kTOffRing + kTStages * kTSlotBytes;
+constexpr int kTOffBars = kTOffB + kTSmemB;
 constexpr int kTOffTab = kTOffBars + 256;
 constexpr int kTSmemBytes = kTOffTab + 4 * (kTTokens * kTMaxSplits + 2 * kTTokens) + 1024;
 static_assert(sizeof(TBars) <= 256, "barrier block");
@@ -287,7 +293,6 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
                          float* __restrict__ lse_out, int T, int* status, bool weights_early) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
   uint8_t* sB = smem + kTOffB;
   uint8_t* ring = smem + kTOffRing;
   TBars& bars = *reinterpret_cast<TBars*>(smem + kTOffBars);
@@ -305,25 +310,34 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
   const uint32_t tmem_cols = 32;  // npad <= 32
   const bool merge = src_lse != nullptr;
 
-  auto load_w = [&]() {
-    mbar_arrive_expect_tx(smem_u32(&bars.w_full), kSmemA);
-    for (int c = 0; c < kLatent / 64; ++c)
-      tma_load_2d(smem_u32(sA + c * kChunk), &tm_w, 64 * c, h * kNope, smem_u32(&bars.w_full));
+  constexpr int kNChunks = kLatent / 64;
+  // weight chunk k (64 m x 128 d) into slot k % kTStages
+  auto load_w = [&](int k) {
+    const int slot = k % kTStages;
+    mbar_arrive_expect_tx(smem_u32(&bars.w_full[slot]), kChunk);
+    tma_load_2d(smem_u32(ring + slot * kTSlotBytes), &tm_w, 64 * k, h * kNope, smem_u32(&bars.w_full[slot]));
+  };
+  auto load_w_first = [&]() {
+    for (int k = 0; k < kTStages; ++k) load_w(k);
+    for (int k = kTStages; k < kNChunks; ++k) tma_prefetch_l2_2d(&tm_w, 64 * k, h * kNope);
   };
   // box k: rows (t0 + t) * S + s, t < ntile, columns [64k, 64k + 64) of head h
   auto load_p = [&](int k) {
     const int slot = k % kTStages;
     mbar_arrive_expect_tx(smem_u32(&bars.p_full[slot]), 256u * ntile * S);  // the whole box, rows past T * S as zeros
-    tma_load_3d(smem_u32(ring + slot * kTBoxBytes), &tm_p, 64 * k, h, t0 * S, smem_u32(&bars.p_full[slot]));
+    tma_load_3d(smem_u32(ring + slot * kTSlotBytes + kChunk), &tm_p, 64 * k, h, t0 * S, smem_u32(&bars.p_full[slot]));
   };
 
   if (tid == 256) {
-    mbar_init(smem_u32(&bars.w_full), 1);
-    for (int i = 0; i < kTStages; ++i) mbar_init(smem_u32(&bars.p_full[i]), 1);
-    for (int i = 0; i < kLatent / 64; ++i) mbar_init(smem_u32(&bars.b_full[i]), 256);
+    for (int i = 0; i < kTStages; ++i) {
+      mbar_init(smem_u32(&bars.w_full[i]), 1);
+      mbar_init(smem_u32(&bars.p_full[i]), 1);
+      mbar_init(smem_u32(&bars.s_free[i]), 1);
+    }
+    for (int i = 0; i < kNChunks; ++i) mbar_init(smem_u32(&bars.b_full[i]), 256);
     mbar_init(smem_u32(&bars.mma_done), 1);
     fence_mbar_init();
-    if (weights_early) load_w();
+    if (weights_early) load_w_first();
   }
   if (warp == 8) {
     tmem_alloc(smem_u32(&bars.tmem_slot), tmem_cols);
@@ -339,22 +353,32 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
   if (warp == 8) {
     // ------------------------------------------------ loads and MMAs
     if (lane == 0) {
-      if (!weights_early) load_w();
+      if (!weights_early) load_w_first();
       for (int k = 0; k < kTStages; ++k) load_p(k);
-      bool ok = mbar_wait(smem_u32(&bars.w_full), 0, status);
       const uint32_t idesc = idesc_bf16(128, npad, /*a_mn=*/0, /*b_mn=*/0);
-      const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-      for (int k = 0; k < kLatent / 64 && ok; ++k) {
-        ok = mbar_wait(smem_u32(&bars.b_full[k]), 0, status);
+      const uint32_t b0 = smem_u32(sB);
+      bool ok = true;
+      for (int k = 0; k < kNChunks && ok; ++k) {
+        const int slot = k % kTStages;
+        const uint32_t use = (k / kTStages) & 1;
+        ok = mbar_wait(smem_u32(&bars.w_full[slot]), use, status) && mbar_wait(smem_u32(&bars.b_full[k]), 0, status);
         if (!ok) break;
         tc_fence_after();
+        const uint32_t a0 = smem_u32(ring + slot * kTSlotBytes);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint64_t ad = smem_desc(a0 + k * kChunk + q * 32, 16, 1024, kSw128);
+          const uint64_t ad = smem_desc(a0 + q * 32, 16, 1024, kSw128);
           const uint64_t bd = smem_desc(b0 + k * npad * 128 + q * 32, 16, 1024, kSw128);
           mma_ss(tmem, ad, bd, idesc, (k | q) ? 1u : 0u);
         }
-        if (k + kTStages < kLatent / 64) load_p(k + kTStages);  // box k has been read
+        mma_commit(smem_u32(&bars.s_free[slot]));
+        if (k + kTStages < kNChunks) {
+          // box k has been merged (b_full); the slot is free once these MMAs have read its weights
+          ok = mbar_wait(smem_u32(&bars.s_free[slot]), use, status);
+          if (!ok) break;
+          load_w(k + kTStages);
+          load_p(k + kTStages);
+        }
       }
       if (ok) mma_commit(smem_u32(&bars.mma_done));
       else mbar_arrive(smem_u32(&bars.mma_done));  // no result: release the epilogue (the status is set)
@@ -389,7 +413,7 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
 #pragma unroll
         for (int e = 0; e < 8; ++e) a[e] = 0.f;
         if (live) {
-          const uint8_t* box = ring + slot * kTBoxBytes;
+          const uint8_t* box = ring + slot * kTSlotBytes + kChunk;
           for (int s = 0; s < S; ++s) {
             const float w = merge ? s_w[t * S + s] : 1.f;
             if (w >= 0.f) {
