@@ -13,7 +13,6 @@ import math
 import os
 
 import numpy as np
-import pytest
 import torch
 
 from oracle import mla_oracle as O
