@@ -64,3 +64,28 @@ def test_invalid_arguments_are_rejected_before_any_launch(lib):
     n = ctypes.c_int(0)
     assert lib.mla_decode_num_splits(1, 9, 100, 4, ctypes.byref(n)) == 1
     assert lib.mla_decode_num_splits(1, 2, 1, 4, ctypes.byref(n)) == 1  # max_kv_len < n_q
+
+
+def test_new_entry_points_validate_before_any_launch(lib):
+    """Argument checks of the fused prologue, the pair projection, the host-link copy and the
+    timeout self-test, all of which return before touching the device."""
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.mla_append_absorb_q.argtypes = [P, P, P, P, P, P, I, P, P, I, P, I64, P, I, I, P]
+    # n_q = 0 and n_q = 9 are outside [1, MLA_MAX_NQ]; null pointers with B > 0
+    assert lib.mla_append_absorb_q(*([None] * 6), 1, None, None, 1, None, 1, None, 1, 0, None) == 1
+    assert lib.mla_append_absorb_q(*([None] * 6), 1, None, None, 1, None, 1, None, 1, 9, None) == 1
+    assert lib.mla_append_absorb_q(*([None] * 6), 1, None, None, 1, None, 1, None, 1, 1, None) == 1
+    assert lib.mla_append_absorb_q(*([None] * 6), 1, None, None, 1, None, 1, None, 0, 1, None) == 0  # B = 0
+    lib.mla_linear_pair_workspace_size.argtypes = [I, I, I, I, ctypes.POINTER(SZ)]
+    sz = SZ(0)
+    assert lib.mla_linear_pair_workspace_size(32, 100, 512, 64, ctypes.byref(sz)) == 1  # K % 64
+    assert lib.mla_linear_pair_workspace_size(0, 128, 512, 64, ctypes.byref(sz)) == 1   # T < 1
+    assert lib.mla_linear_pair_workspace_size(32, 128, 512, 0, ctypes.byref(sz)) == 1   # N1 < 1
+    lib.mla_linear_pair.argtypes = [P, I, I, P, I, P, P, I, P, P, SZ, P]
+    assert lib.mla_linear_pair(None, 32, 128, None, 512, None, None, 64, None, None, 0, None) == 1
+    lib.mla_copy_async.argtypes = [P, P, SZ, P]
+    assert lib.mla_copy_async(None, None, 0, None) == 0   # nothing to copy
+    assert lib.mla_copy_async(None, None, 16, None) == 1
+    lib.mla_selftest_wait_timeout.argtypes = [I64, P]
+    assert lib.mla_selftest_wait_timeout(0, None) == 1
+    assert lib.mla_selftest_wait_timeout(3_000_000_000, None) == 1
