@@ -26,7 +26,8 @@
 // loads the page's 4 KB of key by TMA into the stage (its layout is the
 // stage's) and pulls the next page's codes into L2; warp 1 issues QK^T, warp 2
 // P V, warp 3 recycles the exchange buffers, and warps 4-11 are the two row
-// warpgroups.  Without a landing ring for the codes, four float16 stages fit.  Score exchange, lazy reference max,
+// warpgroups.  Without a landing ring for the codes, four float16 stages fit.
+// Score exchange, lazy reference max,
 // packed softmax arithmetic, TMEM layout and epilogue follow the bf16 kernel.
 #include <cuda_fp16.h>
 

@@ -15,12 +15,13 @@
 // 2-stage key ring, and another the values into a 2-stage value ring: a key
 // stage is free again as soon as its S = Q K^T has been computed, so the next
 // keys load while the softmax runs.  S (M = 128 queries, N = 128 keys, K = 192)
-// goes to one of two TMEM buffers, the softmax warps (one thread per query)
-// apply the causal mask and an online softmax with a lazily updated reference
-// max (O is rescaled only when a row's max grows by more than 2^8), write P as
-// bf16 into one of two TMEM buffers (so P of the next tile never waits for P V
-// of this one), and O += P V (N = 128, K = 128 keys) accumulates in TMEM.  Query j of sequence b sits at position seq_lens_before[b] + j and sees
-// the keys 0 .. seq_lens_before[b] + j.
+// goes to one of two TMEM buffers; the softmax warps (two threads per query,
+// one per 64-key half of the tile) apply the causal mask and an online softmax
+// with a lazily updated reference max (O is rescaled only when a row's max
+// grows by more than 2^8), write P as bf16 into one of two TMEM buffers (so P
+// of the next tile never waits for P V of this one), and O += P V (N = 128,
+// K = 128 keys) accumulates in TMEM.  Query j of sequence b sits at position
+// seq_lens_before[b] + j and sees the keys 0 .. seq_lens_before[b] + j.
 #include "sm100.cuh"
 #include "tmap.cuh"
 
