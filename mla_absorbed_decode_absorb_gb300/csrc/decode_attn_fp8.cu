@@ -27,8 +27,8 @@
 // stage's) and pulls the next page's codes into L2; warp 1 issues QK^T, warp 2
 // P V, warp 3 recycles the exchange buffers, and warps 4-11 are the two row
 // warpgroups.  Without a landing ring for the codes, four float16 stages fit.
-// Score exchange, lazy reference max,
-// packed softmax arithmetic, TMEM layout and epilogue follow the bf16 kernel.
+// Score exchange, lazy reference max, packed softmax arithmetic, TMEM layout
+// and epilogue follow the bf16 kernel.
 #include <cuda_fp16.h>
 
 #include "sm100.cuh"
