@@ -67,6 +67,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU-oracle sample budget")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-per-workload", action="store_true",
+                   help="skip the short per-workload pass over the other decode workloads")
+    p.add_argument("--per-workload-steps", type=int, default=20)
     p.add_argument("--launch-overlap", type=int, default=2, choices=[0, 1, 2],
                    help="mla_set_launch_overlap level (2: weights are constant, read ahead)")
     return p.parse_args(argv)
@@ -106,6 +109,11 @@ def host_cores():
         return len(os.sched_getaffinity(0))
     except Exception:
         return os.cpu_count() or 1
+
+
+def cpu_cores_info():
+    """Threads the oracle's BLAS runs on (its ``cores``) and the cores this process may use."""
+    return {"cores": blas_threads(), "blas_threads": blas_threads(), "host_cores": host_cores()}
 
 
 def blas_threads():
@@ -323,7 +331,7 @@ def run_reference(args, wl):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_t * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(wl, inp, world, {"sample": sample}),
-        "cpu_baseline": {"value": value, "unit": unit, "cores": blas_threads(), "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": unit, **cpu_cores_info(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -349,6 +357,78 @@ def profiled_traffic(workload: str):
         return None if rec is None else float(rec["dram_bytes_per_launch"])
     except Exception:
         return None
+
+
+def measure_decode_workload(name, dev, stream, flush_l2, steps, peaks):
+    """A short pass over one more decode workload, measured like the headline one:
+    whole steps and the split attention between CUDA events with L2 flushed
+    before every step, plus warm-L2 steps back to back, eager and replayed from
+    a CUDA graph (the number that matters for a cache that fits in L2)."""
+    from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
+
+    wl = W.WORKLOADS[name]
+    inp = W.generate(wl, seed=0)
+    s = DecodeSession(inp, device=dev)
+    kv_list = inp.kv_lens.tolist()
+    step_bytes = A.step_cache_bytes(kv_list)
+    step_flops = A.step_attention_flops(kv_list, wl.n_q)
+    for _ in range(3):
+        flush_l2()
+        s.step()
+    torch.cuda.synchronize()
+    stages = s.stage_names()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(stages) + 1)] for _ in range(steps)]
+    tot = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        flush_l2()
+        tot[k][0].record(stream)
+        s.step()
+        tot[k][1].record(stream)
+    for k in range(steps):
+        flush_l2()
+        ev[k][0].record(stream)
+        for i, st in enumerate(stages):
+            getattr(s, st)()
+            ev[k][i + 1].record(stream)
+    torch.cuda.synchronize()
+    step_ms = sum(a.elapsed_time(b) for a, b in tot) / steps
+    stage_ms = {st: sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(steps)) / steps
+                for i, st in enumerate(stages)}
+    attn_ms = stage_ms["attend_partial"]
+    w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0.record(stream)
+    for _ in range(steps):
+        s.step()
+    w1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = w0.elapsed_time(w1) / steps
+    g = s.capture()
+    torch.cuda.synchronize()
+    w0.record(stream)
+    for _ in range(steps):
+        g.replay()
+    w1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = w0.elapsed_time(w1) / steps
+    from mla_absorbed_decode_absorb_gb300 import ops
+    if ops.mla_get_device_status() != ops.MLA_OK:
+        raise RuntimeError(f"device status set during the {name} pass")
+    t_roof, bound = A.roofline_seconds(kv_list, wl.n_q, peaks["hbm_gbs"], peaks["bf16_tflops"])
+    if bound == "hbm":
+        achieved, peak, unit = step_bytes / (attn_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = step_flops / (attn_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    out = {"B": wl.batch, "n_q": wl.n_q, "kv_tokens": int(sum(kv_list)), "split_pages": s.split_pages,
+           "num_splits": s.num_splits, "us_per_step": step_ms * 1e3, "attn_us": attn_ms * 1e3,
+           "stage_us": {k: v * 1e3 for k, v in stage_ms.items()},
+           "us_per_step_warm_l2": warm_ms * 1e3, "us_per_step_graph_warm_l2": graph_ms * 1e3,
+           "algorithmic_bytes": step_bytes, "algorithmic_flops": step_flops,
+           "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                        "roofline_us": t_roof * 1e6},
+           "steps": steps}
+    del g, s
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, wl):
@@ -495,12 +575,41 @@ def run_ours(args, wl):
         e2e = {"value": total_bytes / (m * 1e-3) / (1 if prefill else 1e9), "unit": "tokens/s" if prefill else "GB/s",
                "ms_per_step": m, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
+    # mla_decode_attn as the C ABI defines it (split attention, then the separate
+    # log-sum-exp merge kernel), timed apart from the step in which the merge is
+    # fused into the out-projection
+    attn_combine_ms = None
+    if isinstance(s, DecodeSession) and s.path == "absorbed":
+        ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K3)]
+        for k in range(K3):
+            flush_l2()
+            ea[k][0].record(stream)
+            s.attend_partial()
+            if s.num_splits > 1:
+                s.combine()
+            ea[k][1].record(stream)
+        torch.cuda.synchronize()
+        (attn_combine_ms,), _ = reduce_over_ranks([sum(a.elapsed_time(b) for a, b in ea) / K3], 0, dev)
+
+    peaks, peak_src = load_peaks()
+    split_info = {"split_pages": s.split_pages, "num_splits": s.num_splits}
+    path_name, launches = s.path, s.launches_per_step() * K
+    per_workload = None
+    if (world == 1 and not args.no_per_workload and isinstance(s, DecodeSession) and s.path == "absorbed"
+            and not fp8):
+        del s
+        torch.cuda.empty_cache()
+        per_workload = {}
+        for other in W.DECODE_REPORT_WORKLOADS:
+            if other != wl.name:
+                per_workload[other] = measure_decode_workload(other, dev, stream, flush_l2, args.per_workload_steps,
+                                                              peaks)
+
     if world > 1:
         dist.destroy_process_group()
     if rank != 0:
         return 0
 
-    peaks, peak_src = load_peaks()
     t_mem, bound = A.roofline_seconds(kv_list, wl.n_q, peaks["hbm_gbs"], peaks["bf16_tflops"])
     attn_s = attn_ms * 1e-3
     if prefill:
@@ -520,19 +629,19 @@ def run_ours(args, wl):
     cpu_absorbed = None
     if world == 1 and not args.no_cpu_baseline and prefill:
         ntok, secs, desc = oracle_prefill_sample(inp, args.cpu_seconds)
-        cpu = {"value": ntok / secs, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle", "sample": desc}
+        cpu = {"value": ntok / secs, "unit": "tokens/s", **cpu_cores_info(), "kind": "oracle", "sample": desc}
     elif world == 1 and not args.no_cpu_baseline and layer:
         nseq, secs = oracle_layer_sample(li, args.cpu_seconds)
-        cpu = {"value": step_units / (secs / nseq * inp.batch) / 1e9, "unit": "GB/s", "cores": blas_threads(),
+        cpu = {"value": step_units / (secs / nseq * inp.batch) / 1e9, "unit": "GB/s", **cpu_cores_info(),
                "kind": "oracle",
                "sample": f"{nseq} of {inp.batch} sequences through the fp64 layer ({secs:.1f} s), a step costing "
                          f"{inp.batch} sequences"}
     elif world == 1 and not args.no_cpu_baseline:
         nb, secs, nseq = oracle_sample(inp, args.cpu_seconds)
-        cpu = {"value": nb / secs / 1e9, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+        cpu = {"value": nb / secs / 1e9, "unit": "GB/s", **cpu_cores_info(), "kind": "oracle",
                "sample": f"{nseq} of {inp.batch} sequences, all 128 heads, fp64 non-absorbed form ({secs:.1f} s)"}
         nb2, secs2, nseq2 = oracle_sample(inp, min(5.0, args.cpu_seconds), absorbed=True)
-        cpu_absorbed = {"value": nb2 / secs2 / 1e9, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
+        cpu_absorbed = {"value": nb2 / secs2 / 1e9, "unit": "GB/s", **cpu_cores_info(), "kind": "oracle",
                         "sample": f"{nseq2} of {inp.batch} sequences, all 128 heads, fp64 absorbed form ({secs2:.1f} s)"}
 
     line = {
@@ -540,25 +649,33 @@ def run_ours(args, wl):
         "value": total_bytes / (mean_ms * 1e-3) / (1 if prefill else 1e9), "unit": "tokens/s" if prefill else "GB/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": mean_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16" if fp8 else "bf16",
+        "cache_dtype": "e4m3 codes, one fp32 scale per token (the MMAs run on f16)" if fp8 else "bf16",
         "data": "synthetic",
-        "config": workload_config(wl, inp, world, {"split_pages": s.split_pages, "num_splits": s.num_splits}),
+        "config": workload_config(wl, inp, world, split_info),
         "us_per_step": mean_ms * 1e3,
         "attn_us": attn_ms * 1e3,
         "attn_tflops": step_flops / attn_s / 1e12,
         "attn_gbs": step_bytes / attn_s / 1e9,
-        "path": s.path,
+        "path": path_name,
         "decompress_tflops": (decompress_flops / (1e-3 * sum(per_stage[stages.index("decompress")]) / K3) / 1e12
                               if prefill else None),
         "stage_us": {n: 1e3 * sum(v) / K3 for n, v in zip(stages, per_stage)},
         "launch_overlap": ops.mla_get_launch_overlap(),
         "roofline_time_us": t_mem * 1e6,
         "roofline": roofline,
+        "decode_attn_with_combine": None if attn_combine_ms is None else {
+            "us": attn_combine_ms * 1e3,
+            "achieved_gbs": step_bytes / (attn_combine_ms * 1e-3) / 1e9,
+            "frac_of_hbm": step_bytes / (attn_combine_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "what": "mla_decode_attn: split attention plus the separate log-sum-exp merge kernel (in the step "
+                    "the merge runs fused into the out-projection)"},
+        "per_workload": per_workload,
         "cpu_baseline": cpu,
         "cpu_baseline_absorbed": cpu_absorbed,
         "us_per_step_warm_l2": warm_ms * 1e3,
         "us_per_step_graph_warm_l2": None if graph_ms is None else graph_ms * 1e3,
         "e2e": e2e,
-        "gpu_launches": s.launches_per_step() * K,
+        "gpu_launches": launches,
         "clocks": clk,
         "wall_s_timed_region": t_wall,
     }

@@ -336,7 +336,9 @@ mla_status mla_decode_attn_fp8_partial(const mla_bf16* q_abs, const uint8_t* cac
  * MLA_ERR_WORKSPACE and launches nothing.
  * The first call on a device looks up the array's device address (one
  * cudaGetSymbolAddress with that device current); make that first call before
- * any stream capture.  All calls share the one array, so calls whose work
+ * any stream capture.  The looked-up address belongs to the device's context:
+ * after cudaDeviceReset it is stale, so do not call this entry point again in
+ * that process.  All calls share the one array, so calls whose work
  * overlaps on the GPU (different streams, no ordering between them) race and
  * corrupt each other's partials; the array keeps the last call's contents,
  * which are fully rewritten by each call before they are read.  No memory is

@@ -27,14 +27,24 @@ std::mutex g_scratch_mutex;
 void* g_scratch_ptr[kMaxDevices];
 
 // Device address of the scratch array on the current device, looked up once per
-// device (the array's host-side name is not a device address).
+// device (the array's host-side name is not a device address).  A failed lookup
+// clears the runtime's pending error, so that it is not reported later by an
+// unrelated launch of this library.  The cached address belongs to the device's
+// current context: after cudaDeviceReset it is stale, and this entry point must
+// not be called again in that process.
 void* scratch_ptr() {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_scratch_mutex);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
     g_scratch_ptr[dev] = p;
   }
   return g_scratch_ptr[dev];

@@ -114,6 +114,9 @@ LAYER_WORKLOADS: dict[str, Workload] = {
 }
 
 DEFAULT_BENCH_WORKLOAD = "batched_b32_l4096"
+# The decode workloads every default bench run reports (the headline one in full,
+# the others in its per-workload pass).
+DECODE_REPORT_WORKLOADS = tuple(WORKLOADS)
 
 
 def custom(name: str, lengths, n_q: int = 1, split_pages: int = 0, cache_format: str = "bf16") -> Workload:

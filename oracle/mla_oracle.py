@@ -292,21 +292,6 @@ def _softmax_lse(s: np.ndarray):
     return e / z, m + math.log(z)
 
 
-def attention_weights_mha(q_nope_h, q_rope_h, w_uk_h, c, kr, pos: int) -> np.ndarray:
-    """alpha_{t} for one head and one query at position ``pos`` (non-absorbed form).
-
-    ``score_t = q^T k_t / sqrt(d_h + d_h^R)`` with ``q = [q^C ; RoPE(q^R, pos)]``
-    ([DP] eq. (9)) and ``k_t = [W_UK[h] c_t ; k^R_t]`` ([DP] eq. (2), (4)), over
-    the visible tokens ``t <= pos`` ([DP] eq. (10) sums ``j = 1..t``).
-    """
-    d_h, d_r = q_nope_h.shape[-1], q_rope_h.shape[-1]
-    vis = pos + 1
-    k = np.concatenate([c[:vis] @ np.asarray(w_uk_h, np.float64).T, kr[:vis]], axis=1)
-    q = np.concatenate([np.asarray(q_nope_h, np.float64), rope_f64(q_rope_h, pos)])
-    alpha, _ = _softmax_lse((k @ q) / math.sqrt(d_h + d_r))
-    return alpha
-
-
 def decode_mha(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len: int, heads=None):
     """One sequence's decode outputs by the plain definition (non-absorbed, fp64).
 
@@ -360,40 +345,49 @@ def decompress_kv(c, w_uk, w_uv):
 
 def decode_absorbed(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len: int, heads=None,
                     token_range: tuple[int, int] | None = None):
-    """The absorbed form in fp64, used only to cross-check the absorption identity.
+    """The absorbed form in fp64: the cross-check of the absorption identity, and
+    (being far cheaper than the plain definition) the full-size reference for
+    every sequence and head once that identity is pinned.
 
     ``q~ = W_UK[h]^T q^C`` ([DP] key absorption; [MA] §2.1 ``Q' = Q W_UK^T``),
     ``score_t = (q~ . c_t + RoPE(q^R) . k^R_t) / sqrt(d_h + d_h^R)`` ([MA] §4.1 score
     split), ``m = sum_t alpha_t c_t`` and ``o = W_UV[h] m`` ([DP] value absorption).
-    With ``token_range=(t0, t1)`` only tokens in ``[t0, t1)`` take part and the
-    result is that split's partial: ``o_lat`` normalised within the split and its
-    ``lse`` (``-inf`` and zeros when the split holds no visible token).
+    All selected heads of one query are computed together as matrix products (the
+    scores of every head are one ``[T, d_c] x [d_c, H]`` product).  With
+    ``token_range=(t0, t1)`` only tokens in ``[t0, t1)`` take part and the result is
+    that split's partial: ``o_lat`` normalised within the split and its ``lse``
+    (``-inf`` and zeros when the split holds no visible token).
     """
     q_nope = np.asarray(q_nope, np.float64)
     q_rope = np.asarray(q_rope, np.float64)
     w_uk = np.asarray(w_uk, np.float64)
     w_uv = np.asarray(w_uv, np.float64)
+    c = np.asarray(c, np.float64)
+    kr = np.asarray(kr, np.float64)
     n_q, n_h, d_h = q_nope.shape
     d_r = q_rope.shape[-1]
     d_c = c.shape[1]
     heads = list(range(n_h)) if heads is None else list(heads)
     scale = 1.0 / math.sqrt(d_h + d_r)
     t0, t1 = token_range if token_range is not None else (0, c.shape[0])
+    w_uk_s, w_uv_s = w_uk[heads], w_uv[heads]
     o = np.zeros((n_q, len(heads), w_uv.shape[1]))
     o_lat = np.zeros((n_q, len(heads), d_c))
     lse = np.full((n_q, len(heads)), -np.inf)
-    for hi, h in enumerate(heads):
-        for j in range(n_q):
-            pos = prior_len + j
-            hi_t = min(t1, pos + 1)
-            if hi_t <= t0:
-                continue
-            q_t = w_uk[h].T @ q_nope[j, h]
-            q_r = rope_f64(q_rope[j, h], pos)
-            s = (c[t0:hi_t] @ q_t + kr[t0:hi_t] @ q_r) * scale
-            alpha, lse[j, hi] = _softmax_lse(s)
-            o_lat[j, hi] = alpha @ c[t0:hi_t]
-            o[j, hi] = w_uv[h] @ o_lat[j, hi]
+    for j in range(n_q):
+        pos = prior_len + j
+        hi_t = min(t1, pos + 1)
+        if hi_t <= t0:
+            continue
+        q_t = np.einsum("hd,hdm->hm", q_nope[j, heads], w_uk_s)          # [H, d_c]
+        q_r = rope_f64(q_rope[j, heads], pos)                           # [H, d_R]
+        s = (c[t0:hi_t] @ q_t.T + kr[t0:hi_t] @ q_r.T) * scale          # [T, H]
+        m = s.max(axis=0)
+        e = np.exp(s - m)
+        z = e.sum(axis=0)
+        o_lat[j] = (e / z).T @ c[t0:hi_t]
+        lse[j] = m + np.log(z)
+        o[j] = np.einsum("hm,hdm->hd", o_lat[j], w_uv_s)
     return o, o_lat, lse
 
 

@@ -92,6 +92,22 @@ def test_layer_fold_parity_small(name):
     assert rel_l2(np.concatenate(ys), np.concatenate(yr)) <= Y_REL_L2, rel_l2(np.concatenate(ys), np.concatenate(yr))
 
 
+def test_layer_fold_full_size_sampled():
+    """The folded layer benchmark workload at full size (B = 32, context 4096, the
+    1.2 GB of folded weights), in the bench's launch configuration; the oracle
+    checks the first and the last sequence."""
+    li = W.generate_layer(W.LAYER_WORKLOADS["layer_b32_l4096_fold"], seed=0)
+    s = run_layer(li, fold=True)
+    y = s.y.float().cpu().numpy().reshape(li.workload.batch, li.workload.n_q, -1)
+    ys, yr = [], []
+    for b in (0, li.workload.batch - 1):  # the folded path has no per-head O: the layer output is checked
+        y_ref, _ = oracle_layer(li, b)
+        ys.append(y[b]), yr.append(y_ref)
+    err = rel_l2(np.concatenate(ys), np.concatenate(yr))
+    print(f"layer_b32_l4096_fold: rel-L2 y {err:.3e}")
+    assert err <= Y_REL_L2, err
+
+
 def test_fold_weights_match_their_definition():
     """W_QK[(h, m), c] = sum_d W_UK[h, d, m] W_UQ[h*128 + d, c] and
     W_OV[j, (h, m)] = sum_d W_O[j, h*128 + d] W_UV[h, d, m], on sampled heads."""

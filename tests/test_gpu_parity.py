@@ -301,19 +301,58 @@ def test_invalid_arguments_raise():
 FULL = ["tiny_b1_l256", "batched_b32_l4096", "ragged_b128_l1024_8192", "long_b8_l32768", "mtp_b64_l8192_q4"]
 
 
+def oracle_sequence_absorbed(inp: W.Inputs, b: int, w_uk, w_uv):
+    """The oracle's absorbed fp64 form for sequence b, all heads (tied to the plain
+    definition by the absorption-identity pins)."""
+    c_bits, k_bits = (bits(x) for x in inp.sequence(b))
+    kv = c_bits.shape[0]
+    c = O.bf16_bits_to_f64(c_bits)
+    kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(kv)))
+    return O.decode_absorbed(O.bf16_bits_to_f64(bits(inp.q_nope[b])), O.bf16_bits_to_f64(bits(inp.q_rope[b])),
+                             w_uk, w_uv, c, kr, int(inp.prior_lens[b]))
+
+
 @pytest.mark.parametrize("name", FULL)
-def test_full_workload_sampled(name):
+def test_full_workload_every_sequence_and_head(name):
     """The five benchmark workloads at full size, in the bench's launch configuration.
 
-    The oracle checks sampled sequences (first, middle, last) on sampled heads,
-    and the cache rows of those sequences bit for bit.
+    Every sequence, query and head against the oracle's absorbed fp64 form (O, O'
+    and lse; relative L2 per sequence as well as overall, so that one mis-gathered
+    page in one sequence of many cannot hide in the aggregate); the plain
+    non-absorbed definition on sampled sequences and heads; the cache rows of the
+    sampled sequences bit for bit and this step's rows of every sequence.
     """
     wl = W.WORKLOADS[name]
     inp = W.generate(wl, seed=0)
     s = run_session(inp)
+    if s.fused_finish and s.num_splits > 1:
+        s.combine()
+        torch.cuda.synchronize()
+    o_gpu = s.out.float().cpu().numpy()
+    lat_gpu = s.o_latent.cpu().numpy()
+    lse_gpu = s.lse.cpu().numpy()
+    assert np.isfinite(o_gpu).all() and np.isfinite(lat_gpu).all() and np.isfinite(lse_gpu).all()
+    w_uk, w_uv = O.bf16_bits_to_f64(bits(inp.w_uk)), O.bf16_bits_to_f64(bits(inp.w_uv))
+    num = {"o": 0.0, "lat": 0.0}
+    den = {"o": 0.0, "lat": 0.0}
+    worst = {"o": 0.0, "lat": 0.0, "lse": 0.0, "o_abs": 0.0}
+    for b in range(inp.batch):
+        o_ref, lat_ref, lse_ref = oracle_sequence_absorbed(inp, b, w_uk, w_uv)
+        for key, got, ref in (("o", o_gpu[b], o_ref), ("lat", lat_gpu[b], lat_ref)):
+            d2, r2 = float(((got - ref) ** 2).sum()), float((ref ** 2).sum())
+            num[key] += d2
+            den[key] += r2
+            worst[key] = max(worst[key], (d2 / r2) ** 0.5)
+        worst["lse"] = max(worst["lse"], float(np.abs(lse_gpu[b] - lse_ref).max()))
+        worst["o_abs"] = max(worst["o_abs"], float(np.abs(o_gpu[b] - o_ref).max()))
+    print(f"{name}: rel-L2 O {(num['o'] / den['o']) ** 0.5:.3e} O' {(num['lat'] / den['lat']) ** 0.5:.3e}; "
+          f"worst sequence O {worst['o']:.3e} O' {worst['lat']:.3e}; max |dlse| {worst['lse']:.3e}; "
+          f"max |dO| {worst['o_abs']:.3e}")
+    assert worst["o"] <= O_REL_L2 and worst["lat"] <= LAT_REL_L2, worst
+    assert worst["lse"] <= LSE_MAX_ABS and worst["o_abs"] <= O_MAX_ABS, worst
+    # the plain definition on a sample (first, middle, last sequence; three heads)
     seqs = sorted({0, inp.batch // 2, inp.batch - 1})
-    heads = [0, 41, 127] if inp.batch > 1 else None
-    check_outputs(s, inp, seqs, heads)
+    check_outputs(s, inp, seqs, [0, 41, 127] if inp.batch > 1 else None)
     cache = s.cache
     pt = inp.page_table.numpy()
     for b in seqs:
@@ -323,3 +362,11 @@ def test_full_workload_sampled(name):
         c_bits, k_bits = (bits(x) for x in inp.sequence(b))
         assert np.array_equal(rows[:, :512], c_bits)
         assert np.array_equal(rows[:, 512:], O.rope_key_bf16_bits(k_bits, np.arange(kv)))
+    # this step's new rows of every sequence
+    c_new, k_new = inp.new_tokens()
+    pos = inp.prior_lens.numpy()[:, None] + np.arange(inp.n_q)[None, :]
+    pages = np.take_along_axis(pt, pos // 64, axis=1)
+    rows = bits(cache[torch.as_tensor(pages).long().to(cache.device), torch.as_tensor(pos % 64).to(cache.device)])
+    assert np.array_equal(rows[..., :512], bits(c_new))
+    assert np.array_equal(rows[..., 512:].reshape(-1, 64),
+                          O.rope_key_bf16_bits(bits(k_new).reshape(-1, 64), pos.reshape(-1)))

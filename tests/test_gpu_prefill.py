@@ -88,3 +88,30 @@ def test_both_paths_agree_on_short_steps(n_q):
     assert a.path == "absorbed" and n.path == "non_absorbed"
     check_prefill(n, inp, heads=[0, 31, 127])
     assert rel_l2(n.out.float().cpu().numpy(), a.out.float().cpu().numpy()) <= 2 * O_REL_L2
+
+
+@pytest.mark.parametrize("name", sorted(n for n in W.PREFILL_WORKLOADS if not n.startswith("chunk_b1")))
+def test_prefill_full_size_sampled(name):
+    """The benched non-absorbed workloads at full size, in the bench's launch
+    configuration: a chunk of 512 new tokens after 4096 (B = 4; four query tiles
+    over 4,608 keys) and a 2048-token prompt (B = 8; sixteen query tiles per head).
+    The oracle checks every new token of the first and the last sequence on three
+    heads (the decompressed keys and values, O and lse), which spans every query
+    tile and every key tile of those sequences."""
+    inp = W.generate(W.PREFILL_WORKLOADS[name], seed=0)
+    s = session(inp)
+    assert s.path == "non_absorbed"
+    heads = [0, 77, 127]
+    o_gpu = s.out.float().cpu().numpy()
+    lse_gpu = s.lse.cpu().numpy()
+    o_all, r_all = [], []
+    for b in sorted({0, inp.batch - 1}):
+        o_ref, _, lse_ref = oracle_sequence(inp, b, heads)
+        o = o_gpu[b][:, heads]
+        assert np.isfinite(o).all()
+        assert np.abs(lse_gpu[b][:, heads] - lse_ref).max() <= LSE_MAX_ABS
+        o_all.append(o), r_all.append(o_ref)
+    o, r = np.concatenate(o_all), np.concatenate(r_all)
+    print(f"{name}: rel-L2 O {rel_l2(o, r):.3e} max |dO| {np.abs(o - r).max():.3e}")
+    assert np.abs(o - r).max() <= O_MAX_ABS, np.abs(o - r).max()
+    assert rel_l2(o, r) <= O_REL_L2, rel_l2(o, r)

@@ -197,14 +197,92 @@ def test_decompressed_keys_obey_the_absorption_identity():
             assert abs(lse[j, h] - (sc.max() + np.log(a.sum()))) <= 1e-12
 
 
+def check_softmax_weights(decode=O.decode_mha, seed=5):
+    """decode_mha's own weights, read out through its latent output: with one-hot
+    latent rows c_t = e_t, O' = sum_t alpha_t e_t is the weight vector itself.  Each
+    row must be >= 0, sum to 1, vanish past the query's position, and equal the
+    softmax of the scores computed by explicit loops over eq. (2)."""
+    rng = np.random.default_rng(seed)
+    kv, n_q, d_c = 7, 7, 8
+    p = tiny(rng, kv=kv, n_q=n_q, d_c=d_c)
+    p["c"] = np.eye(kv, d_c)
+    _, o_lat, _ = decode(p["q_nope"], p["q_rope"], p["w_uk"], p["w_uv"], p["c"], p["kr"], prior_len=0)
+    for j in range(n_q):          # query j sits at position j and sees tokens 0..j
+        for h in range(2):
+            a = o_lat[j, h]
+            if (a < 0).any() or abs(a.sum() - 1.0) > 1e-14 or np.abs(a[j + 1:]).max(initial=0.0) != 0.0:
+                return False
+            s = [score_loops(p["q_nope"][j, h], p["q_rope"][j, h], p["w_uk"][h], p["c"][t], p["kr"][t], j)
+                 for t in range(j + 1)]
+            e = [math.exp(x - max(s)) for x in s]
+            if not np.allclose(a[:j + 1], [x / sum(e) for x in e], rtol=1e-12, atol=1e-15):
+                return False
+    return True
+
+
 def test_softmax_rows_sum_to_one():
-    rng = np.random.default_rng(5)
-    p = tiny(rng, kv=7)
-    for pos in range(7):
-        a = O.attention_weights_mha(p["q_nope"][0, 1], p["q_rope"][0, 1], p["w_uk"][1], p["c"], p["kr"], pos)
-        assert a.shape == (pos + 1,)
-        assert (a >= 0).all()
-        assert abs(a.sum() - 1.0) <= 1e-14
+    assert check_softmax_weights()
+
+
+def check_out_absorb(out_absorb=O.out_absorb, seed=21):
+    """O[..., h, d] = sum_m O'[..., h, m] W_UV[h, d, m] ([N1] final einsum 'bhm,hdm->bhd')
+    by explicit loops, on a non-square case with leading batch/query axes."""
+    rng = np.random.default_rng(seed)
+    B, n_q, n_h, d_v, d_c = 2, 3, 3, 5, 7
+    o_lat = rng.normal(size=(B, n_q, n_h, d_c))
+    w_uv = rng.normal(size=(n_h, d_v, d_c))
+    got = out_absorb(o_lat, w_uv)
+    if got.shape != (B, n_q, n_h, d_v):
+        return False
+    for b in range(B):
+        for j in range(n_q):
+            for h in range(n_h):
+                want = value_loops(w_uv[h], o_lat[b, j, h])
+                if not np.allclose(got[b, j, h], want, rtol=1e-13, atol=1e-13):
+                    return False
+    return True
+
+
+def test_out_absorb_matches_explicit_loops():
+    assert check_out_absorb()
+
+
+def test_out_absorb_of_the_latent_output_is_the_output():
+    """Value absorption ([DP] "3) MLA 中怎么吸收"): W_UV applied to O' = sum alpha c gives
+    decode_mha's non-absorbed O = sum alpha W_UV c."""
+    rng = np.random.default_rng(22)
+    p = tiny(rng, kv=6, n_q=3, d_h=5, d_c=9)
+    o, o_lat, _ = O.decode_mha(p["q_nope"], p["q_rope"], p["w_uk"], p["w_uv"], p["c"], p["kr"], prior_len=3)
+    assert relerr(O.out_absorb(o_lat, p["w_uv"]), o) <= 1e-12
+
+
+def check_absorb_query(absorb=O.absorb_query, seed=23):
+    """The absorbed query of every token of a multi-token, multi-sequence step:
+    latent half q~[m] = sum_d q^C[d] W_UK[h, d, m] by loops ([N1] 'bhd,hdm->bhm'),
+    position half RoPE(q^R) at position L_b + j as a complex rotation ([DP] eq. (8))."""
+    rng = np.random.default_rng(seed)
+    B, n_q, n_h, d_h, d_c, d_r = 3, 4, 2, 3, 5, 8
+    q_nope = rng.normal(size=(B, n_q, n_h, d_h))
+    q_rope = rng.normal(size=(B, n_q, n_h, d_r))
+    w_uk = rng.normal(size=(n_h, d_h, d_c))
+    prior = np.array([0, 17, 4093])
+    pos = prior[:, None] + np.arange(n_q)[None, :]
+    got = absorb(q_nope, q_rope, w_uk, pos)
+    if got.shape != (B, n_q, n_h, d_c + d_r):
+        return False
+    for b in range(B):
+        for j in range(n_q):
+            for h in range(n_h):
+                lat = [sum(q_nope[b, j, h, d] * w_uk[h, d, m] for d in range(d_h)) for m in range(d_c)]
+                rot = rope_complex(list(q_rope[b, j, h]), int(pos[b, j]))
+                if not (np.allclose(got[b, j, h, :d_c], lat, rtol=1e-13, atol=1e-13)
+                        and np.allclose(got[b, j, h, d_c:], rot, rtol=1e-12, atol=1e-12)):
+                    return False
+    return True
+
+
+def test_absorb_query_latent_and_rope_halves():
+    assert check_absorb_query()
 
 
 def test_one_token_closed_form():
@@ -408,6 +486,19 @@ def test_planted_mistakes(monkeypatch):
         return O.decode_mha(q_nope, q_rope, w_uk, w_uv, c, np.zeros_like(kr), prior_len, heads)
     assert not check_two_tokens(decode=mha_no_rope)
     assert not check_absorbed_identity(mha=mha_no_rope)
+
+    # the softmax weights: a wrong scale or a dropped RoPE term moves them off the loop scores
+    assert not check_softmax_weights(decode=mha_no_rope)
+
+    # out_absorb: the wrong head's weights, or W_UV's output and latent axes swapped on a square slice
+    assert not check_out_absorb(lambda o, w: O.out_absorb(o, np.roll(w, 1, axis=0)))
+    assert not check_out_absorb(lambda o, w: np.einsum("...hm,hmd->...hd", o[..., :5],
+                                                       np.asarray(w)[:, :, :5]))
+
+    # absorb_query: RoPE at position pos - 1, no RoPE at all, or W_UK's rows for the wrong head
+    assert not check_absorb_query(lambda qn, qr, w, pos: O.absorb_query(qn, qr, w, np.asarray(pos) - 1))
+    assert not check_absorb_query(lambda qn, qr, w, pos: O.absorb_query(qn, qr, w, np.zeros_like(pos)))
+    assert not check_absorb_query(lambda qn, qr, w, pos: O.absorb_query(qn, qr, np.roll(w, 1, axis=0), pos))
 
     # a causal off-by-one (query sees one token too few)
     def mha_off_by_one(q_nope, q_rope, w_uk, w_uv, c, kr, prior_len, heads=None):
