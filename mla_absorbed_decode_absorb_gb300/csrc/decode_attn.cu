@@ -28,23 +28,37 @@
 // for the TMA writes and the score exchange (SS MMAs, which also read A from
 // shared memory, slowed down severalfold next to them).  Only the 32 RoPE query
 // columns stay in shared memory.  TMEM then holds O' (256 columns), the query
-// (128) and two 64-column score buffers, one per row warpgroup, so QK^T of the
-// next page never waits for the scores of the last one to be read; P goes to
-// shared memory (the A operand of P V, which reads it once per page), with a
-// 4-stage ring of half-pages beside it.
+// (128) and two 64-column score buffers (page i uses buffer i & 1), so QK^T of
+// the next page never waits for the scores of the last one to be read (with a
+// single score buffer that hand-over, some 700 cycles per page, bounded the
+// page rate); P goes to shared memory (the A operand of P V), with a 4-slot ring
+// of half-pages beside it.
 //
-// Warp roles: warp 0 issues TMA loads (page ids are read 32 at a time); warp 1
-// allocates TMEM and one of its threads issues the QK^T MMAs, while one thread
-// of warp 11 issues the P V MMAs: an MMA issue blocks until the tensor pipe
-// takes it, so with a single issuer a ready P V waited behind a whole QK^T
-// batch (and the reverse); warps 2-9 are two row warpgroups, one thread per head row,
-// and warpgroup g handles the pages i = g (mod 2): it reads the partial scores
-// of page i from its TMEM score buffer (which frees it for QK^T of page i + 2),
-// swaps them with the peer CTA, adds them, runs the softmax step and writes
-// P(i) into its own shared-memory P buffer.  The two warpgroups
-// pass only the running reference max to each other, so the exchange of page
-// i + 1 overlaps the softmax of page i.  Warp 10 re-arms each exchange buffer
-// once it has been read and tells the peer (a cluster-scope release that would
+// The per-page work of the row threads is a chain of waits (the peer's partial
+// scores arrive some 1,300 cycles after a CTA sends its own, and the two CTAs
+// of a cluster drift apart by up to a page), about 3,900 cycles in all, so
+// three row warpgroups take the pages in turn (page i goes to warpgroup i mod 3)
+// and the chain of one page overlaps those of the next two.  Exchange buffers
+// and P buffers are used by page parity: a warpgroup waits on a buffer only
+// until the page two before its own has released it.  The mbarriers that signal
+// those buffers (P V finished, partial scores landed, partial scores read by the
+// peer, scores in TMEM, scores read) are kept per page mod 4, not per page
+// parity: a parity wait is only
+// sound when the waiter cannot be two phases ahead, and a warpgroup's own
+// history (its page three back, and the max handed down to it) guarantees the
+// events of page i - 4 but not those of page i - 2.
+//
+// Warp roles: warp 0 issues TMA loads (the query first, then the pages; page
+// ids are read 32 at a time); warp 1 allocates TMEM and one of its threads
+// issues the QK^T MMAs, while one thread of warp 15 issues the P V MMAs: an MMA
+// issue blocks until the tensor pipe takes it, so with a single issuer a ready
+// P V waited behind a whole QK^T batch (and the reverse); warps 2-13 are the
+// three row warpgroups, one thread per head row: warpgroup g reads the partial
+// scores of its page from its TMEM score buffer (which frees it for QK^T two
+// pages on), swaps them with the peer CTA, adds them, runs the softmax step
+// and writes P into shared memory.  The warpgroups pass only the running reference max
+// on to the next page's warpgroup.  Warp 14 re-arms each exchange buffer once it
+// has been read and tells the peer (a cluster-scope release that would
 // otherwise stall a row warpgroup).  The reference max is updated lazily: O' in
 // TMEM is rescaled only when a page raises a row's max by more than 2^8; each
 // warpgroup keeps its own partial row sum relative to the max it last used.
@@ -59,21 +73,22 @@ using namespace sm100;
 constexpr int kStages = 4;
 // When the producer turns to page i it first pulls page i + kL2Ahead into L2:
 // that page's TMA load, issued about one slot period later, then pays the L2
-// latency instead of the DRAM one, which shortens the life of a ring slot (the
-// four slots bound the page rate).  Measured at B = 32, L = 4096: 1 or 2 ahead
-// 53.3-53.6 us, 4 ahead 55.0, 8 ahead 60.1, 12 ahead 64.8, none 60.4.
+// latency instead of the DRAM one, which shortens the life of a ring slot.
+// Measured at B = 32, L = 4096: 1 or 2 ahead 53.3-53.6 us, 4 ahead 55.0,
+// 8 ahead 60.1, 12 ahead 64.8, none 60.4.
 constexpr int kL2Ahead = 1;
-constexpr int kThreads = 384;
+constexpr int kRowWGs = 3;
+constexpr int kThreads = 128 * kRowWGs + 128;
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kRowWarp0 = 2;        // warps 2-5: row warpgroup 0, warps 6-9: row warpgroup 1
-constexpr int kSignalWarp = 10;
-constexpr int kPvWarp = 11;
+constexpr int kRowWarp0 = 2;        // warps 2-13: row warpgroups 0, 1, 2
+constexpr int kSignalWarp = kRowWarp0 + 4 * kRowWGs;
+constexpr int kPvWarp = kSignalWarp + 1;
 constexpr int kRowThreads = 128;    // threads of each row warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O' half: [0, 256)
-constexpr uint32_t kTmemS = 256;    // score buffer of warpgroup g: [256 + 64g, 320 + 64g)
-constexpr uint32_t kTmemQ = 384;    // the CTA's 256 latent query columns as bf16 pairs: [384, 512)
+constexpr uint32_t kTmemQ = 256;    // the CTA's 256 latent query columns as bf16 pairs: [256, 384)
+constexpr uint32_t kTmemS = 384;    // partial scores of page i: [384 + 64 (i & 1), 448 + 64 (i & 1))
 
 constexpr int kQRope = 128 * 64;      // 32 RoPE query columns x 128 heads, 64-byte rows (SW64)
 constexpr int kPChunk = 64 * 128;     // 64 latent columns x 64 tokens (SW128)
@@ -93,20 +108,29 @@ constexpr float kSumScaleLog2 = kScaleLog2 * 256.f;
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kOffQ + kQRope;
 constexpr int kOffX = kOffStage + kStages * kStageBytes;
-// P of warpgroup g: 128 rows x 64 bf16, K-major with the 128-byte swizzle (the A
-// operand of P V), row r at r * 128 with 16-byte chunk c at (c ^ (r & 7)) * 16.
+// P of page i in buffer i & 1: 128 rows x 64 bf16, K-major with the 128-byte
+// swizzle (the A operand of P V), row r at r * 128 with 16-byte chunk c at
+// (c ^ (r & 7)) * 16.
 constexpr int kPBytes = kHeads * 128;
 constexpr int kOffP = kOffX + 2 * kXBufBytes;
 constexpr int kOffBar = kOffP + 2 * kPBytes;
-constexpr int kOffMax = kOffBar + 256;          // per-row reference max handed between warpgroups
+// At the start the CTA's 256 latent query columns (128 rows) land by TMA in ring
+// slots 2 and 3 as four 64-column boxes with the 128-byte swizzle (row r of box b
+// at b * 16 KB + r * 128, its 16-byte chunk c at (c ^ (r & 7)) * 16); row
+// warpgroups 0 and 1 move them into TMEM, and only then do pages 2 and 3 load there.
+constexpr int kQBoxBytes = kHeads * 128;
+constexpr int kQStageSlot = 2;
+constexpr int kOffQStage = kOffStage + kQStageSlot * kStageBytes;
+static_assert(kQStageSlot + 2 == kStages && 4 * kQBoxBytes <= 2 * kStageBytes, "query staging fits in the last two slots");
+constexpr int kOffMax = kOffBar + 512;            // per-row reference max handed between warpgroups
 constexpr int kOffFin = kOffMax + 4 * kHeads;     // per-warpgroup (max, sum) per row at the end
-constexpr int kSmemBytes = kOffFin + 8 * 2 * kHeads + 1024;  // + 1 KB alignment slack
+constexpr int kSmemBytes = kOffFin + 8 * kRowWGs * kHeads + 1024;  // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1 KB");
 
 constexpr float kRescaleLog2 = 8.f;
-// Output staging at the end: warpgroup g's 128 x 128 fp32 tile of O' as four
-// 32-column boxes in the ring (idle by then).
+// Output staging at the end: row warpgroup g < 2 stages its 128 x 128 fp32 tile
+// of O' as four 32-column boxes in the ring (idle by then).
 constexpr int kOBoxBytes = 128 * 128;
 constexpr int kOTileBytes = 4 * kOBoxBytes;
 static_assert(2 * kOTileBytes <= kStages * kStageBytes, "output staging fits in the ring");
@@ -114,28 +138,28 @@ static_assert(2 * kOTileBytes <= kStages * kStageBytes, "output staging fits in 
 struct Bars {
   uint64_t full[kStages];
   uint64_t empty[kStages];
-  uint64_t q_full;      // RoPE query columns in shared memory
-  uint64_t q_tmem;      // latent query columns in TMEM
-  uint64_t s_full[2];   // partial scores of warpgroup g's current page are in the score buffer
-  uint64_t s_free[2];   // warpgroup g has read them
-  uint64_t p_full[2];   // P of warpgroup g's current page is in its P buffer (and O' rescaled)
-  uint64_t pv_done[2];  // P V of the last page of warpgroup g has finished
-  uint64_t x_full[2];   // peer's partial scores landed in exchange buffer g
-  uint64_t x_free[2];   // peer has read our partial scores from its buffer g
-  uint64_t x_read[2];   // all rows of warpgroup g have read exchange buffer g
-  uint64_t hand[2];     // warpgroup g has published the reference max of its page
-  uint64_t fin;         // both warpgroups have published their final (max, sum)
-  uint64_t drain;       // both issuers' MMAs have finished
+  uint64_t q_full;            // RoPE query columns in shared memory
+  uint64_t q_lat;             // latent query columns staged in ring slots 3-4
+  uint64_t q_tmem;            // latent query columns in TMEM
+  uint64_t s_full[4];         // partial scores of the last page i = k (mod 4) are in score buffer i & 1
+  uint64_t s_free[4];         // ... and have been read (QK^T of page i + 2 may overwrite them)
+  uint64_t hand[kRowWGs];     // warpgroup g has published the reference max of its page
+  uint64_t p_full[2];         // P of the current page of parity k is in P buffer k (and O' rescaled)
+  uint64_t pv_done[4];        // P V of the last page i = k (mod 4) has finished
+  uint64_t x_full[4];         // peer's partial scores of page i = k (mod 4) landed (buffer i & 1)
+  uint64_t x_free[4];         // peer has read our partial scores of page i = k (mod 4)
+  uint64_t x_read[2];         // all rows have read exchange buffer k
+  uint64_t fin;               // every warpgroup has published its final (max, sum)
+  uint64_t drain;             // both issuers' MMAs have finished
   uint32_t tmem_base;
   int abort;
-  int wg_bad[2];        // a row of warpgroup g has no valid result: it writes zeros
+  int wg_bad[kRowWGs];        // a row of warpgroup g has no valid result: the outputs are zeros
 };
-static_assert(sizeof(Bars) <= 256, "barrier block");
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 struct Params {
   const int32_t* page_table;
   const int32_t* kv_lens;
-  const uint16_t* q_abs;
   float* o_out;
   float* lse_out;
   int* status;
@@ -150,7 +174,8 @@ struct Params {
 __device__ __forceinline__ uint32_t bar_addr(uint64_t& b) { return smem_u32(&b); }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_constant__ CUtensorMap tm_c128,
+decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_constant__ CUtensorMap tm_q64,
+                      const __grid_constant__ CUtensorMap tm_c128,
                       const __grid_constant__ CUtensorMap tm_c64, const __grid_constant__ CUtensorMap tm_o,
                       const Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -172,25 +197,29 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       mbar_init(bar_addr(bars.empty[s]), 1);
     }
     mbar_init(bar_addr(bars.q_full), 1);
+    mbar_init(bar_addr(bars.q_lat), 1);
     mbar_init(bar_addr(bars.q_tmem), 2 * kRowThreads);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_addr(bars.s_full[s]), 1);
-      mbar_init(bar_addr(bars.s_free[s]), kRowThreads);
-      mbar_init(bar_addr(bars.p_full[s]), kRowThreads);
-      mbar_init(bar_addr(bars.pv_done[s]), 1);
-      mbar_init(bar_addr(bars.x_full[s]), 1);
-      mbar_init(bar_addr(bars.x_free[s]), 1);
-      mbar_init(bar_addr(bars.x_read[s]), kRowThreads);
-      mbar_init(bar_addr(bars.hand[s]), kRowThreads);
+    for (int g = 0; g < kRowWGs; ++g) {
+      mbar_init(bar_addr(bars.hand[g]), kRowThreads);
+      bars.wg_bad[g] = 0;
     }
-    mbar_init(bar_addr(bars.fin), 2 * kRowThreads);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(bar_addr(bars.p_full[k]), kRowThreads);
+      mbar_init(bar_addr(bars.x_read[k]), kRowThreads);
+    }
+    for (int k = 0; k < 4; ++k) {
+      mbar_init(bar_addr(bars.s_full[k]), 1);
+      mbar_init(bar_addr(bars.s_free[k]), kRowThreads);
+      mbar_init(bar_addr(bars.pv_done[k]), 1);
+      mbar_init(bar_addr(bars.x_full[k]), 1);
+      mbar_init(bar_addr(bars.x_free[k]), 1);
+    }
+    mbar_init(bar_addr(bars.fin), kRowWGs * kRowThreads);
     mbar_init(bar_addr(bars.drain), 2);
     bars.abort = 0;
-    bars.wg_bad[0] = bars.wg_bad[1] = 0;
     fence_mbar_init();
-    // arm the first use of both exchange buffers: 16 KB of the peer's partial scores each
-    mbar_arrive_expect_tx(bar_addr(bars.x_full[0]), kXTxBytes);
-    mbar_arrive_expect_tx(bar_addr(bars.x_full[1]), kXTxBytes);
+    // armed for pages 0-3: 16 KB of the peer's partial scores each
+    for (int k = 0; k < 4; ++k) mbar_arrive_expect_tx(bar_addr(bars.x_full[k]), kXTxBytes);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars.tmem_base), kTmemCols);
@@ -205,6 +234,27 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
   grid_dep_wait();
   grid_dep_launch();
 
+  // The query (its latent half r and RoPE half r) does not depend on the unit's
+  // token range: it is requested first, and the page ids of the split are read
+  // while the sequence length is still on its way.
+  int ids = 0, ids_next = 0;
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_qlat);
+      tma_prefetch_desc(&tm_q64);
+      mbar_arrive_expect_tx(bar_addr(bars.q_lat), 4 * kQBoxBytes);
+      tma_load_3d(smem_u32(smem + kOffQStage), &tm_qlat, 0, bj * kHeads, 4 * rank, bar_addr(bars.q_lat));
+      mbar_arrive_expect_tx(bar_addr(bars.q_full), kQRope);
+      tma_load_2d(smem_u32(smem + kOffQ), &tm_q64, kLatent + 32 * rank, bj * kHeads, bar_addr(bars.q_full));
+      tma_prefetch_desc(&tm_c128);
+      tma_prefetch_desc(&tm_c64);
+    }
+    const int pb = split * p.split_pages;
+    const int32_t* pt0 = p.page_table + static_cast<int64_t>(b) * p.pt_stride + pb;
+    ids = pb + lane < p.pt_stride ? pt0[lane] : 0;
+    ids_next = pb + 32 + lane < p.pt_stride ? pt0[32 + lane] : 0;
+  }
+
   // The unit's token range [t_begin, t_end): identical in both CTAs of the cluster.
   const int kv = p.kv_lens[b];
   const bool bad = kv > p.max_kv_len || kv < p.n_q || (kv + kPage - 1) / kPage > p.pt_stride;
@@ -218,26 +268,12 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     // ------------------------------------------------------------ TMA producer
     if (n_pages > 0) {
       const int32_t* pt = p.page_table + static_cast<int64_t>(b) * p.pt_stride + page_begin;
-      int ids = lane < n_pages ? pt[lane] : 0;
-      int ids_next = 32 + lane < n_pages ? pt[32 + lane] : 0;
-      if (lane == 0) {
-        tma_prefetch_desc(&tm_q64);
-        tma_prefetch_desc(&tm_c128);
-        tma_prefetch_desc(&tm_c64);
-        // the RoPE query half r into shared memory
-        mbar_arrive_expect_tx(bar_addr(bars.q_full), kQRope);
-        tma_load_2d(smem_u32(smem + kOffQ), &tm_q64, kLatent + 32 * rank, bj * kHeads, bar_addr(bars.q_full));
-      }
       // this CTA's 288 columns of a page into L2
       auto prefetch = [&](int page) {
         if (page < 0 || page >= p.num_pages) return;
         tma_prefetch_l2_3d(&tm_c128, 0, page * kPage, 4 * rank);
         tma_prefetch_l2_2d(&tm_c64, kLatent + 32 * rank, page * kPage);
       };
-      for (int q = kStages; q < min(kL2Ahead, n_pages); ++q) {
-        const int page = __shfl_sync(0xffffffffu, ids, q);
-        if (lane == 0) prefetch(page);
-      }
       bool ok = true;
       for (int base = 0; base < n_pages && ok; base += 32) {
         const int cnt = min(32, n_pages - base);
@@ -249,7 +285,9 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
           if (lane == 0 && i + kL2Ahead < n_pages) prefetch(k + kL2Ahead < 32 ? ahead_a : ahead_b);
           if (lane == 0) {
             const int s = i % kStages;
-            ok = mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
+            // slots 3-4 hold the staged query until the row threads have moved it to TMEM
+            if (i == kQStageSlot) ok = mbar_wait(bar_addr(bars.q_tmem), 0, p.status, abort);
+            ok = ok && mbar_wait(bar_addr(bars.empty[s]), ((i / kStages) & 1) ^ 1, p.status, abort);
             if (ok) {
               if (page < 0 || page >= p.num_pages) {
                 record_status(p.status, MLA_ERR_BOUNDS);
@@ -268,10 +306,15 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         ids = ids_next;
         ids_next = base + 64 + lane < n_pages ? pt[base + 64 + lane] : 0;
       }
+    } else if (lane == 0) {
+      // nothing to do, but no copy into this CTA's shared memory may still be in
+      // flight when it exits
+      mbar_wait(bar_addr(bars.q_lat), 0, p.status, abort);
+      mbar_wait(bar_addr(bars.q_full), 0, p.status, abort);
     }
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ------------------------------------------------------------ tcgen05 issuers
-    // One thread of warp 1 issues QK^T and one thread of warp 11 issues P V,
+    // One thread of warp 1 issues QK^T and one thread of warp 15 issues P V,
     // each blocking on its own barriers, so that neither kind waits behind the
     // other's issue (an MMA issue returns only once the tensor pipe accepts it).
     // They touch disjoint TMEM (scores / O' and P) and a stage is released by
@@ -290,7 +333,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       // scores of page i - 2 have been read out of that buffer.
       for (int i = 0; i < n_pages && ok; ++i) {
         ok = mbar_wait(bar_addr(bars.full[i % kStages]), (i / kStages) & 1, p.status, abort);
-        if (ok && i > 1) ok = mbar_wait(bar_addr(bars.s_free[i & 1]), ((i - 2) >> 1) & 1, p.status, abort);
+        if (ok && i > 1) ok = mbar_wait(bar_addr(bars.s_free[(i - 2) & 3]), ((i - 2) >> 2) & 1, p.status, abort);
         if (!ok) break;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(((i % kStages) * kStageBytes) >> 4);
@@ -303,15 +346,15 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         // RoPE part: A = query columns in shared memory
         mma_ss(d, d_qr, d_k64 + so, idesc_qk, 1u);
         mma_ss(d, d_qr + 2, d_k64 + so + 2, idesc_qk, 1u);
-        mma_commit(bar_addr(bars.s_full[i & 1]));
+        mma_commit(bar_addr(bars.s_full[i & 3]));
       }
     }
     if (n_pages > 0 && lane == 0 && warp == kPvWarp) {
       const uint32_t idesc_pv = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/1);
       const uint64_t d_v = smem_desc(st0, kPChunk, 1024, kSw128);  // values (MN-major)
-      const uint64_t d_p = smem_desc(smem_u32(smem + kOffP), 16, 1024, kSw128);  // P of warpgroup 0 (K-major)
+      const uint64_t d_p = smem_desc(smem_u32(smem + kOffP), 16, 1024, kSw128);  // P buffer 0 (K-major)
       // O' += P(i) V(i) once P(i) is written; then page i's stage goes back to
-      // the producer and warpgroup i & 1 may reuse its P buffer.
+      // the producer and page i + 2 may reuse the P buffer.
       for (int i = 0; i < n_pages; ++i) {
         if (!mbar_wait(bar_addr(bars.p_full[i & 1]), (i >> 1) & 1, p.status, abort)) break;
         tc_fence_after();
@@ -321,7 +364,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
 #pragma unroll
         for (int k = 1; k < 4; ++k) mma_ss(tmem + kTmemO, a + 2 * k, vb + 128 * k, idesc_pv, 1u);
         mma_commit(bar_addr(bars.empty[i % kStages]));
-        mma_commit(bar_addr(bars.pv_done[i & 1]));
+        mma_commit(bar_addr(bars.pv_done[i & 3]));
       }
     }
     if (n_pages > 0 && lane == 0) {
@@ -334,42 +377,46 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
     // ------------------------------------------------------------ exchange buffer recycling
     if (lane == 0) {
       for (int i = 0; i < n_pages; ++i) {
-        const int buf = i & 1;
-        if (!mbar_wait(bar_addr(bars.x_read[buf]), (i >> 1) & 1, p.status, abort)) break;
-        mbar_arrive_expect_tx(bar_addr(bars.x_full[buf]), kXTxBytes);   // armed for the buffer's next use
-        mbar_arrive_remote(mapa(bar_addr(bars.x_free[buf]), peer));      // the peer may refill it
+        if (!mbar_wait(bar_addr(bars.x_read[i & 1]), (i >> 1) & 1, p.status, abort)) break;
+        mbar_arrive_expect_tx(bar_addr(bars.x_full[i & 3]), kXTxBytes);  // armed for page i + 4
+        mbar_arrive_remote(mapa(bar_addr(bars.x_free[i & 3]), peer));     // the peer may refill buffer i & 1
       }
     }
   } else {
     // ------------------------------------------------------------ row warpgroups
-    const int g = (warp - kRowWarp0) >> 2;  // warpgroup: pages i = g (mod 2)
+    const int g = (warp - kRowWarp0) >> 2;  // warpgroup: pages i = g (mod 3)
     const int quad = warp & 3;               // TMEM lane quarter this warp may access
     const int row = quad * 32 + lane;        // head
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     float* m_slot = reinterpret_cast<float*>(smem + kOffMax) + row;
     float2* fin = reinterpret_cast<float2*>(smem + kOffFin);
     bool ok = n_pages > 0;
-    if (ok) {
+    if (ok && g < 2) {
       // The query goes into the MMAs times 2^-8 (exact in bf16), so that the
       // partial scores come out as S_r * 2^-8, the form they are exchanged in.
-      // Latent query columns [256r + 128g, 256r + 128g + 128) of the row into TMEM as bf16 pairs.
-      const uint4* qsrc = reinterpret_cast<const uint4*>(p.q_abs + (static_cast<int64_t>(bj) * kHeads + row) * kRow +
-                                                         256 * rank + 128 * g);
+      // Latent query columns [256r + 128g, 256r + 128g + 128) of the row into TMEM
+      // as bf16 pairs, from the two 64-column boxes the producer staged by TMA
+      // (one bulk request per CTA instead of 16 scattered loads per thread, which
+      // the L1's outstanding-miss limit had spread over several microseconds).
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.q_lat), 0, p.status, abort));
+      if (ok) {
+        const uint8_t* qst = smem + kOffQStage + (2 * g) * kQBoxBytes + row * 128;
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
-        uint32_t w[32];
+        for (int h = 0; h < 2; ++h) {
+          uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = qsrc[8 * h + q];
-          w[4 * q] = bf16x2_times_2m8(v.x);
-          w[4 * q + 1] = bf16x2_times_2m8(v.y);
-          w[4 * q + 2] = bf16x2_times_2m8(v.z);
-          w[4 * q + 3] = bf16x2_times_2m8(v.w);
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4*>(qst + h * kQBoxBytes + ((q ^ (row & 7)) << 4));
+            w[4 * q] = bf16x2_times_2m8(v.x);
+            w[4 * q + 1] = bf16x2_times_2m8(v.y);
+            w[4 * q + 2] = bf16x2_times_2m8(v.z);
+            w[4 * q + 3] = bf16x2_times_2m8(v.w);
+          }
+          tmem_st32(tmem + lane_off + kTmemQ + 64 * g + 32 * h, w);
         }
-        tmem_st32(tmem + lane_off + kTmemQ + 64 * g + 32 * h, w);
       }
       tmem_wait_st();
-      if (g == 0) {
+      if (g == 0 && ok) {
         // the RoPE query columns (landed by TMA): this thread scales the 64 bytes of its row
         ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.q_full), 0, p.status, abort));
         if (ok) {
@@ -389,20 +436,20 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       tc_fence_before();
       mbar_arrive(bar_addr(bars.q_tmem));
     }
-    // exchange buffer g, this row: 16-byte unit q at q * 2048 + row * 16
-    uint8_t* xrow = smem + kOffX + g * kXBufBytes + row * 16;
-    const uint32_t x_remote = mapa(smem_u32(xrow), peer);
-    const uint32_t xfull_remote = mapa(bar_addr(bars.x_full[g]), peer);
-    const uint32_t s_addr = tmem + lane_off + kTmemS + 64 * g;
-    uint8_t* prow = smem + kOffP + g * kPBytes + row * 128;  // this row of P
+    // exchange buffer k, this row: 16-byte unit q at q * 2048 + row * 16
+    uint8_t* xrow0 = smem + kOffX + row * 16;
+    const uint32_t x_remote0 = mapa(smem_u32(xrow0), peer);
+    const uint32_t xfull_remote0 = mapa(bar_addr(bars.x_full[0]), peer);  // the peer's x_full[k] is 8k bytes on
+    const uint32_t s_addr0 = tmem + lane_off + kTmemS;
     const uint64_t scale2 = f32x2(kSumScaleLog2, kSumScaleLog2);
     float m_mine = -INFINITY, l = 0.f;  // reference max this warpgroup last used, and its partial sum
-    for (int i = g; i < n_pages && ok; i += 2) {
-      const uint32_t use = (i >> 1) & 1;
+    for (int i = g; i < n_pages && ok; i += kRowWGs) {
+      const int xb = i & 1;                      // score, exchange and P buffer of the page
       const int n_valid = min(kPage, t_end - (page_begin + i) * kPage);  // visible tokens of the page
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[g]), use, p.status, abort));
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.s_full[i & 3]), (i >> 2) & 1, p.status, abort));
       if (!ok) break;
       tc_fence_after();
+      const uint32_t s_addr = s_addr0 + 64 * xb;
       // this CTA's partial scores S_r * 2^-8 as fp16 pairs: word w holds columns 2w, 2w + 1
       uint32_t mine[32];
       {
@@ -411,24 +458,30 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         tmem_ld32(s_addr + 32, c);
         tmem_wait_ld();
         tc_fence_before();
-        mbar_arrive(bar_addr(bars.s_free[g]));  // QK^T of page i + 2 may overwrite the buffer
+        mbar_arrive(bar_addr(bars.s_free[i & 3]));  // QK^T of page i + 2 may overwrite the buffer
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
           mine[q] = pack_f16x2(__uint_as_float(a[2 * q]), __uint_as_float(a[2 * q + 1]));
           mine[16 + q] = pack_f16x2(__uint_as_float(c[2 * q]), __uint_as_float(c[2 * q + 1]));
         }
       }
-      // send: wait until the peer has read what this warpgroup sent two pages ago
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free[g]), use ^ 1u, p.status, abort));
-      if (!ok) break;
+      // send: wait until the peer has read what was sent for page i - 2 (same buffer)
+      if (i >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_free[(i - 2) & 3]), ((i - 2) >> 2) & 1,
+                                                       p.status, abort));
+        if (!ok) break;
+      }
+      const uint32_t x_remote = x_remote0 + xb * kXBufBytes;
+      const uint32_t xfull_remote = xfull_remote0 + 8 * (i & 3);
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         st_async_v4(x_remote + q * (kRowThreads * 16), mine[4 * q], mine[4 * q + 1], mine[4 * q + 2], mine[4 * q + 3],
                     xfull_remote);
       // receive the peer's partial scores; both CTAs add fp16(S_0) + fp16(S_1)
       // in fp16, in the same order, so they hold the same S * 2^-8
-      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full[g]), use, p.status, abort));
+      ok = __all_sync(0xffffffffu, mbar_wait_cluster(bar_addr(bars.x_full[i & 3]), (i >> 2) & 1, p.status, abort));
       if (!ok) break;
+      const uint8_t* xrow = xrow0 + xb * kXBufBytes;
       uint32_t sh[32];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -438,7 +491,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
         sh[4 * q + 2] = hadd2(mine[4 * q + 2], v.z);
         sh[4 * q + 3] = hadd2(mine[4 * q + 3], v.w);
       }
-      mbar_arrive(bar_addr(bars.x_read[g]));  // warp 10 recycles the exchange buffer
+      mbar_arrive(bar_addr(bars.x_read[xb]));  // warp 14 recycles the exchange buffer
       if (n_valid < kPage) {
         // columns past the last visible token (they may hold anything) become
         // -inf: out of the max, and exp gives 0 for them
@@ -458,13 +511,14 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       const uint32_t mm = hmax2(hmax2(hmax2(m8[0], m8[1]), hmax2(m8[2], m8[3])), hmax2(hmax2(m8[4], m8[5]), hmax2(m8[6], m8[7])));
       const float2 mf = unpack_f16x2(mm);
       const float mx = fmaxf(mf.x, mf.y) * kSumScaleLog2;
-      // the reference max after page i - 1 (from the other warpgroup)
+      // the reference max after page i - 1 (from the warpgroup of page i - 1)
       bool rescale = false;
       float factor = 1.f;
       if (i == 0) {
         m_mine = mx;
       } else {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.hand[g ^ 1]), ((i - 1) >> 1) & 1, p.status, abort));
+        const int gp = (i - 1) % kRowWGs;
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.hand[gp]), ((i - 1) / kRowWGs) & 1, p.status, abort));
         if (!ok) break;
         const float m_prev = *m_slot;
         if (m_prev != m_mine) {  // raised since this warpgroup's last page
@@ -511,16 +565,17 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
       // The P buffer is free once P V(i - 2) has finished; O' may only be
       // rescaled once P V(i - 1) has.
       if (i >= 2) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[g]), use ^ 1u, p.status, abort));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[(i - 2) & 3]), ((i - 2) >> 2) & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after();
       }
+      uint8_t* prow = smem + kOffP + xb * kPBytes + row * 128;  // this row of P(i)
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();  // visible to the P V MMAs
       if (__any_sync(0xffffffffu, rescale)) {
-        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[g ^ 1]), ((i - 1) >> 1) & 1, p.status, abort));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[(i - 1) & 3]), ((i - 1) >> 2) & 1, p.status, abort));
         if (!ok) break;
         tc_fence_after();
         for (int c0 = 0; c0 < 256; c0 += 32) {
@@ -531,62 +586,76 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_c
           for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
           tmem_st32(tmem + lane_off + kTmemO + c0, r);
         }
-        tmem_wait_st();
-        tc_fence_before();
       }
-      mbar_arrive(bar_addr(bars.p_full[g]));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_addr(bars.p_full[xb]));
     }
     // Exchanged partials are fp16(S_r / 256): one beyond |S_r| = 65520 * 256
     // (or a NaN) becomes infinite or NaN and leaves the row's max or sum non-finite.
     if (ok && g < n_pages && !(isfinite(l) && isfinite(m_mine))) record_status(p.status, MLA_ERR_RANGE);
 
-    // epilogue: combine the two warpgroups' sums, then warpgroup g writes
+    // epilogue: combine the warpgroups' sums, then warpgroup g < 2 writes
     // columns [128g, 128g + 128) of this CTA's half of O' (normalised)
     fin[g * kHeads + row] = make_float2(m_mine, l);
+    if (!ok) bars.wg_bad[g] = 1;
     mbar_arrive(bar_addr(bars.fin));
-    ok = ok && __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.fin), 0, p.status, abort));
-    const int last = n_pages - 1;
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[last & 1]), (last >> 1) & 1, p.status, abort));
-    tc_fence_after();
-    const int64_t out_row = (static_cast<int64_t>(bj) * p.num_splits + split) * kHeads + row;
-    // One decision per warpgroup: its 128 x 128 tile of O' is staged in the
-    // (now idle) ring and stored by TMA, or, if any of its rows has no valid
-    // result, the warpgroup writes zeros directly.
-    if (!ok && lane == 0) bars.wg_bad[g] = 1;
-    named_barrier_sync(1 + g, kRowThreads);
-    if (*reinterpret_cast<volatile int*>(&bars.wg_bad[g]) == 0) {
-      const float2 f0 = fin[row], f1 = fin[kHeads + row];
-      const float m = fmaxf(f0.x, f1.x);
-      const float lt = (f0.y > 0.f ? f0.y * ex2_approx(f0.x - m) : 0.f) + (f1.y > 0.f ? f1.y * ex2_approx(f1.x - m) : 0.f);
-      const float inv = 1.f / lt;
-      // four boxes of 32 fp32 columns x 128 rows, 128-byte swizzle: row r at
-      // r * 128, 16-byte chunk c at (c ^ (r & 7)) * 16
-      uint8_t* tile = smem + kOffStage + g * kOTileBytes;
-      const int32_t y0 = static_cast<int32_t>(out_row) - row;  // row 0 of the unit
-#pragma unroll 1
-      for (int k = 0; k < 4; ++k) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lane_off + kTmemO + 128 * g + 32 * k, r);
-        tmem_wait_ld();
-        uint8_t* brow = tile + k * kOBoxBytes + row * 128;
+    if (g < 2) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.fin), 0, p.status, abort));
+      const int last = n_pages - 1;
+      if (ok && last >= 0)
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_addr(bars.pv_done[last & 3]), (last >> 2) & 1, p.status, abort));
+      tc_fence_after();
+      const int64_t out_row = (static_cast<int64_t>(bj) * p.num_splits + split) * kHeads + row;
+      // One decision per warpgroup: its 128 x 128 tile of O' is staged in the
+      // (now idle) ring and stored by TMA, or, if any row of the CTA has no
+      // valid result, the warpgroup writes zeros directly.
+      if (!ok && lane == 0) bars.wg_bad[g] = 1;
+      named_barrier_sync(1 + g, kRowThreads);
+      volatile int* wb = bars.wg_bad;
+      bool any_bad = false;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          *reinterpret_cast<float4*>(brow + ((c ^ (row & 7)) << 4)) =
-              make_float4(__uint_as_float(r[4 * c]) * inv, __uint_as_float(r[4 * c + 1]) * inv,
-                          __uint_as_float(r[4 * c + 2]) * inv, __uint_as_float(r[4 * c + 3]) * inv);
-        fence_proxy_async_smem();  // visible to the TMA store
-        named_barrier_sync(1 + g, kRowThreads);
-        if (row == 0) {  // each box goes out as soon as it is staged
-          tma_store_2d(&tm_o, smem_u32(tile + k * kOBoxBytes), static_cast<int32_t>(rank * 256 + 128 * g + 32 * k), y0);
-          bulk_commit_group();
+      for (int k = 0; k < kRowWGs; ++k) any_bad = any_bad || wb[k] != 0;
+      if (!any_bad && n_pages > 0) {
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kRowWGs; ++k) m = fmaxf(m, fin[k * kHeads + row].x);
+        float lt = 0.f;
+#pragma unroll
+        for (int k = 0; k < kRowWGs; ++k) {
+          const float2 f = fin[k * kHeads + row];
+          lt += f.y > 0.f ? f.y * ex2_approx(f.x - m) : 0.f;
         }
+        const float inv = 1.f / lt;
+        // four boxes of 32 fp32 columns x 128 rows, 128-byte swizzle: row r at
+        // r * 128, 16-byte chunk c at (c ^ (r & 7)) * 16
+        uint8_t* tile = smem + kOffStage + g * kOTileBytes;
+        const int32_t y0 = static_cast<int32_t>(out_row) - row;  // row 0 of the unit
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          uint32_t r[32];
+          tmem_ld32(tmem + lane_off + kTmemO + 128 * g + 32 * k, r);
+          tmem_wait_ld();
+          uint8_t* brow = tile + k * kOBoxBytes + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(brow + ((c ^ (row & 7)) << 4)) =
+                make_float4(__uint_as_float(r[4 * c]) * inv, __uint_as_float(r[4 * c + 1]) * inv,
+                            __uint_as_float(r[4 * c + 2]) * inv, __uint_as_float(r[4 * c + 3]) * inv);
+          fence_proxy_async_smem();  // visible to the TMA store
+          named_barrier_sync(1 + g, kRowThreads);
+          if (row == 0) {  // each box goes out as soon as it is staged
+            tma_store_2d(&tm_o, smem_u32(tile + k * kOBoxBytes), static_cast<int32_t>(rank * 256 + 128 * g + 32 * k), y0);
+            bulk_commit_group();
+          }
+        }
+        if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
+        if (row == 0) bulk_wait_all();
+      } else {
+        float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
+        for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = -INFINITY;
       }
-      if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
-      if (row == 0) bulk_wait_all();
-    } else {
-      float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
-      for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = -INFINITY;
     }
   }
 
@@ -651,10 +720,11 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   if (units == 0) return cudaSuccess;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || !configure(dev)) return cudaErrorInvalidDevice;
-  CUtensorMap tq64, tc128, tc64, to;
+  CUtensorMap tqlat, tq64, tc128, tc64, to;
   const uint64_t q_rows = static_cast<uint64_t>(B) * n_q * kHeads;
   const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
-  if (!make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
+  if (!make_tmap_bf16_chunks(&tqlat, q_abs, q_rows, kRow, 128, 4) ||
+      !make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_bf16_chunks(&tc128, cache, c_rows, kRow, 64, 4) ||
       !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_f32_2d(&to, o_out, static_cast<uint64_t>(units) * kHeads, kLatent, kLatent, 32, 128,
@@ -663,7 +733,6 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   Params prm;
   prm.page_table = page_table;
   prm.kv_lens = kv_lens;
-  prm.q_abs = q_abs;
   prm.o_out = o_out;
   prm.lse_out = lse_out;
   prm.status = status;
@@ -674,7 +743,7 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   prm.split_pages = plan.split_pages;
   prm.num_splits = plan.num_splits;
   return launch_kernel(decode_attn_tc_kernel, dim3(static_cast<unsigned>(2 * units)), dim3(kThreads), kSmemBytes, stream,
-                       tq64, tc128, tc64, to, prm);
+                       tqlat, tq64, tc128, tc64, to, prm);
 }
 
 }  // namespace mla

@@ -16,7 +16,13 @@ pytestmark = pytest.mark.gpu
 
 O_MAX_ABS, O_REL_L2 = 1e-2, 5e-3       # final output O
 LAT_REL_L2 = 5e-3                      # latent output O'
-LSE_MAX_ABS = 2e-2                     # natural-log units
+# log-sum-exp, natural-log units.  Its error comes from the bf16 query (2^-9
+# relative per element) and the fp16 partial-score exchange.  With one or two
+# visible tokens the lse is essentially one score and carries that error whole
+# (up to 2.3e-3 seen in the small cases); over thousands of tokens the softmax
+# weights average it down (at most 6.0e-4 over every head and query of the five
+# full-size workloads).  The bound keeps a margin of about 2x over the largest.
+LSE_MAX_ABS = 5e-3
 
 
 def bits(t: torch.Tensor) -> np.ndarray:

@@ -104,14 +104,15 @@ def test_prefill_full_size_sampled(name):
     heads = [0, 77, 127]
     o_gpu = s.out.float().cpu().numpy()
     lse_gpu = s.lse.cpu().numpy()
-    o_all, r_all = [], []
+    o_all, r_all, dl = [], [], 0.0
     for b in sorted({0, inp.batch - 1}):
         o_ref, _, lse_ref = oracle_sequence(inp, b, heads)
         o = o_gpu[b][:, heads]
         assert np.isfinite(o).all()
-        assert np.abs(lse_gpu[b][:, heads] - lse_ref).max() <= LSE_MAX_ABS
+        dl = max(dl, float(np.abs(lse_gpu[b][:, heads] - lse_ref).max()))
         o_all.append(o), r_all.append(o_ref)
     o, r = np.concatenate(o_all), np.concatenate(r_all)
-    print(f"{name}: rel-L2 O {rel_l2(o, r):.3e} max |dO| {np.abs(o - r).max():.3e}")
+    print(f"{name}: rel-L2 O {rel_l2(o, r):.3e} max |dO| {np.abs(o - r).max():.3e} max |dlse| {dl:.3e}")
+    assert dl <= LSE_MAX_ABS, dl
     assert np.abs(o - r).max() <= O_MAX_ABS, np.abs(o - r).max()
     assert rel_l2(o, r) <= O_REL_L2, rel_l2(o, r)
