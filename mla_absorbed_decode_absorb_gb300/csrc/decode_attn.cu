@@ -227,7 +227,6 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any remote traffic
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   // global memory only from here on: the previous kernel of the stream has finished
@@ -263,6 +262,9 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_
   const int page_begin = t_begin / kPage;
   const int n_pages = t_end > t_begin ? (t_end + kPage - 1) / kPage - page_begin : 0;
   if (tid == 0 && bad && rank == 0) record_status(p.status, MLA_ERR_BOUNDS);
+  // the peer's barriers exist before any remote traffic (the first partial
+  // scores, long after the loads above are on their way)
+  cluster_sync();
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -650,7 +652,7 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_
           }
         }
         if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
-        if (row == 0) bulk_wait_all();
+        if (row == 0) bulk_wait_read<0>();  // the staging area has been read (the writes complete with the grid)
       } else {
         float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
         for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -610,7 +610,7 @@ decode_attn_fp8_kernel(const __grid_constant__ CUtensorMap tm_q64, const __grid_
         }
       }
       if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
-      if (row == 0) bulk_wait_all();
+      if (row == 0) bulk_wait_read<0>();  // the staging area has been read (the writes complete with the grid)
     } else {
       float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
       for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);

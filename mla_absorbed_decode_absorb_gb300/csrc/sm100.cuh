@@ -138,6 +138,10 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Every bulk store this thread committed has finished (shared memory read, global memory written).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// At most `n` of this thread's committed bulk stores may still be reading their
+// shared-memory source (their global writes may still be in flight).
+template <int n>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(n) : "memory"); }
 
 // 3-D variant of tma_prefetch_l2_2d.
 __device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, int32_t y, int32_t z) {
@@ -310,6 +314,18 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
       ::"r"(remote_addr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
       : "memory");
+}
+
+// 8- and 4-byte variants of st_async_v4.
+__device__ __forceinline__ void st_async_v2(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+               ::"r"(remote_addr), "r"(a), "r"(b), "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t a, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+               ::"r"(remote_addr), "r"(a), "r"(remote_bar)
+               : "memory");
 }
 
 // 128-byte swizzle of a byte offset inside a 1024-byte-aligned atom (16-byte
