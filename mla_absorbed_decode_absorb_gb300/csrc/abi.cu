@@ -526,7 +526,8 @@ mla_status mla_prefill_attn(const mla_bf16* q_nope, const mla_bf16* q_rope, cons
   if (!q_nope || !q_rope || !seq_lens_before || !rope_table || !k_nope || !v || !cache || !page_table ||
       !kv_lens || !out)
     return MLA_ERR_INVALID_ARG;
-  if (!aligned16(q_nope) || !aligned16(k_nope) || !aligned16(v) || !aligned16(cache) || !aligned16(out))
+  if (!aligned16(q_nope) || !aligned16(q_rope) || !aligned16(rope_table) || !aligned16(k_nope) || !aligned16(v) ||
+      !aligned16(cache) || !aligned16(out))
     return MLA_ERR_INVALID_ARG;
   if (pt_stride < (max_kv_len + kPage - 1) / kPage) return MLA_ERR_INVALID_ARG;
   int* st = status_ptr();

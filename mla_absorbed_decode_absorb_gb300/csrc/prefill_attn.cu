@@ -107,7 +107,7 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
       mbar_init(smem_u32(&bars.vfull[s]), 1);
       mbar_init(smem_u32(&bars.vempty[s]), 1);
     }
-    mbar_init(smem_u32(&bars.q_ready), 128);
+    mbar_init(smem_u32(&bars.q_ready), kSoftThreads);  // both halves of every query row
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_u32(&bars.s_full[s]), 1);
       mbar_init(smem_u32(&bars.s_free[s]), kSoftThreads);
@@ -268,38 +268,76 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     float* hmax = reinterpret_cast<float*>(smem + kOffHx);  // [4 tiles][2 halves][128 rows]
     float* fin = hmax + 4 * 2 * kQTile;                      // [2 halves][128 rows]
-    // query row: [q^C ; RoPE(q^R, pos)] into the three SW128 chunks (half 0)
-    if (hf == 0) {
-      const int64_t qrow = (static_cast<int64_t>(b) * p.n_q + j) * kHeads + h;
+    // The query tile [q^C ; RoPE(q^R, pos)] into the three SW128 chunks, by all 256
+    // softmax threads in 16-byte units: consecutive lanes take consecutive units of a
+    // row (a row of one head is 256 + 128 contiguous bytes, the next token's row of the
+    // same head 32 KB further on), so a warp's load covers two q^C rows or four q^R rows
+    // instead of 32 separate lines.  Every load is issued before the first shared-memory
+    // store (a store through a byte pointer may alias any load).
+    {
+      const int t = tid - 32 * kSoftWarp0;   // 0 .. 255
       uint8_t* qs = smem + kOffQ;
-      if (live && !bad) {
-        const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + qrow * kNope);
+      auto row_ok = [&](int rr) { return !bad && j0 + rr < p.n_q; };
+      auto qrow_of = [&](int rr) { return (static_cast<int64_t>(b) * p.n_q + j0 + rr) * kHeads + h; };
+      uint4 qn[8];       // q^C: unit u = t + 256 i, row u / 16, 16-byte column u % 16
+      uint4 qr[4];       // q^R: unit u = t + 256 i, row u / 8, elements 8 (u % 8) .. + 7
+      float4 cs[4][4];   // cos and sin of those elements' frequencies (two float4 each)
 #pragma unroll
-        for (int u = 0; u < 16; ++u)
-          *reinterpret_cast<uint4*>(qs + (u >> 3) * kChunk + sw128(r * 128 + (u & 7) * 16)) = qn[u];
-        const uint16_t* qr = p.q_rope + qrow * kRope;
-        const float* cs = p.rope + static_cast<int64_t>(pos) * kRope;
-        uint32_t w[32];
+      for (int i = 0; i < 8; ++i) {
+        const int u = t + 256 * i, rr = u >> 4;
+        qn[i] = row_ok(rr) ? __ldg(reinterpret_cast<const uint4*>(p.q_nope + qrow_of(rr) * kNope) + (u & 15))
+                           : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int f = 0; f < kHalfRope; f += 2) {
-          float o[4];
+      for (int i = 0; i < 4; ++i) {
+        const int u = t + 256 * i, rr = u >> 3, f0 = 8 * (u & 3);  // frequencies f0 .. f0 + 7
+        if (row_ok(rr)) {
+          qr[i] = __ldg(reinterpret_cast<const uint4*>(p.q_rope + qrow_of(rr) * kRope) + (u & 7));
+          const float4* tab = reinterpret_cast<const float4*>(p.rope + static_cast<int64_t>(L + j0 + rr) * kRope);
+          cs[i][0] = __ldg(tab + f0 / 4);
+          cs[i][1] = __ldg(tab + f0 / 4 + 1);
+          cs[i][2] = __ldg(tab + (kHalfRope + f0) / 4);
+          cs[i][3] = __ldg(tab + (kHalfRope + f0) / 4 + 1);
+        } else {
+          qr[i] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) cs[i][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int u = t + 256 * i;
+        *reinterpret_cast<uint4*>(qs + ((u & 15) >> 3) * kChunk + sw128((u >> 4) * 128 + (u & 7) * 16)) = qn[i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        // rotate-half: element f < 32 pairs with f + 32, four units (lane ^ 4) away
+        const int u = t + 256 * i;
+        const bool second = (u & 4) != 0;   // this unit holds elements 32 + f
+        const uint32_t mine[4] = {qr[i].x, qr[i].y, qr[i].z, qr[i].w};
+        uint32_t other[4], w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) other[k] = __shfl_xor_sync(0xffffffffu, mine[k], 4);
+        const float c8[8] = {cs[i][0].x, cs[i][0].y, cs[i][0].z, cs[i][0].w,
+                             cs[i][1].x, cs[i][1].y, cs[i][1].z, cs[i][1].w};
+        const float s8[8] = {cs[i][2].x, cs[i][2].y, cs[i][2].z, cs[i][2].w,
+                             cs[i][3].x, cs[i][3].y, cs[i][3].z, cs[i][3].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float o[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float x1 = bf16_bits_to_f32(qr[f + e]), x2 = bf16_bits_to_f32(qr[f + e + kHalfRope]);
-            const float c = cs[f + e], sn = cs[kHalfRope + f + e];
-            o[e] = __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn));
-            o[2 + e] = __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn));
+            const float a = __uint_as_float(e ? mine[k] & 0xffff0000u : mine[k] << 16);
+            const float bb = __uint_as_float(e ? other[k] & 0xffff0000u : other[k] << 16);
+            const float x1 = second ? bb : a, x2 = second ? a : bb;
+            const float c = c8[2 * k + e], sn = s8[2 * k + e];
+            o[e] = second ? __fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, sn))
+                          : __fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, sn));
           }
-          w[f / 2] = pack_bf16x2(o[0], o[1]);
-          w[16 + f / 2] = pack_bf16x2(o[2], o[3]);
+          w[k] = pack_bf16x2(o[0], o[1]);
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(qs + 2 * kChunk + sw128(r * 128 + u * 16)) =
-              make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-      } else {
-        for (int u = 0; u < 24; ++u)
-          *reinterpret_cast<uint4*>(qs + (u >> 3) * kChunk + sw128(r * 128 + (u & 7) * 16)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qs + 2 * kChunk + sw128((u >> 3) * 128 + (u & 7) * 16)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars.q_ready));
