@@ -56,6 +56,22 @@ inline bool make_tmap_bf16_chunks(CUtensorMap* map, const void* base, uint64_t r
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 tensor [d2][d1][d0] (d0 contiguous) with byte strides s1, s2 between
+// consecutive d1 and d2; box b0 x b1 x b2; out-of-range elements of a box read as zero.
+inline bool make_tmap_bf16_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                              uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2,
+                              CUtensorMapSwizzle swizzle) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Row-major byte matrix [rows, cols] with `row_stride` bytes between rows.
 inline bool make_tmap_u8_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t row_stride,
                             uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
