@@ -172,7 +172,12 @@ mla_status mla_append_absorb_q(const mla_bf16* c_kv_new, const mla_bf16* k_pe_ne
  *              (causal among the new tokens); kv_lens[b] >= n_q.
  *   max_kv_len host-side upper bound of kv_lens (sizes the grid without a sync);
  *              a sequence longer than it sets MLA_ERR_BOUNDS.
- *   split_pages pages per KV split (0 = choose automatically).
+ *   split_pages pages per KV split (0 = choose automatically: at most 2
+ *              (sequence, query) units over at most 1024 cached tokens then run
+ *              the short-context kernel, one CTA per 8 heads on warp-level
+ *              tensor-core tiles and no split, which mla_decode_uses_short_path
+ *              reports; otherwise the split count that fills the GPU with 2-CTA
+ *              tcgen05 clusters).
  *   workspace  device scratch of at least mla_decode_workspace_size() bytes
  *              (may be NULL when that size is 0).
  *   o_latent   [B, n_q, 128, 512] float32 out: O'[h] = sum_t alpha_t c_t
@@ -189,6 +194,8 @@ mla_status mla_decode_workspace_size(int B, int n_q, int max_kv_len, int split_p
                                      size_t* bytes);
 mla_status mla_decode_num_splits(int B, int n_q, int max_kv_len, int split_pages,
                                  int* num_splits);
+mla_status mla_decode_uses_short_path(int B, int n_q, int max_kv_len, int split_pages,
+                                      int* is_short);
 mla_status mla_decode_attn(const mla_bf16* q_abs, const mla_bf16* cache, int64_t num_pages,
                            const int32_t* page_table, int pt_stride, const int32_t* kv_lens,
                            int B, int n_q, int max_kv_len, int split_pages,

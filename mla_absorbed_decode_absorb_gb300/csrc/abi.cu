@@ -100,6 +100,9 @@ bool device_view(const void* p, size_t bytes, void** out, bool* host) {
 bool make_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan) {
   if (B < 0 || n_q < 1 || n_q > MLA_MAX_NQ || max_kv_len < n_q || split_pages < 0) return false;
   plan->max_pages = (max_kv_len + kPage - 1) / kPage;
+  plan->short_path = split_pages == 0 && max_kv_len <= kShortMaxKv &&
+                     static_cast<int64_t>(B) * n_q <= kShortMaxUnits;
+  if (plan->short_path) split_pages = plan->max_pages;  // one split: no merge
   if (split_pages == 0) {
     const int64_t units = static_cast<int64_t>(B > 0 ? B : 1) * n_q;
     const int64_t slots = decode_cluster_slots();
@@ -410,6 +413,13 @@ mla_status mla_decode_num_splits(int B, int n_q, int max_kv_len, int split_pages
   SplitPlan plan;
   if (num_splits == nullptr || !make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
   *num_splits = plan.num_splits;
+  return MLA_OK;
+}
+
+mla_status mla_decode_uses_short_path(int B, int n_q, int max_kv_len, int split_pages, int* is_short) {
+  SplitPlan plan;
+  if (is_short == nullptr || !make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
+  *is_short = plan.short_path ? 1 : 0;
   return MLA_OK;
 }
 

@@ -111,22 +111,45 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t* __r
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
   }
   // RoPE of the query's position branch while the copies are in flight; the
-  // head's M tiles share the (token, frequency) pairs.
-  for (int i = blockIdx.x * kThreads + tid; i < nt * kHalfRope; i += gridDim.x * kThreads) {
-    const int t = t0 + i / kHalfRope, f = i % kHalfRope;
-    const int b = t / n_q, j = t % n_q;
-    const int64_t pos = static_cast<int64_t>(lens[b]) + j;
-    uint16_t* row = q_abs + (static_cast<int64_t>(t) * kHeads + h) * kRow + kLatent;
-    if (pos < 0 || pos >= rope_max_pos) {
-      record_status(status, MLA_ERR_BOUNDS);
-      row[f] = row[f + kHalfRope] = 0;
-      continue;
+  // head's M tiles share the (token, frequency) pairs.  Four items per thread at a
+  // time with all their loads in flight together: the lengths, then the query
+  // pairs and the cos / sin pairs (two round trips per four items, not per item).
+  constexpr int kRopeBatch = 4;
+  const int rope_stride = gridDim.x * kThreads;
+  for (int i0 = blockIdx.x * kThreads + tid; i0 < nt * kHalfRope; i0 += kRopeBatch * rope_stride) {
+    int64_t pos[kRopeBatch];
+    bool on[kRopeBatch];
+#pragma unroll
+    for (int k = 0; k < kRopeBatch; ++k) {
+      const int i = i0 + k * rope_stride;
+      on[k] = i < nt * kHalfRope;
+      const int t = t0 + (on[k] ? i : 0) / kHalfRope;
+      pos[k] = on[k] ? static_cast<int64_t>(lens[t / n_q]) + t % n_q : 0;
     }
-    const uint16_t* x = q_rope + (static_cast<int64_t>(t) * kHeads + h) * kRope;
-    const float x1 = bf16_bits_to_f32(x[f]), x2 = bf16_bits_to_f32(x[f + kHalfRope]);
-    const float c = rope[pos * kRope + f], s = rope[pos * kRope + kHalfRope + f];
-    row[f] = f32_to_bf16_bits(__fsub_rn(__fmul_rn(x1, c), __fmul_rn(x2, s)));
-    row[f + kHalfRope] = f32_to_bf16_bits(__fadd_rn(__fmul_rn(x2, c), __fmul_rn(x1, s)));
+    float x1[kRopeBatch], x2[kRopeBatch], c[kRopeBatch], sn[kRopeBatch];
+#pragma unroll
+    for (int k = 0; k < kRopeBatch; ++k) {
+      const int i = i0 + k * rope_stride, t = t0 + i / kHalfRope, f = i % kHalfRope;
+      const bool in = on[k] && pos[k] >= 0 && pos[k] < rope_max_pos;
+      const uint16_t* x = q_rope + (static_cast<int64_t>(t) * kHeads + h) * kRope;
+      x1[k] = in ? bf16_bits_to_f32(x[f]) : 0.f;
+      x2[k] = in ? bf16_bits_to_f32(x[f + kHalfRope]) : 0.f;
+      c[k] = in ? rope[pos[k] * kRope + f] : 0.f;
+      sn[k] = in ? rope[pos[k] * kRope + kHalfRope + f] : 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < kRopeBatch; ++k) {
+      if (!on[k]) continue;
+      const int i = i0 + k * rope_stride, t = t0 + i / kHalfRope, f = i % kHalfRope;
+      uint16_t* row = q_abs + (static_cast<int64_t>(t) * kHeads + h) * kRow + kLatent;
+      if (pos[k] < 0 || pos[k] >= rope_max_pos) {
+        record_status(status, MLA_ERR_BOUNDS);
+        row[f] = row[f + kHalfRope] = 0;
+        continue;
+      }
+      row[f] = f32_to_bf16_bits(__fsub_rn(__fmul_rn(x1[k], c[k]), __fmul_rn(x2[k], sn[k])));
+      row[f + kHalfRope] = f32_to_bf16_bits(__fadd_rn(__fmul_rn(x2[k], c[k]), __fmul_rn(x1[k], sn[k])));
+    }
   }
   cp_async_wait_all();
   fence_proxy_async_smem();

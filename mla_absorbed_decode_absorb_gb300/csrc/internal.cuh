@@ -44,10 +44,17 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
 }
 
 // Split-KV layout shared by the attention kernel, the combine and the workspace.
+// Short contexts: with an automatic split, at most kShortMaxUnits (sequence, query)
+// units over at most kShortMaxKv cached tokens take the short-context kernel
+// (csrc/decode_short.cu), one CTA per 8 heads and no split.
+constexpr int kShortMaxKv = 1024;
+constexpr int kShortMaxUnits = 2;
+
 struct SplitPlan {
   int max_pages;    // ceil(max_kv_len / 64)
   int split_pages;  // pages per split
   int num_splits;   // ceil(max_pages / split_pages)
+  bool short_path;  // the short-context kernel (then num_splits == 1)
   size_t o_part_bytes;
   size_t lse_part_bytes;
   size_t workspace_bytes;  // 0 when num_splits == 1
@@ -129,6 +136,12 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   const int32_t* kv_lens, int B, int n_q, int max_kv_len,
                                   const SplitPlan& plan, float* o_out, float* lse_out,
                                   int* status, cudaStream_t stream);
+
+// One CTA per (sequence, query, 8 heads), warp-level MMAs, no split: O' and lse
+// straight into o_out / lse_out (csrc/decode_short.cu); max_kv_len <= kShortMaxKv.
+cudaError_t launch_decode_short(const uint16_t* q_abs, const uint16_t* cache, int64_t num_pages,
+                                const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
+                                int max_kv_len, float* o_out, float* lse_out, int* status, cudaStream_t stream);
 
 cudaError_t launch_decode_partial_fp8(const uint16_t* q_abs, const uint8_t* cache_c8, const float* cache_scale,
                                       const uint16_t* cache_kr, int64_t num_pages, const int32_t* page_table,

@@ -45,6 +45,7 @@ _SIGS = {
     "mla_append_absorb_q_fp8": ([_p, _p, _p, _p, _p, _p, _i, _p, _p, _i, _p, _p, _p, _i64, _p, _i, _i, _p], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_decode_num_splits": ([_i, _i, _i, _i, ctypes.POINTER(_i)], _i),
+    "mla_decode_uses_short_path": ([_i, _i, _i, _i, ctypes.POINTER(_i)], _i),
     "mla_decode_attn": ([_p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
     "mla_decode_attn_partial": ([_p, _p, _i64, _p, _i, _p, _i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
     "mla_decode_combine": ([_i, _i, _i, _i, _p, _sz, _p, _p, _p], _i),
@@ -395,6 +396,13 @@ def mla_decode_num_splits(B: int, n_q: int, max_kv_len: int, split_pages: int = 
     _check("mla_decode_num_splits",
            lib.mla_decode_num_splits(int(B), int(n_q), int(max_kv_len), int(split_pages), ctypes.byref(out)))
     return int(out.value)
+
+
+def mla_decode_uses_short_path(B: int, n_q: int, max_kv_len: int, split_pages: int = 0) -> bool:
+    out = _i(0)
+    _check("mla_decode_uses_short_path",
+           lib.mla_decode_uses_short_path(int(B), int(n_q), int(max_kv_len), int(split_pages), ctypes.byref(out)))
+    return bool(out.value)
 
 
 def alloc_workspace(B, n_q, max_kv_len, split_pages=0, device=None):

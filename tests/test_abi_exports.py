@@ -54,6 +54,21 @@ def test_host_only_entry_points(lib):
     assert sz.value == 0  # a single split needs no workspace
 
 
+def test_short_context_plan(lib):
+    """With an automatic split, at most two (sequence, query) units over at most 1024
+    cached tokens take the short-context kernel with a single split; an explicit split,
+    more units or a longer context keep the tensor-core split kernel.  The cases
+    below need no device query."""
+    flag, n = ctypes.c_int(-1), ctypes.c_int(0)
+    for B, n_q, kv, sp, short in [(1, 1, 257, 0, 1), (2, 1, 1024, 0, 1), (1, 2, 1024, 0, 1), (1, 1, 1, 0, 1),
+                                  (1, 1, 257, 1, 0), (1, 1, 257, 1000, 0), (1, 1, 1025, 64, 0), (3, 1, 100, 4, 0)]:
+        assert lib.mla_decode_uses_short_path(B, n_q, kv, sp, ctypes.byref(flag)) == 0
+        assert flag.value == short, (B, n_q, kv, sp)
+        if short:
+            assert lib.mla_decode_num_splits(B, n_q, kv, sp, ctypes.byref(n)) == 0 and n.value == 1
+    assert lib.mla_decode_uses_short_path(1, 1, 100, 0, None) == 1
+
+
 def test_invalid_arguments_are_rejected_before_any_launch(lib):
     lib.mla_append_kv.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                                           ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,

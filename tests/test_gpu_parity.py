@@ -238,6 +238,38 @@ def test_decode_parity_shapes(name):
     assert np.array_equal(bits(f.out), bits(s.out))
 
 
+SHORT = {
+    # at most two (sequence, query) units over at most 1024 tokens: a single token, a
+    # page, a page and one, the 1024-token limit, two queries of one sequence, two
+    # sequences of different lengths
+    "short_kv1": W.custom("short_kv1", [0], n_q=1),
+    "short_page": W.custom("short_page", [63], n_q=1),
+    "short_page_plus1": W.custom("short_page_plus1", [64], n_q=1),
+    "short_kv1024": W.custom("short_kv1024", [1023], n_q=1),
+    "short_q2": W.custom("short_q2", [500], n_q=2),
+    "short_b2": W.custom("short_b2", [10, 700], n_q=1),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SHORT))
+def test_short_context_path(name):
+    """Short contexts with an automatic split run the short-context kernel (one CTA
+    per 8 heads, no split): every head against the oracle, and close to the 2-CTA
+    split kernel on the same inputs (forced by an explicit split; both round P to
+    bf16 against their own running max, and the split kernel also exchanges fp16
+    partial scores)."""
+    from mla_absorbed_decode_absorb_gb300 import ops
+    inp = W.generate(SHORT[name], seed=31)
+    s = run_session(inp, split_pages=0, fused_finish=False)
+    assert s.num_splits == 1 and ops.mla_decode_uses_short_path(s.B, s.n_q, s.max_kv_len, 0)
+    o_err, lat_err = check_outputs(s, inp, range(inp.batch))
+    t = run_session(inp, split_pages=1000, fused_finish=False)
+    assert not ops.mla_decode_uses_short_path(t.B, t.n_q, t.max_kv_len, 1000)
+    d = rel_l2(s.o_latent.cpu().numpy(), t.o_latent.cpu().numpy())
+    print(f"{name}: rel-L2 O {o_err:.3e} O' {lat_err:.3e}; against the split kernel {d:.3e}")
+    assert d < 3e-3
+
+
 def test_split_count_invariance():
     """Split count changes only rounding: P is a bf16 MMA operand and each split
     rounds it against its own running max, so two split layouts differ by about

@@ -40,7 +40,7 @@ def bits32(t):
     return t.detach().cpu().contiguous().view(torch.int32).numpy()
 
 
-@pytest.mark.parametrize("lens,n_q,split_pages", [([1500, 900, 2000], 2, 4), ([300, 40], 1, 1000)])
+@pytest.mark.parametrize("lens,n_q,split_pages", [([1500, 900, 2000], 2, 4), ([300, 40], 1, 1000), ([300], 1, 0)])
 def test_noalloc_equals_decode_attn_twice(lens, n_q, split_pages):
     from mla_absorbed_decode_absorb_gb300 import ops
     from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
@@ -53,7 +53,8 @@ def test_noalloc_equals_decode_attn_twice(lens, n_q, split_pages):
                                          split_pages)
     torch.cuda.synchronize()
     # the first case sends its partials through the library's array, the second
-    # (splits longer than the sequences) has one split and writes O' directly
+    # (splits longer than the sequences) has one split and writes O' directly, the
+    # third (one short sequence, automatic split) runs the short-context kernel
     assert (s.num_splits > 1) == (split_pages == 4)
     for _ in range(2):
         o = torch.full_like(ref_o, float("nan"))
