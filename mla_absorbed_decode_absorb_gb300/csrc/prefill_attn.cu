@@ -526,18 +526,30 @@ prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_co
         }
         const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
         // P = 2^(S scale - m): exponent arguments on packed fp32 pairs; the row sum
-        // adds the bf16-rounded P that P V uses, in four independent pair chains
+        // adds the float32 weights before their rounding to bf16 (round-to-nearest-even
+        // is unbiased), in four independent pair chains.  Only a row's diagonal key
+        // tile has masked columns, so the other tiles skip the compare and select.
         uint32_t pk[32];
         const uint64_t scale2 = f32x2(kScaleL2, kScaleL2), negm2 = f32x2(neg_m, neg_m);
         uint64_t s4[4] = {0ull, 0ull, 0ull, 0ull};
+        if (n_mine >= 64) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float2 e = f32x2_split(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), scale2, negm2));
-          float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
-          if (2 * c >= n_mine) p0 = 0.f;
-          if (2 * c + 1 >= n_mine) p1 = 0.f;
-          pk[c] = pack_bf16x2(p0, p1);
-          s4[c & 3] = add_f32x2(s4[c & 3], f32x2(__uint_as_float(pk[c] << 16), __uint_as_float(pk[c] & 0xffff0000u)));
+          for (int c = 0; c < 32; ++c) {
+            const float2 e = f32x2_split(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), scale2, negm2));
+            const float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
+            pk[c] = pack_bf16x2(p0, p1);
+            s4[c & 3] = add_f32x2(s4[c & 3], f32x2(p0, p1));
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float2 e = f32x2_split(fma_f32x2(f32x2(sv[2 * c], sv[2 * c + 1]), scale2, negm2));
+            float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
+            if (2 * c >= n_mine) p0 = 0.f;
+            if (2 * c + 1 >= n_mine) p1 = 0.f;
+            pk[c] = pack_bf16x2(p0, p1);
+            s4[c & 3] = add_f32x2(s4[c & 3], f32x2(p0, p1));
+          }
         }
         const float2 s2 = f32x2_split(add_f32x2(add_f32x2(s4[0], s4[1]), add_f32x2(s4[2], s4[3])));
         l = l * factor + (s2.x + s2.y);

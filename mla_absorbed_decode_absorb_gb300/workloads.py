@@ -86,6 +86,9 @@ PREFILL_WORKLOADS: dict[str, Workload] = {
         Workload("chunk_b1_l4096_c512", batch=1, n_q=512, context=4096,
                  description="B=1, a chunk of 512 new tokens after 4096 (the chunk case at the size "
                              "a full counter capture handles)"),
+        Workload("prompt_b2_c2048", batch=2, n_q=2048, context=0,
+                 description="B=2, a 2048-token prompt each (the prompt case at the size a full "
+                             "counter capture handles)"),
     ]
 }
 

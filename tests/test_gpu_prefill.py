@@ -4,7 +4,8 @@ mla_decompress_kv must give the oracle's per-head keys and values (bf16 outputs 
 an fp32 accumulation: within 2^-8 relative plus a small absolute floor), and
 zeros in the rows up to the next 128-token boundary; mla_prefill_attn must give
 the oracle's output O within max-abs 1e-2 and relative L2 5e-3 (as the absorbed
-path), and its log-sum-exp within 2e-2.  The same session switches to this path
+path), and its log-sum-exp within 5e-3 (the largest error seen is 1.5e-3, on the
+2048-token prompt).  The same session switches to this path
 for steps of 64 or more new tokens.
 """
 
@@ -19,7 +20,7 @@ from test_gpu_parity import bits, oracle_sequence, rel_l2
 
 pytestmark = pytest.mark.gpu
 
-O_MAX_ABS, O_REL_L2, LSE_MAX_ABS = 1e-2, 5e-3, 2e-2
+O_MAX_ABS, O_REL_L2, LSE_MAX_ABS = 1e-2, 5e-3, 5e-3
 
 
 def session(inp, **kw):
@@ -35,14 +36,17 @@ def session(inp, **kw):
 def check_prefill(s, inp, heads):
     o_gpu = s.out.float().cpu().numpy()
     lse_gpu = s.lse.cpu().numpy()
-    o_all, r_all = [], []
+    o_all, r_all, dl = [], [], 0.0
     for b in range(inp.batch):
         o_ref, _, lse_ref = oracle_sequence(inp, b, heads)
         o = o_gpu[b][:, heads]
         assert np.isfinite(o).all()
-        assert np.abs(lse_gpu[b][:, heads] - lse_ref).max() <= LSE_MAX_ABS
+        dl = max(dl, float(np.abs(lse_gpu[b][:, heads] - lse_ref).max()))
         o_all.append(o), r_all.append(o_ref)
     o, r = np.concatenate(o_all), np.concatenate(r_all)
+    print(f"prefill {inp.batch} x {inp.n_q}: rel-L2 O {rel_l2(o, r):.3e} max |dO| {np.abs(o - r).max():.3e} "
+          f"max |dlse| {dl:.3e}")
+    assert dl <= LSE_MAX_ABS, dl
     assert np.abs(o - r).max() <= O_MAX_ABS, np.abs(o - r).max()
     assert rel_l2(o, r) <= O_REL_L2, rel_l2(o, r)
     return rel_l2(o, r)
@@ -90,7 +94,7 @@ def test_both_paths_agree_on_short_steps(n_q):
     assert rel_l2(n.out.float().cpu().numpy(), a.out.float().cpu().numpy()) <= 2 * O_REL_L2
 
 
-@pytest.mark.parametrize("name", sorted(n for n in W.PREFILL_WORKLOADS if not n.startswith("chunk_b1")))
+@pytest.mark.parametrize("name", sorted(n for n in W.PREFILL_WORKLOADS if n in ("chunk_b4_l4096_c512", "prompt_b8_c2048")))
 def test_prefill_full_size_sampled(name):
     """The benched non-absorbed workloads at full size, in the bench's launch
     configuration: a chunk of 512 new tokens after 4096 (B = 4; four query tiles
