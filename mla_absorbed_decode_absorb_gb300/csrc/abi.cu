@@ -445,7 +445,7 @@ mla_status mla_decode_attn_partial(const mla_bf16* q_abs, const mla_bf16* cache,
     o_out = static_cast<float*>(workspace);
     lse_out = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.o_part_bytes);
   }
-  return from_cuda(launch_decode_partial(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q,
+  return from_cuda(launch_decode_planned(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q,
                                          max_kv_len, plan, o_out, lse_out, st, stream));
 }
 

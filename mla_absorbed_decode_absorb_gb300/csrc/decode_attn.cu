@@ -720,9 +720,6 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   int* status, cudaStream_t stream) {
   const int64_t units = static_cast<int64_t>(B) * n_q * plan.num_splits;
   if (units == 0) return cudaSuccess;
-  if (plan.short_path)
-    return launch_decode_short(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, o_out,
-                               lse_out, status, stream);
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || !configure(dev)) return cudaErrorInvalidDevice;
   CUtensorMap tqlat, tq64, tc128, tc64, to;

@@ -70,7 +70,7 @@ extern "C" mla_status mla_decode_attn_noalloc(const mla_bf16* q_abs, const mla_b
   int* st = device_status_word();
   if (st == nullptr) return MLA_ERR_CUDA;
   if (plan.num_splits == 1)
-    return launch_decode_partial(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, plan,
+    return launch_decode_planned(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, plan,
                                  o_latent, lse, st, stream) == cudaSuccess
                ? MLA_OK
                : MLA_ERR_CUDA;
@@ -78,7 +78,7 @@ extern "C" mla_status mla_decode_attn_noalloc(const mla_bf16* q_abs, const mla_b
   if (ws == nullptr) return MLA_ERR_CUDA;
   float* o_part = reinterpret_cast<float*>(ws);
   float* lse_part = reinterpret_cast<float*>(ws + plan.o_part_bytes);
-  if (launch_decode_partial(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, plan, o_part,
+  if (launch_decode_planned(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, plan, o_part,
                             lse_part, st, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   return launch_combine(o_part, lse_part, B, n_q, plan.num_splits, o_latent, lse, stream) == cudaSuccess

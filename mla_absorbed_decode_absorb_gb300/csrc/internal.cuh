@@ -143,6 +143,13 @@ cudaError_t launch_decode_short(const uint16_t* q_abs, const uint16_t* cache, in
                                 const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
                                 int max_kv_len, float* o_out, float* lse_out, int* status, cudaStream_t stream);
 
+// The attention a plan asks for: the short-context kernel when plan.short_path,
+// else the 2-CTA split kernel (csrc/decode_short.cu).
+cudaError_t launch_decode_planned(const uint16_t* q_abs, const uint16_t* cache, int64_t num_pages,
+                                  const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
+                                  int max_kv_len, const SplitPlan& plan, float* o_out, float* lse_out, int* status,
+                                  cudaStream_t stream);
+
 cudaError_t launch_decode_partial_fp8(const uint16_t* q_abs, const uint8_t* cache_c8, const float* cache_scale,
                                       const uint16_t* cache_kr, int64_t num_pages, const int32_t* page_table,
                                       int pt_stride, const int32_t* kv_lens, int B, int n_q, int max_kv_len,
