@@ -6,15 +6,25 @@
 // to this path for chunks of about 64 new tokens or more); "DeepSeek-MLA-
 // Principle" section 6 (prefill vs decode, the L^2 terms favour decompression).
 //
-// One CTA per (sequence, 128-token tile, group of 8 heads).  The tile's latent
-// rows (128 x 512 bf16, 128 KB) are read once by TMA from the paged cache into
-// shared memory and stay there; for each of the 8 heads and for W_UK and W_UV
-// the 128 x 512 weight matrix streams through a 4-slot ring in 64-column chunks,
-// one chain of 32 tcgen05 MMAs (M = 128 tokens, N = 128, K = 512) accumulates in
-// one of four 128-column TMEM buffers, and four epilogue warps convert and store
-// the buffer while the next head's MMAs run.  Rows of the tile past the
-// sequence's length are written as zeros, so an attention kernel that reads whole
-// 128-token tiles multiplies finite values there.
+// A dense contraction per 128-token tile of a sequence: the tile's latent rows
+// C (128 x 512) against each of the 256 weight matrices W_UK[h], W_UV[h]
+// (128 x 512).  The work is a list of units (tile, head, K or V), tile-major;
+// each persistent CTA (one per SM) takes a contiguous range of it, so the ranges
+// differ by at most one unit and a CTA changes tiles about twice.
+//
+// The latent rows are the A operand of all 256 units of their tile, so they sit
+// in TMEM (256 columns of bf16 pairs) for the whole tile and the MMAs (M = 128
+// tokens, N = 128, K = 512) read only the weights from shared memory.  Weights
+// stream from L2 in 16 KB chunks (64 K-columns of one matrix) through a 12-slot
+// ring: a chunk takes a few thousand cycles to arrive against 256 cycles of MMAs,
+// and with 4 slots the tensor pipe sat idle most of the time.  A tile's latent
+// rows come through the same ring, as 8 chunks of 64 columns issued after the
+// last weight chunk of the tile before; the four epilogue warps move them into
+// TMEM once the MMAs of that tile are done, then release their slots.  Two
+// 128-column accumulators let the same four warps convert one unit to bf16 and
+// store it by TMA while the MMAs of the next unit run.  Rows of a tile past the
+// sequence's length are written as zeros (an attention kernel that reads whole
+// 128-token tiles multiplies finite values there); tiles past it are not touched.
 #include "sm100.cuh"
 #include "tmap.cuh"
 
@@ -23,74 +33,94 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTile = 128;          // tokens per CTA
-constexpr int kHeadsPerCta = 8;
-constexpr int kUnits = 2 * kHeadsPerCta;  // (head, K or V)
-constexpr int kWStages = 4;
-constexpr int kThreads = 192;       // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
-constexpr int kChunkBytes = 128 * 128;   // 128 rows x 64 bf16 columns (SW128)
-constexpr int kOffA = 0;                 // 8 latent chunks of the tile
-constexpr int kOffW = kOffA + 8 * kChunkBytes;
-constexpr int kOffBar = kOffW + kWStages * kChunkBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;
+constexpr int kTile = 128;                  // tokens per tile
+constexpr int kUnitsPerTile = 2 * kHeads;   // unit w of a tile: head w / 2, V if w is odd
+constexpr int kStages = 12;                 // ring slots
+constexpr int kAChunks = 8;                 // latent chunks of a tile (64 columns each)
+constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kTmaWarp = 0;
+constexpr int kMmaWarp = 1;
+constexpr int kEpiWarp0 = 2;
+constexpr int kEpiThreads = 128;
+constexpr int kChunkBytes = 128 * 128;                 // 128 rows x 64 bf16 columns (SW128)
+constexpr int kOffRing = 0;
+constexpr int kOffO = kOffRing + kStages * kChunkBytes;  // output tile: 2 boxes of 64 columns
+constexpr int kOffBar = kOffO + 2 * kChunkBytes;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;       // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kAChunks < kStages, "a tile's latent chunks fit the ring beside a weight chunk");
+constexpr uint32_t kTmemD = 0;    // accumulator of the CTA's unit i: columns [128 (i & 1), 128 (i & 1) + 128)
+constexpr uint32_t kTmemA = 256;  // latent rows of the current tile, bf16 pairs: columns [256, 512)
 
 struct Bars {
-  uint64_t a_full;
-  uint64_t w_full[kWStages];
-  uint64_t w_empty[kWStages];
-  uint64_t d_full[4];
-  uint64_t d_empty[4];
+  uint64_t full[kStages];   // the slot's chunk has landed
+  uint64_t empty[kStages];  // the slot's chunk has been consumed (MMAs finished, or moved to TMEM)
+  uint64_t a_moved;         // the CTA's k-th tile's latent rows are in TMEM
+  uint64_t a_free;          // the MMAs of the k-th tile have finished: TMEM A may be overwritten
+  uint64_t d_full[2];
+  uint64_t d_empty[2];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 struct Params {
   const int32_t* page_table;
   const int32_t* kv_lens;
-  uint16_t* k_out;
-  uint16_t* v_out;
   int* status;
   int64_t num_pages;
+  int64_t units;  // B * tiles * kUnitsPerTile
   int pt_stride;
   int max_kv_len;
+  int tiles;      // tiles per sequence, ceil(max_kv_len / 128)
 };
+
+// Global tile g: its sequence, first token, tokens of the sequence in it (0 for
+// none, or for a sequence whose length is inconsistent).
+struct TileInfo {
+  int b, t0, valid;
+  bool bad;
+};
+__device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t g) {
+  TileInfo ti;
+  ti.b = static_cast<int>(g / p.tiles);
+  ti.t0 = static_cast<int>(g % p.tiles) * kTile;
+  const int kv = p.kv_lens[ti.b];
+  ti.bad = kv < 0 || kv > p.max_kv_len || (kv + kPage - 1) / kPage > p.pt_stride;
+  ti.valid = ti.bad ? 0 : max(0, min(kTile, kv - ti.t0));
+  return ti;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_wk,
-                        const __grid_constant__ CUtensorMap tm_wv, const Params p) {
+                        const __grid_constant__ CUtensorMap tm_wv, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort = &bars.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int tile = blockIdx.x, hg = blockIdx.y, b = blockIdx.z;
-
-  grid_dep_wait();
-  grid_dep_launch();
-  const int kv = p.kv_lens[b];
-  if (kv < 0 || kv > p.max_kv_len || (kv + kPage - 1) / kPage > p.pt_stride) {
-    if (tid == 0 && tile == 0 && hg == 0) record_status(p.status, MLA_ERR_BOUNDS);
-    return;
-  }
-  const int t0 = tile * kTile;
-  if (t0 >= kv) return;  // nothing of this sequence in the tile
-  const int valid = min(kTile, kv - t0);
+  // this CTA's units [u_begin, u_end)
+  const int64_t u_begin = p.units * blockIdx.x / gridDim.x;
+  const int64_t u_end = p.units * (blockIdx.x + 1) / gridDim.x;
 
   if (tid == 0) {
-    mbar_init(smem_u32(&bars.a_full), 1);
-    for (int s = 0; s < kWStages; ++s) {
-      mbar_init(smem_u32(&bars.w_full[s]), 1);
-      mbar_init(smem_u32(&bars.w_empty[s]), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bars.full[s]), 1);
+      mbar_init(smem_u32(&bars.empty[s]), 1);
     }
-    for (int s = 0; s < 4; ++s) {
-      mbar_init(smem_u32(&bars.d_full[s]), 1);
-      mbar_init(smem_u32(&bars.d_empty[s]), 128);
+    mbar_init(smem_u32(&bars.a_moved), kEpiThreads);
+    mbar_init(smem_u32(&bars.a_free), 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(smem_u32(&bars.d_full[x]), 1);
+      mbar_init(smem_u32(&bars.d_empty[x]), kEpiThreads);
     }
+    mbar_init(smem_u32(&bars.drain), 1);
     bars.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(&bars.tmem_base), 512);
     tmem_relinquish();
   }
@@ -98,103 +128,203 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  grid_dep_wait();
+  grid_dep_launch();
 
-  if (warp == 0) {
+  // Every role walks the same tiles of [u_begin, u_end) in the same order and
+  // skips the same empty ones, so they agree on the k-th tile, the i-th unit and
+  // the n-th ring chunk: per tile, 8 latent chunks, then 8 weight chunks per unit.
+  if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_c);
       tma_prefetch_desc(&tm_wk);
       tma_prefetch_desc(&tm_wv);
-      // the tile's latent rows: two 64-token pages x eight 64-column chunks
-      mbar_arrive_expect_tx(smem_u32(&bars.a_full), 8 * kChunkBytes);
-      for (int pg = 0; pg < 2; ++pg) {
-        int page = 0;
-        if (pg * kPage < valid) {
-          page = p.page_table[static_cast<int64_t>(b) * p.pt_stride + (t0 / kPage) + pg];
-          if (page < 0 || page >= p.num_pages) {
-            record_status(p.status, MLA_ERR_BOUNDS);
-            page = 0;  // stay in bounds; the result of this tile is not meaningful
+      bool ok = true;
+      int n = 0;  // chunks issued
+      auto slot = [&](int& s) {
+        s = n % kStages;
+        ok = mbar_wait(smem_u32(&bars.empty[s]), ((n / kStages) & 1) ^ 1, p.status, abort);
+        if (ok) mbar_arrive_expect_tx(smem_u32(&bars.full[s]), kChunkBytes);
+        return ok;
+      };
+      for (int64_t u = u_begin; u < u_end && ok;) {
+        const int64_t g = u / kUnitsPerTile;
+        const int64_t u_hi = min(u_end, (g + 1) * kUnitsPerTile);
+        const TileInfo ti = tile_info(p, g);
+        if (ti.bad) record_status(p.status, MLA_ERR_BOUNDS);
+        if (ti.valid > 0) {
+          // the tile's latent rows: two 64-token pages per chunk; a page past the
+          // sequence's end is read from page 0 (its rows are written as zeros)
+          int page[2] = {0, 0};
+          for (int pg = 0; pg < 2; ++pg) {
+            if (pg * kPage < ti.valid) {
+              page[pg] = p.page_table[static_cast<int64_t>(ti.b) * p.pt_stride + ti.t0 / kPage + pg];
+              if (page[pg] < 0 || page[pg] >= p.num_pages) {
+                record_status(p.status, MLA_ERR_BOUNDS);
+                page[pg] = 0;  // stay in bounds; the result of this tile is not meaningful
+              }
+            }
+          }
+          for (int c = 0; c < kAChunks && ok; ++c, ++n) {
+            int s;
+            if (!slot(s)) break;
+            for (int pg = 0; pg < 2; ++pg)
+              tma_load_2d(smem_u32(smem + kOffRing + s * kChunkBytes + pg * (kChunkBytes / 2)), &tm_c, 64 * c,
+                          page[pg] * kPage, smem_u32(&bars.full[s]));
+          }
+          for (int64_t w = u; w < u_hi && ok; ++w) {
+            const int uw = static_cast<int>(w % kUnitsPerTile);
+            const CUtensorMap* tm = (uw & 1) ? &tm_wv : &tm_wk;
+            for (int kc = 0; kc < 8 && ok; ++kc, ++n) {
+              int s;
+              if (!slot(s)) break;
+              tma_load_2d(smem_u32(smem + kOffRing + s * kChunkBytes), tm, 64 * kc, (uw >> 1) * kNope,
+                          smem_u32(&bars.full[s]));
+            }
           }
         }
-        for (int c = 0; c < 8; ++c)
-          tma_load_2d(smem_u32(smem + kOffA + c * kChunkBytes + pg * (kChunkBytes / 2)), &tm_c, 64 * c,
-                      page * kPage, smem_u32(&bars.a_full));
-      }
-      // weight chunks: unit u = (head kHeadsPerCta*hg + u/2, u%2 ? W_UV : W_UK), 8 chunks each
-      for (int i = 0; i < kUnits * 8; ++i) {
-        const int u = i >> 3, kc = i & 7, s = i % kWStages;
-        if (!mbar_wait(smem_u32(&bars.w_empty[s]), ((i / kWStages) & 1) ^ 1, p.status, abort)) break;
-        const int h = kHeadsPerCta * hg + (u >> 1);
-        mbar_arrive_expect_tx(smem_u32(&bars.w_full[s]), kChunkBytes);
-        tma_load_2d(smem_u32(smem + kOffW + s * kChunkBytes), (u & 1) ? &tm_wv : &tm_wk, 64 * kc, h * kNope,
-                    smem_u32(&bars.w_full[s]));
+        u = u_hi;
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/0);
-      const uint64_t d_a = smem_desc(smem_u32(smem + kOffA), 16, 1024, kSw128);
-      const uint64_t d_w = smem_desc(smem_u32(smem + kOffW), 16, 1024, kSw128);
-      bool ok = mbar_wait(smem_u32(&bars.a_full), 0, p.status, abort);
-      for (int u = 0; u < kUnits && ok; ++u) {
-        const int buf = u & 3;
-        ok = mbar_wait(smem_u32(&bars.d_empty[buf]), ((u >> 2) & 1) ^ 1, p.status, abort);
-        tc_fence_after();
-        for (int kc = 0; kc < 8 && ok; ++kc) {
-          const int i = u * 8 + kc, s = i % kWStages;
-          ok = mbar_wait(smem_u32(&bars.w_full[s]), (i / kWStages) & 1, p.status, abort);
-          if (!ok) break;
-          tc_fence_after();
+      const uint64_t d_w = smem_desc(smem_u32(smem + kOffRing), 16, 1024, kSw128);
+      bool ok = true;
+      int k = 0, i = 0, n = 0;  // tiles, units, ring chunks
+      for (int64_t u = u_begin; u < u_end && ok;) {
+        const int64_t g = u / kUnitsPerTile;
+        const int64_t u_hi = min(u_end, (g + 1) * kUnitsPerTile);
+        if (tile_info(p, g).valid > 0) {
+          n += kAChunks;  // the latent chunks are the epilogue warps'
+          ok = mbar_wait(smem_u32(&bars.a_moved), k & 1, p.status, abort);
+          for (int64_t w = u; w < u_hi && ok; ++w, ++i) {
+            const int buf = i & 1;
+            ok = mbar_wait(smem_u32(&bars.d_empty[buf]), ((i >> 1) & 1) ^ 1, p.status, abort);
+            tc_fence_after();
+            for (int kc = 0; kc < 8 && ok; ++kc, ++n) {
+              const int s = n % kStages;
+              ok = mbar_wait(smem_u32(&bars.full[s]), (n / kStages) & 1, p.status, abort);
+              if (!ok) break;
+              tc_fence_after();
+              // A: latent columns [64 kc + 16 k4, +16) = TMEM columns kTmemA + 32 kc + 8 k4
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + 128 * buf, d_a + ((kc * kChunkBytes) >> 4) + 2 * k,
-                   d_w + ((s * kChunkBytes) >> 4) + 2 * k, idesc, (kc > 0 || k > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&bars.w_empty[s]));
+              for (int k4 = 0; k4 < 4; ++k4)
+                mma_ts(tmem + kTmemD + 128 * buf, tmem + kTmemA + 32 * kc + 8 * k4,
+                       d_w + ((s * kChunkBytes) >> 4) + 2 * k4, idesc, (kc > 0 || k4 > 0) ? 1u : 0u);
+              mma_commit(smem_u32(&bars.empty[s]));
+            }
+            if (ok) mma_commit(smem_u32(&bars.d_full[buf]));
+          }
+          if (ok) mma_commit(smem_u32(&bars.a_free));
+          ++k;
         }
-        if (ok) mma_commit(smem_u32(&bars.d_full[buf]));
+        u = u_hi;
       }
       // no tcgen05 operation may still be running when TMEM is released
-      mma_commit(smem_u32(&bars.a_full));
-      mbar_wait(smem_u32(&bars.a_full), 1, p.status, nullptr);
+      mma_commit(smem_u32(&bars.drain));
+      mbar_wait(smem_u32(&bars.drain), 0, p.status, nullptr);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue: token rows
+    // Thread r owns token row r of the tile (TMEM lane r).  The four warps leave
+    // their loop together: each wait's outcome is ANDed over them.
     const int quad = warp & 3;
-    const int r = quad * 32 + lane;  // token row of the tile (TMEM lane)
+    const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const int64_t t = t0 + r;
-    for (int u = 0; u < kUnits; ++u) {
-      const int buf = u & 3;
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&bars.d_full[buf]), (u >> 2) & 1, p.status, abort))) break;
-      tc_fence_after();
-      const int h = kHeadsPerCta * hg + (u >> 1);
-      uint16_t* dst = ((u & 1) ? p.v_out : p.k_out) +
-                      ((static_cast<int64_t>(b) * kHeads + h) * p.max_kv_len + t) * kNope;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem + lane_off + 128 * buf + c0, v);
-        tmem_wait_ld();
-        if (t < p.max_kv_len) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+    const bool leader = warp == kEpiWarp0 && lane == 0;
+    bool ok = true;
+    int k = 0, i = 0, n = 0;
+    for (int64_t u = u_begin; u < u_end && ok;) {
+      const int64_t g = u / kUnitsPerTile;
+      const int64_t u_hi = min(u_end, (g + 1) * kUnitsPerTile);
+      const TileInfo ti = tile_info(p, g);
+      if (ti.valid > 0) {
+        // the tile's latent rows from the ring into TMEM, once the last tile's MMAs are done
+        bool okl = k == 0 || mbar_wait(smem_u32(&bars.a_free), (k - 1) & 1, p.status, abort);
+        for (int c = 0; c < kAChunks; ++c)
+          okl = okl && mbar_wait(smem_u32(&bars.full[(n + c) % kStages]), ((n + c) / kStages) & 1, p.status, abort);
+        ok = named_barrier_and(1, kEpiThreads, okl);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < kAChunks; ++c) {
+          // row r of the chunk: page 0's rows, then page 1's, 128 bytes each
+          const uint8_t* src = smem + kOffRing + ((n + c) % kStages) * kChunkBytes + r * 128;
+          uint32_t wv[32];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const bool live = r < valid;
-            d4[q] = make_uint4(live ? pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])) : 0u,
-                               live ? pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])) : 0u,
-                               live ? pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])) : 0u,
-                               live ? pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])) : 0u);
+          for (int q = 0; q < 8; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + ((q ^ (r & 7)) << 4));
+            wv[4 * q] = v.x;
+            wv[4 * q + 1] = v.y;
+            wv[4 * q + 2] = v.z;
+            wv[4 * q + 3] = v.w;
+          }
+          tmem_st32(tmem + lane_off + kTmemA + 32 * c, wv);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars.a_moved));
+        // every thread has read the chunks: their slots go back to the producer
+        named_barrier_sync(1, kEpiThreads);
+        if (leader)
+          for (int c = 0; c < kAChunks; ++c) mbar_arrive(smem_u32(&bars.empty[(n + c) % kStages]));
+        n += kAChunks;
+        ++k;
+        const bool live = r < ti.valid;
+        for (int64_t w = u; w < u_hi; ++w, ++i) {
+          n += 8;  // the unit's weight chunks are the MMAs'
+          const int uw = static_cast<int>(w % kUnitsPerTile);
+          const int buf = i & 1;
+          // the last unit's TMA stores have read the output tile
+          if (leader) bulk_wait_read<0>();
+          ok = named_barrier_and(1, kEpiThreads,
+                                 mbar_wait(smem_u32(&bars.d_full[buf]), (i >> 1) & 1, p.status, abort));
+          if (!ok) break;
+          tc_fence_after();
+          // row r into box c0 / 64 of the output tile: 128-byte rows, 16-byte unit
+          // q at (q ^ (r & 7)) * 16, the 128-byte swizzle of the store's tensor map
+          uint8_t* orow = smem + kOffO + r * 128;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_off + kTmemD + 128 * buf + c0, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int unit = ((c0 & 63) >> 3) + q;
+              const uint4 val =
+                  live ? make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                    pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])))
+                       : make_uint4(0u, 0u, 0u, 0u);
+              *reinterpret_cast<uint4*>(orow + (c0 >> 6) * kChunkBytes + ((unit ^ (r & 7)) << 4)) = val;
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars.d_empty[buf]));  // the MMAs may refill the accumulator
+          fence_proxy_async_smem();                   // the tile is visible to the TMA store
+          named_barrier_sync(1, kEpiThreads);
+          if (leader) {
+            const CUtensorMap* tm = (uw & 1) ? &tm_v : &tm_k;
+            const int z = ti.b * kHeads + (uw >> 1);
+            tma_store_3d(tm, smem_u32(smem + kOffO), 0, ti.t0, z);
+            tma_store_3d(tm, smem_u32(smem + kOffO + kChunkBytes), 64, ti.t0, z);
+            bulk_commit_group();
           }
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars.d_empty[buf]));
+      u = u_hi;
     }
+    if (leader) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 bool g_configured[64];
@@ -214,24 +344,36 @@ cudaError_t launch_decompress_kv(const uint16_t* cache, int64_t num_pages, const
     if (e != cudaSuccess) return e;
     g_configured[dev] = true;
   }
-  CUtensorMap tc, twk, twv;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return cudaErrorInvalidDevice;
+  CUtensorMap tc, twk, twv, tk, tv;
   const uint64_t c_rows = static_cast<uint64_t>(num_pages) * kPage;
   const uint64_t w_rows = static_cast<uint64_t>(kHeads) * kNope;
+  const uint64_t bh = static_cast<uint64_t>(B) * kHeads;
+  const uint64_t row_bytes = kNope * 2;
+  // K and V as [B * 128 heads][max_kv_len tokens][128]: a 128-token box that runs
+  // past max_kv_len is clipped there instead of spilling into the next head
   if (!make_tmap_bf16_2d(&tc, cache, c_rows, kRow, kRow, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_tmap_bf16_2d(&twk, w_uk, w_rows, kLatent, kLatent, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_bf16_2d(&twv, w_uv, w_rows, kLatent, kLatent, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_tmap_bf16_2d(&twv, w_uv, w_rows, kLatent, kLatent, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_3d(&tk, k_out, kNope, max_kv_len, bh, row_bytes, row_bytes * max_kv_len, 64, kTile, 1,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_bf16_3d(&tv, v_out, kNope, max_kv_len, bh, row_bytes, row_bytes * max_kv_len, 64, kTile, 1,
+                         CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   Params prm;
   prm.page_table = page_table;
   prm.kv_lens = kv_lens;
-  prm.k_out = k_out;
-  prm.v_out = v_out;
   prm.status = status;
   prm.num_pages = num_pages;
   prm.pt_stride = pt_stride;
   prm.max_kv_len = max_kv_len;
-  dim3 grid((max_kv_len + kTile - 1) / kTile, kHeads / kHeadsPerCta, B);
-  return launch_kernel(decompress_kv_tc_kernel, grid, dim3(kThreads), kSmemBytes, stream, tc, twk, twv, prm);
+  prm.tiles = (max_kv_len + kTile - 1) / kTile;
+  prm.units = static_cast<int64_t>(B) * prm.tiles * kUnitsPerTile;
+  const int64_t grid = prm.units < sms ? prm.units : sms;
+  return launch_kernel(decompress_kv_tc_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
+                       stream, tc, twk, twv, tk, tv, prm);
 }
 
 }  // namespace mla

@@ -60,7 +60,7 @@ def test_decompress_kv_parity():
     w_uv = O.bf16_bits_to_f64(bits(inp.w_uv))
     k_gpu = s.k_nope.float().cpu().numpy()
     v_gpu = s.v.float().cpu().numpy()
-    heads = [0, 5, 64, 127]
+    heads = list(range(128))  # every (head, K or V) unit of the decompression's work list
     for b in range(inp.batch):
         c_bits, _ = (bits(x) for x in inp.sequence(b))
         c = O.bf16_bits_to_f64(c_bits)
@@ -72,6 +72,38 @@ def test_decompress_kv_parity():
             assert (np.abs(g - ref) <= tol).all(), np.abs(g - ref).max()
             pad_end = min(s.max_kv_len, (kv + 127) // 128 * 128)
             assert (got[b][:, kv:pad_end] == 0).all()
+
+
+def test_decompress_kv_ragged_writes_only_its_tiles():
+    """Ragged lengths (half a tile, one past a page, tile edges, one long
+    sequence): the oracle's keys and values for sampled heads, zeros up to the
+    next 128-token boundary, and nothing written past it (the outputs start
+    filled with a sentinel)."""
+    from mla_absorbed_decode_absorb_gb300 import ops
+    inp = W.generate(W.custom("decompress_ragged", [0, 1, 127, 128, 300, 0, 900], n_q=64), seed=24)
+    s = session(inp)
+    sentinel = 7.0
+    k = torch.full(tuple(s.k_nope.shape), sentinel, dtype=torch.bfloat16, device=s.k_nope.device)
+    v = torch.full_like(k, sentinel)
+    ops.mla_decompress_kv(s.cache, s.page_table, s.kv_lens, s.max_kv_len, s.w_uk, s.w_uv, k_nope=k, v=v)
+    torch.cuda.synchronize()
+    assert ops.mla_get_device_status() == ops.MLA_OK
+    w_uk = O.bf16_bits_to_f64(bits(inp.w_uk))
+    w_uv = O.bf16_bits_to_f64(bits(inp.w_uv))
+    heads = [0, 1, 63, 64, 126, 127]
+    k_gpu = k.float().cpu().numpy()
+    v_gpu = v.float().cpu().numpy()
+    for b in range(inp.batch):
+        c = O.bf16_bits_to_f64(bits(inp.sequence(b)[0]))
+        kv = c.shape[0]
+        k_ref, v_ref = O.decompress_kv(c, w_uk[heads], w_uv[heads])
+        pad_end = min(s.max_kv_len, (kv + 127) // 128 * 128)
+        for got, ref in ((k_gpu, k_ref), (v_gpu, v_ref)):
+            g = got[b][heads][:, :kv].transpose(1, 0, 2)
+            tol = 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max()
+            assert (np.abs(g - ref) <= tol).all(), (b, np.abs(g - ref).max())
+            assert (got[b][:, kv:pad_end] == 0).all(), b
+            assert (got[b][:, pad_end:] == sentinel).all(), b
 
 
 @pytest.mark.parametrize("lengths,n_q", [([0, 1, 63, 500], 64), ([130, 0], 100), ([64, 1000], 129), ([300], 256)])
