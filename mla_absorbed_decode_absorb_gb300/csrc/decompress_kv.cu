@@ -37,6 +37,10 @@ constexpr int kTile = 128;                  // tokens per tile
 constexpr int kUnitsPerTile = 2 * kHeads;   // unit w of a tile: head w / 2, V if w is odd
 constexpr int kStages = 12;                 // ring slots
 constexpr int kAChunks = 8;                 // latent chunks of a tile (64 columns each)
+// With each weight chunk the producer pulls the one kL2Ahead chunks later into L2,
+// so that the ring's loads do not wait for DRAM: the weights' lines compete in L2
+// with the keys and values streaming out.
+constexpr int kL2Ahead = 24;
 constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -177,6 +181,11 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
             const int uw = static_cast<int>(w % kUnitsPerTile);
             const CUtensorMap* tm = (uw & 1) ? &tm_wv : &tm_wk;
             for (int kc = 0; kc < 8 && ok; ++kc, ++n) {
+              const int64_t wa = w + (kc + kL2Ahead) / 8;  // unit of the chunk kL2Ahead on
+              if (wa < u_end) {
+                const int ua = static_cast<int>(wa % kUnitsPerTile);
+                tma_prefetch_l2_2d((ua & 1) ? &tm_wv : &tm_wk, 64 * ((kc + kL2Ahead) % 8), (ua >> 1) * kNope);
+              }
               int s;
               if (!slot(s)) break;
               tma_load_2d(smem_u32(smem + kOffRing + s * kChunkBytes), tm, 64 * kc, (uw >> 1) * kNope,
