@@ -7,24 +7,27 @@
 // Principle" section 6 (prefill vs decode, the L^2 terms favour decompression).
 //
 // A dense contraction per 128-token tile of a sequence: the tile's latent rows
-// C (128 x 512) against each of the 256 weight matrices W_UK[h], W_UV[h]
-// (128 x 512).  The work is a list of units (tile, head, K or V), tile-major;
-// each persistent CTA (one per SM) takes a contiguous range of it, so the ranges
+// C (128 x 512) against the 128 per-head weight pairs [W_UK[h]; W_UV[h]]
+// (256 x 512).  The work is a list of units (tile, head), tile-major; each
+// persistent CTA (one per SM) takes a contiguous range of it, so the ranges
 // differ by at most one unit and a CTA changes tiles about twice.
 //
-// The latent rows are the A operand of all 256 units of their tile, so they sit
-// in TMEM (256 columns of bf16 pairs) for the whole tile and the MMAs (M = 128
-// tokens, N = 128, K = 512) read only the weights from shared memory.  Weights
-// stream from L2 in 16 KB chunks (64 K-columns of one matrix) through a 12-slot
-// ring: a chunk takes a few thousand cycles to arrive against 256 cycles of MMAs,
-// and with 4 slots the tensor pipe sat idle most of the time.  A tile's latent
-// rows come through the same ring, as 8 chunks of 64 columns issued after the
-// last weight chunk of the tile before; the four epilogue warps move them into
-// TMEM once the MMAs of that tile are done, then release their slots.  Two
-// 128-column accumulators let the same four warps convert one unit to bf16 and
-// store it by TMA while the MMAs of the next unit run.  Rows of a tile past the
-// sequence's length are written as zeros (an attention kernel that reads whole
-// 128-token tiles multiplies finite values there); tiles past it are not touched.
+// The latent rows are the A operand of all 128 units of their tile, so they sit
+// in TMEM (256 columns of bf16 pairs) for the whole tile and the MMAs read only
+// the weights from shared memory.  One MMA (M = 128 tokens, N = 256, K = 16)
+// makes the head's keys and values together: at N = 128 the same work took about
+// twice the tensor-pipe time per MMA, so N = 256 leaves a single 256-column
+// accumulator beside the latent rows.  The epilogue warps move it to registers
+// (a few hundred cycles against the unit's ~4,500 cycles of MMAs), hand it back
+// to the MMAs, and then convert the keys and values to bf16 and store them by
+// TMA, one 128 x 128 tile after the other.  Weights stream from L2 in 32 KB
+// chunks (64 K-columns of W_UK[h] and of W_UV[h]) through a 6-slot ring; a
+// tile's latent rows come through the same ring, two 64-column chunks per slot,
+// issued after the last weight chunk of the tile before, and the epilogue warps
+// move them into TMEM once the MMAs of that tile are done, then release their
+// slots.  Rows of a tile past the sequence's length are written as zeros (an
+// attention kernel that reads whole 128-token tiles multiplies finite values
+// there); tiles past it are not touched.
 #include "sm100.cuh"
 #include "tmap.cuh"
 
@@ -34,35 +37,36 @@ namespace {
 using namespace sm100;
 
 constexpr int kTile = 128;                  // tokens per tile
-constexpr int kUnitsPerTile = 2 * kHeads;   // unit w of a tile: head w / 2, V if w is odd
-constexpr int kStages = 12;                 // ring slots
-constexpr int kAChunks = 8;                 // latent chunks of a tile (64 columns each)
-// With each weight chunk the producer pulls the one kL2Ahead chunks later into L2,
+constexpr int kUnitsPerTile = kHeads;       // unit w of a tile: head w, keys and values
+constexpr int kChunkBytes = 128 * 128;      // 128 rows x 64 bf16 columns (SW128)
+constexpr int kSlotBytes = 2 * kChunkBytes;  // a ring slot: two such chunks
+constexpr int kStages = 6;                  // ring slots
+constexpr int kASlots = 4;                  // latent rows of a tile: 8 chunks of 64 columns, 2 per slot
+// With each weight slot the producer pulls the one kL2Ahead slots later into L2,
 // so that the ring's loads do not wait for DRAM: the weights' lines compete in L2
 // with the keys and values streaming out.
-constexpr int kL2Ahead = 24;
+constexpr int kL2Ahead = 12;
 constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiThreads = 128;
-constexpr int kChunkBytes = 128 * 128;                 // 128 rows x 64 bf16 columns (SW128)
 constexpr int kOffRing = 0;
-constexpr int kOffO = kOffRing + kStages * kChunkBytes;  // output tile: 2 boxes of 64 columns
+constexpr int kOffO = kOffRing + kStages * kSlotBytes;  // output tile: 2 boxes of 64 columns
 constexpr int kOffBar = kOffO + 2 * kChunkBytes;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;       // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kAChunks < kStages, "a tile's latent chunks fit the ring beside a weight chunk");
-constexpr uint32_t kTmemD = 0;    // accumulator of the CTA's unit i: columns [128 (i & 1), 128 (i & 1) + 128)
+static_assert(kASlots < kStages, "a tile's latent chunks fit the ring beside a weight slot");
+constexpr uint32_t kTmemD = 0;    // accumulator: keys in columns [0, 128), values in [128, 256)
 constexpr uint32_t kTmemA = 256;  // latent rows of the current tile, bf16 pairs: columns [256, 512)
 
 struct Bars {
-  uint64_t full[kStages];   // the slot's chunk has landed
-  uint64_t empty[kStages];  // the slot's chunk has been consumed (MMAs finished, or moved to TMEM)
+  uint64_t full[kStages];   // the slot's chunks have landed
+  uint64_t empty[kStages];  // the slot's chunks have been consumed (MMAs finished, or moved to TMEM)
   uint64_t a_moved;         // the CTA's k-th tile's latent rows are in TMEM
   uint64_t a_free;          // the MMAs of the k-th tile have finished: TMEM A may be overwritten
-  uint64_t d_full[2];
-  uint64_t d_empty[2];
+  uint64_t d_full;          // the accumulator holds the current unit
+  uint64_t d_empty;         // the epilogue has read it
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -116,10 +120,8 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
     }
     mbar_init(smem_u32(&bars.a_moved), kEpiThreads);
     mbar_init(smem_u32(&bars.a_free), 1);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(smem_u32(&bars.d_full[x]), 1);
-      mbar_init(smem_u32(&bars.d_empty[x]), kEpiThreads);
-    }
+    mbar_init(smem_u32(&bars.d_full), 1);
+    mbar_init(smem_u32(&bars.d_empty), kEpiThreads);
     mbar_init(smem_u32(&bars.drain), 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -137,7 +139,7 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
 
   // Every role walks the same tiles of [u_begin, u_end) in the same order and
   // skips the same empty ones, so they agree on the k-th tile, the i-th unit and
-  // the n-th ring chunk: per tile, 8 latent chunks, then 8 weight chunks per unit.
+  // the n-th ring slot: per tile, 4 latent slots, then 8 weight slots per unit.
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -145,11 +147,11 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
       tma_prefetch_desc(&tm_wk);
       tma_prefetch_desc(&tm_wv);
       bool ok = true;
-      int n = 0;  // chunks issued
+      int n = 0;  // slots issued
       auto slot = [&](int& s) {
         s = n % kStages;
         ok = mbar_wait(smem_u32(&bars.empty[s]), ((n / kStages) & 1) ^ 1, p.status, abort);
-        if (ok) mbar_arrive_expect_tx(smem_u32(&bars.full[s]), kChunkBytes);
+        if (ok) mbar_arrive_expect_tx(smem_u32(&bars.full[s]), kSlotBytes);
         return ok;
       };
       for (int64_t u = u_begin; u < u_end && ok;) {
@@ -170,25 +172,29 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
               }
             }
           }
-          for (int c = 0; c < kAChunks && ok; ++c, ++n) {
+          for (int j = 0; j < kASlots && ok; ++j, ++n) {
             int s;
             if (!slot(s)) break;
-            for (int pg = 0; pg < 2; ++pg)
-              tma_load_2d(smem_u32(smem + kOffRing + s * kChunkBytes + pg * (kChunkBytes / 2)), &tm_c, 64 * c,
-                          page[pg] * kPage, smem_u32(&bars.full[s]));
+            for (int cc = 0; cc < 2; ++cc)
+              for (int pg = 0; pg < 2; ++pg)
+                tma_load_2d(smem_u32(smem + kOffRing + s * kSlotBytes + cc * kChunkBytes + pg * (kChunkBytes / 2)),
+                            &tm_c, 64 * (2 * j + cc), page[pg] * kPage, smem_u32(&bars.full[s]));
           }
           for (int64_t w = u; w < u_hi && ok; ++w) {
-            const int uw = static_cast<int>(w % kUnitsPerTile);
-            const CUtensorMap* tm = (uw & 1) ? &tm_wv : &tm_wk;
+            const int h = static_cast<int>(w % kUnitsPerTile);
             for (int kc = 0; kc < 8 && ok; ++kc, ++n) {
-              const int64_t wa = w + (kc + kL2Ahead) / 8;  // unit of the chunk kL2Ahead on
+              const int64_t wa = w + (kc + kL2Ahead) / 8;  // unit of the slot kL2Ahead on
               if (wa < u_end) {
-                const int ua = static_cast<int>(wa % kUnitsPerTile);
-                tma_prefetch_l2_2d((ua & 1) ? &tm_wv : &tm_wk, 64 * ((kc + kL2Ahead) % 8), (ua >> 1) * kNope);
+                const int ha = static_cast<int>(wa % kUnitsPerTile), ka = (kc + kL2Ahead) % 8;
+                tma_prefetch_l2_2d(&tm_wk, 64 * ka, ha * kNope);
+                tma_prefetch_l2_2d(&tm_wv, 64 * ka, ha * kNope);
               }
               int s;
               if (!slot(s)) break;
-              tma_load_2d(smem_u32(smem + kOffRing + s * kChunkBytes), tm, 64 * kc, (uw >> 1) * kNope,
+              // rows 0-127 of the B operand: W_UK[h]; rows 128-255: W_UV[h]
+              tma_load_2d(smem_u32(smem + kOffRing + s * kSlotBytes), &tm_wk, 64 * kc, h * kNope,
+                          smem_u32(&bars.full[s]));
+              tma_load_2d(smem_u32(smem + kOffRing + s * kSlotBytes + kChunkBytes), &tm_wv, 64 * kc, h * kNope,
                           smem_u32(&bars.full[s]));
             }
           }
@@ -199,19 +205,18 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tcgen05 issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, 128, /*a_mn=*/0, /*b_mn=*/0);
+      const uint32_t idesc = idesc_bf16(128, 256, /*a_mn=*/0, /*b_mn=*/0);
       const uint64_t d_w = smem_desc(smem_u32(smem + kOffRing), 16, 1024, kSw128);
       bool ok = true;
-      int k = 0, i = 0, n = 0;  // tiles, units, ring chunks
+      int k = 0, i = 0, n = 0;  // tiles, units, ring slots
       for (int64_t u = u_begin; u < u_end && ok;) {
         const int64_t g = u / kUnitsPerTile;
         const int64_t u_hi = min(u_end, (g + 1) * kUnitsPerTile);
         if (tile_info(p, g).valid > 0) {
-          n += kAChunks;  // the latent chunks are the epilogue warps'
+          n += kASlots;  // the latent slots are the epilogue warps'
           ok = mbar_wait(smem_u32(&bars.a_moved), k & 1, p.status, abort);
           for (int64_t w = u; w < u_hi && ok; ++w, ++i) {
-            const int buf = i & 1;
-            ok = mbar_wait(smem_u32(&bars.d_empty[buf]), ((i >> 1) & 1) ^ 1, p.status, abort);
+            ok = mbar_wait(smem_u32(&bars.d_empty), (i & 1) ^ 1, p.status, abort);
             tc_fence_after();
             for (int kc = 0; kc < 8 && ok; ++kc, ++n) {
               const int s = n % kStages;
@@ -221,11 +226,11 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
               // A: latent columns [64 kc + 16 k4, +16) = TMEM columns kTmemA + 32 kc + 8 k4
 #pragma unroll
               for (int k4 = 0; k4 < 4; ++k4)
-                mma_ts(tmem + kTmemD + 128 * buf, tmem + kTmemA + 32 * kc + 8 * k4,
-                       d_w + ((s * kChunkBytes) >> 4) + 2 * k4, idesc, (kc > 0 || k4 > 0) ? 1u : 0u);
+                mma_ts(tmem + kTmemD, tmem + kTmemA + 32 * kc + 8 * k4, d_w + ((s * kSlotBytes) >> 4) + 2 * k4,
+                       idesc, (kc > 0 || k4 > 0) ? 1u : 0u);
               mma_commit(smem_u32(&bars.empty[s]));
             }
-            if (ok) mma_commit(smem_u32(&bars.d_full[buf]));
+            if (ok) mma_commit(smem_u32(&bars.d_full));
           }
           if (ok) mma_commit(smem_u32(&bars.a_free));
           ++k;
@@ -254,15 +259,16 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
       if (ti.valid > 0) {
         // the tile's latent rows from the ring into TMEM, once the last tile's MMAs are done
         bool okl = k == 0 || mbar_wait(smem_u32(&bars.a_free), (k - 1) & 1, p.status, abort);
-        for (int c = 0; c < kAChunks; ++c)
-          okl = okl && mbar_wait(smem_u32(&bars.full[(n + c) % kStages]), ((n + c) / kStages) & 1, p.status, abort);
+        for (int j = 0; j < kASlots; ++j)
+          okl = okl && mbar_wait(smem_u32(&bars.full[(n + j) % kStages]), ((n + j) / kStages) & 1, p.status, abort);
         ok = named_barrier_and(1, kEpiThreads, okl);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < kAChunks; ++c) {
-          // row r of the chunk: page 0's rows, then page 1's, 128 bytes each
-          const uint8_t* src = smem + kOffRing + ((n + c) % kStages) * kChunkBytes + r * 128;
+        for (int c = 0; c < 8; ++c) {
+          // row r of latent chunk c: page 0's rows, then page 1's, 128 bytes each
+          const uint8_t* src =
+              smem + kOffRing + ((n + c / 2) % kStages) * kSlotBytes + (c & 1) * kChunkBytes + r * 128;
           uint32_t wv[32];
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
@@ -280,50 +286,57 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
         // every thread has read the chunks: their slots go back to the producer
         named_barrier_sync(1, kEpiThreads);
         if (leader)
-          for (int c = 0; c < kAChunks; ++c) mbar_arrive(smem_u32(&bars.empty[(n + c) % kStages]));
-        n += kAChunks;
+          for (int j = 0; j < kASlots; ++j) mbar_arrive(smem_u32(&bars.empty[(n + j) % kStages]));
+        n += kASlots;
         ++k;
         const bool live = r < ti.valid;
         for (int64_t w = u; w < u_hi; ++w, ++i) {
-          n += 8;  // the unit's weight chunks are the MMAs'
-          const int uw = static_cast<int>(w % kUnitsPerTile);
-          const int buf = i & 1;
+          n += 8;  // the unit's weight slots are the MMAs'
+          const int h = static_cast<int>(w % kUnitsPerTile);
           // the last unit's TMA stores have read the output tile
           if (leader) bulk_wait_read<0>();
-          ok = named_barrier_and(1, kEpiThreads,
-                                 mbar_wait(smem_u32(&bars.d_full[buf]), (i >> 1) & 1, p.status, abort));
+          ok = named_barrier_and(1, kEpiThreads, mbar_wait(smem_u32(&bars.d_full), i & 1, p.status, abort));
           if (!ok) break;
           tc_fence_after();
-          // row r into box c0 / 64 of the output tile: 128-byte rows, 16-byte unit
-          // q at (q ^ (r & 7)) * 16, the 128-byte swizzle of the store's tensor map
-          uint8_t* orow = smem + kOffO + r * 128;
-#pragma unroll 1
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_off + kTmemD + 128 * buf + c0, v);
+          // the accumulator into registers as bf16 pairs: word j holds columns 2j, 2j + 1
+          uint32_t kv[128];
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) {
+            uint32_t va[32], vb[32];
+            tmem_ld32(tmem + lane_off + kTmemD + 64 * c2, va);
+            tmem_ld32(tmem + lane_off + kTmemD + 64 * c2 + 32, vb);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int unit = ((c0 & 63) >> 3) + q;
-              const uint4 val =
-                  live ? make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
-                                    pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
-                                    pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
-                                    pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])))
-                       : make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(orow + (c0 >> 6) * kChunkBytes + ((unit ^ (r & 7)) << 4)) = val;
+            for (int e = 0; e < 16; ++e) {
+              kv[32 * c2 + e] = live ? pack_bf16x2(__uint_as_float(va[2 * e]), __uint_as_float(va[2 * e + 1])) : 0u;
+              kv[32 * c2 + 16 + e] =
+                  live ? pack_bf16x2(__uint_as_float(vb[2 * e]), __uint_as_float(vb[2 * e + 1])) : 0u;
             }
           }
           tc_fence_before();
-          mbar_arrive(smem_u32(&bars.d_empty[buf]));  // the MMAs may refill the accumulator
-          fence_proxy_async_smem();                   // the tile is visible to the TMA store
-          named_barrier_sync(1, kEpiThreads);
-          if (leader) {
-            const CUtensorMap* tm = (uw & 1) ? &tm_v : &tm_k;
-            const int z = ti.b * kHeads + (uw >> 1);
-            tma_store_3d(tm, smem_u32(smem + kOffO), 0, ti.t0, z);
-            tma_store_3d(tm, smem_u32(smem + kOffO + kChunkBytes), 64, ti.t0, z);
-            bulk_commit_group();
+          mbar_arrive(smem_u32(&bars.d_empty));  // the MMAs of the next unit may start
+          // keys (x = 0), then values (x = 1): row r into the two 64-column boxes of
+          // the output tile, 128-byte rows, 16-byte unit q at (q ^ (r & 7)) * 16
+          uint8_t* orow = smem + kOffO + r * 128;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (x == 1) {
+              if (leader) bulk_wait_read<0>();  // the keys' stores have read the tile
+              named_barrier_sync(1, kEpiThreads);
+            }
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              *reinterpret_cast<uint4*>(orow + (q >> 3) * kChunkBytes + (((q & 7) ^ (r & 7)) << 4)) =
+                  make_uint4(kv[64 * x + 4 * q], kv[64 * x + 4 * q + 1], kv[64 * x + 4 * q + 2], kv[64 * x + 4 * q + 3]);
+            fence_proxy_async_smem();  // the tile is visible to the TMA store
+            named_barrier_sync(1, kEpiThreads);
+            if (leader) {
+              const CUtensorMap* tm = x ? &tm_v : &tm_k;
+              const int z = ti.b * kHeads + h;
+              tma_store_3d(tm, smem_u32(smem + kOffO), 0, ti.t0, z);
+              tma_store_3d(tm, smem_u32(smem + kOffO + kChunkBytes), 64, ti.t0, z);
+              bulk_commit_group();
+            }
           }
         }
       }
