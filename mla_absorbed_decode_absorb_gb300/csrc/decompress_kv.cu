@@ -8,9 +8,13 @@
 //
 // A dense contraction per 128-token tile of a sequence: the tile's latent rows
 // C (128 x 512) against the 128 per-head weight pairs [W_UK[h]; W_UV[h]]
-// (256 x 512).  The work is a list of units (tile, head), tile-major; each
-// persistent CTA (one per SM) takes a contiguous range of it, so the ranges
-// differ by at most one unit and a CTA changes tiles about twice.
+// (256 x 512).  The two CTAs of a cluster take two consecutive tiles through the
+// same heads: the work is a list of units (tile pair, head), tile-major, and
+// each persistent cluster (one CTA per SM) takes a contiguous range of it, so the
+// ranges differ by at most one unit and a cluster changes tile pairs about
+// twice.  Of every weight slot, CTA 0 loads the W_UK chunk and CTA 1 the W_UV
+// chunk, each multicast to both: the weights stream from L2, and L2's bandwidth
+// into the SMs bounded a CTA that fetched all of them itself.
 //
 // The latent rows are the A operand of all 128 units of their tile, so they sit
 // in TMEM (256 columns of bf16 pairs) for the whole tile and the MMAs read only
@@ -25,7 +29,7 @@
 // tile's latent rows come through the same ring, two 64-column chunks per slot,
 // issued after the last weight chunk of the tile before, and the epilogue warps
 // move them into TMEM once the MMAs of that tile are done, then release their
-// slots.  Rows of a tile past the sequence's length are written as zeros (an
+// slots.  A slot is refilled once both CTAs have consumed it.  Rows of a tile past the sequence's length are written as zeros (an
 // attention kernel that reads whole 128-token tiles multiplies finite values
 // there); tiles past it are not touched.
 #include "sm100.cuh"
@@ -46,6 +50,7 @@ constexpr int kASlots = 4;                  // latent rows of a tile: 8 chunks o
 // so that the ring's loads do not wait for DRAM: the weights' lines compete in L2
 // with the keys and values streaming out.
 constexpr int kL2Ahead = 12;
+constexpr uint16_t kBoth = 0x3;             // both CTAs of the cluster
 constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -62,7 +67,7 @@ constexpr uint32_t kTmemA = 256;  // latent rows of the current tile, bf16 pairs
 
 struct Bars {
   uint64_t full[kStages];   // the slot's chunks have landed
-  uint64_t empty[kStages];  // the slot's chunks have been consumed (MMAs finished, or moved to TMEM)
+  uint64_t empty[kStages];  // both CTAs have consumed the slot's chunks (MMAs finished, or moved to TMEM)
   uint64_t a_moved;         // the CTA's k-th tile's latent rows are in TMEM
   uint64_t a_free;          // the MMAs of the k-th tile have finished: TMEM A may be overwritten
   uint64_t d_full;          // the accumulator holds the current unit
@@ -78,20 +83,28 @@ struct Params {
   const int32_t* kv_lens;
   int* status;
   int64_t num_pages;
-  int64_t units;  // B * tiles * kUnitsPerTile
+  int64_t units;        // tile pairs * kUnitsPerTile
+  int64_t total_tiles;  // B * tiles
   int pt_stride;
   int max_kv_len;
   int tiles;      // tiles per sequence, ceil(max_kv_len / 128)
 };
 
 // Global tile g: its sequence, first token, tokens of the sequence in it (0 for
-// none, or for a sequence whose length is inconsistent).
+// none, for a sequence whose length is inconsistent, or for g past the last tile).
 struct TileInfo {
   int b, t0, valid;
   bool bad;
 };
 __device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t g) {
   TileInfo ti;
+  if (g >= p.total_tiles) {
+    ti.b = 0;
+    ti.t0 = 0;
+    ti.valid = 0;
+    ti.bad = false;
+    return ti;
+  }
   ti.b = static_cast<int>(g / p.tiles);
   ti.t0 = static_cast<int>(g % p.tiles) * kTile;
   const int kv = p.kv_lens[ti.b];
@@ -100,7 +113,12 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t g) {
   return ti;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Tile pair q is live if either of its tiles holds tokens: both CTAs then run it.
+__device__ __forceinline__ bool pair_live(const Params& p, int64_t q) {
+  return tile_info(p, 2 * q).valid > 0 || tile_info(p, 2 * q + 1).valid > 0;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_wk,
                         const __grid_constant__ CUtensorMap tm_wv, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -109,14 +127,16 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
   Bars& bars = *reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort = &bars.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // this CTA's units [u_begin, u_end)
-  const int64_t u_begin = p.units * blockIdx.x / gridDim.x;
-  const int64_t u_end = p.units * (blockIdx.x + 1) / gridDim.x;
+  const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
+  // this cluster's units [u_begin, u_end); the CTA works on tile 2 q + rank of pair q
+  const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
+  const int64_t u_begin = p.units * cluster / clusters;
+  const int64_t u_end = p.units * (cluster + 1) / clusters;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(&bars.full[s]), 1);
-      mbar_init(smem_u32(&bars.empty[s]), 1);
+      mbar_init(smem_u32(&bars.empty[s]), 2);  // one consumer in each CTA
     }
     mbar_init(smem_u32(&bars.a_moved), kEpiThreads);
     mbar_init(smem_u32(&bars.a_free), 1);
@@ -134,6 +154,7 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
+  cluster_sync();  // the peer's barriers exist before any chunk is multicast or slot released
   grid_dep_wait();
   grid_dep_launch();
 
@@ -155,13 +176,14 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
         return ok;
       };
       for (int64_t u = u_begin; u < u_end && ok;) {
-        const int64_t g = u / kUnitsPerTile;
-        const int64_t u_hi = min(u_end, (g + 1) * kUnitsPerTile);
-        const TileInfo ti = tile_info(p, g);
+        const int64_t q = u / kUnitsPerTile;
+        const int64_t u_hi = min(u_end, (q + 1) * kUnitsPerTile);
+        const TileInfo ti = tile_info(p, 2 * q + rank);
         if (ti.bad) record_status(p.status, MLA_ERR_BOUNDS);
-        if (ti.valid > 0) {
+        if (pair_live(p, q)) {
           // the tile's latent rows: two 64-token pages per chunk; a page past the
-          // sequence's end is read from page 0 (its rows are written as zeros)
+          // sequence's end (or of a tile with no tokens) is read from page 0 (its
+          // rows are not stored)
           int page[2] = {0, 0};
           for (int pg = 0; pg < 2; ++pg) {
             if (pg * kPage < ti.valid) {
@@ -183,19 +205,16 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
           for (int64_t w = u; w < u_hi && ok; ++w) {
             const int h = static_cast<int>(w % kUnitsPerTile);
             for (int kc = 0; kc < 8 && ok; ++kc, ++n) {
+              const CUtensorMap* tm = rank ? &tm_wv : &tm_wk;  // this CTA's half of the slot
               const int64_t wa = w + (kc + kL2Ahead) / 8;  // unit of the slot kL2Ahead on
-              if (wa < u_end) {
-                const int ha = static_cast<int>(wa % kUnitsPerTile), ka = (kc + kL2Ahead) % 8;
-                tma_prefetch_l2_2d(&tm_wk, 64 * ka, ha * kNope);
-                tma_prefetch_l2_2d(&tm_wv, 64 * ka, ha * kNope);
-              }
+              if (wa < u_end)
+                tma_prefetch_l2_2d(tm, 64 * ((kc + kL2Ahead) % 8), static_cast<int>(wa % kUnitsPerTile) * kNope);
               int s;
               if (!slot(s)) break;
-              // rows 0-127 of the B operand: W_UK[h]; rows 128-255: W_UV[h]
-              tma_load_2d(smem_u32(smem + kOffRing + s * kSlotBytes), &tm_wk, 64 * kc, h * kNope,
-                          smem_u32(&bars.full[s]));
-              tma_load_2d(smem_u32(smem + kOffRing + s * kSlotBytes + kChunkBytes), &tm_wv, 64 * kc, h * kNope,
-                          smem_u32(&bars.full[s]));
+              // rows 0-127 of the B operand: W_UK[h] (from CTA 0); rows 128-255:
+              // W_UV[h] (from CTA 1); each lands in both CTAs' slot s
+              tma_load_2d_mc(smem_u32(smem + kOffRing + s * kSlotBytes + rank * kChunkBytes), tm, 64 * kc, h * kNope,
+                             smem_u32(&bars.full[s]), kBoth);
             }
           }
         }
@@ -210,9 +229,9 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
       bool ok = true;
       int k = 0, i = 0, n = 0;  // tiles, units, ring slots
       for (int64_t u = u_begin; u < u_end && ok;) {
-        const int64_t g = u / kUnitsPerTile;
-        const int64_t u_hi = min(u_end, (g + 1) * kUnitsPerTile);
-        if (tile_info(p, g).valid > 0) {
+        const int64_t q = u / kUnitsPerTile;
+        const int64_t u_hi = min(u_end, (q + 1) * kUnitsPerTile);
+        if (pair_live(p, q)) {
           n += kASlots;  // the latent slots are the epilogue warps'
           ok = mbar_wait(smem_u32(&bars.a_moved), k & 1, p.status, abort);
           for (int64_t w = u; w < u_hi && ok; ++w, ++i) {
@@ -228,7 +247,7 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
               for (int k4 = 0; k4 < 4; ++k4)
                 mma_ts(tmem + kTmemD, tmem + kTmemA + 32 * kc + 8 * k4, d_w + ((s * kSlotBytes) >> 4) + 2 * k4,
                        idesc, (kc > 0 || k4 > 0) ? 1u : 0u);
-              mma_commit(smem_u32(&bars.empty[s]));
+              mma_commit_mc(smem_u32(&bars.empty[s]), kBoth);  // the slot is free here and in the peer
             }
             if (ok) mma_commit(smem_u32(&bars.d_full));
           }
@@ -253,10 +272,10 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
     bool ok = true;
     int k = 0, i = 0, n = 0;
     for (int64_t u = u_begin; u < u_end && ok;) {
-      const int64_t g = u / kUnitsPerTile;
-      const int64_t u_hi = min(u_end, (g + 1) * kUnitsPerTile);
-      const TileInfo ti = tile_info(p, g);
-      if (ti.valid > 0) {
+      const int64_t q = u / kUnitsPerTile;
+      const int64_t u_hi = min(u_end, (q + 1) * kUnitsPerTile);
+      const TileInfo ti = tile_info(p, 2 * q + rank);
+      if (pair_live(p, q)) {
         // the tile's latent rows from the ring into TMEM, once the last tile's MMAs are done
         bool okl = k == 0 || mbar_wait(smem_u32(&bars.a_free), (k - 1) & 1, p.status, abort);
         for (int j = 0; j < kASlots; ++j)
@@ -283,10 +302,14 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.a_moved));
-        // every thread has read the chunks: their slots go back to the producer
+        // every thread has read the chunks: their slots are free here (and in the peer)
         named_barrier_sync(1, kEpiThreads);
         if (leader)
-          for (int j = 0; j < kASlots; ++j) mbar_arrive(smem_u32(&bars.empty[(n + j) % kStages]));
+          for (int j = 0; j < kASlots; ++j) {
+            const uint32_t e = smem_u32(&bars.empty[(n + j) % kStages]);
+            mbar_arrive(e);
+            mbar_arrive_remote(mapa(e, peer));
+          }
         n += kASlots;
         ++k;
         const bool live = r < ti.valid;
@@ -330,7 +353,7 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
                   make_uint4(kv[64 * x + 4 * q], kv[64 * x + 4 * q + 1], kv[64 * x + 4 * q + 2], kv[64 * x + 4 * q + 3]);
             fence_proxy_async_smem();  // the tile is visible to the TMA store
             named_barrier_sync(1, kEpiThreads);
-            if (leader) {
+            if (leader && ti.valid > 0) {  // a tile with no tokens is not stored
               const CUtensorMap* tm = x ? &tm_v : &tm_k;
               const int z = ti.b * kHeads + h;
               tma_store_3d(tm, smem_u32(smem + kOffO), 0, ti.t0, z);
@@ -347,9 +370,35 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
   tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+  cluster_sync();  // no CTA leaves while its peer may still address its shared memory
 }
 
 bool g_configured[64];
+int g_cluster_slots[64];
+
+// Clusters of this kernel that can be resident at once (the persistent grid is
+// sized to one wave of them).
+int cluster_slots(int dev, int sms) {
+  if (g_cluster_slots[dev] > 0) return g_cluster_slots[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, decompress_kv_tc_kernel, &cfg) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = sms / 2;
+  }
+  g_cluster_slots[dev] = n;
+  return n;
+}
 
 }  // namespace
 
@@ -392,8 +441,11 @@ cudaError_t launch_decompress_kv(const uint16_t* cache, int64_t num_pages, const
   prm.pt_stride = pt_stride;
   prm.max_kv_len = max_kv_len;
   prm.tiles = (max_kv_len + kTile - 1) / kTile;
-  prm.units = static_cast<int64_t>(B) * prm.tiles * kUnitsPerTile;
-  const int64_t grid = prm.units < sms ? prm.units : sms;
+  prm.total_tiles = static_cast<int64_t>(B) * prm.tiles;
+  prm.units = (prm.total_tiles + 1) / 2 * kUnitsPerTile;
+  const int slots = cluster_slots(dev, sms);
+  const int64_t clusters = prm.units < slots ? prm.units : slots;
+  const int64_t grid = 2 * (clusters > 0 ? clusters : 1);
   return launch_kernel(decompress_kv_tc_kernel, dim3(static_cast<unsigned>(grid)), dim3(kThreads), kSmemBytes,
                        stream, tc, twk, twv, tk, tv, prm);
 }
