@@ -21,11 +21,12 @@
 // the weights from shared memory.  One MMA (M = 128 tokens, N = 256, K = 16)
 // makes the head's keys and values together: at N = 128 the same work took about
 // twice the tensor-pipe time per MMA, so N = 256 leaves a single 256-column
-// accumulator beside the latent rows.  The epilogue warps move it to registers
-// (a few hundred cycles against the unit's ~4,500 cycles of MMAs), hand it back
-// to the MMAs, and then convert the keys and values to bf16 and store them by
-// TMA, one 128 x 128 tile after the other.  Weights stream from L2 in 32 KB
-// chunks (64 K-columns of W_UK[h] and of W_UV[h]) through a 6-slot ring; a
+// accumulator beside the latent rows.  Two epilogue warpgroups, one for the keys'
+// 128 columns and one for the values', move it to registers together (the MMAs
+// of the next head wait for that), hand it back, and then convert their half to
+// bf16 and store it by TMA, one 64-column box at a time from a staging box of
+// their own.  Weights stream from L2 in 32 KB chunks (64 K-columns of W_UK[h]
+// and of W_UV[h]) through a 6-slot ring; a
 // tile's latent rows come through the same ring, two 64-column chunks per slot,
 // issued after the last weight chunk of the tile before, and the epilogue warps
 // move them into TMEM once the MMAs of that tile are done, then release their
@@ -51,13 +52,14 @@ constexpr int kASlots = 4;                  // latent rows of a tile: 8 chunks o
 // with the keys and values streaming out.
 constexpr int kL2Ahead = 12;
 constexpr uint16_t kBoth = 0x3;             // both CTAs of the cluster
-constexpr int kThreads = 192;               // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kThreads = 320;               // warp 0 TMA, warp 1 MMA, warps 2-5 keys, warps 6-9 values
 constexpr int kTmaWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kEpiWarp0 = 2;
-constexpr int kEpiThreads = 128;
+constexpr int kEpiThreads = 256;            // both epilogue warpgroups
+constexpr int kGroupThreads = 128;          // one of them
 constexpr int kOffRing = 0;
-constexpr int kOffO = kOffRing + kStages * kSlotBytes;  // output tile: 2 boxes of 64 columns
+constexpr int kOffO = kOffRing + kStages * kSlotBytes;  // output boxes (keys, values): 64 columns each
 constexpr int kOffBar = kOffO + 2 * kChunkBytes;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;       // + 1 KB alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -263,12 +265,17 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue: token rows
-    // Thread r owns token row r of the tile (TMEM lane r).  The four warps leave
-    // their loop together: each wait's outcome is ANDed over them.
+    // Warpgroup x (warps 2-5: x = 0, keys; warps 6-9: x = 1, values); thread r
+    // owns token row r of the tile (TMEM lane r) and the accumulator's columns
+    // [128 x, 128 x + 128).  The four warps of a warpgroup leave their loop
+    // together: each wait's outcome is ANDed over them.
+    const int x = (warp - kEpiWarp0) >> 2;
+    const uint32_t bar_id = 1 + x;
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    const bool leader = warp == kEpiWarp0 && lane == 0;
+    const bool leader = warp == kEpiWarp0 + 4 * x && lane == 0;
+    uint8_t* stage = smem + kOffO + x * kChunkBytes;
     bool ok = true;
     int k = 0, i = 0, n = 0;
     for (int64_t u = u_begin; u < u_end && ok;) {
@@ -276,37 +283,40 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
       const int64_t u_hi = min(u_end, (q + 1) * kUnitsPerTile);
       const TileInfo ti = tile_info(p, 2 * q + rank);
       if (pair_live(p, q)) {
-        // the tile's latent rows from the ring into TMEM, once the last tile's MMAs are done
+        // latent chunks 4x .. 4x + 3 (ring slots n + 2x, n + 2x + 1) into TMEM,
+        // once the last tile's MMAs are done
         bool okl = k == 0 || mbar_wait(smem_u32(&bars.a_free), (k - 1) & 1, p.status, abort);
-        for (int j = 0; j < kASlots; ++j)
-          okl = okl && mbar_wait(smem_u32(&bars.full[(n + j) % kStages]), ((n + j) / kStages) & 1, p.status, abort);
-        ok = named_barrier_and(1, kEpiThreads, okl);
+        for (int j = 0; j < 2; ++j)
+          okl = okl && mbar_wait(smem_u32(&bars.full[(n + 2 * x + j) % kStages]), ((n + 2 * x + j) / kStages) & 1,
+                                 p.status, abort);
+        ok = named_barrier_and(bar_id, kGroupThreads, okl);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * x; c < 4 * x + 4; ++c) {
           // row r of latent chunk c: page 0's rows, then page 1's, 128 bytes each
           const uint8_t* src =
               smem + kOffRing + ((n + c / 2) % kStages) * kSlotBytes + (c & 1) * kChunkBytes + r * 128;
           uint32_t wv[32];
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint4 v = *reinterpret_cast<const uint4*>(src + ((q ^ (r & 7)) << 4));
-            wv[4 * q] = v.x;
-            wv[4 * q + 1] = v.y;
-            wv[4 * q + 2] = v.z;
-            wv[4 * q + 3] = v.w;
+          for (int e = 0; e < 8; ++e) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + ((e ^ (r & 7)) << 4));
+            wv[4 * e] = v.x;
+            wv[4 * e + 1] = v.y;
+            wv[4 * e + 2] = v.z;
+            wv[4 * e + 3] = v.w;
           }
           tmem_st32(tmem + lane_off + kTmemA + 32 * c, wv);
         }
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars.a_moved));
-        // every thread has read the chunks: their slots are free here (and in the peer)
-        named_barrier_sync(1, kEpiThreads);
+        // every thread of the warpgroup has read its two slots: they are free
+        // here (and in the peer)
+        named_barrier_sync(bar_id, kGroupThreads);
         if (leader)
-          for (int j = 0; j < kASlots; ++j) {
-            const uint32_t e = smem_u32(&bars.empty[(n + j) % kStages]);
+          for (int j = 0; j < 2; ++j) {
+            const uint32_t e = smem_u32(&bars.empty[(n + 2 * x + j) % kStages]);
             mbar_arrive(e);
             mbar_arrive_remote(mapa(e, peer));
           }
@@ -316,18 +326,19 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
         for (int64_t w = u; w < u_hi; ++w, ++i) {
           n += 8;  // the unit's weight slots are the MMAs'
           const int h = static_cast<int>(w % kUnitsPerTile);
-          // the last unit's TMA stores have read the output tile
+          // the last unit's TMA stores have read this warpgroup's output box
           if (leader) bulk_wait_read<0>();
-          ok = named_barrier_and(1, kEpiThreads, mbar_wait(smem_u32(&bars.d_full), i & 1, p.status, abort));
+          ok = named_barrier_and(bar_id, kGroupThreads, mbar_wait(smem_u32(&bars.d_full), i & 1, p.status, abort));
           if (!ok) break;
           tc_fence_after();
-          // the accumulator into registers as bf16 pairs: word j holds columns 2j, 2j + 1
-          uint32_t kv[128];
+          // this warpgroup's 128 columns into registers as bf16 pairs: word j
+          // holds columns 128 x + 2j, 128 x + 2j + 1
+          uint32_t kv[64];
 #pragma unroll
-          for (int c2 = 0; c2 < 4; ++c2) {
+          for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t va[32], vb[32];
-            tmem_ld32(tmem + lane_off + kTmemD + 64 * c2, va);
-            tmem_ld32(tmem + lane_off + kTmemD + 64 * c2 + 32, vb);
+            tmem_ld32(tmem + lane_off + kTmemD + 128 * x + 64 * c2, va);
+            tmem_ld32(tmem + lane_off + kTmemD + 128 * x + 64 * c2 + 32, vb);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -337,27 +348,26 @@ decompress_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_c
             }
           }
           tc_fence_before();
-          mbar_arrive(smem_u32(&bars.d_empty));  // the MMAs of the next unit may start
-          // keys (x = 0), then values (x = 1): row r into the two 64-column boxes of
-          // the output tile, 128-byte rows, 16-byte unit q at (q ^ (r & 7)) * 16
-          uint8_t* orow = smem + kOffO + r * 128;
+          mbar_arrive(smem_u32(&bars.d_empty));  // with the other warpgroup's: the next head may start
+          // the two 64-column boxes in turn: row r into the staging box (128-byte
+          // rows, 16-byte unit e at (e ^ (r & 7)) * 16), then one TMA store
+          uint8_t* orow = stage + r * 128;
 #pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (x == 1) {
-              if (leader) bulk_wait_read<0>();  // the keys' stores have read the tile
-              named_barrier_sync(1, kEpiThreads);
+          for (int bx = 0; bx < 2; ++bx) {
+            if (bx == 1) {
+              if (leader) bulk_wait_read<0>();  // the first box's store has read the staging box
+              named_barrier_sync(bar_id, kGroupThreads);
             }
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-              *reinterpret_cast<uint4*>(orow + (q >> 3) * kChunkBytes + (((q & 7) ^ (r & 7)) << 4)) =
-                  make_uint4(kv[64 * x + 4 * q], kv[64 * x + 4 * q + 1], kv[64 * x + 4 * q + 2], kv[64 * x + 4 * q + 3]);
-            fence_proxy_async_smem();  // the tile is visible to the TMA store
-            named_barrier_sync(1, kEpiThreads);
+            for (int e = 0; e < 8; ++e)
+              *reinterpret_cast<uint4*>(orow + ((e ^ (r & 7)) << 4)) =
+                  make_uint4(kv[32 * bx + 4 * e], kv[32 * bx + 4 * e + 1], kv[32 * bx + 4 * e + 2],
+                             kv[32 * bx + 4 * e + 3]);
+            fence_proxy_async_smem();  // the box is visible to the TMA store
+            named_barrier_sync(bar_id, kGroupThreads);
             if (leader && ti.valid > 0) {  // a tile with no tokens is not stored
               const CUtensorMap* tm = x ? &tm_v : &tm_k;
-              const int z = ti.b * kHeads + h;
-              tma_store_3d(tm, smem_u32(smem + kOffO), 0, ti.t0, z);
-              tma_store_3d(tm, smem_u32(smem + kOffO + kChunkBytes), 64, ti.t0, z);
+              tma_store_3d(tm, smem_u32(stage), 64 * bx, ti.t0, ti.b * kHeads + h);
               bulk_commit_group();
             }
           }
