@@ -19,20 +19,21 @@
 // The latent rows are the A operand of all 128 units of their tile, so they sit
 // in TMEM (256 columns of bf16 pairs) for the whole tile and the MMAs read only
 // the weights from shared memory.  One MMA (M = 128 tokens, N = 256, K = 16)
-// makes the head's keys and values together: at N = 128 the same work took about
-// twice the tensor-pipe time per MMA, so N = 256 leaves a single 256-column
-// accumulator beside the latent rows.  Two epilogue warpgroups, one for the keys'
-// 128 columns and one for the values', move it to registers together (the MMAs
-// of the next head wait for that), hand it back, and then convert their half to
-// bf16 and store it by TMA, one 64-column box at a time from a staging box of
-// their own.  Weights stream from L2 in 32 KB chunks (64 K-columns of W_UK[h]
-// and of W_UV[h]) through a 6-slot ring; a
-// tile's latent rows come through the same ring, two 64-column chunks per slot,
-// issued after the last weight chunk of the tile before, and the epilogue warps
-// move them into TMEM once the MMAs of that tile are done, then release their
-// slots.  A slot is refilled once both CTAs have consumed it.  Rows of a tile past the sequence's length are written as zeros (an
-// attention kernel that reads whole 128-token tiles multiplies finite values
-// there); tiles past it are not touched.
+// makes the head's keys and values together: an MMA holds its issuing thread
+// ~113 cycles at N = 128 and ~138 at N = 256 (A in TMEM), so N = 256 does twice
+// the work for 1.2 times the issue time.  That leaves a single 256-column
+// accumulator beside the latent rows.  Two epilogue warpgroups, one for the
+// keys' 128 columns and one for the values', move it to registers together (the
+// MMAs of the next head wait for that), hand it back, and then convert their
+// half to bf16 and store it by TMA, one 64-column box at a time from a staging
+// box of their own.  Weights stream from L2 in 32 KB slots (64 K-columns of
+// W_UK[h] and of W_UV[h]) through a 6-slot ring; a tile's latent rows come
+// through the same ring, two 64-column chunks per slot, issued after the last
+// weight slot of the tile before, and the epilogue warps move them into TMEM
+// once the MMAs of that tile are done, then release their slots.  A slot is
+// refilled once both CTAs have consumed it.  Rows of a tile past the sequence's
+// length are written as zeros (an attention kernel that reads whole 128-token
+// tiles multiplies finite values there); tiles past it are not touched.
 #include "sm100.cuh"
 #include "tmap.cuh"
 
