@@ -106,6 +106,48 @@ def test_decompress_kv_ragged_writes_only_its_tiles():
             assert (got[b][:, pad_end:] == sentinel).all(), b
 
 
+def test_decompress_kv_bad_inputs_leave_other_sequences_intact():
+    """A page id past the pool, then a length past max_kv_len, in one sequence:
+    MLA_ERR_BOUNDS (read and cleared), and every other sequence's keys and values
+    are still the oracle's, although the CTA pairs that share weight loads mix
+    tiles of different sequences."""
+    from mla_absorbed_decode_absorb_gb300 import ops
+    inp = W.generate(W.custom("decompress_bad", [200, 0, 130, 300], n_q=64), seed=25)
+    s = session(inp)
+    w_uk = O.bf16_bits_to_f64(bits(inp.w_uk))
+    w_uv = O.bf16_bits_to_f64(bits(inp.w_uv))
+    heads = [0, 77, 127]
+
+    def check(k, v, skip):
+        k_gpu, v_gpu = k.float().cpu().numpy(), v.float().cpu().numpy()
+        for b in range(inp.batch):
+            if b == skip:
+                continue
+            c = O.bf16_bits_to_f64(bits(inp.sequence(b)[0]))
+            kv = c.shape[0]
+            k_ref, v_ref = O.decompress_kv(c, w_uk[heads], w_uv[heads])
+            for got, ref in ((k_gpu, k_ref), (v_gpu, v_ref)):
+                g = got[b][heads][:, :kv].transpose(1, 0, 2)
+                tol = 2.0 ** -8 * np.abs(ref) + 1e-3 * np.abs(ref).max()
+                assert (np.abs(g - ref) <= tol).all(), (b, np.abs(g - ref).max())
+
+    pt = s.page_table.clone()
+    pt[1, 0] = inp.num_pages + 5   # sequence 1's only page, past the pool
+    k, v = ops.mla_decompress_kv(s.cache, pt, s.kv_lens, s.max_kv_len, s.w_uk, s.w_uv)
+    torch.cuda.synchronize()
+    assert ops.mla_get_device_status() == ops.MLA_ERR_BOUNDS
+    assert ops.mla_get_device_status() == ops.MLA_OK
+    check(k, v, skip=1)
+
+    kv_lens = s.kv_lens.clone()
+    kv_lens[2] = s.max_kv_len + 1   # longer than the buffers
+    k, v = ops.mla_decompress_kv(s.cache, s.page_table, kv_lens, s.max_kv_len, s.w_uk, s.w_uv)
+    torch.cuda.synchronize()
+    assert ops.mla_get_device_status() == ops.MLA_ERR_BOUNDS
+    assert ops.mla_get_device_status() == ops.MLA_OK
+    check(k, v, skip=2)
+
+
 @pytest.mark.parametrize("lengths,n_q", [([0, 1, 63, 500], 64), ([130, 0], 100), ([64, 1000], 129), ([300], 256)])
 def test_prefill_parity(lengths, n_q):
     inp = W.generate(W.custom("prefill", lengths, n_q=n_q), seed=22)
