@@ -188,7 +188,11 @@ mla_status mla_append_absorb_q(const mla_bf16* c_kv_new, const mla_bf16* k_pe_ne
  * split, the float32 log-sum-exp combine.  The two halves are also exposed
  * separately (same arguments): mla_decode_attn_partial writes per-split partials
  * into the workspace (or the final outputs when there is a single split) and
- * mla_decode_combine merges them (a no-op for a single split).
+ * mla_decode_combine merges them (a no-op for a single split).  A split's partial
+ * O' rows are stored in bf16: each is normalised within its split, a convex
+ * combination of cache rows, so rounding it costs at most half a bf16 ulp of a
+ * cache-sized value per element; the partial log-sum-exps and the merge stay
+ * float32.
  */
 mla_status mla_decode_workspace_size(int B, int n_q, int max_kv_len, int split_pages,
                                      size_t* bytes);
@@ -338,8 +342,8 @@ mla_status mla_decode_attn_fp8_partial(const mla_bf16* q_abs, const uint8_t* cac
  *
  * Arguments, outputs and semantics are those of mla_decode_attn without
  * `workspace`/`workspace_bytes`.  Limit: the split plan must fit the array,
- * i.e. B * n_q * num_splits <= 63 units of split partials (each 128 x 513
- * floats); a single-split plan needs none.  A larger plan returns
+ * i.e. B * n_q * num_splits <= 127 units of split partials (each 128 x 512
+ * bf16 values and 128 floats); a single-split plan needs none.  A larger plan returns
  * MLA_ERR_WORKSPACE and launches nothing.
  * The first call on a device looks up the array's device address (one
  * cudaGetSymbolAddress with that device current); make that first call before

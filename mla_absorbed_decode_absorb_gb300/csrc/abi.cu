@@ -122,7 +122,7 @@ bool make_plan(int B, int n_q, int max_kv_len, int split_pages, SplitPlan* plan)
   plan->split_pages = split_pages;
   plan->num_splits = (plan->max_pages + split_pages - 1) / split_pages;
   const size_t rows = static_cast<size_t>(B) * n_q * plan->num_splits * kHeads;
-  plan->o_part_bytes = round_up(rows * kLatent * sizeof(float), 256);
+  plan->o_part_bytes = round_up(rows * kLatent * sizeof(uint16_t), 256);  // bf16 partials
   plan->lse_part_bytes = round_up(rows * sizeof(float), 256);
   plan->workspace_bytes = plan->num_splits > 1 ? plan->o_part_bytes + plan->lse_part_bytes : 0;
   return true;
@@ -235,10 +235,10 @@ mla_status mla_decode_attn_fp8_partial(const mla_bf16* q_abs, const uint8_t* cac
     return MLA_ERR_WORKSPACE;
   int* st = status_ptr();
   if (st == nullptr) return MLA_ERR_CUDA;
-  float* o_out = o_latent;
+  void* o_out = o_latent;
   float* lse_out = lse;
   if (plan.num_splits > 1) {
-    o_out = static_cast<float*>(workspace);
+    o_out = workspace;
     lse_out = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.o_part_bytes);
   }
   return from_cuda(launch_decode_partial_fp8(q_abs, cache_c8, cache_scale, cache_kr, num_pages, page_table,
@@ -439,10 +439,10 @@ mla_status mla_decode_attn_partial(const mla_bf16* q_abs, const mla_bf16* cache,
     return MLA_ERR_WORKSPACE;
   int* st = status_ptr();
   if (st == nullptr) return MLA_ERR_CUDA;
-  float* o_out = o_latent;
+  void* o_out = o_latent;
   float* lse_out = lse;
   if (plan.num_splits > 1) {
-    o_out = static_cast<float*>(workspace);
+    o_out = workspace;
     lse_out = reinterpret_cast<float*>(static_cast<char*>(workspace) + plan.o_part_bytes);
   }
   return from_cuda(launch_decode_planned(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q,
@@ -457,7 +457,7 @@ mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
   if (B == 0 || plan.num_splits == 1) return MLA_OK;
   if (!o_latent || !aligned16(o_latent)) return MLA_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return MLA_ERR_WORKSPACE;
-  const float* o_part = static_cast<const float*>(workspace);
+  const uint16_t* o_part = static_cast<const uint16_t*>(workspace);
   const float* lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + plan.o_part_bytes);
   return from_cuda(launch_combine(o_part, lse_part, B, n_q, plan.num_splits, o_latent, lse, stream));
 }
@@ -502,7 +502,7 @@ mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_page
   if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return MLA_ERR_WORKSPACE;
   int* st = status_ptr();
   if (st == nullptr) return MLA_ERR_CUDA;
-  const float* o_part = static_cast<const float*>(workspace);
+  const uint16_t* o_part = static_cast<const uint16_t*>(workspace);
   const float* lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + plan.o_part_bytes);
   return from_cuda(launch_combine_out_absorb(o_part, lse_part, plan.num_splits, w_uv, static_cast<uint16_t*>(od), lse,
                                              B, n_q, st, stream));

@@ -1,4 +1,4 @@
-// Split-KV merge by log-sum-exp, in float32.
+// Split-KV merge by log-sum-exp, in float32 (the splits' partials O'_s arrive as bf16).
 //
 // "DeepSeek-MLA-Principle", FlashMLA point 3: the history is processed in
 // blocks with the softmax normalisation updated online; splitting the blocks
@@ -14,7 +14,7 @@ namespace {
 constexpr int kThreads = 128;  // 4 latent columns per thread
 
 __global__ void __launch_bounds__(kThreads)
-combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+combine_kernel(const uint16_t* __restrict__ o_part, const float* __restrict__ lse_part,
                int num_splits, float* __restrict__ o_latent, float* __restrict__ lse) {
   grid_dep_wait();
   grid_dep_launch();
@@ -31,8 +31,9 @@ combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_p
       if (l == -INFINITY) continue;
       const float w = expf(l - m);
       z += w;
-      const float4 v = reinterpret_cast<const float4*>(
-          o_part + ((bj * num_splits + s) * kHeads + h) * kLatent)[threadIdx.x];
+      const uint2 b = reinterpret_cast<const uint2*>(o_part + ((bj * num_splits + s) * kHeads + h) * kLatent)[threadIdx.x];
+      const float4 v = make_float4(__uint_as_float(b.x << 16), __uint_as_float(b.x & 0xffff0000u),
+                                   __uint_as_float(b.y << 16), __uint_as_float(b.y & 0xffff0000u));
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
@@ -64,7 +65,7 @@ cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, cudaS
                        stream, src, dst, n);
 }
 
-cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
+cudaError_t launch_combine(const uint16_t* o_part, const float* lse_part, int B, int n_q,
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(B) * n_q * kHeads;
   if (rows == 0) return cudaSuccess;

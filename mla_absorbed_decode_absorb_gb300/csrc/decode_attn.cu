@@ -129,8 +129,9 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kOffStage % 1024 == 0 && kStageBytes % 1024 == 0 && kOffP % 1024 == 0, "swizzled tiles start on 1 KB");
 
 constexpr float kRescaleLog2 = 8.f;
-// Output staging at the end: row warpgroup g < 2 stages its 128 x 128 fp32 tile
-// of O' as four 32-column boxes in the ring (idle by then).
+// Output staging at the end: row warpgroup g < 2 stages its 128 x 128 tile of O'
+// in the ring (idle by then): four 32-column fp32 boxes for the final O' of a
+// single split, two 64-column bf16 boxes for a split's partial.
 constexpr int kOBoxBytes = 128 * 128;
 constexpr int kOTileBytes = 4 * kOBoxBytes;
 static_assert(2 * kOTileBytes <= kStages * kStageBytes, "output staging fits in the ring");
@@ -160,8 +161,9 @@ static_assert(sizeof(Bars) <= 512, "barrier block");
 struct Params {
   const int32_t* page_table;
   const int32_t* kv_lens;
-  float* o_out;
+  void* o_out;         // fp32 O' (one split), or the splits' bf16 partials (out_bf16)
   float* lse_out;
+  int out_bf16;
   int* status;
   int64_t num_pages;
   int pt_stride;
@@ -633,8 +635,39 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_
         // r * 128, 16-byte chunk c at (c ^ (r & 7)) * 16
         uint8_t* tile = smem + kOffStage + g * kOTileBytes;
         const int32_t y0 = static_cast<int32_t>(out_row) - row;  // row 0 of the unit
+        if (p.out_bf16) {
+          // a split's partial: two boxes of 64 bf16 columns x 128 rows, 128-byte
+          // swizzle: row r at r * 128, 16-byte chunk c at (c ^ (r & 7)) * 16
 #pragma unroll 1
-        for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 2; ++k) {
+            uint8_t* brow = tile + k * kOBoxBytes + row * 128;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {  // 32 columns (four 16-byte chunks) at a time
+              uint32_t r[32];
+              tmem_ld32(tmem + lane_off + kTmemO + 128 * g + 64 * k + 32 * hh, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const uint32_t* q = r + 8 * c4;
+                const int c = 4 * hh + c4;
+                *reinterpret_cast<uint4*>(brow + ((c ^ (row & 7)) << 4)) =
+                    make_uint4(pack_bf16x2(__uint_as_float(q[0]) * inv, __uint_as_float(q[1]) * inv),
+                               pack_bf16x2(__uint_as_float(q[2]) * inv, __uint_as_float(q[3]) * inv),
+                               pack_bf16x2(__uint_as_float(q[4]) * inv, __uint_as_float(q[5]) * inv),
+                               pack_bf16x2(__uint_as_float(q[6]) * inv, __uint_as_float(q[7]) * inv));
+              }
+            }
+            fence_proxy_async_smem();  // visible to the TMA store
+            named_barrier_sync(1 + g, kRowThreads);
+            if (row == 0) {
+              tma_store_2d(&tm_o, smem_u32(tile + k * kOBoxBytes), static_cast<int32_t>(rank * 256 + 128 * g + 64 * k),
+                           y0);
+              bulk_commit_group();
+            }
+          }
+        }
+#pragma unroll 1
+        for (int k = 0; k < (p.out_bf16 ? 0 : 4); ++k) {
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + kTmemO + 128 * g + 32 * k, r);
           tmem_wait_ld();
@@ -654,8 +687,14 @@ decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_qlat, const __grid_
         if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = (m + log2f(lt)) * kLn2;
         if (row == 0) bulk_wait_read<0>();  // the staging area has been read (the writes complete with the grid)
       } else {
-        float* orow = p.o_out + out_row * kLatent + rank * 256 + 128 * g;
-        for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int64_t o0 = out_row * kLatent + rank * 256 + 128 * g;
+        if (p.out_bf16) {
+          uint16_t* orow = static_cast<uint16_t*>(p.o_out) + o0;
+          for (int c0 = 0; c0 < 128; c0 += 8) *reinterpret_cast<uint4*>(orow + c0) = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          float* orow = static_cast<float*>(p.o_out) + o0;
+          for (int c0 = 0; c0 < 128; c0 += 4) *reinterpret_cast<float4*>(orow + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         if (rank == 0 && g == 0 && p.lse_out != nullptr) p.lse_out[out_row] = -INFINITY;
       }
     }
@@ -716,7 +755,7 @@ int decode_cluster_slots() {
 cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   int64_t num_pages, const int32_t* page_table, int pt_stride,
                                   const int32_t* kv_lens, int B, int n_q, int max_kv_len,
-                                  const SplitPlan& plan, float* o_out, float* lse_out,
+                                  const SplitPlan& plan, void* o_out, float* lse_out,
                                   int* status, cudaStream_t stream) {
   const int64_t units = static_cast<int64_t>(B) * n_q * plan.num_splits;
   if (units == 0) return cudaSuccess;
@@ -728,15 +767,19 @@ cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
   if (!make_tmap_bf16_chunks(&tqlat, q_abs, q_rows, kRow, 128, 4) ||
       !make_tmap_bf16_2d(&tq64, q_abs, q_rows, kRow, kRow, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       !make_tmap_bf16_chunks(&tc128, cache, c_rows, kRow, 64, 4) ||
-      !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_tmap_f32_2d(&to, o_out, static_cast<uint64_t>(units) * kHeads, kLatent, kLatent, 32, 128,
-                        CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_tmap_bf16_2d(&tc64, cache, c_rows, kRow, kRow, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  const bool out_bf16 = plan.num_splits > 1;  // partials for the merge
+  const uint64_t o_rows = static_cast<uint64_t>(units) * kHeads;
+  if (out_bf16 ? !make_tmap_bf16_2d(&to, o_out, o_rows, kLatent, kLatent, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+               : !make_tmap_f32_2d(&to, o_out, o_rows, kLatent, kLatent, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   Params prm;
   prm.page_table = page_table;
   prm.kv_lens = kv_lens;
   prm.o_out = o_out;
   prm.lse_out = lse_out;
+  prm.out_bf16 = out_bf16;
   prm.status = status;
   prm.num_pages = num_pages;
   prm.pt_stride = pt_stride;

@@ -76,7 +76,7 @@ extern "C" mla_status mla_decode_attn_noalloc(const mla_bf16* q_abs, const mla_b
                : MLA_ERR_CUDA;
   char* ws = static_cast<char*>(scratch_ptr());
   if (ws == nullptr) return MLA_ERR_CUDA;
-  float* o_part = reinterpret_cast<float*>(ws);
+  uint16_t* o_part = reinterpret_cast<uint16_t*>(ws);  // bf16 partials
   float* lse_part = reinterpret_cast<float*>(ws + plan.o_part_bytes);
   if (launch_decode_planned(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, plan, o_part,
                             lse_part, st, stream) != cudaSuccess)

@@ -423,11 +423,11 @@ cudaError_t launch_decode_short(const uint16_t* q_abs, const uint16_t* cache, in
 
 cudaError_t launch_decode_planned(const uint16_t* q_abs, const uint16_t* cache, int64_t num_pages,
                                   const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
-                                  int max_kv_len, const SplitPlan& plan, float* o_out, float* lse_out, int* status,
+                                  int max_kv_len, const SplitPlan& plan, void* o_out, float* lse_out, int* status,
                                   cudaStream_t stream) {
-  if (plan.short_path)
-    return launch_decode_short(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, o_out,
-                               lse_out, status, stream);
+  if (plan.short_path)  // a single split: o_out is the final fp32 O'
+    return launch_decode_short(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len,
+                               static_cast<float*>(o_out), lse_out, status, stream);
   return launch_decode_partial(q_abs, cache, num_pages, page_table, pt_stride, kv_lens, B, n_q, max_kv_len, plan,
                                o_out, lse_out, status, stream);
 }

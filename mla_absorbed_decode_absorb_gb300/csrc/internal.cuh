@@ -131,10 +131,14 @@ cudaError_t launch_copy(void* dst, const void* src, size_t bytes, bool src_is_ho
 // One warp waiting on an mbarrier nothing completes, given up after limit_ns (csrc/selftest.cu).
 cudaError_t launch_wait_timeout(int* status, uint64_t limit_ns, cudaStream_t stream);
 
+// o_out: with one split the final O' (fp32 [B, n_q, 128, 512]); with several,
+// the splits' partials O'_s as bf16 [B, n_q, splits, 128, 512] (the merge reads
+// them; each is normalised within its split, so bf16 keeps its relative error
+// at 2^-9 whatever the context length).  lse_out: fp32, per split likewise.
 cudaError_t launch_decode_partial(const uint16_t* q_abs, const uint16_t* cache,
                                   int64_t num_pages, const int32_t* page_table, int pt_stride,
                                   const int32_t* kv_lens, int B, int n_q, int max_kv_len,
-                                  const SplitPlan& plan, float* o_out, float* lse_out,
+                                  const SplitPlan& plan, void* o_out, float* lse_out,
                                   int* status, cudaStream_t stream);
 
 // One CTA per (sequence, query, 8 heads), warp-level MMAs, no split: O' and lse
@@ -147,13 +151,13 @@ cudaError_t launch_decode_short(const uint16_t* q_abs, const uint16_t* cache, in
 // else the 2-CTA split kernel (csrc/decode_short.cu).
 cudaError_t launch_decode_planned(const uint16_t* q_abs, const uint16_t* cache, int64_t num_pages,
                                   const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
-                                  int max_kv_len, const SplitPlan& plan, float* o_out, float* lse_out, int* status,
+                                  int max_kv_len, const SplitPlan& plan, void* o_out, float* lse_out, int* status,
                                   cudaStream_t stream);
 
 cudaError_t launch_decode_partial_fp8(const uint16_t* q_abs, const uint8_t* cache_c8, const float* cache_scale,
                                       const uint16_t* cache_kr, int64_t num_pages, const int32_t* page_table,
                                       int pt_stride, const int32_t* kv_lens, int B, int n_q, int max_kv_len,
-                                      const SplitPlan& plan, float* o_out, float* lse_out, int* status,
+                                      const SplitPlan& plan, void* o_out, float* lse_out, int* status,
                                       cudaStream_t stream);
 
 cudaError_t launch_append_kv_fp8(const uint16_t* c_kv_new, const uint16_t* k_pe_new,
@@ -172,7 +176,8 @@ cudaError_t launch_rope_q(const uint16_t* q_rope, const int32_t* seq_lens_before
                           int rope_max_pos, uint16_t* q_abs, int B, int n_q, int* status, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const float* src, uint16_t* dst, int64_t n, cudaStream_t stream);
 
-cudaError_t launch_combine(const float* o_part, const float* lse_part, int B, int n_q,
+// o_part: the bf16 partials of launch_decode_partial
+cudaError_t launch_combine(const uint16_t* o_part, const float* lse_part, int B, int n_q,
                            int num_splits, float* o_latent, float* lse, cudaStream_t stream);
 
 cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint16_t* out,
@@ -189,7 +194,7 @@ cudaError_t launch_prefill_attn(const uint16_t* q_nope, const uint16_t* q_rope, 
                                 const int32_t* page_table, int pt_stride, const int32_t* kv_lens, int B, int n_q,
                                 uint16_t* out, float* lse, int* status, cudaStream_t stream);
 
-cudaError_t launch_combine_out_absorb(const float* o_part, const float* lse_part, int num_splits,
+cudaError_t launch_combine_out_absorb(const uint16_t* o_part, const float* lse_part, int num_splits,
                                       const uint16_t* w_uv, uint16_t* out, float* lse, int B, int n_q,
                                       int* status, cudaStream_t stream);
 

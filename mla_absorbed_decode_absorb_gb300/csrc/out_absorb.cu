@@ -44,12 +44,12 @@ __host__ __device__ inline int smem_bytes_for(int T, int num_splits) {
   return kSmemA + (kLatent / 64) * nb * 128 + 24 + 4 * (2 * kNMax + table) + 1024;
 }
 
-// src: O' rows; with src_lse == nullptr, row (t, h) is src[(t * 128 + h) * 512]
-// (one source); otherwise num_splits partial rows src[((t * S + s) * 128 + h) * 512]
-// with log-sum-exps src_lse[(t * S + s) * 128 + h] are merged first, and the
-// merged log-sum-exp goes to lse_out[t * 128 + h] (if non-null).
+// src: O' rows; with src_lse == nullptr, row (t, h) is the fp32 row
+// src[(t * 128 + h) * 512] (one source); otherwise num_splits partial rows in bf16,
+// src[((t * S + s) * 128 + h) * 512], with log-sum-exps src_lse[(t * S + s) * 128 + h]
+// are merged first, and the merged log-sum-exp goes to lse_out[t * 128 + h] (if non-null).
 __global__ void __launch_bounds__(kThreads, 1)
-out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __restrict__ src,
+out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const void* __restrict__ src,
                      const float* __restrict__ src_lse, int num_splits, uint16_t* __restrict__ out, float* __restrict__ lse_out,
                      int T, int* status, bool weights_early) {
   extern __shared__ uint8_t smem_raw[];
@@ -134,7 +134,9 @@ out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __re
       for (int k = 0; k < 8; ++k) {
         const int t = tq + 4 * (i0 + k);
         if (t < nt) {
-          const float4* p = reinterpret_cast<const float4*>(src + (static_cast<int64_t>(t0 + t) * kHeads + h) * kLatent) + 2 * u;
+          const float4* p =
+              reinterpret_cast<const float4*>(static_cast<const float*>(src) + (static_cast<int64_t>(t0 + t) * kHeads + h) * kLatent) +
+              2 * u;
           a[k] = p[0];
           b[k] = p[1];
         }
@@ -150,9 +152,11 @@ out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __re
             x[j][k] = y[j][k] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (t < nt && s0 + j < num_splits) {
               const int64_t r = (static_cast<int64_t>(t0 + t) * S + s0 + j) * kHeads + h;
-              const float4* p = reinterpret_cast<const float4*>(src + r * kLatent) + 2 * u;
-              x[j][k] = p[0];
-              y[j][k] = p[1];
+              const uint4 q = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(src) + r * kLatent)[u];
+              x[j][k] = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                                    __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+              y[j][k] = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xffff0000u),
+                                    __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xffff0000u));
             }
           }
         if (!weights_ready) {
@@ -262,7 +266,7 @@ out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const float* __re
 constexpr int kTTokens = 32;                   // tokens per CTA (at most)
 constexpr int kTBoxRows = 64;                  // O' rows (token x split) per box
 constexpr int kTStages = 5;
-constexpr int kTBoxBytes = 64 * 4 * kTBoxRows;  // 16 KB
+constexpr int kTBoxBytes = 64 * 4 * kTBoxRows;  // 16 KB (fp32 rows; bf16 partial rows use half)
 constexpr int kTSlotBytes = kChunk + kTBoxBytes;  // W_UV chunk, then the O' box
 constexpr int kTThreads = 288;                 // warps 0-7 merge, warp 8 loads and issues MMAs
 constexpr int kTMaxSplits = 16;
@@ -322,9 +326,10 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
     for (int k = kTStages; k < kNChunks; ++k) tma_prefetch_l2_2d(&tm_w, 64 * k, h * kNope);
   };
   // box k: rows (t0 + t) * S + s, t < ntile, columns [64k, 64k + 64) of head h
+  const uint32_t prow_bytes = merge ? 128u : 256u;  // 64 columns of a bf16 partial row, or of an fp32 O' row
   auto load_p = [&](int k) {
     const int slot = k % kTStages;
-    mbar_arrive_expect_tx(smem_u32(&bars.p_full[slot]), 256u * ntile * S);  // the whole box, rows past T * S as zeros
+    mbar_arrive_expect_tx(smem_u32(&bars.p_full[slot]), prow_bytes * ntile * S);  // the whole box, rows past T * S as zeros
     tma_load_3d(smem_u32(ring + slot * kTSlotBytes + kChunk), &tm_p, 64 * k, h, t0 * S, smem_u32(&bars.p_full[slot]));
   };
 
@@ -417,8 +422,18 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
           for (int s = 0; s < S; ++s) {
             const float w = merge ? s_w[t * S + s] : 1.f;
             if (w >= 0.f) {
-              const float4* r = reinterpret_cast<const float4*>(box + (t * S + s) * 256 + u * 32);
-              const float4 x = r[0], y = r[1];
+              float4 x, y;
+              if (merge) {
+                const uint4 q = *reinterpret_cast<const uint4*>(box + (t * S + s) * 128 + u * 16);
+                x = make_float4(__uint_as_float(q.x << 16), __uint_as_float(q.x & 0xffff0000u),
+                                __uint_as_float(q.y << 16), __uint_as_float(q.y & 0xffff0000u));
+                y = make_float4(__uint_as_float(q.z << 16), __uint_as_float(q.z & 0xffff0000u),
+                                __uint_as_float(q.w << 16), __uint_as_float(q.w & 0xffff0000u));
+              } else {
+                const float4* r = reinterpret_cast<const float4*>(box + (t * S + s) * 256 + u * 32);
+                x = r[0];
+                y = r[1];
+              }
               a[0] = fmaf(w, x.x, a[0]); a[1] = fmaf(w, x.y, a[1]); a[2] = fmaf(w, x.z, a[2]); a[3] = fmaf(w, x.w, a[3]);
               a[4] = fmaf(w, y.x, a[4]); a[5] = fmaf(w, y.y, a[5]); a[6] = fmaf(w, y.z, a[6]); a[7] = fmaf(w, y.w, a[7]);
             }
@@ -459,7 +474,7 @@ out_absorb_stream_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_
   if (warp == 8) tmem_dealloc(tmem, tmem_cols);
 }
 
-cudaError_t launch_stream(const float* src, const float* src_lse, int num_splits, const uint16_t* w_uv, uint16_t* out,
+cudaError_t launch_stream(const void* src, const float* src_lse, int num_splits, const uint16_t* w_uv, uint16_t* out,
                           float* lse_out, int T, int* status, cudaStream_t stream) {
   static bool configured[kMaxDevicesLocal] = {};  // the attribute is per device
   const int dev_ = current_device_index();
@@ -473,18 +488,23 @@ cudaError_t launch_stream(const float* src, const float* src_lse, int num_splits
   const int S = num_splits;
   const int ntile = t_tile(S);
   // W_UV as a [128 * 128, 512] matrix: box 64 columns x 128 rows, 128-byte swizzle;
-  // O' rows as [T * S][128 heads][512]: box 64 columns x 1 head x (ntile * S) rows
+  // O' rows as [T * S][128 heads][512] (bf16 partials when merging, else fp32): box
+  // 64 columns x 1 head x (ntile * S) rows
+  const uint64_t rows = static_cast<uint64_t>(T) * S;
+  const bool merge = src_lse != nullptr;
   if (!make_tmap_bf16_2d(&tw, w_uv, static_cast<uint64_t>(kHeads) * kNope, kLatent, kLatent, 64, 128,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap_f32_3d(&tp, src, kLatent, kHeads, static_cast<uint64_t>(T) * S, kLatent * 4ull,
-                        static_cast<uint64_t>(kHeads) * kLatent * 4ull, 64, 1, static_cast<uint32_t>(ntile * S)))
+      (merge ? !make_tmap_bf16_3d(&tp, src, kLatent, kHeads, rows, kLatent * 2ull, static_cast<uint64_t>(kHeads) * kLatent * 2ull,
+                                  64, 1, static_cast<uint32_t>(ntile * S), CU_TENSOR_MAP_SWIZZLE_NONE)
+             : !make_tmap_f32_3d(&tp, src, kLatent, kHeads, rows, kLatent * 4ull, static_cast<uint64_t>(kHeads) * kLatent * 4ull,
+                                 64, 1, static_cast<uint32_t>(ntile * S))))
     return cudaErrorInvalidValue;
   dim3 grid(kHeads, (T + ntile - 1) / ntile);
   return launch_kernel(out_absorb_stream_kernel, grid, dim3(kTThreads), kTSmemBytes, stream, tw, tp, src_lse,
                        num_splits, out, lse_out, T, status, launch_overlap() >= 2);
 }
 
-cudaError_t launch(const float* src, const float* src_lse, int num_splits, const uint16_t* w_uv, uint16_t* out,
+cudaError_t launch(const void* src, const float* src_lse, int num_splits, const uint16_t* w_uv, uint16_t* out,
                    float* lse_out, int T, int* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   if (num_splits <= kTMaxSplits && (reinterpret_cast<uintptr_t>(src) & 15u) == 0)
@@ -515,7 +535,7 @@ cudaError_t launch_out_absorb(const float* o_latent, const uint16_t* w_uv, uint1
   return launch(o_latent, nullptr, 1, w_uv, out, nullptr, B * n_q, status, stream);
 }
 
-cudaError_t launch_combine_out_absorb(const float* o_part, const float* lse_part, int num_splits,
+cudaError_t launch_combine_out_absorb(const uint16_t* o_part, const float* lse_part, int num_splits,
                                       const uint16_t* w_uv, uint16_t* out, float* lse, int B, int n_q,
                                       int* status, cudaStream_t stream) {
   return launch(o_part, lse_part, num_splits, w_uv, out, lse, B * n_q, status, stream);

@@ -49,7 +49,7 @@ def test_host_only_entry_points(lib):
     assert n.value == 9  # 513 pages in 64-page chunks
     sz = ctypes.c_size_t(0)
     assert lib.mla_decode_workspace_size(8, 1, 32769, 64, ctypes.byref(sz)) == 0
-    assert sz.value >= 8 * 9 * 128 * (512 + 1) * 4
+    assert sz.value >= 8 * 9 * 128 * (512 * 2 + 4)  # bf16 partial rows + float32 log-sum-exps
     assert lib.mla_decode_workspace_size(8, 1, 4096, 64, ctypes.byref(sz)) == 0
     assert sz.value == 0  # a single split needs no workspace
 

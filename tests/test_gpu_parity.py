@@ -274,7 +274,9 @@ def test_split_count_invariance():
     """Split count changes only rounding: P is a bf16 MMA operand and each split
     rounds it against its own running max, so two split layouts differ by about
     two independent bf16 roundings of the weights (rms 2^-9/sqrt(3) each, about
-    1.6e-3 relative in L2); the merge itself is exact up to fp32."""
+    1.6e-3 relative in L2); a split's partial O' is stored in bf16 (one more such
+    rounding, which a single split, writing O' in fp32, does not have), and the
+    merge itself is exact up to fp32."""
     inp = W.generate(W.custom("splits", [700, 1000, 64], n_q=2), seed=4)
     ref = run_session(inp, split_pages=1000)
     assert ref.num_splits == 1

@@ -72,7 +72,7 @@ def test_noalloc_refuses_a_plan_larger_than_its_array():
 
     f = _noalloc(ops.lib)
     inp = W.generate(W.custom("noalloc_big", [4000] * 8, n_q=1), seed=8)
-    s = DecodeSession(inp, split_pages=1)   # 8 sequences x 63 splits > 63 units
+    s = DecodeSession(inp, split_pages=1)   # 8 sequences x 63 splits > 127 units
     s.step()
     o = torch.zeros_like(s.o_latent)
     lse = torch.zeros_like(s.lse)
