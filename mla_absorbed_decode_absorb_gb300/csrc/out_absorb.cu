@@ -255,7 +255,8 @@ out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const void* __res
 // 128 KB of W_UV in shared memory, while a TMA box lands in shared memory
 // directly.  Per CTA (head h, up to kTTokens tokens), latent chunk k (64 m)
 // travels through a 5-slot ring as W_UV[h]'s chunk k (a 64 m x 128 d box) and the
-// rows (token t, split s) of O' (one box of up to 64 rows): the first five
+// rows (token t, split s) of O' (one box of up to 128 bf16 partial rows, or of
+// up to 32 fp32 rows of a single source): the first five
 // weight chunks are requested before the previous kernel has finished (where
 // the launch allows) and the last three pulled into L2, so that the O' of five
 // chunks is in flight at once (two round trips to L2 for the tile, where a
@@ -264,9 +265,10 @@ out_absorb_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const void* __res
 // bf16 chunk k of B, and warp 8 issues the chunk's 4 MMAs as soon as it is
 // written, then refills the slot once they have finished.
 constexpr int kTTokens = 32;                   // tokens per CTA (at most)
-constexpr int kTBoxRows = 64;                  // O' rows (token x split) per box
+constexpr int kTBoxRows = 128;                 // O' rows (token x split) per box
 constexpr int kTStages = 5;
-constexpr int kTBoxBytes = 64 * 4 * kTBoxRows;  // 16 KB (fp32 rows; bf16 partial rows use half)
+constexpr int kTBoxBytes = 64 * 2 * kTBoxRows;  // 16 KB: 128 rows of 64 bf16 partial values
+static_assert(kTTokens * 64 * 4 <= kTBoxBytes, "a single source's fp32 rows (one per token) fit the box");
 constexpr int kTSlotBytes = kChunk + kTBoxBytes;  // W_UV chunk, then the O' box
 constexpr int kTThreads = 288;                 // warps 0-7 merge, warp 8 loads and issues MMAs
 constexpr int kTMaxSplits = 16;
@@ -288,7 +290,8 @@ constexpr int kTSmemBytes = kTOffTab + 4 * (kTTokens * kTMaxSplits + 2 * kTToken
 static_assert(sizeof(TBars) <= 256, "barrier block");
 static_assert(kTSmemBytes <= 232448, "shared memory budget");
 
-// Tokens per CTA for S splits: whole tokens' rows fit one box.
+// Tokens per CTA for S splits: whole tokens' rows fit one box (S = 1: at most
+// kTTokens fp32 rows).
 __host__ __device__ inline int t_tile(int S) { return min(kTTokens, kTBoxRows / S); }
 
 __global__ void __launch_bounds__(kTThreads, 1)
@@ -492,6 +495,7 @@ cudaError_t launch_stream(const void* src, const float* src_lse, int num_splits,
   // 64 columns x 1 head x (ntile * S) rows
   const uint64_t rows = static_cast<uint64_t>(T) * S;
   const bool merge = src_lse != nullptr;
+  if (!merge && S != 1) return cudaErrorInvalidValue;  // fp32 rows: one source only
   if (!make_tmap_bf16_2d(&tw, w_uv, static_cast<uint64_t>(kHeads) * kNope, kLatent, kLatent, 64, 128,
                          CU_TENSOR_MAP_SWIZZLE_128B) ||
       (merge ? !make_tmap_bf16_3d(&tp, src, kLatent, kHeads, rows, kLatent * 2ull, static_cast<uint64_t>(kHeads) * kLatent * 2ull,
