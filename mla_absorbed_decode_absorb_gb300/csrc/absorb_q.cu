@@ -7,7 +7,8 @@
 //
 // tcgen05 version, operands swapped so the large side is M: per head h the CTA
 // computes D[m, t] = sum_d W_UK[h][d][m] * q_nope[t][h][d] for 128 latent
-// columns m (M = 128) and up to 256 query tokens t (N).  A = W_UK[h] is
+// columns m (M = 128) and up to 64 query tokens t (N; more tokens take more CTAs,
+// which also spreads the RoPE half and the append over more threads).  A = W_UK[h] is
 // MN-major (m contiguous), B = q_nope rows are K-major (d contiguous); both are
 // staged into shared memory in the 128-byte-swizzled canonical layouts (A by
 // two TMA boxes of 64 m x 128 d, B by 16-byte asynchronous copies), one MMA
@@ -27,11 +28,11 @@ namespace {
 using namespace sm100;
 
 constexpr int kMTile = 128;   // latent columns per CTA
-constexpr int kNMax = 256;    // query tokens per CTA
+constexpr int kNMax = 64;     // query tokens per CTA
 constexpr int kThreads = 128;
 constexpr int kAChunk = 128 * 128;          // bytes of one 64-column MN chunk: 128 d rows x 128 B
 constexpr int kSmemA = 2 * kAChunk;         // 32 KB
-constexpr int kSmemB = 2 * kNMax * 128;     // two 64-wide K chunks of up to 256 rows: 64 KB
+constexpr int kSmemB = 2 * kNMax * 128;     // two 64-wide K chunks of up to 64 rows: 16 KB
 constexpr int kSmemBytes = kSmemA + kSmemB + 1024 /*align*/ + 64;
 
 // Tokens of the widest tile (rounded up to the MMA's N granularity of 16), and
@@ -54,7 +55,7 @@ absorb_q_tc_kernel(const __grid_constant__ CUtensorMap tm_w, const uint16_t* __r
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kSmemA;
-  // B and TMEM are sized for the widest token tile of this launch (<= 256)
+  // B and TMEM are sized for the widest token tile of this launch (<= 64)
   const int nb = tile_tokens(T);
   const uint32_t tmem_cols = tmem_cols_for(nb);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sB + 2 * nb * 128);
