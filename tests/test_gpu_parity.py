@@ -287,6 +287,45 @@ def test_split_count_invariance():
         assert np.abs(s.lse.cpu().numpy() - ref.lse.cpu().numpy()).max() < 2e-3
 
 
+def test_split_partials_in_the_workspace():
+    """The split kernel leaves every split's partial in the workspace: O' over the
+    split's visible tokens, normalised within the split, in bf16 at rows
+    ((t * S + s) * 128 + h) of 512 (t = b * n_q + j), then the splits' log-sum-exps
+    in float32; a split with no visible token has lse -inf and a zero row.  Each
+    against the oracle's partial over the same token range (FlashMLA point 3 of
+    "DeepSeek-MLA-Principle": per-block results merged by their log-sum-exps)."""
+    inp = W.generate(W.custom("partials", [700, 130, 0], n_q=2), seed=12)
+    s = run_session(inp, split_pages=3)  # the fused finish reads the partials, it does not move them
+    S, B, n_q = s.num_splits, inp.batch, inp.n_q
+    assert S == 4
+    rows = B * n_q * S * 128
+    ws = s.workspace.cpu()
+    part = ws[:rows * 512 * 2].view(torch.bfloat16).float().numpy().reshape(B, n_q, S, 128, 512)
+    lse = ws[rows * 512 * 2:rows * 512 * 2 + rows * 4].view(torch.float32).numpy().reshape(B, n_q, S, 128)
+    span = 3 * 64
+    w_uk = O.bf16_bits_to_f64(bits(inp.w_uk))
+    w_uv = O.bf16_bits_to_f64(bits(inp.w_uv))
+    seen_empty = seen_full = 0
+    for b in range(B):
+        c_bits, k_bits = (bits(x) for x in inp.sequence(b))
+        c = O.bf16_bits_to_f64(c_bits)
+        kr = O.bf16_bits_to_f64(O.rope_key_bf16_bits(k_bits, np.arange(c_bits.shape[0])))
+        q_nope = O.bf16_bits_to_f64(bits(inp.q_nope[b]))
+        q_rope = O.bf16_bits_to_f64(bits(inp.q_rope[b]))
+        for sp in range(S):
+            _, lat_ref, lse_ref = O.decode_absorbed(q_nope, q_rope, w_uk, w_uv, c, kr, int(inp.prior_lens[b]),
+                                                    token_range=(sp * span, (sp + 1) * span))
+            for j in range(n_q):
+                if np.isneginf(lse_ref[j]).all():
+                    assert np.isneginf(lse[b, j, sp]).all() and not part[b, j, sp].any(), (b, j, sp)
+                    seen_empty += 1
+                    continue
+                assert np.abs(lse[b, j, sp] - lse_ref[j]).max() <= LSE_MAX_ABS, (b, j, sp)
+                assert rel_l2(part[b, j, sp], lat_ref[j]) <= LAT_REL_L2, (b, j, sp, rel_l2(part[b, j, sp], lat_ref[j]))
+                seen_full += 1
+    assert seen_empty > 0 and seen_full > 0
+
+
 def test_out_of_range_page_is_reported():
     from mla_absorbed_decode_absorb_gb300 import ops
     from mla_absorbed_decode_absorb_gb300.runtime import DecodeSession
