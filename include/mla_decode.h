@@ -178,8 +178,9 @@ mla_status mla_append_absorb_q(const mla_bf16* c_kv_new, const mla_bf16* k_pe_ne
  *              tensor-core tiles and no split, which mla_decode_uses_short_path
  *              reports; otherwise the split count that fills the GPU with 2-CTA
  *              tcgen05 clusters).
- *   workspace  device scratch of at least mla_decode_workspace_size() bytes
- *              (may be NULL when that size is 0).
+ *   workspace  device scratch of at least mla_decode_workspace_size() bytes,
+ *              16-byte aligned (may be NULL when that size is 0); a missing, short
+ *              or misaligned workspace returns MLA_ERR_WORKSPACE.
  *   o_latent   [B, n_q, 128, 512] float32 out: O'[h] = sum_t alpha_t c_t
  *   lse        [B, n_q, 128] float32 out (nullable): natural log-sum-exp of the
  *              scaled scores.
@@ -398,7 +399,8 @@ mla_status mla_out_absorb(const float* o_latent, const mla_bf16* w_uv, mla_bf16*
  * as mla_decode_combine, rounded to bf16 and multiplied as in mla_out_absorb, so
  * `out` equals combine-then-out_absorb bit for bit; O' itself is not written to
  * o_latent.  Errors: MLA_ERR_INVALID_ARG for bad sizes or unaligned pointers,
- * MLA_ERR_WORKSPACE if the workspace is smaller than the plan needs.
+ * MLA_ERR_WORKSPACE if the workspace is smaller than the plan needs or not 16-byte
+ * aligned.
  */
 mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_pages,
                                   const void* workspace, size_t workspace_bytes, const float* o_latent,

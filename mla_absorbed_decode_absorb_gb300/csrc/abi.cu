@@ -456,7 +456,7 @@ mla_status mla_decode_combine(int B, int n_q, int max_kv_len, int split_pages,
   if (!make_plan(B, n_q, max_kv_len, split_pages, &plan)) return MLA_ERR_INVALID_ARG;
   if (B == 0 || plan.num_splits == 1) return MLA_OK;
   if (!o_latent || !aligned16(o_latent)) return MLA_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return MLA_ERR_WORKSPACE;
+  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   const uint16_t* o_part = static_cast<const uint16_t*>(workspace);
   const float* lse_part = reinterpret_cast<const float*>(static_cast<const char*>(workspace) + plan.o_part_bytes);
   return from_cuda(launch_combine(o_part, lse_part, B, n_q, plan.num_splits, o_latent, lse, stream));
@@ -499,7 +499,7 @@ mla_status mla_combine_out_absorb(int B, int n_q, int max_kv_len, int split_page
   void* od = nullptr;
   if (!output_view(out, static_cast<size_t>(B) * n_q * kHeads * kNope * 2, &od)) return MLA_ERR_INVALID_ARG;
   if (!aligned16(w_uv) || !aligned16(od)) return MLA_ERR_INVALID_ARG;
-  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes) return MLA_ERR_WORKSPACE;
+  if (workspace == nullptr || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)) return MLA_ERR_WORKSPACE;
   int* st = status_ptr();
   if (st == nullptr) return MLA_ERR_CUDA;
   const uint16_t* o_part = static_cast<const uint16_t*>(workspace);

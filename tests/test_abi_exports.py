@@ -104,3 +104,20 @@ def test_new_entry_points_validate_before_any_launch(lib):
     lib.mla_selftest_wait_timeout.argtypes = [I64, P]
     assert lib.mla_selftest_wait_timeout(0, None) == 1
     assert lib.mla_selftest_wait_timeout(3_000_000_000, None) == 1
+
+
+def test_merge_refuses_a_short_or_misaligned_workspace(lib):
+    """The merge entry point validates the workspace on the host before it launches
+    anything: a workspace smaller than the plan or not 16-byte aligned returns
+    MLA_ERR_WORKSPACE (the pointers below are never dereferenced)."""
+    B, n_q, kv, sp = 2, 1, 1000, 4  # 16 pages in 4 splits
+    n = ctypes.c_int(0)
+    assert lib.mla_decode_num_splits(B, n_q, kv, sp, ctypes.byref(n)) == 0 and n.value == 4
+    sz = ctypes.c_size_t(0)
+    assert lib.mla_decode_workspace_size(B, n_q, kv, sp, ctypes.byref(sz)) == 0 and sz.value > 0
+    f = lib.mla_decode_combine
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_size_t] + [ctypes.c_void_p] * 3
+    o_latent = ctypes.c_void_p(0x20000)
+    assert f(B, n_q, kv, sp, ctypes.c_void_p(0x10008), sz.value, o_latent, None, None) == 3  # misaligned
+    assert f(B, n_q, kv, sp, ctypes.c_void_p(0x10000), sz.value - 256, o_latent, None, None) == 3  # short
+    assert f(B, n_q, kv, sp, None, sz.value, o_latent, None, None) == 3  # missing
